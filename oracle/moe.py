@@ -1,0 +1,245 @@
+"""Float64 reference of the MoE layer: router, top-k, pull schedule, SwiGLU experts, combine,
+and the backward pass.  Test infrastructure only (see the package docstring).
+
+Layouts follow the problem statement of the layer: x[T,d], W_router[d,E], per routed expert
+W_gate/W_up[d,F] and W_down[F,d] (stacked as [E,d,F] / [E,F,d]), shared expert
+Ws_gate/Ws_up[d,Fs], Ws_down[Fs,d].  Row vectors: g = x @ W_gate.
+
+Every floating-point quantity is computed in float64 from the (bf16-exact) inputs and is not
+rounded to a narrower type, except the router logits used for the *top-k decision*, which are
+rounded to float32 first because the GPU takes that integer decision on float32 logits.
+"""
+
+import numpy as np
+
+
+def to_f64(a):
+    """Exact conversion of a bf16/fp32/fp64 array (numpy or CPU torch tensor) to float64."""
+    try:
+        import torch  # only for accepting CPU tensors; no arithmetic of the method
+
+        if isinstance(a, torch.Tensor):
+            return a.detach().to("cpu").to(torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------------------
+# Router.  Page "Mixture-of-Kittens: Nhân kernel MoE ...", section "Chồng lấp tính toán và
+# truyền tải trong MoE": a router projection selects the top-k routed experts per token and
+# assigns each a router weight.  Plain reading: logits = x @ W_router + b, softmax over all
+# experts, top-k on the logits (descending, ties to the lower expert index), weights are the
+# selected probabilities renormalised to sum to one.
+# --------------------------------------------------------------------------------------
+
+def router_logits(x, W_router, bias=None):
+    """l[t,e] = sum_i x[t,i] W_router[i,e] + b[e], float64.  Pinned via the top-k and weight
+    pins (brute-force subsets, softmax identities) and the finite-difference pin of dW_router."""
+    l = x @ W_router
+    if bias is not None:
+        l = l + np.asarray(bias, dtype=np.float64)[None, :]
+    return l
+
+
+def topk_select(logits32, k):
+    """Indices of the k largest float32 logits per row, in order (logit descending, expert
+    index ascending among equal logits).  Pinned against brute-force enumeration of all
+    k-subsets in tests."""
+    l32 = np.asarray(logits32, dtype=np.float32)
+    # stable sort of the negated values keeps equal logits in ascending index order
+    order = np.argsort(-l32, axis=1, kind="stable")
+    return order[:, :k].astype(np.int32)
+
+
+def topk_gap(logits32, k):
+    """Gap between the k-th and (k+1)-th largest float32 logit of each row (inf when k == E).
+    Tokens with a gap below 1e-4 are near ties whose selection is not compared bit-exactly."""
+    l32 = np.asarray(logits32, dtype=np.float32).astype(np.float64)
+    E = l32.shape[1]
+    if k >= E:
+        return np.full(l32.shape[0], np.inf)
+    s = -np.sort(-l32, axis=1)
+    return s[:, k - 1] - s[:, k]
+
+
+def weights_for_selection(logits, topk_idx):
+    """w_j = p[e_j] / sum_{i in selection} p[e_i] with p = softmax(logits) over all experts.
+    Pinned by the closed-form identity w = softmax over the selected logits only, sum w = 1,
+    and k = E giving w = p."""
+    l = np.asarray(logits, dtype=np.float64)
+    m = l.max(axis=1, keepdims=True)
+    ex = np.exp(l - m)
+    p = ex / ex.sum(axis=1, keepdims=True)
+    sel = np.take_along_axis(p, np.asarray(topk_idx, dtype=np.int64), axis=1)
+    return sel / sel.sum(axis=1, keepdims=True)
+
+
+def route(x, W_router, bias, k):
+    """Router of the layer.  Returns (logits64, logits32, topk_idx, topk_w)."""
+    l64 = router_logits(x, W_router, bias)
+    l32 = l64.astype(np.float32)
+    idx = topk_select(l32, k)
+    w = weights_for_selection(l64, idx)
+    return l64, l32, idx, w
+
+
+# --------------------------------------------------------------------------------------
+# Pull schedule.  Page "Mixture-of-Kittens: Nhân kernel MoE ...", section "Lập lịch": the
+# schedule is built without a sort by scanning the routing tensor and appending every route
+# that targets a (local) expert; outputs are tokens per expert, region offsets and a table
+# whose row is the destination row.  On one GPU every expert is local and the source rank is 0.
+# Page "Метод и эксперименты": each expert then reads its own tokens, e.g. E2 <- [0,2,9,15].
+# --------------------------------------------------------------------------------------
+
+def dispatch(topk_idx, E):
+    """Returns counts[E], offsets[E+1] (exclusive prefix sum), sorted_tok[T*k] (token of each
+    destination row; tokens ascending inside an expert's region) and inv_pos[T,k] (destination
+    row of route (t,j)).  Pinned by the worked example fixture and permutation checks."""
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    T, k = idx.shape
+    counts = np.zeros(E, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            counts[idx[t, j]] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+    fill = offsets[:-1].copy()
+    sorted_tok = np.zeros(T * k, dtype=np.int64)
+    inv_pos = np.zeros((T, k), dtype=np.int64)
+    for t in range(T):  # scanning tokens in order appends them in ascending order per expert
+        for j in range(k):
+            e = idx[t, j]
+            pos = fill[e]
+            fill[e] += 1
+            sorted_tok[pos] = t
+            inv_pos[t, j] = pos
+    return (counts.astype(np.int32), offsets.astype(np.int32),
+            sorted_tok.astype(np.int32), inv_pos.astype(np.int32))
+
+
+# --------------------------------------------------------------------------------------
+# Expert FFN.  Same page, section "Chồng lấp tính toán ...": up and gate projections, SwiGLU
+# activation, down projection.  SiLU(z) = z * sigmoid(z).
+# --------------------------------------------------------------------------------------
+
+def silu(z):
+    """z / (1 + exp(-z)).  Pinned at closed-form points (0, +-ln 3, large |z|)."""
+    return z / (1.0 + np.exp(-z))
+
+
+def expert_ffn(X, Wg, Wu, Wd):
+    """SwiGLU FFN of one expert on rows X[n,d]: g = X Wg, u = X Wu, h = SiLU(g) u, y = h Wd.
+    Returns (g, u, h, y).  Pinned with permutation-matrix weights (closed form) and
+    linearity/zero-gate invariants."""
+    g = X @ Wg
+    u = X @ Wu
+    h = silu(g) * u
+    return g, u, h, h @ Wd
+
+
+# --------------------------------------------------------------------------------------
+# Layer forward.  y[t] = shared(x_t) + sum_j w_j y_{e_j}(x_t).
+# --------------------------------------------------------------------------------------
+
+def _experts_used(topk_idx):
+    return sorted(set(int(e) for e in np.asarray(topk_idx).ravel()))
+
+
+def moe_forward(x, Wg, Wu, Wd, shared, topk_idx, topk_w):
+    """Layer output for the rows of x.  ``Wg/Wu/Wd`` are indexable by expert id (a stacked
+    array or any lazy accessor returning float64 [d,F] / [F,d] matrices); ``shared`` is
+    (Ws_gate, Ws_up, Ws_down) or None.  Pinned by: k = E with identical experts reduces to
+    shared + FFN; token permutation permutes outputs; a zero router weight contributes nothing;
+    E = k = 1 gives shared + FFN."""
+    x = np.asarray(x, dtype=np.float64)
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    w = np.asarray(topk_w, dtype=np.float64)
+    y = np.zeros_like(x)
+    if shared is not None:
+        y += expert_ffn(x, *shared)[3]
+    for e in _experts_used(idx):  # float64: the summation order does not matter here
+        rows, slots = np.nonzero(idx == e)
+        ye = expert_ffn(x[rows], Wg[e], Wu[e], Wd[e])[3]
+        np.add.at(y, rows, w[rows, slots][:, None] * ye)
+    return y
+
+
+def moe_forward_from_logits(x, logits, topk_idx, Wg, Wu, Wd, shared):
+    """Forward with the selection held fixed and the weights recomputed from ``logits``
+    (used for finite differences with respect to the logits and the router weights)."""
+    w = weights_for_selection(logits, topk_idx)
+    return moe_forward(x, Wg, Wu, Wd, shared, topk_idx, w)
+
+
+# --------------------------------------------------------------------------------------
+# Backward.  Gradients of L = sum(dY * y) with the top-k selection held constant; experts that
+# a token did not select get no gradient from it.  Pinned by central finite differences.
+# --------------------------------------------------------------------------------------
+
+def moe_backward(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_experts=None):
+    """``only_experts`` (optional) restricts the routed-expert terms to those expert ids (for
+    checks of sampled experts on large inputs; dX and the router terms are then partial).
+    Returns a dict with dX[T,d], dW_gate/dW_up[E,d,F], dW_down[E,F,d], dWs_gate/dWs_up[d,Fs],
+    dWs_down[Fs,d] (None without a shared expert), dlogits[T,E], dW_router[d,E] and the
+    per-route router-weight gradients dw[T,k] (= <dY_t, y_{e_j}(x_t)>)."""
+    x = np.asarray(x, dtype=np.float64)
+    dY = np.asarray(dY, dtype=np.float64)
+    Wr = np.asarray(W_router, dtype=np.float64)
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    T, d = x.shape
+    E = Wr.shape[1]
+    k = idx.shape[1]
+    w = weights_for_selection(logits, idx)
+    F = Wg[0].shape[1]
+    dX = np.zeros_like(x)
+    dWg = np.zeros((E, d, F))
+    dWu = np.zeros((E, d, F))
+    dWd = np.zeros((E, F, d))
+    dw = np.zeros((T, k))
+
+    def ffn_backward(X, dYr, wr, Wge, Wue, Wde):
+        g = X @ Wge
+        u = X @ Wue
+        s = 1.0 / (1.0 + np.exp(-g))
+        h = g * s * u
+        a = dYr @ Wde.T                      # dL/d(h) before the router weight
+        dwr = (a * h).sum(axis=1)            # <dY, h Wd> = <a, h>
+        dh = wr[:, None] * a
+        dg = dh * u * s * (1.0 + g * (1.0 - s))   # d SiLU(g)/dg = s (1 + g (1 - s))
+        du = dh * g * s
+        dWde = (wr[:, None] * h).T @ dYr
+        dWge = X.T @ dg
+        dWue = X.T @ du
+        dXr = dg @ Wge.T + du @ Wue.T
+        return dXr, dWge, dWue, dWde, dwr
+
+    for e in (range(E) if only_experts is None else only_experts):
+        rows, slots = np.nonzero(idx == e)
+        if rows.size == 0:
+            continue
+        dXr, dWg[e], dWu[e], dWd[e], dwr = ffn_backward(
+            x[rows], dY[rows], w[rows, slots], Wg[e], Wu[e], Wd[e])
+        np.add.at(dX, rows, dXr)
+        dw[rows, slots] = dwr
+
+    dWs = None
+    if shared is not None:
+        dXs, dWsg, dWsu, dWsd, _ = ffn_backward(x, dY, np.ones(T), *shared)
+        dX += dXs
+        dWs = (dWsg, dWsu, dWsd)
+
+    # w_j = exp(l_j) / sum_{i in S} exp(l_i)  =>  dl_m = w_m (dw_m - sum_j w_j dw_j), m in S
+    dl = np.zeros((T, E))
+    inner = (w * dw).sum(axis=1, keepdims=True)
+    np.put_along_axis(dl, idx, w * (dw - inner), axis=1)
+    dX += dl @ Wr.T
+    dWr = x.T @ dl
+    return {
+        "dX": dX, "dW_gate": dWg, "dW_up": dWu, "dW_down": dWd,
+        "dWs_gate": None if dWs is None else dWs[0],
+        "dWs_up": None if dWs is None else dWs[1],
+        "dWs_down": None if dWs is None else dWs[2],
+        "dlogits": dl, "dW_router": dWr, "dw": dw,
+    }

@@ -1,0 +1,85 @@
+"""Pins of the oracle's MXFP8 quantiser (E4M3 values, UE8M0 scale per 32 elements), on the CPU.
+
+* Exhaustive: every E4M3 code decodes to a value that encodes back to the same code.
+* Library special case: encoding agrees bit for bit with the torch.float8_e4m3fn conversion
+  routine on random and edge values inside the finite range.
+* Closed forms: saturation to +-448, the scale of blocks whose amax is 448 * 2^s exactly or just
+  above it, the all-zero block, and the half-ulp bound of quantise -> dequantise.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def test_all_codes_round_trip():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes)
+    nan = np.isnan(vals)
+    assert sorted(codes[nan].tolist()) == [0x7F, 0xFF]
+    back = oracle.e4m3_encode(vals)
+    assert (back[~nan] == codes[~nan]).all()
+    assert vals[0x7E] == 448.0 and vals[0x01] == 2.0 ** -9 and vals[0x08] == 2.0 ** -6
+    # known values of the format: 1.0 = 0x38, -2.0 = 0xC0, 0.5 = 0x30
+    assert oracle.e4m3_encode(np.array([1.0, -2.0, 0.5])).tolist() == [0x38, 0xC0, 0x30]
+
+
+def _torch_e4m3(v32):
+    return torch.from_numpy(v32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_encode_matches_library_conversion():
+    rng = np.random.default_rng(0)
+    parts = [
+        rng.standard_normal(20000).astype(np.float32) * s for s in (1e-3, 0.05, 1.0, 30.0, 200.0)
+    ]
+    # exact midpoints between neighbouring codes exercise ties-to-even
+    pos = oracle.e4m3_decode(np.arange(0, 127, dtype=np.uint8))
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    parts += [mids, -mids, pos.astype(np.float32), np.array([0.0, -0.0, 448.0, -448.0], np.float32)]
+    v = np.concatenate(parts)
+    v = v[np.abs(v) <= 448.0]
+    got = oracle.e4m3_encode(v.astype(np.float64))
+    want = _torch_e4m3(v)
+    assert (got == want).all(), np.nonzero(got != want)[0][:10]
+
+
+def test_saturation():
+    got = oracle.e4m3_encode(np.array([449.0, 1e6, -500.0, np.inf, -np.inf]))
+    assert got.tolist() == [0x7E, 0x7E, 0xFE, 0x7E, 0xFE]
+
+
+def test_scale_rule_closed_forms():
+    s = np.array([-10, -1, 0, 3, 20])
+    exact = 448.0 * np.exp2(s)
+    assert (oracle.mx_scale_exponent(exact) == s).all()
+    above = np.nextafter(exact.astype(np.float32), np.float32(np.inf)).astype(np.float64)
+    assert (oracle.mx_scale_exponent(above) == s + 1).all()
+    assert oracle.mx_scale_exponent(np.array([0.0]))[0] == -127
+    assert oracle.mx_scale_exponent(np.array([1e-300]))[0] == -127     # clamped
+    # amax = 1 -> 448 * 2^-8 = 1.75 >= 1 > 0.875: s = -8
+    assert oracle.mx_scale_exponent(np.array([1.0]))[0] == -8
+
+
+def test_quantize_block_layout_and_error_bound():
+    rng = np.random.default_rng(1)
+    v = (rng.standard_normal((3, 96)) * np.array([[1e-4], [1.0], [1e3]])).astype(np.float32).astype(np.float64)
+    v[1, 32:64] = 0.0
+    q, sb = oracle.mx_quantize(v)
+    assert q.shape == (3, 96) and sb.shape == (3, 3)
+    assert sb[1, 1] == 0 and (q[1, 32:64] == 0).all()
+    deq = oracle.mx_dequantize(q, sb)
+    for r in range(3):
+        for b in range(3):
+            blk = v[r, 32 * b:32 * b + 32]
+            amax = np.abs(blk).max()
+            if amax == 0:
+                continue
+            s = int(sb[r, b]) - 127
+            assert 448.0 * 2.0 ** (s - 1) < amax <= 448.0 * 2.0 ** s
+            # nearest rounding: error at most half the spacing at each magnitude (3 mantissa bits)
+            err = np.abs(deq[r, 32 * b:32 * b + 32] - blk)
+            spacing = np.maximum(2.0 ** (np.floor(np.log2(np.maximum(np.abs(blk) / 2.0 ** s, 2.0 ** -6))) - 3), 2.0 ** -9)
+            assert (err <= 0.5 * spacing * 2.0 ** s * (1 + 1e-12)).all()
