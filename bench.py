@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 MoE layer (forward of a DeepSeek-V3-shaped layer by default).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl mok|reference]
+
+One step = one pass of the whole layer forward over one batch of T tokens: router GEMM + top-k,
+pull-schedule counting sort, pull gather, gate/up GEMM + SwiGLU, down GEMM + router weight,
+fixed-order combine (training workloads add the backward).  Inputs are synthetic, seeded, and
+resident in HBM before the timed region; the 22+ GB of expert weights read every step exceed the
+129 MB L2, so no explicit flush is needed.  Prints ONE JSON line on rank 0.
+
+--impl reference times the float64 CPU oracle (as it stands) on the host cores on a bounded
+sample of the same workload, one sampled token per step.
+
+Multi-GPU (torchrun, N > 1): every rank runs an independent replica of the workload on its own
+GPU (the layer has no exchange step on one node here); barrier + max-over-ranks timing only.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(PEAKS_FALLBACK)
+    d["source"] = "fallback"
+    return d
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def dist_max(value, world):
+    """Max of a float over ranks (timing plumbing only, CPU tensors over gloo)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks during the timed region
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ algorithmic work model
+def work_model(shape, counts):
+    """Algorithmic FLOPs and HBM bytes per step for the whole layer and per kernel.
+    counts: tokens per routed expert (for the active-expert weight bytes)."""
+    T, d, E, k, F, Fs, ns = shape.T, shape.d, shape.E, shape.k, shape.F, shape.F_shared, shape.n_shared
+    R = T * k
+    Rs = R + T * ns
+    e_act = sum(1 for c in counts if c > 0)
+    wb = 2  # bf16
+    m = {}
+    m["route"] = {"flops": 2.0 * T * d * E, "bytes": wb * (T * d + d * E) + 8.0 * T * k}
+    # x is read once (repeated rows of a token hit L2), every destination row written once
+    m["gather"] = {"flops": 0.0, "bytes": wb * (T * d + R * d) + 4.0 * R}
+    m["gemm_fwd_gate_up"] = {
+        "flops": 2.0 * (R * 2 * F * d + T * ns * 2 * Fs * d),
+        "bytes": wb * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + Rs * d + R * F + T * ns * Fs)}
+    m["gemm_fwd_down"] = {
+        "flops": 2.0 * (R * F * d + T * ns * Fs * d),
+        "bytes": wb * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + R * F + T * ns * Fs + Rs * d)}
+    m["combine"] = {"flops": 0.0, "bytes": wb * (Rs * d + T * d) + 8.0 * R}
+    layer_flops = T * (2.0 * d * E + (k * 6.0 * d * F) + ns * 6.0 * d * Fs)
+    return m, layer_flops, e_act
+
+
+def roofline_of(name, model, ms_per_launch, peaks):
+    w = model[name]
+    t_flop = w["flops"] / (peaks["bf16_tflops"] * 1e12) if w["flops"] else 0.0
+    t_byte = w["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    secs = ms_per_launch / 1e3
+    if t_flop > t_byte:
+        achieved = w["flops"] / secs / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "algorithmic_per_launch": w["flops"]}
+    achieved = w["bytes"] / secs / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "algorithmic_per_launch": w["bytes"]}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def oracle_sample_inputs(L, shape, tokens):
+    """Host float64 copies of what the oracle needs for `tokens` (untimed set-up)."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    f64 = lambda t: t.detach().to("cpu").to(torch.float64).numpy()  # noqa: E731
+    x = f64(L["x"][tokens])
+    Wr = f64(L["W_router"])
+    b = None if L["bias"] is None else f64(L["bias"])
+    _, _, idx, _ = oracle.route(x, Wr, b, shape.k)
+    experts = sorted(set(int(e) for e in np.asarray(idx).ravel()))
+    Wg = {e: f64(L["W_gate"][e]) for e in experts}
+    Wu = {e: f64(L["W_up"][e]) for e in experts}
+    Wd = {e: f64(L["W_down"][e]) for e in experts}
+    shared = (f64(L["Ws_gate"]), f64(L["Ws_up"]), f64(L["Ws_down"])) if shape.n_shared else None
+    return dict(x=x, Wr=Wr, b=b, Wg=Wg, Wu=Wu, Wd=Wd, shared=shared)
+
+
+def oracle_step(O, shape, rows):
+    """One timed oracle step on sampled token rows: router, pull schedule, experts, combine."""
+    import oracle
+
+    x = O["x"][rows]
+    l64, _, idx, w = oracle.route(x, O["Wr"], O["b"], shape.k)
+    oracle.dispatch(idx, shape.E)
+    return oracle.moe_forward(x, O["Wg"], O["Wu"], O["Wd"], O["shared"], idx, w)
+
+
+def oracle_cores():
+    try:
+        import threadpoolctl
+
+        info = threadpoolctl.threadpool_info()
+        blas = [i.get("num_threads") for i in info if i.get("user_api") == "blas"]
+        if blas:
+            return int(max(blas))
+    except ImportError:
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline(L, shape, pool_tokens=2, budget_s=12.0, max_steps=64):
+    tokens = list(range(pool_tokens))
+    O = oracle_sample_inputs(L, shape, tokens)
+    oracle_step(O, shape, [0])  # warm-up
+    t_total, n = 0.0, 0
+    while t_total < budget_s and n < max_steps:
+        t0 = time.perf_counter()
+        oracle_step(O, shape, [n % pool_tokens])
+        t_total += time.perf_counter() - t0
+        n += 1
+    return {"value": n / t_total, "unit": "tokens/s", "cores": oracle_cores(), "kind": "oracle",
+            "sample": (f"{n} steps of 1 token each, cycling over tokens 0..{pool_tokens - 1} of the "
+                       f"{shape.name} batch (T={shape.T}); per step: float64 router over all "
+                       f"{shape.E} experts, pull schedule, {shape.k} routed SwiGLU experts + the "
+                       f"shared expert, combine; weights converted to float64 once, untimed")}
+
+
+# ------------------------------------------------------------------ the GB300 arm
+def run_mok(args, shape, rank, world, local_rank):
+    import torch
+
+    import mixture_experts_layer_14_gb300 as mok
+    from mixture_experts_layer_14_gb300.synthetic import make_layer
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks = load_peaks()
+    L = make_layer(shape, dev, with_dy=shape.backward)
+    D = mok.dims(shape.T, shape.d, shape.E, shape.k, shape.F, shape.F_shared, shape.n_shared)
+    layer = mok.MoELayer(D, L, dev)
+    x = L["x"]
+    torch.cuda.synchronize()
+
+    def step():
+        y = layer.forward(x, training=shape.backward)
+        n = mok.last_launch_count()
+        n_route = 1
+        if shape.backward:
+            layer.backward(x, L["dY"])
+            n += mok.last_launch_count()
+        return y, n + n_route + 3  # route (1) + dispatch (3) + forward/backward launches
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    counts = layer.routing["counts"].cpu().tolist()
+
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    mok.timing_enable(True)
+    ev0.record(stream)
+    launches = 0
+    for _ in range(args.steps):
+        _, n = step()
+        launches += n
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    mok.timing_enable(False)
+    clocks = sampler.stop()
+    dist_barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    kern = mok.timing_collect()
+    status = mok.read_status(layer.ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    ms_max = dist_max(ms, world)
+
+    model, layer_flops, e_act = work_model(shape, counts)
+    kernels = {}
+    for name, (n, tms) in sorted(kern.items(), key=lambda kv: -kv[1][1]):
+        entry = {"launches": n, "ms_total": round(tms, 4), "ms_per_launch": round(tms / max(n, 1), 5),
+                 "share": round(tms / max(ms, 1e-9), 4)}
+        if name in model:
+            r = roofline_of(name, model, tms / max(n, 1), peaks)
+            entry["roofline"] = {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in r.items()}
+        kernels[name] = entry
+    dominant = max((n for n in kern if n in model), key=lambda n: kern[n][1])
+    dn, dms = kern[dominant]
+    roof = roofline_of(dominant, model, dms / dn, peaks)
+    roof.update({"kernel": dominant, "traffic": None, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
+                 if peaks["source"] == "measured" else "fallback"})
+
+    tokens = world * shape.T * args.steps
+    value = tokens / (ms_max / 1e3)
+    tflops = layer_flops * args.steps / (ms / 1e3) / 1e12
+
+    e2e = None
+    if not args.no_e2e and not shape.backward:
+        e2e = run_e2e(args, mok, D, L, shape, dev, world)
+
+    line = {
+        "metric": "MoE-layer forward tokens/s" if not shape.backward else "MoE-layer fwd+bwd tokens/s",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/sqrt(fan_in)) bf16 weights, random init)",
+        "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E, "k": shape.k,
+                   "F": shape.F, "F_shared": shape.F_shared, "n_shared": shape.n_shared,
+                   "router_bias": shape.bias, "active_experts": e_act,
+                   "global_batch_tokens": world * shape.T, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: every step streams >22 GB of expert weights"},
+        "tflops": round(tflops, 2),
+        "tflops_frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
+        "roofline": {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in roof.items()},
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(L, shape, budget_s=args.cpu_seconds)
+    return line
+
+
+def run_e2e(args, mok, D, L, shape, dev, world):
+    """Same metric through the host-buffer C-ABI call: H2D copy of x from pinned memory, the
+    layer, D2H copy of y, every step."""
+    import torch
+
+    ws = torch.zeros(mok.workspace_size(D) + mok.host_extra_size(D), dtype=torch.uint8, device=dev)
+    xh = L["x"].cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    for _ in range(max(args.warmup, 1)):
+        mok.layer_forward_host(D, L, xh, yh, ws)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        mok.layer_forward_host(D, L, xh, yh, ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist_max(e0.elapsed_time(e1), world)
+    nbytes = shape.T * shape.d * 2
+    return {"value": round(world * shape.T * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
+            "ms_per_step": round(ms / args.steps, 4)}
+
+
+# ------------------------------------------------------------------ the reference arm (oracle)
+def run_reference(args, shape, rank, world, local_rank):
+    import torch
+
+    from mixture_experts_layer_14_gb300.synthetic import make_layer
+
+    dev = torch.device("cuda", local_rank) if torch.cuda.is_available() else torch.device("cpu")
+    if dev.type == "cuda":
+        torch.cuda.set_device(local_rank)
+    L = make_layer(shape, dev)
+    pool = 2
+    O = oracle_sample_inputs(L, shape, list(range(pool)))
+    del L
+    for i in range(args.warmup):
+        oracle_step(O, shape, [i % pool])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_step(O, shape, [i % pool])
+    secs = time.perf_counter() - t0
+    value = args.steps / secs
+    sample = (f"1 token per step cycling over tokens 0..{pool - 1} of the {shape.name} batch "
+              f"(T={shape.T}): float64 router, pull schedule, {shape.k} routed experts + shared, "
+              f"combine; weights converted to float64 once, untimed")
+    return {
+        "metric": "MoE-layer forward tokens/s", "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E, "k": shape.k,
+                   "F": shape.F, "F_shared": shape.F_shared},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": oracle_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    from mixture_experts_layer_14_gb300.synthetic import WORKLOADS
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
+    ap.add_argument("--workload", default="dsv3_bf16_fwd", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_env()
+    shape = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        line = run_reference(args, shape, rank, world, local_rank)
+    else:
+        dist_init(world)
+        line = run_mok(args, shape, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

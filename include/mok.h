@@ -1,0 +1,191 @@
+/*
+ * mok.h — C ABI of the GB300 (sm_103a) DeepSeek-V3-style mixture-of-experts layer.
+ *
+ * The layer (page "Mixture-of-Kittens: Nhân kernel MoE nguồn mở tối ưu cho hệ thống NVL72",
+ * section "Chồng lấp tính toán và truyền tải trong MoE"): a router projection picks the top-k
+ * routed experts of every token and gives each a router weight; every selected expert runs a
+ * SwiGLU FFN (gate and up projections, SiLU(gate) * up, down projection); the output is the
+ * always-on shared expert plus the router-weighted sum of the routed experts:
+ *
+ *     logits = x W_router + b                     (fp32)
+ *     topk   = the k largest logits, ties to the lower expert index
+ *     w_j    = softmax(logits)[e_j] / sum_{i<k} softmax(logits)[e_i]
+ *     y      = FFN_shared(x) + sum_j w_j FFN_{e_j}(x),   FFN(x) = (SiLU(x Wg) * (x Wu)) Wd
+ *
+ * Dispatch follows the pull schedule of the same page, section "Lập lịch" (each expert's
+ * destination rows list its source tokens; one GPU, so the source rank is always 0) and the
+ * pull example of the page "Метод и эксперименты" (tokens ascend inside an expert's region).
+ * Results are bit-identical from run to run (page "Mixture-of-Kittens; MoE megakernel", key
+ * points): every reduction runs in a fixed order and no floating-point atomics are used.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller unless stated otherwise.
+ *    The library never allocates, frees or synchronises (except mok_read_device_status and the
+ *    host-buffer entry point, which say so).  Work is enqueued on `stream` and runs
+ *    asynchronously.
+ *  - Layouts are row-major and dense: x[T,d], W_router[d,E], W_gate/W_up[E,d,F],
+ *    W_down[E,F,d], Ws_gate/Ws_up[d,Fs], Ws_down[Fs,d]; bf16 unless noted.
+ *  - Preconditions (checked on the host; violations return MOK_ERR_UNSUPPORTED or
+ *    MOK_ERR_INVALID_ARG and enqueue nothing): T >= 0; d % 128 == 0; F % 128 == 0;
+ *    Fs % 128 == 0 when n_shared == 1; n_shared in {0,1}; 1 <= k <= 8; k <= E <= 512;
+ *    E % 8 == 0; every pointer 16-byte aligned; workspace at least mok_workspace_size().
+ *  - Device-side failures (a bounded wait that ran out, an out-of-range expert index) are
+ *    recorded as a nonzero status word inside the workspace; nothing traps.  Read it with
+ *    mok_read_device_status().  The word is sticky: clear it with mok_clear_device_status()
+ *    (or allocate the workspace zeroed).
+ *  - Return value: MOK_OK or a negative mok_status.  No entry point exits or aborts.
+ */
+#ifndef MOK_H
+#define MOK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *mok_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  MOK_OK = 0,
+  MOK_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad enum */
+  MOK_ERR_UNSUPPORTED = -2, /* shape or alignment outside the preconditions */
+  MOK_ERR_WORKSPACE = -3,   /* workspace too small */
+  MOK_ERR_CUDA = -4,        /* a CUDA runtime / driver call failed */
+  MOK_ERR_TIMEOUT = -5,     /* (device status) a bounded wait inside a kernel ran out */
+  MOK_ERR_DEVICE_CHECK = -6 /* (device status) an index failed a device-side range check */
+} mok_status;
+
+typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_dtype;
+
+typedef enum { MOK_PASS_FORWARD = 0, MOK_PASS_BACKWARD = 1 } mok_pass;
+
+/* Sizes of one layer call.  T tokens, d model dim, E routed experts, k experts per token,
+ * F routed-expert intermediate, F_shared shared-expert intermediate, n_shared in {0,1},
+ * dtype = arithmetic of the expert GEMMs (MOK_MXFP8: E4M3 values with one UE8M0 scale per
+ * 32 elements along the reduction dimension; the router and combine stay fp32/bf16). */
+typedef struct {
+  int64_t T;
+  int32_t d, E, k, F, F_shared, n_shared;
+  int32_t dtype;
+} mok_dims;
+
+/* Layer weights (device, caller-owned). `prepared` is the output of mok_prepare_weights and is
+ * required when dtype == MOK_MXFP8 (ignored for MOK_BF16). */
+typedef struct {
+  const void *W_router;     /* [d,E] bf16 */
+  const float *router_bias; /* [E] fp32, or NULL */
+  const void *W_gate;       /* [E,d,F] bf16 */
+  const void *W_up;         /* [E,d,F] bf16 */
+  const void *W_down;       /* [E,F,d] bf16 */
+  const void *Ws_gate;      /* [d,Fs] bf16 (NULL when n_shared == 0) */
+  const void *Ws_up;        /* [d,Fs] bf16 */
+  const void *Ws_down;      /* [Fs,d] bf16 */
+  const void *prepared;     /* mok_prepared_size() bytes, or NULL */
+} mok_weights;
+
+/* Bytes of device workspace needed by the entry points of `pass` (MOK_PASS_FORWARD covers
+ * mok_route, mok_dispatch_index and mok_moe_forward; MOK_PASS_BACKWARD covers
+ * mok_moe_backward).  Returns 0 for invalid dims. */
+size_t mok_workspace_size(const mok_dims *dims, int pass);
+
+/* Bytes of the activations mok_moe_forward saves for mok_moe_backward (G and U, bf16, for the
+ * routed rows and the shared expert). */
+size_t mok_saved_size(const mok_dims *dims);
+
+/* Bytes of the prepared-weights buffer for dims->dtype (0 for MOK_BF16). */
+size_t mok_prepared_size(const mok_dims *dims);
+
+/* MXFP8: quantise the routed and shared expert weights once into `prepared` (E4M3 values and
+ * UE8M0 scales, blocks of 32 along each weight's reduction dimension).  No-op for MOK_BF16. */
+int mok_prepare_weights(const mok_dims *dims, const mok_weights *w, void *prepared,
+                        mok_stream_t stream);
+
+/* Router: logits = x W_router + bias in fp32 (bf16 tensor-core products, fp32 accumulation),
+ * top-k by (logit descending, index ascending), weights = softmax over all experts
+ * renormalised over the selected ones.  Page "Mixture-of-Kittens: Nhân kernel MoE ...",
+ * section "Chồng lấp tính toán và truyền tải trong MoE".
+ *   x[T,d] bf16, W_router[d,E] bf16, bias[E] fp32 or NULL
+ *   -> topk_idx[T,k] int32 (slot order = descending logit), topk_w[T,k] fp32,
+ *      logits[T,E] fp32 (optional, NULL to skip). */
+int mok_route(const mok_dims *dims, const void *x, const void *W_router, const float *bias,
+              int32_t *topk_idx, float *topk_w, float *logits, void *ws, size_t ws_bytes,
+              mok_stream_t stream);
+
+/* Pull schedule (page "Mixture-of-Kittens: Nhân kernel MoE ...", section "Lập lịch"): a
+ * deterministic counting sort of the T*k routes by expert, built from per-chunk histograms and
+ * a prefix scan, with no atomics.  Within an expert, routes are ordered by token id.
+ *   topk_idx[T,k] int32 (each value in [0,E)), topk_w[T,k] fp32
+ *   -> counts[E], offsets[E+1] (offsets[0]=0, offsets[E]=T*k), sorted_tok[T*k] (token of each
+ *      destination row), sorted_w[T*k] (its router weight), inv_pos[T,k] (destination row of
+ *      route (t,j)).  An index outside [0,E) sets MOK_ERR_DEVICE_CHECK in the status word and
+ *      that route is dropped. */
+int mok_dispatch_index(const mok_dims *dims, const int32_t *topk_idx, const float *topk_w,
+                       int32_t *counts, int32_t *offsets, int32_t *sorted_tok, float *sorted_w,
+                       int32_t *inv_pos, void *ws, size_t ws_bytes, mok_stream_t stream);
+
+/* Forward of the expert part given a routing (the output of mok_dispatch_index):
+ * pull-gathers each expert's rows, runs the gate/up GEMM with SiLU(gate)*up fused in its
+ * epilogue and the down GEMM with the router weight fused in its epilogue (routed experts and
+ * the shared expert in one persistent launch per phase), then combines every token's rows in
+ * ascending expert order on top of the shared-expert row (fp32 accumulation, one bf16
+ * rounding).
+ *   -> y[T,d] bf16.  `saved` (mok_saved_size bytes or NULL) receives G and U for backward. */
+int mok_moe_forward(const mok_dims *dims, const mok_weights *w, const void *x,
+                    const int32_t *topk_idx, const int32_t *offsets, const int32_t *sorted_tok,
+                    const float *sorted_w, const int32_t *inv_pos, void *y, void *saved,
+                    void *ws, size_t ws_bytes, mok_stream_t stream);
+
+/* Backward of the layer for upstream gradient dY[T,d] bf16, with the top-k selection held
+ * constant (unselected experts get no gradient).  Uses `saved` from mok_moe_forward with the
+ * same routing.  Outputs (bf16 unless noted; fp32 accumulation, fixed summation order):
+ *   dX[T,d] (including the router path dlogits W_router^T), dW_gate/dW_up[E,d,F],
+ *   dW_down[E,F,d] (experts with no token get zeros), dWs_gate/dWs_up[d,Fs], dWs_down[Fs,d]
+ *   (NULL when n_shared == 0), dlogits[T,E] fp32 (zero off the selection),
+ *   dW_router[d,E] (NULL to skip). */
+int mok_moe_backward(const mok_dims *dims, const mok_weights *w, const void *x, const void *dY,
+                     const void *saved, const int32_t *topk_idx, const float *topk_w,
+                     const int32_t *offsets, const int32_t *sorted_tok, const float *sorted_w,
+                     const int32_t *inv_pos, void *dX, void *dW_gate, void *dW_up, void *dW_down,
+                     void *dWs_gate, void *dWs_up, void *dWs_down, float *dlogits,
+                     void *dW_router, void *ws, size_t ws_bytes, mok_stream_t stream);
+
+/* The whole layer forward (route, dispatch, expert forward) with x and y in HOST memory:
+ * copies x_host[T,d] (bf16) to the workspace, runs the layer and copies y back to
+ * y_host[T,d].  Pinned host memory makes the copies asynchronous; the call returns without
+ * waiting (synchronise the stream before reading y_host).  Routing tensors live inside the
+ * workspace (mok_workspace_size(dims, MOK_PASS_FORWARD) + mok_layer_host_extra_size(dims)). */
+size_t mok_layer_host_extra_size(const mok_dims *dims);
+int mok_layer_forward_host(const mok_dims *dims, const mok_weights *w, const void *x_host,
+                           void *y_host, void *ws, size_t ws_bytes, mok_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *mok_status_string(int status);
+
+/* Synchronises `stream`, copies the device status word of `ws` into *status_out (MOK_OK or a
+ * negative code).  The one entry point that waits on the GPU. */
+int mok_read_device_status(const void *ws, int *status_out, mok_stream_t stream);
+
+/* Enqueues a reset of the device status word of `ws` to MOK_OK. */
+int mok_clear_device_status(void *ws, mok_stream_t stream);
+
+/* Number of kernel launches the last successful call of each entry point enqueued on this
+ * host thread (for launch accounting in benchmarks). */
+int mok_last_launch_count(void);
+
+/* Kernel timing for benchmarks.  While enabled on the calling host thread, every entry point
+ * records a CUDA event pair around each kernel it launches, on the launch stream (the events do
+ * not change what the GPU executes).  enable = 0 stops recording. */
+int mok_timing_enable(int enable);
+
+/* Waits for the recorded events, then returns per kernel name (up to max_kernels entries,
+ * `names` holds max_kernels * 32 bytes, NUL-terminated) the number of launches and their summed
+ * device time in milliseconds; *n_out = entries written.  Clears the record. */
+int mok_timing_collect(char *names, int *launches, double *ms, int max_kernels, int *n_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOK_H */

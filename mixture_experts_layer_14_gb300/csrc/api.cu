@@ -1,0 +1,634 @@
+// C-ABI entry points of libmok: argument checks, workspace layout, TMA tensor maps and the
+// launch sequence of each call.  Host code only; every step of the layer runs in the kernels
+// of route.cu, dispatch.cu, elementwise.cu and moe_gemm.cu.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "mok_internal.h"
+
+namespace mok {
+
+static thread_local int g_last_launches = 0;
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+// ------------------------------------------------------------------ tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor of `rank` dims (innermost first), 128-byte swizzle, zero fill out of bounds.
+static bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims,
+                  strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+// 2D row-major [rows, cols] bf16, box {bc, br}
+static bool map2d(CUtensorMap* m, const void* p, uint64_t rows, uint64_t cols, uint32_t bc,
+                  uint32_t br) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t str[1] = {cols * 2};
+  const uint32_t box[2] = {bc, br};
+  return make_map(m, p, 2, dims, str, box);
+}
+// 3D row-major [n, rows, cols] bf16, box {bc, br, 1}
+static bool map3d(CUtensorMap* m, const void* p, uint64_t n, uint64_t rows, uint64_t cols,
+                  uint32_t bc, uint32_t br) {
+  const uint64_t dims[3] = {cols, rows, n};
+  const uint64_t str[2] = {cols * 2, rows * cols * 2};
+  const uint32_t box[3] = {bc, br, 1};
+  return make_map(m, p, 3, dims, str, box);
+}
+
+// ------------------------------------------------------------------ checks and layouts
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_dims(const mok_dims* d) {
+  if (!d) return MOK_ERR_INVALID_ARG;
+  if (d->T < 0 || d->T > 0x7fffffffLL / 8) return MOK_ERR_UNSUPPORTED;
+  if (d->d <= 0 || d->d % 128) return MOK_ERR_UNSUPPORTED;
+  if (d->F <= 0 || d->F % 128) return MOK_ERR_UNSUPPORTED;
+  if (d->n_shared != 0 && d->n_shared != 1) return MOK_ERR_UNSUPPORTED;
+  if (d->n_shared == 1 && (d->F_shared <= 0 || d->F_shared % 128)) return MOK_ERR_UNSUPPORTED;
+  if (d->k < 1 || d->k > kMaxK || d->E < d->k || d->E > kMaxE || d->E % 8) return MOK_ERR_UNSUPPORTED;
+  if (d->dtype != MOK_BF16 && d->dtype != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
+  if (d->dtype == MOK_MXFP8) return MOK_ERR_UNSUPPORTED;
+  return MOK_OK;
+}
+
+struct Layout {
+  size_t off[32];
+  size_t total;
+};
+static size_t al(size_t x) { return (x + 1023) & ~size_t(1023); }
+
+enum FwdSlot { FW_STATUS, FW_HIST, FW_XS, FW_H, FW_HSH, FW_YS, FW_YSH, FW_N };
+enum BwdSlot {
+  BW_STATUS, BW_XS, BW_DYS, BW_DG, BW_DU, BW_HW, BW_DGSH, BW_DUSH, BW_HWSH, BW_P, BW_DL,
+  BW_DXS, BW_DXSH, BW_N
+};
+enum SavedSlot { SV_G, SV_U, SV_GSH, SV_USH, SV_N };
+enum HostSlot { HS_X, HS_Y, HS_IDX, HS_W, HS_CNT, HS_OFF, HS_STOK, HS_SW, HS_INV, HS_N };
+
+static int bn_for(int a, int b, int c) { return (a % 256 == 0 && b % 256 == 0 && c % 256 == 0) ? 256 : 128; }
+
+static Layout layout_fwd(const mok_dims* d) {
+  const int64_t T = d->T, R = T * d->k;
+  const int Fs = d->n_shared ? d->F_shared : 0;
+  const int64_t nblk = (T + kDispatchChunk - 1) / kDispatchChunk;
+  size_t sz[FW_N] = {};
+  sz[FW_STATUS] = 256;
+  sz[FW_HIST] = sizeof(int32_t) * d->E * std::max<int64_t>(nblk, 1);
+  sz[FW_XS] = 2ull * R * d->d;
+  sz[FW_H] = 2ull * R * d->F;
+  sz[FW_HSH] = 2ull * T * Fs;
+  sz[FW_YS] = 2ull * R * d->d;
+  sz[FW_YSH] = 2ull * T * d->d * d->n_shared;
+  Layout L{};
+  size_t o = 0;
+  for (int i = 0; i < FW_N; ++i) { L.off[i] = o; o += al(sz[i]); }
+  L.total = o;
+  return L;
+}
+
+static int bwd_bn_da(const mok_dims* d) { return bn_for(d->F, d->n_shared ? d->F_shared : 256, 256); }
+
+static Layout layout_bwd(const mok_dims* d) {
+  const int64_t T = d->T, R = T * d->k;
+  const int Fs = d->n_shared ? d->F_shared : 0;
+  const int ldl = (d->E + 63) & ~63;
+  const int ntda = d->F / bwd_bn_da(d);
+  size_t sz[BW_N] = {};
+  sz[BW_STATUS] = 256;
+  sz[BW_XS] = 2ull * R * d->d;
+  sz[BW_DYS] = 2ull * R * d->d;
+  sz[BW_DG] = sz[BW_DU] = sz[BW_HW] = 2ull * R * d->F;
+  sz[BW_DGSH] = sz[BW_DUSH] = sz[BW_HWSH] = 2ull * T * Fs;
+  sz[BW_P] = 4ull * R * ntda;
+  sz[BW_DL] = 2ull * T * ldl;
+  sz[BW_DXS] = 2ull * R * d->d;
+  sz[BW_DXSH] = 2ull * T * d->d;
+  Layout L{};
+  size_t o = 0;
+  for (int i = 0; i < BW_N; ++i) { L.off[i] = o; o += al(sz[i]); }
+  L.total = o;
+  return L;
+}
+
+static Layout layout_saved(const mok_dims* d) {
+  const int64_t T = d->T, R = T * d->k;
+  const int Fs = d->n_shared ? d->F_shared : 0;
+  size_t sz[SV_N] = {2ull * R * d->F, 2ull * R * d->F, 2ull * T * Fs, 2ull * T * Fs};
+  Layout L{};
+  size_t o = 0;
+  for (int i = 0; i < SV_N; ++i) { L.off[i] = o; o += al(sz[i]); }
+  L.total = o;
+  return L;
+}
+
+static Layout layout_host(const mok_dims* d) {
+  const int64_t T = d->T, R = T * d->k;
+  size_t sz[HS_N] = {2ull * T * d->d, 2ull * T * d->d, 4ull * R, 4ull * R, 4ull * d->E,
+                     4ull * (d->E + 1), 4ull * R, 4ull * R, 4ull * R};
+  Layout L{};
+  size_t o = 0;
+  for (int i = 0; i < HS_N; ++i) { L.off[i] = o; o += al(sz[i]); }
+  L.total = o;
+  return L;
+}
+
+template <class P>
+static P at(void* base, size_t off) {
+  return reinterpret_cast<P>(static_cast<char*>(base) + off);
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA; }
+
+}  // namespace mok
+
+using namespace mok;
+
+extern "C" {
+
+size_t mok_workspace_size(const mok_dims* dims, int pass) {
+  if (check_dims(dims) != MOK_OK) return 0;
+  if (pass == MOK_PASS_FORWARD) return layout_fwd(dims).total;
+  if (pass == MOK_PASS_BACKWARD) return layout_bwd(dims).total;
+  return 0;
+}
+
+size_t mok_saved_size(const mok_dims* dims) {
+  if (check_dims(dims) != MOK_OK) return 0;
+  return layout_saved(dims).total;
+}
+
+size_t mok_prepared_size(const mok_dims* dims) {
+  if (check_dims(dims) != MOK_OK) return 0;
+  return 0;
+}
+
+size_t mok_layer_host_extra_size(const mok_dims* dims) {
+  if (check_dims(dims) != MOK_OK) return 0;
+  return layout_host(dims).total;
+}
+
+int mok_prepare_weights(const mok_dims* dims, const mok_weights* w, void* prepared,
+                        mok_stream_t stream) {
+  (void)prepared;
+  (void)stream;
+  int rc = check_dims(dims);
+  if (rc != MOK_OK) return rc;
+  if (!w) return MOK_ERR_INVALID_ARG;
+  g_last_launches = 0;
+  return MOK_OK;
+}
+
+const char* mok_status_string(int s) {
+  switch (s) {
+    case MOK_OK: return "MOK_OK";
+    case MOK_ERR_INVALID_ARG: return "MOK_ERR_INVALID_ARG: null pointer, negative size or bad enum";
+    case MOK_ERR_UNSUPPORTED: return "MOK_ERR_UNSUPPORTED: shape or alignment outside the preconditions";
+    case MOK_ERR_WORKSPACE: return "MOK_ERR_WORKSPACE: workspace too small";
+    case MOK_ERR_CUDA: return "MOK_ERR_CUDA: a CUDA call failed";
+    case MOK_ERR_TIMEOUT: return "MOK_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+    case MOK_ERR_DEVICE_CHECK: return "MOK_ERR_DEVICE_CHECK: an index failed a device-side range check";
+    default: return "unknown mok status";
+  }
+}
+
+int mok_read_device_status(const void* ws, int* status_out, mok_stream_t stream) {
+  if (!ws || !status_out) return MOK_ERR_INVALID_ARG;
+  int v = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return MOK_ERR_CUDA;
+  *status_out = v;
+  return MOK_OK;
+}
+
+int mok_clear_device_status(void* ws, mok_stream_t stream) {
+  if (!ws) return MOK_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mok_last_launch_count(void) { return g_last_launches; }
+
+int mok_route(const mok_dims* dims, const void* x, const void* W_router, const float* bias,
+              int32_t* topk_idx, float* topk_w, float* logits, void* ws, size_t ws_bytes,
+              mok_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != MOK_OK) return rc;
+  if (!ws || (dims->T > 0 && (!x || !W_router || !topk_idx || !topk_w))) return MOK_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_router) || !aligned16(ws)) return MOK_ERR_UNSUPPORTED;
+  if (ws_bytes < layout_fwd(dims).total) return MOK_ERR_WORKSPACE;
+  g_last_launches = 0;
+  if (dims->T == 0) return MOK_OK;
+  RouteParams p{};
+  if (!map2d(&p.map_x, x, dims->T, dims->d, 64, 128)) return MOK_ERR_CUDA;
+  if (!map2d(&p.map_w, W_router, dims->d, dims->E, 64, 64)) return MOK_ERR_CUDA;
+  p.bias = bias;
+  p.topk_idx = topk_idx;
+  p.topk_w = topk_w;
+  p.logits = logits;
+  p.T = (int)dims->T;
+  p.d = dims->d;
+  p.E = dims->E;
+  p.k = dims->k;
+  p.status = static_cast<int*>(ws);
+  rc = cuda_status(launch_route(p, reinterpret_cast<cudaStream_t>(stream)));
+  if (rc == MOK_OK) g_last_launches = 1;
+  return rc;
+}
+
+int mok_dispatch_index(const mok_dims* dims, const int32_t* topk_idx, const float* topk_w,
+                       int32_t* counts, int32_t* offsets, int32_t* sorted_tok, float* sorted_w,
+                       int32_t* inv_pos, void* ws, size_t ws_bytes, mok_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != MOK_OK) return rc;
+  if (!ws || !counts || !offsets || (dims->T > 0 && (!topk_idx || !topk_w || !sorted_tok || !sorted_w || !inv_pos)))
+    return MOK_ERR_INVALID_ARG;
+  if (ws_bytes < layout_fwd(dims).total) return MOK_ERR_WORKSPACE;
+  g_last_launches = 0;
+  const Layout L = layout_fwd(dims);
+  int n = 0;
+  rc = cuda_status(launch_dispatch(dims->T, dims->E, dims->k, topk_idx, topk_w, counts, offsets,
+                                   sorted_tok, sorted_w, inv_pos, at<int32_t*>(ws, L.off[FW_HIST]),
+                                   static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream), &n));
+  if (rc == MOK_OK) g_last_launches = n;
+  return rc;
+}
+
+int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
+                    const int32_t* topk_idx, const int32_t* offsets, const int32_t* sorted_tok,
+                    const float* sorted_w, const int32_t* inv_pos, void* y, void* saved, void* ws,
+                    size_t ws_bytes, mok_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != MOK_OK) return rc;
+  if (!w || !ws) return MOK_ERR_INVALID_ARG;
+  if (dims->T == 0) {
+    g_last_launches = 0;
+    return ws_bytes < layout_fwd(dims).total ? MOK_ERR_WORKSPACE : MOK_OK;
+  }
+  if (!y || !x || !topk_idx || !offsets || !sorted_tok || !sorted_w || !inv_pos)
+    return MOK_ERR_INVALID_ARG;
+  if (!w->W_gate || !w->W_up || !w->W_down) return MOK_ERR_INVALID_ARG;
+  if (dims->n_shared && (!w->Ws_gate || !w->Ws_up || !w->Ws_down)) return MOK_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, y, saved, ws, w->W_gate, w->W_up, w->W_down, w->Ws_gate, w->Ws_up, w->Ws_down};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return MOK_ERR_UNSUPPORTED;
+  const Layout L = layout_fwd(dims);
+  if (ws_bytes < L.total) return MOK_ERR_WORKSPACE;
+  g_last_launches = 0;
+  if (dims->T == 0) return MOK_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t T = dims->T, R = T * dims->k;
+  const int d = dims->d, E = dims->E, F = dims->F, Fs = dims->n_shared ? dims->F_shared : 0;
+  const bool sh = dims->n_shared == 1;
+  void* xs = at<void*>(ws, L.off[FW_XS]);
+  void* h = at<void*>(ws, L.off[FW_H]);
+  void* hsh = at<void*>(ws, L.off[FW_HSH]);
+  void* Ys = at<void*>(ws, L.off[FW_YS]);
+  void* Ysh = at<void*>(ws, L.off[FW_YSH]);
+  const Layout S = layout_saved(dims);
+  int launches = 0;
+
+  // 1. pull-gather of every expert's token rows
+  rc = cuda_status(launch_gather_rows(x, sorted_tok, R, d, xs, s));
+  if (rc != MOK_OK) return rc;
+  ++launches;
+
+  const int grid_cap = num_sms();
+  // 2. gate/up GEMM with SiLU(gate)*up fused in the epilogue
+  {
+    GemmParams p{};
+    bool ok = true;
+    if (sh) {
+      ok &= map2d(&p.maps[MS_A0], x, T, d, 64, 128);
+      ok &= map3d(&p.maps[MS_B0], w->Ws_gate, 1, d, Fs, 64, 64);
+      ok &= map3d(&p.maps[MS_B1], w->Ws_up, 1, d, Fs, 64, 64);
+    }
+    ok &= map2d(&p.maps[MS_A3], xs, R, d, 64, 128);
+    ok &= map3d(&p.maps[MS_B3], w->W_gate, E, d, F, 64, 64);
+    ok &= map3d(&p.maps[MS_B4], w->W_up, E, d, F, 64, 64);
+    if (!ok) return MOK_ERR_CUDA;
+    p.offsets = offsets;
+    p.E = E;
+    p.has_shared = sh;
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.nt[0] = Fs / 128;
+    p.nt[1] = F / 128;
+    p.out0[0] = hsh;
+    p.out0[1] = h;
+    if (saved) {
+      p.out1[0] = at<void*>(saved, S.off[SV_GSH]);
+      p.out2[0] = at<void*>(saved, S.off[SV_USH]);
+      p.out1[1] = at<void*>(saved, S.off[SV_G]);
+      p.out2[1] = at<void*>(saved, S.off[SV_U]);
+    }
+    p.status = static_cast<int*>(ws);
+    const int64_t bound = (sh ? (T + BM - 1) / BM * p.nt[0] : 0) + ((R + BM - 1) / BM + E) * p.nt[1];
+    const int grid = (int)std::min<int64_t>(grid_cap, bound);
+    rc = cuda_status(launch_gemm(G_FWD_GU, 256, p, grid, s));
+    if (rc != MOK_OK) return rc;
+    ++launches;
+  }
+  // 3. down GEMM with the router weight fused in the epilogue
+  {
+    const int bn = bn_for(d, 256, 256);
+    GemmParams p{};
+    bool ok = true;
+    if (sh) {
+      ok &= map2d(&p.maps[MS_A0], hsh, T, Fs, 64, 128);
+      ok &= map3d(&p.maps[MS_B0], w->Ws_down, 1, Fs, d, 64, 64);
+    }
+    ok &= map2d(&p.maps[MS_A3], h, R, F, 64, 128);
+    ok &= map3d(&p.maps[MS_B3], w->W_down, E, F, d, 64, 64);
+    if (!ok) return MOK_ERR_CUDA;
+    p.offsets = offsets;
+    p.E = E;
+    p.has_shared = sh;
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.nt[0] = d / bn;
+    p.nt[1] = d / bn;
+    p.out0[0] = Ysh;
+    p.out0[1] = Ys;
+    p.row_w = sorted_w;
+    p.status = static_cast<int*>(ws);
+    const int64_t bound = (sh ? (T + BM - 1) / BM * p.nt[0] : 0) + ((R + BM - 1) / BM + E) * p.nt[1];
+    const int grid = (int)std::min<int64_t>(grid_cap, bound);
+    rc = cuda_status(launch_gemm(G_FWD_DOWN, bn, p, grid, s));
+    if (rc != MOK_OK) return rc;
+    ++launches;
+  }
+  // 4. fixed-order combine
+  rc = cuda_status(launch_combine(T, d, dims->k, topk_idx, inv_pos, Ys, sh ? Ysh : nullptr, y, s));
+  if (rc != MOK_OK) return rc;
+  ++launches;
+  g_last_launches = launches;
+  return MOK_OK;
+}
+
+int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, const void* dY,
+                     const void* saved, const int32_t* topk_idx, const float* topk_w,
+                     const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
+                     const int32_t* inv_pos, void* dX, void* dW_gate, void* dW_up, void* dW_down,
+                     void* dWs_gate, void* dWs_up, void* dWs_down, float* dlogits,
+                     void* dW_router, void* ws, size_t ws_bytes, mok_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != MOK_OK) return rc;
+  if (!w || !ws || !dW_gate || !dW_up || !dW_down) return MOK_ERR_INVALID_ARG;
+  if (dims->T > 0 && (!x || !dY || !saved || !topk_idx || !topk_w || !offsets || !sorted_tok ||
+                      !sorted_w || !inv_pos || !dX || !dlogits))
+    return MOK_ERR_INVALID_ARG;
+  if (!w->W_router || !w->W_gate || !w->W_up || !w->W_down) return MOK_ERR_INVALID_ARG;
+  const bool sh = dims->n_shared == 1;
+  if (sh && (!w->Ws_gate || !w->Ws_up || !w->Ws_down || !dWs_gate || !dWs_up || !dWs_down))
+    return MOK_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, dY, saved, ws, dX, dW_gate, dW_up, dW_down, dWs_gate, dWs_up, dWs_down,
+                        dW_router, w->W_router, w->W_gate, w->W_up, w->W_down, w->Ws_gate, w->Ws_up,
+                        w->Ws_down};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return MOK_ERR_UNSUPPORTED;
+  const Layout L = layout_bwd(dims);
+  if (ws_bytes < L.total) return MOK_ERR_WORKSPACE;
+  g_last_launches = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t T = dims->T, R = T * dims->k;
+  const int d = dims->d, E = dims->E, F = dims->F, Fs = sh ? dims->F_shared : 0;
+  int launches = 0;
+  if (T == 0) {
+    // no tokens: every weight gradient is zero
+    rc = cuda_status(cudaMemsetAsync(dW_gate, 0, 2ull * E * d * F, s));
+    if (rc == MOK_OK) rc = cuda_status(cudaMemsetAsync(dW_up, 0, 2ull * E * d * F, s));
+    if (rc == MOK_OK) rc = cuda_status(cudaMemsetAsync(dW_down, 0, 2ull * E * d * F, s));
+    if (rc == MOK_OK && sh) rc = cuda_status(cudaMemsetAsync(dWs_gate, 0, 2ull * d * Fs, s));
+    if (rc == MOK_OK && sh) rc = cuda_status(cudaMemsetAsync(dWs_up, 0, 2ull * d * Fs, s));
+    if (rc == MOK_OK && sh) rc = cuda_status(cudaMemsetAsync(dWs_down, 0, 2ull * d * Fs, s));
+    if (rc == MOK_OK && dW_router) rc = cuda_status(cudaMemsetAsync(dW_router, 0, 2ull * d * E, s));
+    return rc;
+  }
+  const Layout S = layout_saved(dims);
+  void* xs = at<void*>(ws, L.off[BW_XS]);
+  void* dys = at<void*>(ws, L.off[BW_DYS]);
+  void* dG = at<void*>(ws, L.off[BW_DG]);
+  void* dU = at<void*>(ws, L.off[BW_DU]);
+  void* hw = at<void*>(ws, L.off[BW_HW]);
+  void* dGsh = at<void*>(ws, L.off[BW_DGSH]);
+  void* dUsh = at<void*>(ws, L.off[BW_DUSH]);
+  void* hwsh = at<void*>(ws, L.off[BW_HWSH]);
+  float* P = at<float*>(ws, L.off[BW_P]);
+  void* dl = at<void*>(ws, L.off[BW_DL]);
+  void* dXs = at<void*>(ws, L.off[BW_DXS]);
+  void* dXsh = at<void*>(ws, L.off[BW_DXSH]);
+  const int ldl = (E + 63) & ~63;
+  const int grid_cap = num_sms();
+
+  // 1. gather x and dY rows into each expert's region
+  rc = cuda_status(launch_gather_rows2(x, dY, sorted_tok, R, d, xs, dys, s));
+  if (rc != MOK_OK) return rc;
+  ++launches;
+  // 2. a = dY W_down^T; epilogue: dG, dU, w*h and the router partials <a, h>
+  const int bn_da = bwd_bn_da(dims);
+  {
+    GemmParams p{};
+    bool ok = true;
+    if (sh) {
+      ok &= map2d(&p.maps[MS_A0], dY, T, d, 64, 128);
+      ok &= map3d(&p.maps[MS_B0], w->Ws_down, 1, Fs, d, 64, bn_da);
+    }
+    ok &= map2d(&p.maps[MS_A3], dys, R, d, 64, 128);
+    ok &= map3d(&p.maps[MS_B3], w->W_down, E, F, d, 64, bn_da);
+    if (!ok) return MOK_ERR_CUDA;
+    p.offsets = offsets;
+    p.E = E;
+    p.has_shared = sh;
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.nt[0] = Fs / bn_da;
+    p.nt[1] = F / bn_da;
+    p.in0[0] = at<void*>(const_cast<void*>(saved), S.off[SV_GSH]);
+    p.in1[0] = at<void*>(const_cast<void*>(saved), S.off[SV_USH]);
+    p.in0[1] = at<void*>(const_cast<void*>(saved), S.off[SV_G]);
+    p.in1[1] = at<void*>(const_cast<void*>(saved), S.off[SV_U]);
+    p.out0[0] = dGsh; p.out1[0] = dUsh; p.out2[0] = hwsh;
+    p.out0[1] = dG; p.out1[1] = dU; p.out2[1] = hw;
+    p.row_w = sorted_w;
+    p.partial = P;
+    p.status = static_cast<int*>(ws);
+    const int64_t bound = (sh ? (T + BM - 1) / BM * p.nt[0] : 0) + ((R + BM - 1) / BM + E) * p.nt[1];
+    rc = cuda_status(launch_gemm(G_BWD_DA, bn_da, p, (int)std::min<int64_t>(grid_cap, bound), s));
+    if (rc != MOK_OK) return rc;
+    ++launches;
+  }
+  // 3. router backward: dw, dlogits, bf16 copy of dlogits
+  rc = cuda_status(launch_router_backward(T, E, dims->k, F / bn_da, topk_idx, topk_w, inv_pos, P,
+                                          dlogits, dl, s));
+  if (rc != MOK_OK) return rc;
+  ++launches;
+  // 4. dX_s = dG W_gate^T + dU W_up^T; shared rows also take dl W_router^T
+  {
+    const int bn = bn_for(d, 256, 256);
+    GemmParams p{};
+    bool ok = true;
+    int g0 = 0;
+    if (sh) {
+      ok &= map2d(&p.maps[MS_A0], dGsh, T, Fs, 64, 128);
+      ok &= map3d(&p.maps[MS_B0], w->Ws_gate, 1, d, Fs, 64, bn);
+      ok &= map2d(&p.maps[MS_A1], dUsh, T, Fs, 64, 128);
+      ok &= map3d(&p.maps[MS_B1], w->Ws_up, 1, d, Fs, 64, bn);
+      p.segkb[0][0] = Fs / BK;
+      p.segkb[0][1] = Fs / BK;
+      g0 = 2;
+    }
+    ok &= map2d(&p.maps[MS_A0 + g0], dl, T, ldl, 64, 128);
+    ok &= map3d(&p.maps[MS_B0 + g0], w->W_router, 1, d, E, 64, bn);
+    p.segkb[0][g0] = ldl / BK;
+    ok &= map2d(&p.maps[MS_A3], dG, R, F, 64, 128);
+    ok &= map3d(&p.maps[MS_B3], w->W_gate, E, d, F, 64, bn);
+    ok &= map2d(&p.maps[MS_A4], dU, R, F, 64, 128);
+    ok &= map3d(&p.maps[MS_B4], w->W_up, E, d, F, 64, bn);
+    p.segkb[1][0] = F / BK;
+    p.segkb[1][1] = F / BK;
+    if (!ok) return MOK_ERR_CUDA;
+    p.offsets = offsets;
+    p.E = E;
+    p.has_shared = 1;  // group 0 (shared expert and/or router term) always present
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.nt[0] = d / bn;
+    p.nt[1] = d / bn;
+    p.out0[0] = dXsh;
+    p.out0[1] = dXs;
+    p.status = static_cast<int*>(ws);
+    const int64_t bound = (T + BM - 1) / BM * p.nt[0] + ((R + BM - 1) / BM + E) * p.nt[1];
+    rc = cuda_status(launch_gemm(G_BWD_DX, bn, p, (int)std::min<int64_t>(grid_cap, bound), s));
+    if (rc != MOK_OK) return rc;
+    ++launches;
+  }
+  // 5. weight gradients (K = tokens of each expert, in token order) and x^T dl
+  {
+    const int bn = bn_for(d, F, sh ? Fs : 256);
+    GemmParams p{};
+    bool ok = true;
+    if (sh) {
+      ok &= map2d(&p.maps[MS_A0], x, T, d, 64, 64);
+      ok &= map2d(&p.maps[MS_A1], hwsh, T, Fs, 64, 64);
+      ok &= map2d(&p.maps[MS_B0], dGsh, T, Fs, 64, 64);
+      ok &= map2d(&p.maps[MS_B1], dUsh, T, Fs, 64, 64);
+      ok &= map2d(&p.maps[MS_B2], dY, T, d, 64, 64);
+    }
+    ok &= map2d(&p.maps[MS_A3], xs, R, d, 64, 64);
+    ok &= map2d(&p.maps[MS_A4], hw, R, F, 64, 64);
+    ok &= map2d(&p.maps[MS_B3], dG, R, F, 64, 64);
+    ok &= map2d(&p.maps[MS_B4], dU, R, F, 64, 64);
+    ok &= map2d(&p.maps[MS_B5], dys, R, d, 64, 64);
+    if (dW_router) {
+      ok &= map2d(&p.maps[MS_R_A], x, T, d, 64, 64);
+      ok &= map2d(&p.maps[MS_R_B], dl, T, ldl, 64, 64);
+      p.router_tiles = (d / BM) * ((E + bn - 1) / bn);
+      p.E_cols = E;
+      p.out_router = dW_router;
+    }
+    if (!ok) return MOK_ERR_CUDA;
+    p.offsets = offsets;
+    p.E = E;
+    p.has_shared = sh;
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.out0[0] = dWs_gate; p.out1[0] = dWs_up; p.out2[0] = dWs_down;
+    p.out0[1] = dW_gate; p.out1[1] = dW_up; p.out2[1] = dW_down;
+    p.status = static_cast<int*>(ws);
+    const int64_t total = p.router_tiles +
+                          (sh ? 2 * (d / BM) * (Fs / bn) + (Fs / BM) * (d / bn) : 0) +
+                          (int64_t)E * (2 * (d / BM) * (F / bn) + (F / BM) * (d / bn));
+    rc = cuda_status(launch_gemm(G_BWD_DW, bn, p, (int)std::min<int64_t>(grid_cap, total), s));
+    if (rc != MOK_OK) return rc;
+    ++launches;
+  }
+  // 6. dX = dX_shared (+ router term) + routed rows in ascending expert order
+  rc = cuda_status(launch_combine(T, d, dims->k, topk_idx, inv_pos, dXs, dXsh, dX, s));
+  if (rc != MOK_OK) return rc;
+  ++launches;
+  g_last_launches = launches;
+  return MOK_OK;
+}
+
+int mok_layer_forward_host(const mok_dims* dims, const mok_weights* w, const void* x_host,
+                           void* y_host, void* ws, size_t ws_bytes, mok_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != MOK_OK) return rc;
+  if (!w || !ws || !x_host || !y_host) return MOK_ERR_INVALID_ARG;
+  const size_t fw = layout_fwd(dims).total;
+  const Layout H = layout_host(dims);
+  if (ws_bytes < fw + H.total) return MOK_ERR_WORKSPACE;
+  if (dims->T == 0) return MOK_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ext = static_cast<char*>(ws) + fw;
+  void* x = ext + H.off[HS_X];
+  void* y = ext + H.off[HS_Y];
+  int32_t* idx = reinterpret_cast<int32_t*>(ext + H.off[HS_IDX]);
+  float* tw = reinterpret_cast<float*>(ext + H.off[HS_W]);
+  int32_t* cnt = reinterpret_cast<int32_t*>(ext + H.off[HS_CNT]);
+  int32_t* off = reinterpret_cast<int32_t*>(ext + H.off[HS_OFF]);
+  int32_t* stok = reinterpret_cast<int32_t*>(ext + H.off[HS_STOK]);
+  float* sw = reinterpret_cast<float*>(ext + H.off[HS_SW]);
+  int32_t* inv = reinterpret_cast<int32_t*>(ext + H.off[HS_INV]);
+  const size_t xbytes = 2ull * dims->T * dims->d;
+  if (cudaMemcpyAsync(x, x_host, xbytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOK_ERR_CUDA;
+  int total = 0;
+  rc = mok_route(dims, x, w->W_router, w->router_bias, idx, tw, nullptr, ws, fw, stream);
+  if (rc != MOK_OK) return rc;
+  total += g_last_launches;
+  rc = mok_dispatch_index(dims, idx, tw, cnt, off, stok, sw, inv, ws, fw, stream);
+  if (rc != MOK_OK) return rc;
+  total += g_last_launches;
+  rc = mok_moe_forward(dims, w, x, idx, off, stok, sw, inv, y, nullptr, ws, fw, stream);
+  if (rc != MOK_OK) return rc;
+  total += g_last_launches;
+  if (cudaMemcpyAsync(y_host, y, xbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOK_ERR_CUDA;
+  g_last_launches = total;
+  return MOK_OK;
+}
+
+}  // extern "C"

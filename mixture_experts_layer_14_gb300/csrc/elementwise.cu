@@ -1,0 +1,182 @@
+// Bandwidth-bound kernels of the MoE layer: the pull gather of token rows into each expert's
+// region, the fixed-order combine, and the router-weight backward.  One warp per row, 16-byte
+// vector accesses, grid-stride loops over a grid of a few blocks per SM.
+#include "mok_device.cuh"
+
+namespace mok {
+
+constexpr int kRowThreads = 256;
+
+static int rows_grid(int64_t nrows) {
+  const int64_t blocks = (nrows + (kRowThreads / 32) - 1) / (kRowThreads / 32);  // one warp per row
+  return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)num_sms() * 8));
+}
+
+// dst[r] = src[rows[r]] for r < nrows (page "Метод и эксперименты": each expert pulls its
+// tokens; with the tokens of an expert ascending the reads walk x in order).  A row index
+// outside [0, nsrc) yields a zero row.
+__global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(
+    const uint4* __restrict__ src0, const uint4* __restrict__ src1, const int32_t* __restrict__ rows,
+    int64_t nrows, int64_t nsrc, int vec_per_row, uint4* __restrict__ dst0, uint4* __restrict__ dst1) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wglobal = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = wglobal; r < nrows; r += nwarps) {
+    const int64_t t = rows[r];
+    const bool ok = (t >= 0 && t < nsrc);
+    const uint4* s0 = src0 + t * vec_per_row;
+    uint4* d0 = dst0 + r * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) d0[v] = ok ? s0[v] : make_uint4(0, 0, 0, 0);
+    if (src1) {
+      const uint4* s1 = src1 + t * vec_per_row;
+      uint4* d1 = dst1 + r * vec_per_row;
+      for (int v = lane; v < vec_per_row; v += 32) d1[v] = ok ? s1[v] : make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+cudaError_t launch_gather_rows(const void* src, const int32_t* rows, int64_t nrows, int d,
+                               void* dst, cudaStream_t s) {
+  return launch_gather_rows2(src, nullptr, rows, nrows, d, dst, nullptr, s);
+}
+
+cudaError_t launch_gather_rows2(const void* src0, const void* src1, const int32_t* rows,
+                                int64_t nrows, int d, void* dst0, void* dst1, cudaStream_t s) {
+  if (nrows == 0) return cudaSuccess;
+  // the number of source rows is not needed for addressing; bound the check by INT32 range of
+  // the token ids written by the dispatch (tokens are < T <= 2^31)
+  prof_begin(src1 ? "gather2" : "gather", s);
+  gather_rows_kernel<<<rows_grid(nrows), kRowThreads, 0, s>>>(
+      static_cast<const uint4*>(src0), static_cast<const uint4*>(src1), rows, nrows,
+      (int64_t)0x7fffffff, d / 8, static_cast<uint4*>(dst0), static_cast<uint4*>(dst1));
+  prof_end(s);
+  return cudaGetLastError();
+}
+
+// y[t] = Ysh[t] + sum over the token's routes in ascending expert id of Ys[inv_pos[t,j]]
+// (fp32 accumulation, one bf16 rounding).  The router weight is already inside Ys (it is
+// applied in the down-projection epilogue).  Page "Mixture-of-Kittens: Nhân kernel MoE ...",
+// section "Chồng lấp tính toán ...": the layer combines shared and routed expert outputs with
+// the router weights; the fixed order keeps the result bit-identical across runs.
+__global__ void __launch_bounds__(kRowThreads) combine_kernel(
+    int64_t T, int vec_per_row, int k, const int32_t* __restrict__ topk_idx,
+    const int32_t* __restrict__ inv_pos, const uint4* __restrict__ Ys, const uint4* __restrict__ Ysh,
+    uint4* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wglobal = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = wglobal; t < T; t += nwarps) {
+    // order the token's routes by expert id (k <= 8, distinct experts)
+    int pos[kMaxK];
+    int ex[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      ex[j] = (j < k) ? topk_idx[t * k + j] : 0x7fffffff;
+      pos[j] = (j < k) ? inv_pos[t * k + j] : -1;
+    }
+#pragma unroll
+    for (int a = 1; a < kMaxK; ++a) {
+#pragma unroll
+      for (int b = kMaxK - 1; b >= a; --b) {
+        const bool sw = ex[b] < ex[b - 1];
+        const int e0 = ex[b - 1], e1 = ex[b], p0 = pos[b - 1], p1 = pos[b];
+        ex[b - 1] = sw ? e1 : e0;
+        ex[b] = sw ? e0 : e1;
+        pos[b - 1] = sw ? p1 : p0;
+        pos[b] = sw ? p0 : p1;
+      }
+    }
+    for (int v = lane; v < vec_per_row; v += 32) {
+      float acc[8];
+      if (Ysh) {
+        const uint4 q = Ysh[t * vec_per_row + v];
+        acc[0] = bf16_lo(q.x); acc[1] = bf16_hi(q.x); acc[2] = bf16_lo(q.y); acc[3] = bf16_hi(q.y);
+        acc[4] = bf16_lo(q.z); acc[5] = bf16_hi(q.z); acc[6] = bf16_lo(q.w); acc[7] = bf16_hi(q.w);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k && pos[j] >= 0) {
+          const uint4 q = Ys[(int64_t)pos[j] * vec_per_row + v];
+          acc[0] += bf16_lo(q.x); acc[1] += bf16_hi(q.x); acc[2] += bf16_lo(q.y); acc[3] += bf16_hi(q.y);
+          acc[4] += bf16_lo(q.z); acc[5] += bf16_hi(q.z); acc[6] += bf16_lo(q.w); acc[7] += bf16_hi(q.w);
+        }
+      }
+      y[t * vec_per_row + v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                          pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
+  }
+}
+
+cudaError_t launch_combine(int64_t T, int d, int k, const int32_t* topk_idx, const int32_t* inv_pos,
+                           const void* Ys, const void* Ysh, void* y, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  prof_begin("combine", s);
+  combine_kernel<<<rows_grid(T), kRowThreads, 0, s>>>(T, d / 8, k, topk_idx, inv_pos,
+                                                      static_cast<const uint4*>(Ys),
+                                                      static_cast<const uint4*>(Ysh),
+                                                      static_cast<uint4*>(y));
+  prof_end(s);
+  return cudaGetLastError();
+}
+
+// Router backward for one token per warp.  dw_j = <dY_t, y_{e_j}(x_t)> is the fixed-order sum
+// of the per-N-tile partials <a, h> written by the down-projection backward epilogue; with
+// w_j = exp(l_j) / sum_{i in S} exp(l_i) (the renormalised softmax over the selection S),
+// dl_m = w_m (dw_m - sum_j w_j dw_j) for m in S and 0 elsewhere.  Writes dlogits[T,E] fp32 and
+// a bf16 copy dl[T,ldl] (columns E..ldl zero) that feeds the tensor-core GEMMs dl W_r^T, x^T dl.
+__global__ void __launch_bounds__(kRowThreads) router_backward_kernel(
+    int64_t T, int E, int k, int ldp, int ldl, const int32_t* __restrict__ topk_idx,
+    const float* __restrict__ topk_w, const int32_t* __restrict__ inv_pos,
+    const float* __restrict__ partial, float* __restrict__ dlogits, __nv_bfloat16* __restrict__ dl) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wglobal = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = wglobal; t < T; t += nwarps) {
+    float dw = 0.0f, w = 0.0f;
+    int e = -1;
+    if (lane < k) {
+      const int64_t r = t * k + lane;
+      e = topk_idx[r];
+      w = topk_w[r];
+      const int pos = inv_pos[r];
+      if (pos >= 0)
+        for (int n = 0; n < ldp; ++n) dw += partial[(int64_t)pos * ldp + n];
+    }
+    float inner = 0.0f;  // sum_j w_j dw_j in slot order, identical on every lane
+    for (int j = 0; j < k; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const float dj = __shfl_sync(0xffffffffu, dw, j);
+      inner += wj * dj;
+    }
+    const float dlj = w * (dw - inner);
+    for (int c = lane; c < ldl; c += 32) {
+      float v = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const int ej = __shfl_sync(0xffffffffu, e, j);
+        const float vj = __shfl_sync(0xffffffffu, dlj, j);
+        if (ej == c) v = vj;
+      }
+      if (c < E) dlogits[t * E + c] = v;
+      dl[t * ldl + c] = __float2bfloat16_rn(v);
+    }
+  }
+}
+
+cudaError_t launch_router_backward(int64_t T, int E, int k, int ldp, const int32_t* topk_idx,
+                                   const float* topk_w, const int32_t* inv_pos,
+                                   const float* partial, float* dlogits, void* dl_bf16,
+                                   cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int ldl = (E + 63) & ~63;
+  prof_begin("router_bwd", s);
+  router_backward_kernel<<<rows_grid(T), kRowThreads, 0, s>>>(
+      T, E, k, ldp, ldl, topk_idx, topk_w, inv_pos, partial, dlogits,
+      static_cast<__nv_bfloat16*>(dl_bf16));
+  prof_end(s);
+  return cudaGetLastError();
+}
+
+}  // namespace mok

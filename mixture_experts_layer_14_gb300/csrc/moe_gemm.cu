@@ -1,0 +1,585 @@
+// Persistent, warp-specialised grouped GEMM for the expert FFNs of the MoE layer (forward and
+// backward), written for sm_103a with TMA, tcgen05.mma and TMEM accumulators.
+//
+// One CTA per SM.  Warp 0: TMA producer (one elected lane).  Warp 1: TMEM owner and UMMA
+// issuer (one elected lane).  Warps 2..5: epilogue, one TMEM lane quarter each (thread = one
+// output row).  A ring of STAGES shared-memory stages (A tile 128x64, B tile BNx64, both bf16
+// in the 128-byte swizzled layout written by TMA) feeds the MMAs; two TMEM accumulators of BN
+// fp32 columns let the epilogue of tile i overlap the MMAs of tile i+1.
+//
+// Scheduling: tiles are numbered on the device from the routing (pull schedule of the page
+// "Mixture-of-Kittens: Nhân kernel MoE ...", section "Lập lịch": each expert's rows are a
+// contiguous region of the destination buffer, so an expert's M tiles are contiguous row
+// blocks pulled straight from it).  CTA c takes tiles c, c+grid, c+2*grid, ...  Every output
+// element is produced by exactly one CTA with a fixed K order, so results are bit-identical
+// from run to run.  No host synchronisation: the tile count is read on the device.
+#include "mok_device.cuh"
+
+namespace mok {
+
+struct Tile {
+  int g;     // 0 shared expert, 1 routed experts, 2 router GEMM (G_BWD_DW only)
+  int e;     // expert index (coordinate of 3D weight maps; 0 for the shared expert)
+  int sub;   // G_BWD_DW: 0 dW_gate, 1 dW_up, 2 dW_down
+  int row0;  // M-grouped: first A row; K-grouped: first K row
+  int rows;  // M-grouped: valid rows of the tile; K-grouped: K rows of the problem
+  int m0;    // K-grouped: first output row (element offset along M)
+  int n;     // N tile index
+  int nkb;   // k-blocks
+};
+
+template <int MODE, int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr bool A_MN = (MODE == G_BWD_DW);
+  static constexpr bool B_MN = (MODE == G_FWD_GU || MODE == G_FWD_DOWN || MODE == G_BWD_DW);
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr uint32_t IDESC = make_idesc_bf16(BN, A_MN, B_MN);
+  static constexpr bool K_GROUPED = (MODE == G_BWD_DW);
+};
+
+constexpr int kAuxBytes = 1024;                      // barriers, TMEM address, abort flag
+constexpr int kSchedBytes = 2 * (kMaxE + 1) * 4;     // expert row offsets + M-tile prefix
+
+template <int MODE, int BN>
+constexpr int smem_bytes_for() {
+  return Cfg<MODE, BN>::STAGES * Cfg<MODE, BN>::STAGE_BYTES + kAuxBytes + kSchedBytes + 1024;
+}
+
+int gemm_smem_bytes(int bn, int /*E*/) {
+  return bn == 256 ? smem_bytes_for<G_FWD_GU, 256>() : smem_bytes_for<G_FWD_GU, 128>();
+}
+
+// ------------------------------------------------------------------ tile decode
+template <int MODE, int BN>
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_off,
+                                            const int* s_mt, int tile) {
+  Tile t;
+  t.sub = 0;
+  t.m0 = 0;
+  if constexpr (!Cfg<MODE, BN>::K_GROUPED) {
+    const int mt0 = p.has_shared ? (p.T + BM - 1) / BM : 0;
+    const int tiles0 = mt0 * p.nt[0];
+    if (tile < tiles0) {
+      const int n = tile / mt0, m = tile - n * mt0;
+      t.g = 0;
+      t.e = 0;
+      t.row0 = m * BM;
+      t.rows = min(BM, p.T - m * BM);
+      t.n = n;
+    } else {
+      const int l = tile - tiles0;
+      const int nt = p.nt[1];
+      int lo = 0, hi = p.E;  // largest e with s_mt[e]*nt <= l
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_mt[mid] * nt <= l) lo = mid; else hi = mid;
+      }
+      const int e = lo;
+      const int mte = s_mt[e + 1] - s_mt[e];
+      const int l2 = l - s_mt[e] * nt;
+      const int n = l2 / mte, m = l2 - n * mte;
+      t.g = 1;
+      t.e = e;
+      t.row0 = s_off[e] + m * BM;
+      t.rows = min(BM, s_off[e + 1] - s_off[e] - m * BM);
+      t.n = n;
+    }
+    int nkb;
+    if constexpr (MODE == G_FWD_GU || MODE == G_BWD_DA) nkb = p.d / BK;
+    else if constexpr (MODE == G_FWD_DOWN) nkb = (t.g ? p.F : p.Fs) / BK;
+    else nkb = p.segkb[t.g][0] + p.segkb[t.g][1] + p.segkb[t.g][2];
+    t.nkb = nkb;
+  } else {
+    int l = tile;
+    if (l < p.router_tiles) {
+      const int mt = p.d / BM;
+      t.g = 2;
+      t.e = 0;
+      t.m0 = (l % mt) * BM;
+      t.n = l / mt;
+      t.row0 = 0;
+      t.rows = p.T;
+    } else {
+      l -= p.router_tiles;
+      const int tiles_sh =
+          p.has_shared ? 2 * (p.d / BM) * (p.Fs / BN) + (p.Fs / BM) * (p.d / BN) : 0;
+      int Fg;
+      if (l < tiles_sh) {
+        t.g = 0;
+        t.e = 0;
+        Fg = p.Fs;
+        t.row0 = 0;
+        t.rows = p.T;
+      } else {
+        l -= tiles_sh;
+        const int per = 2 * (p.d / BM) * (p.F / BN) + (p.F / BM) * (p.d / BN);
+        const int e = l / per;
+        l -= e * per;
+        t.g = 1;
+        t.e = e;
+        Fg = p.F;
+        t.row0 = s_off[e];
+        t.rows = s_off[e + 1] - s_off[e];
+      }
+      const int tg = (p.d / BM) * (Fg / BN);
+      if (l < 2 * tg) {
+        t.sub = l / tg;
+        l -= t.sub * tg;
+        const int mt = p.d / BM;
+        t.m0 = (l % mt) * BM;
+        t.n = l / mt;
+      } else {
+        t.sub = 2;
+        l -= 2 * tg;
+        const int mt = Fg / BM;
+        t.m0 = (l % mt) * BM;
+        t.n = l / mt;
+      }
+    }
+    t.nkb = (t.rows + BK - 1) / BK;
+  }
+  return t;
+}
+
+template <int MODE, int BN>
+__device__ __forceinline__ int total_tiles(const GemmParams& p, const int* s_mt) {
+  if constexpr (!Cfg<MODE, BN>::K_GROUPED) {
+    const int mt0 = p.has_shared ? (p.T + BM - 1) / BM : 0;
+    return mt0 * p.nt[0] + (p.E > 0 ? s_mt[p.E] * p.nt[1] : 0);
+  } else {
+    const int tiles_sh =
+        p.has_shared ? 2 * (p.d / BM) * (p.Fs / BN) + (p.Fs / BM) * (p.d / BN) : 0;
+    const int per = 2 * (p.d / BM) * (p.F / BN) + (p.F / BM) * (p.d / BN);
+    return p.router_tiles + tiles_sh + p.E * per;
+  }
+}
+
+// ------------------------------------------------------------------ producer
+// Map slots per mode (g = group):
+//  G_FWD_GU   A: x / x_sorted (K-major)            B: gate, up weights (MN-major, 3D)
+//  G_FWD_DOWN A: h_sh / h (K-major)                B: down weights (MN-major, 3D)
+//  G_BWD_DA   A: dY / dY_sorted (K-major)          B: down weights (K-major view, 3D)
+//  G_BWD_DX   A: segments dG, dU (, dl)            B: gate, up (, router) weights (K-major view)
+//  G_BWD_DW   A: x / x_sorted, w*h (MN-major)      B: dG, dU, dY (MN-major); router x, dl
+template <int MODE, int BN>
+__device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, int kb,
+                                            uint32_t sA, uint32_t sB, uint32_t bar) {
+  const CUtensorMap* M = p.maps;
+  if constexpr (MODE == G_FWD_GU) {
+    tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
+    const CUtensorMap* bg = &M[t.g ? MS_B3 : MS_B0];
+    const CUtensorMap* bu = &M[t.g ? MS_B4 : MS_B1];
+    const int c0 = t.n * 128;
+    tma_load_3d(sB + 0 * 8192, bg, bar, c0, kb * BK, t.e);
+    tma_load_3d(sB + 1 * 8192, bg, bar, c0 + 64, kb * BK, t.e);
+    tma_load_3d(sB + 2 * 8192, bu, bar, c0, kb * BK, t.e);
+    tma_load_3d(sB + 3 * 8192, bu, bar, c0 + 64, kb * BK, t.e);
+  } else if constexpr (MODE == G_FWD_DOWN) {
+    tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
+    const CUtensorMap* b = &M[t.g ? MS_B3 : MS_B0];
+#pragma unroll
+    for (int i = 0; i < BN / 64; ++i) tma_load_3d(sB + i * 8192, b, bar, t.n * BN + 64 * i, kb * BK, t.e);
+  } else if constexpr (MODE == G_BWD_DA) {
+    tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
+    tma_load_3d(sB, &M[t.g ? MS_B3 : MS_B0], bar, kb * BK, t.n * BN, t.e);
+  } else if constexpr (MODE == G_BWD_DX) {
+    int seg = 0, kk = kb;
+    while (seg < 2 && kk >= p.segkb[t.g][seg]) { kk -= p.segkb[t.g][seg]; ++seg; }
+    tma_load_2d(sA, &M[(t.g ? MS_A3 : MS_A0) + seg], bar, kk * BK, t.row0);
+    tma_load_3d(sB, &M[(t.g ? MS_B3 : MS_B0) + seg], bar, kk * BK, t.n * BN, seg == 2 ? 0 : t.e);
+  } else {  // G_BWD_DW
+    const int krow = t.row0 + kb * BK;
+    int ia, ib;
+    if (t.g == 2) { ia = MS_R_A; ib = MS_R_B; }
+    else if (t.sub == 0) { ia = t.g ? MS_A3 : MS_A0; ib = t.g ? MS_B3 : MS_B0; }
+    else if (t.sub == 1) { ia = t.g ? MS_A3 : MS_A0; ib = t.g ? MS_B4 : MS_B1; }
+    else { ia = t.g ? MS_A4 : MS_A1; ib = t.g ? MS_B5 : MS_B2; }
+    tma_load_2d(sA, &M[ia], bar, t.m0, krow);
+    tma_load_2d(sA + 8192, &M[ia], bar, t.m0 + 64, krow);
+#pragma unroll
+    for (int i = 0; i < BN / 64; ++i) tma_load_2d(sB + i * 8192, &M[ib], bar, t.n * BN + 64 * i, krow);
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+__device__ __forceinline__ void st_row64(void* dst, const uint32_t (&v)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+__device__ __forceinline__ void ld_row64(const void* src, uint32_t (&v)[16]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 q = s[i];
+    v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+  }
+}
+
+template <int MODE, int BN>
+__device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uint32_t tacc,
+                                         int r) {
+  using bf16 = __nv_bfloat16;
+  if constexpr (MODE == G_FWD_GU) {
+    const bool valid = r < t.rows;
+    const int ld = t.g ? p.F : p.Fs;
+    const int64_t row = t.row0 + r;
+    bf16* h = static_cast<bf16*>(p.out0[t.g]) + row * ld + t.n * 128;
+    bf16* G = p.out1[t.g] ? static_cast<bf16*>(p.out1[t.g]) + row * ld + t.n * 128 : nullptr;
+    bf16* U = p.out2[t.g] ? static_cast<bf16*>(p.out2[t.g]) + row * ld + t.n * 128 : nullptr;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      uint32_t gr[32], ur[32];
+      tmem_ld32(tacc + c, gr);
+      tmem_ld32(tacc + 128 + c, ur);
+      tmem_ld_wait();
+      if (valid) {
+        uint32_t hp[16], gp[16], up[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float g0 = __uint_as_float(gr[2 * i]), g1 = __uint_as_float(gr[2 * i + 1]);
+          const float u0 = __uint_as_float(ur[2 * i]), u1 = __uint_as_float(ur[2 * i + 1]);
+          hp[i] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+          gp[i] = pack_bf16x2(g0, g1);
+          up[i] = pack_bf16x2(u0, u1);
+        }
+        st_row64(h + c, hp);
+        if (G) st_row64(G + c, gp);
+        if (U) st_row64(U + c, up);
+      }
+    }
+  } else if constexpr (MODE == G_FWD_DOWN || MODE == G_BWD_DX) {
+    const bool valid = r < t.rows;
+    const int64_t row = t.row0 + r;
+    float s = 1.0f;
+    if (MODE == G_FWD_DOWN && t.g == 1 && valid) s = p.row_w[row];
+    bf16* o = static_cast<bf16*>(p.out0[t.g]) + row * p.d + t.n * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(tacc + c, v);
+      tmem_ld_wait();
+      if (valid) {
+        uint32_t q[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          q[i] = pack_bf16x2(s * __uint_as_float(v[2 * i]), s * __uint_as_float(v[2 * i + 1]));
+        st_row64(o + c, q);
+      }
+    }
+  } else if constexpr (MODE == G_BWD_DA) {
+    const bool valid = r < t.rows;
+    const int ld = t.g ? p.F : p.Fs;
+    const int64_t row = t.row0 + r;
+    const float w = (t.g == 1 && valid) ? p.row_w[row] : 1.0f;
+    const int64_t off = row * ld + t.n * BN;
+    const bf16* Gs = static_cast<const bf16*>(p.in0[t.g]) + off;
+    const bf16* Us = static_cast<const bf16*>(p.in1[t.g]) + off;
+    bf16* dG = static_cast<bf16*>(p.out0[t.g]) + off;
+    bf16* dU = static_cast<bf16*>(p.out1[t.g]) + off;
+    bf16* hw = static_cast<bf16*>(p.out2[t.g]) + off;
+    float pacc = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(tacc + c, v);
+      tmem_ld_wait();
+      if (valid) {
+        uint32_t gq[16], uq[16], o0[16], o1[16], o2[16];
+        ld_row64(Gs + c, gq);
+        ld_row64(Us + c, uq);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float res[2][3];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const float g = h2 ? bf16_hi(gq[i]) : bf16_lo(gq[i]);
+            const float u = h2 ? bf16_hi(uq[i]) : bf16_lo(uq[i]);
+            const float a = __uint_as_float(v[2 * i + h2]);
+            const float sg = sigmoid_f(g);
+            const float hv = g * sg * u;
+            pacc += a * hv;
+            const float dh = w * a;
+            res[h2][0] = dh * u * sg * (1.0f + g * (1.0f - sg));
+            res[h2][1] = dh * g * sg;
+            res[h2][2] = w * hv;
+          }
+          o0[i] = pack_bf16x2(res[0][0], res[1][0]);
+          o1[i] = pack_bf16x2(res[0][1], res[1][1]);
+          o2[i] = pack_bf16x2(res[0][2], res[1][2]);
+        }
+        st_row64(dG + c, o0);
+        st_row64(dU + c, o1);
+        st_row64(hw + c, o2);
+      }
+    }
+    if (valid && t.g == 1) p.partial[row * p.nt[1] + t.n] = pacc;
+  } else {  // G_BWD_DW
+    bf16* o;
+    int ld, ncols;
+    if (t.g == 2) {
+      o = static_cast<bf16*>(p.out_router);
+      ld = p.E_cols;
+      ncols = p.E_cols;
+    } else {
+      const int Fg = t.g ? p.F : p.Fs;
+      if (t.sub < 2) {
+        o = static_cast<bf16*>(t.sub ? p.out1[t.g] : p.out0[t.g]) + (int64_t)t.e * p.d * Fg;
+        ld = Fg;
+      } else {
+        o = static_cast<bf16*>(p.out2[t.g]) + (int64_t)t.e * Fg * p.d;
+        ld = p.d;
+      }
+      ncols = ld;
+    }
+    o += (int64_t)(t.m0 + r) * ld;
+    const bool zero = (t.nkb == 0);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      if (!zero) {
+        tmem_ld32(tacc + c, v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
+      const int col = t.n * BN + c;
+      if (col + 32 <= ncols) {
+        uint32_t q[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          q[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        st_row64(o + col, q);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col + i < ncols) o[col + i] = __float2bfloat16_rn(__uint_as_float(v[i]));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ K-tail masking
+// G_BWD_DW: the last k-block of a problem may hold rows of the next expert; zero them in both
+// operands (MN-major: K is the row index inside every 64-column box, 128 B per row, and the
+// 128-byte swizzle only permutes 16-byte chunks within a row).
+template <int BN>
+__device__ __forceinline__ void zero_k_tail(uint32_t sA, uint32_t sB, int valid, int lane) {
+  const int nrows = BK - valid;
+  const int nboxes = 2 + BN / 64;
+  const int per_box = nrows * 8;  // 16-byte chunks
+  for (int i = lane; i < nboxes * per_box; i += 32) {
+    const int box = i / per_box;
+    const int j = i - box * per_box;
+    const int row = valid + (j >> 3);
+    const uint32_t base = (box < 2) ? sA + box * 8192 : sB + (box - 2) * 8192;
+    const uint32_t addr = base + row * 128 + (j & 7) * 16;
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int MODE, int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using C = Cfg<MODE, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA0 = base;
+  const uint32_t sB0 = base + C::STAGES * C::A_BYTES;
+  uint8_t* aux = gbase + C::STAGES * C::STAGE_BYTES;
+  const uint32_t aux_s = base + C::STAGES * C::STAGE_BYTES;
+  // aux layout: full[S] empty[S] tfull[2] tempty[2] drain | tmem addr | abort
+  const uint32_t bar_full = aux_s;
+  const uint32_t bar_empty = aux_s + 8 * C::STAGES;
+  const uint32_t bar_tfull = aux_s + 16 * C::STAGES;
+  const uint32_t bar_tempty = bar_tfull + 16;
+  const uint32_t bar_drain = bar_tempty + 16;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(aux + 16 * C::STAGES + 40);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(aux + 16 * C::STAGES + 48);
+  int* s_off = reinterpret_cast<int*>(aux + kAuxBytes);
+  int* s_mt = s_off + (kMaxE + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 4 * 32);
+    }
+    mbar_init(bar_drain, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < MS_COUNT; ++i) tma_prefetch_desc(&p.maps[i]);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(s_tmem), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2 && p.E > 0) {
+    // expert row offsets and (M-grouped) the prefix of M tiles per expert, one warp
+    const int per = (p.E + 31) / 32;
+    const int e0 = lane * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = e0 + i;
+      if (e < p.E) {
+        const int o0 = p.offsets[e], o1 = p.offsets[e + 1];
+        s_off[e] = o0;
+        local += (o1 - o0 + BM - 1) / BM;
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int e = e0 + i;
+      if (e < p.E) {
+        s_mt[e] = run;
+        run += (p.offsets[e + 1] - p.offsets[e] + BM - 1) / BM;
+      }
+    }
+    if (lane == 31) {
+      s_mt[p.E] = incl;
+      s_off[p.E] = p.offsets[p.E];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int ntiles = total_tiles<MODE, BN>(p, s_mt);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x) {
+        const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) break;
+          mbar_arrive_expect_tx(bar_full + 8 * stage, C::STAGE_BYTES);
+          issue_loads<MODE, BN>(p, t, kb, sA0 + stage * C::A_BYTES, sB0 + stage * C::B_BYTES,
+                                bar_full + 8 * stage);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x, ++it) {
+      const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
+      const int buf = it & 1;
+      const uint32_t tph = (it >> 1) & 1;
+      if (!mbar_wait(bar_tempty + 8 * buf, tph ^ 1, p.status, s_abort)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      bool ok = true;
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        if (!mbar_wait(bar_full + 8 * stage, phase, p.status, s_abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sA = sA0 + stage * C::A_BYTES, sB = sB0 + stage * C::B_BYTES;
+        if constexpr (C::K_GROUPED) {
+          const int valid = t.rows - kb * BK;
+          if (valid < BK) {
+            zero_k_tail<BN>(sA, sB, valid, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = C::A_MN ? make_sdesc(sA + k * 2048, 8192, 1024)
+                                        : make_sdesc(sA + k * 32, 16, 1024);
+            const uint64_t bd = C::B_MN ? make_sdesc(sB + k * 2048, 8192, 1024)
+                                        : make_sdesc(sB + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
+          }
+          umma_commit(bar_empty + 8 * stage);
+        }
+        __syncwarp();
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(bar_tfull + 8 * buf);
+      __syncwarp();
+    }
+    // every MMA issued by this CTA has completed before TMEM is released
+    if (lane == 0) {
+      umma_commit(bar_drain);
+      volatile int no_abort = 0;
+      mbar_wait(bar_drain, 0, p.status, &no_abort);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter accessible to this warp
+    const int r = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x, ++it) {
+      const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
+      const int buf = it & 1;
+      const uint32_t tph = (it >> 1) & 1;
+      if (!mbar_wait(bar_tfull + 8 * buf, tph, p.status, s_abort)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
+      epilogue<MODE, BN>(p, t, tacc, r);
+      tc_fence_before();
+      mbar_arrive(bar_tempty + 8 * buf);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int MODE, int BN>
+static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
+  constexpr int smem = smem_bytes_for<MODE, BN>();
+  auto k = moe_gemm_kernel<MODE, BN>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  static const char* kNames[] = {"gemm_fwd_gate_up", "gemm_fwd_down", "gemm_bwd_da", "gemm_bwd_dx",
+                                 "gemm_bwd_dw"};
+  prof_begin(kNames[MODE], s);
+  k<<<grid, kGemmThreads, smem, s>>>(p);
+  prof_end(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {
+  switch (mode) {
+    case G_FWD_GU: return launch_one<G_FWD_GU, 256>(p, grid, s);
+    case G_FWD_DOWN:
+      return bn == 256 ? launch_one<G_FWD_DOWN, 256>(p, grid, s) : launch_one<G_FWD_DOWN, 128>(p, grid, s);
+    case G_BWD_DA:
+      return bn == 256 ? launch_one<G_BWD_DA, 256>(p, grid, s) : launch_one<G_BWD_DA, 128>(p, grid, s);
+    case G_BWD_DX:
+      return bn == 256 ? launch_one<G_BWD_DX, 256>(p, grid, s) : launch_one<G_BWD_DX, 128>(p, grid, s);
+    case G_BWD_DW:
+      return bn == 256 ? launch_one<G_BWD_DW, 256>(p, grid, s) : launch_one<G_BWD_DW, 128>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mok

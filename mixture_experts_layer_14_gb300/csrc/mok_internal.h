@@ -1,0 +1,107 @@
+// Internal declarations shared by the host code and the kernels of libmok.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mok.h"
+
+namespace mok {
+
+constexpr uint64_t kWaitNs = 2000000000ull;  // bounded device waits give up after 2 s
+constexpr int BM = 128;                      // UMMA M: rows of a tile (TMEM lanes)
+constexpr int BK = 64;                       // K per pipeline stage: 64 bf16 = one 128 B row
+constexpr int kGemmThreads = 192;            // warp 0 TMA, warp 1 MMA/TMEM, warps 2..5 epilogue
+constexpr int kDispatchChunk = 64;           // tokens per histogram block of the counting sort
+constexpr int kMaxE = 512;
+constexpr int kMaxK = 8;
+
+// ------------------------------------------------------------------ grouped GEMM
+enum GemmMode : int {
+  G_FWD_GU = 0,    // h = SiLU(X Wg) * (X Wu)              M-grouped, A K-major, B MN-major
+  G_FWD_DOWN = 1,  // Y = w * (h Wd)                       M-grouped, A K-major, B MN-major
+  G_BWD_DA = 2,    // a = dY Wd^T -> dG, dU, w*h, <a,h>    M-grouped, A K-major, B K-major
+  G_BWD_DX = 3,    // dX = dG Wg^T + dU Wu^T (+ dl Wr^T)   M-grouped, A K-major, B K-major
+  G_BWD_DW = 4,    // dW = X^T dG, X^T dU, (w h)^T dY, x^T dl  K-grouped, A and B MN-major
+};
+
+// Tensor-map slots.  Group 0 is the shared expert (rows = tokens), group 1 the routed experts
+// (rows = destination rows of the pull schedule).  Which slots a mode uses is listed in
+// moe_gemm.cu next to its producer.
+enum MapSlot : int {
+  MS_A0 = 0, MS_A1 = 1, MS_A2 = 2,  // group 0 A operands (per segment / sub-GEMM)
+  MS_A3 = 3, MS_A4 = 4, MS_A5 = 5,  // group 1 A operands
+  MS_B0 = 6, MS_B1 = 7, MS_B2 = 8,  // group 0 B operands
+  MS_B3 = 9, MS_B4 = 10, MS_B5 = 11,  // group 1 B operands
+  MS_R_A = 12, MS_R_B = 13,           // router GEMM of the backward (x^T dl)
+  MS_COUNT = 14
+};
+
+struct GemmParams {
+  CUtensorMap maps[MS_COUNT];
+  const int* offsets;   // routed row offsets [E+1] (device), NULL when E == 0
+  int E;                // routed experts in this launch (0 = none)
+  int has_shared;       // group 0 present
+  int T;                // rows of group 0
+  int d, F, Fs;         // layer dims
+  int nt[2];            // N tiles per group (M-grouped modes)
+  int nseg[2];          // K segments per group (G_BWD_DX)
+  int segkb[2][3];      // k-blocks of each segment
+  int router_tiles;     // G_BWD_DW: number of x^T dl tiles (0 = none)
+  int E_cols;           // G_BWD_DW: valid columns of dW_router (= E)
+  // epilogue pointers, [group]
+  void* out0[2];        // h / Y / dG / dX / dW_gate
+  void* out1[2];        // G (saved)      / dU / dW_up
+  void* out2[2];        // U (saved)      / w*h / dW_down
+  void* out_router;     // dW_router [d,E]
+  const void* in0[2];   // G (saved) for G_BWD_DA
+  const void* in1[2];   // U (saved)
+  const float* row_w;   // router weight of each routed row (sorted_w)
+  float* partial;       // G_BWD_DA: <a,h> per (routed row, N tile), [R, nt[1]]
+  int* status;
+};
+
+// Launches (moe_gemm.cu).  grid = persistent CTAs.
+cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s);
+int gemm_smem_bytes(int bn, int E);
+
+// Router (route.cu)
+struct RouteParams {
+  CUtensorMap map_x;   // x [T,d] K-major, box {64,128}
+  CUtensorMap map_w;   // W_router [d,E] MN-major, box {64,64}
+  const float* bias;
+  int32_t* topk_idx;
+  float* topk_w;
+  float* logits;
+  int T, d, E, k;
+  int* status;
+};
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
+
+// Dispatch (dispatch.cu)
+cudaError_t launch_dispatch(int64_t T, int E, int k, const int32_t* topk_idx, const float* topk_w,
+                            int32_t* counts, int32_t* offsets, int32_t* sorted_tok,
+                            float* sorted_w, int32_t* inv_pos, int32_t* hist, int* status,
+                            cudaStream_t s, int* launches);
+
+// Elementwise (elementwise.cu)
+cudaError_t launch_gather_rows(const void* src, const int32_t* rows, int64_t nrows, int d,
+                               void* dst, cudaStream_t s);
+cudaError_t launch_gather_rows2(const void* src0, const void* src1, const int32_t* rows,
+                                int64_t nrows, int d, void* dst0, void* dst1, cudaStream_t s);
+cudaError_t launch_combine(int64_t T, int d, int k, const int32_t* topk_idx,
+                           const int32_t* inv_pos, const void* Ys, const void* Ysh, void* y,
+                           cudaStream_t s);
+cudaError_t launch_router_backward(int64_t T, int E, int k, int ldp, const int32_t* topk_idx,
+                                   const float* topk_w, const int32_t* inv_pos,
+                                   const float* partial, float* dlogits, void* dl_bf16,
+                                   cudaStream_t s);
+
+int num_sms();
+
+// Optional per-launch CUDA-event timing (profile.cu); no-ops unless enabled on this thread.
+void prof_begin(const char* name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+
+}  // namespace mok

@@ -1,0 +1,76 @@
+"""The C-ABI library loads and exports every symbol include/mok.h declares; host-side argument
+checks and size queries behave as documented.  No GPU needed: nothing here launches a kernel."""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+
+import mixture_experts_layer_14_gb300 as mok
+from tests._helpers import ROOT, ensure_lib
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "mok.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mok_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("mok_route", "mok_dispatch_index", "mok_moe_forward", "mok_moe_backward"):
+        assert required in names
+    assert sorted(mok.EXPORTED_SYMBOLS) == names
+
+
+def test_library_exports_every_declared_symbol():
+    L = ensure_lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+    out = os.popen(f"nm -D --defined-only {mok.lib_path()}").read()
+    for name in _declared():
+        assert re.search(rf"\bT {name}\b", out), name
+
+
+def test_status_strings_and_size_queries():
+    L = ensure_lib()
+    for code in range(0, -7, -1):
+        assert L.mok_status_string(code).decode().startswith("MOK_")
+    D = mok.dims(4096, 7168, 256, 8, 2048, 2048, 1)
+    fw = mok.workspace_size(D)
+    bw = mok.workspace_size(D, backward=True)
+    R = 4096 * 8
+    assert fw >= 2 * R * 7168 * 2 + R * 2048 * 2          # x_sorted, Y_s and h at least
+    assert bw >= 3 * R * 7168 * 2
+    assert mok.saved_size(D) >= 2 * R * 2048 * 2
+    bad = [mok.dims(16, 100, 8, 2, 128), mok.dims(16, 128, 8, 9, 128), mok.dims(16, 128, 12, 2, 128),
+           mok.dims(16, 128, 8, 2, 96), mok.dims(-1, 128, 8, 2, 128), mok.dims(16, 128, 1024, 2, 128)]
+    for D in bad:
+        assert L.mok_workspace_size(ctypes.byref(D), 0) == 0
+
+
+def test_argument_errors_are_returned_not_raised():
+    L = ensure_lib()
+    D = mok.dims(16, 128, 8, 2, 128, 128, 1)
+    null = None
+    # null outputs: MOK_ERR_INVALID_ARG before any CUDA call
+    rc = L.mok_route(ctypes.byref(D), null, null, null, null, null, null, null, 0, null)
+    assert rc == -1
+    rc = L.mok_dispatch_index(ctypes.byref(D), null, null, null, null, null, null, null, null, 0, null)
+    assert rc == -1
+    # unsupported dims: MOK_ERR_UNSUPPORTED
+    Dbad = mok.dims(16, 100, 8, 2, 128, 128, 1)
+    rc = L.mok_route(ctypes.byref(Dbad), null, null, null, null, null, null, null, 0, null)
+    assert rc == -2
+    # misaligned pointer: MOK_ERR_UNSUPPORTED; too-small workspace: MOK_ERR_WORKSPACE
+    fake = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1001)
+    rc = L.mok_route(ctypes.byref(D), odd, fake, null, fake, fake, null, fake, 1 << 40, null)
+    assert rc == -2
+    rc = L.mok_route(ctypes.byref(D), fake, fake, null, fake, fake, null, fake, 16, null)
+    assert rc == -3
+    with pytest.raises(mok.MokError):
+        mok._check(-3)
