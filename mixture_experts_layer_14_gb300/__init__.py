@@ -30,7 +30,7 @@ EXPORTED_SYMBOLS = [
     "mok_route", "mok_dispatch_index", "mok_moe_forward", "mok_moe_backward",
     "mok_layer_host_extra_size", "mok_layer_forward_host", "mok_status_string",
     "mok_read_device_status", "mok_clear_device_status", "mok_last_launch_count",
-    "mok_timing_enable", "mok_timing_collect",
+    "mok_timing_enable", "mok_timing_collect", "mok_dispatch_index_noalloc",
 ]
 
 
@@ -85,6 +85,7 @@ def lib():
             "mok_clear_device_status": (ctypes.c_int, [_VP, _VP]),
             "mok_last_launch_count": (ctypes.c_int, []),
             "mok_timing_enable": (ctypes.c_int, [ctypes.c_int]),
+            "mok_dispatch_index_noalloc": (ctypes.c_int, [_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
             "mok_timing_collect": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int),
                                                   ctypes.POINTER(ctypes.c_double), ctypes.c_int,
                                                   ctypes.POINTER(ctypes.c_int)]),
@@ -227,6 +228,16 @@ def dispatch_index(D, topk_idx, topk_w, ws):
         ctypes.byref(D), _ptr(topk_idx), _ptr(topk_w), _ptr(out["counts"]), _ptr(out["offsets"]),
         _ptr(out["sorted_tok"]), _ptr(out["sorted_w"]), _ptr(out["inv_pos"]), _ptr(ws), ws.numel(),
         _stream()))
+    return out
+
+
+def dispatch_index_noalloc(D, topk_idx, topk_w, out):
+    """Pull schedule into the caller's preallocated tensors ``out`` (same keys as the dict of
+    :func:`dispatch_index`) without a workspace: for callers that may not allocate device memory
+    while routing.  The library keeps its scratch in a fixed 1 MiB device array."""
+    _check(lib().mok_dispatch_index_noalloc(
+        ctypes.byref(D), _ptr(topk_idx), _ptr(topk_w), _ptr(out["counts"]), _ptr(out["offsets"]),
+        _ptr(out["sorted_tok"]), _ptr(out["sorted_w"]), _ptr(out["inv_pos"]), _stream()))
     return out
 
 
