@@ -156,6 +156,27 @@ def work_model(shape, counts):
     return m, layer_flops, e_act
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures, per weight set
+# streamed (routed experts with tokens + shared expert), valid only while the kernel source is
+# the one that was captured (sha1 prefix).  Source: profiles/gemm_fwd_gate_up_dsv3_slice_e32.md.
+PROFILED_TRAFFIC = {
+    "gemm_fwd_gate_up": ("7de49fbd3f37", (2.015228e9 + 19.432192e6) / 33,
+                         "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"),
+}
+
+
+def profiled_traffic(name, weight_sets):
+    import hashlib
+
+    if name not in PROFILED_TRAFFIC:
+        return None
+    sha, per_set, src = PROFILED_TRAFFIC[name]
+    with open(os.path.join(ROOT, src), "rb") as f:
+        if hashlib.sha1(f.read()).hexdigest()[:12] != sha:
+            return None  # the kernel changed since the counters were taken
+    return per_set * weight_sets
+
+
 def roofline_of(name, model, ms_per_launch, peaks):
     w = model[name]
     t_flop = w["flops"] / (peaks["bf16_tflops"] * 1e12) if w["flops"] else 0.0
@@ -298,7 +319,8 @@ def run_mok(args, shape, rank, world, local_rank):
     dominant = max((n for n in kern if n in model), key=lambda n: kern[n][1])
     dn, dms = kern[dominant]
     roof = roofline_of(dominant, model, dms / dn, peaks)
-    roof.update({"kernel": dominant, "traffic": None, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
+    roof.update({"kernel": dominant, "traffic": profiled_traffic(dominant, e_act + shape.n_shared),
+                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
                  if peaks["source"] == "measured" else "fallback"})
 
     tokens = world * shape.T * args.steps
