@@ -139,20 +139,35 @@ def work_model(shape, counts):
     T, d, E, k, F, Fs, ns = shape.T, shape.d, shape.E, shape.k, shape.F, shape.F_shared, shape.n_shared
     R = T * k
     Rs = R + T * ns
+    Hs = R * F + T * ns * Fs          # elements of one [rows, F] activation, routed + shared
     e_act = sum(1 for c in counts if c > 0)
     wb = 2  # bf16
+    train = shape.backward
     m = {}
     m["route"] = {"flops": 2.0 * T * d * E, "bytes": wb * (T * d + d * E) + 8.0 * T * k}
     # x is read once (repeated rows of a token hit L2), every destination row written once
     m["gather"] = {"flops": 0.0, "bytes": wb * (T * d + R * d) + 4.0 * R}
     m["gemm_fwd_gate_up"] = {
         "flops": 2.0 * (R * 2 * F * d + T * ns * 2 * Fs * d),
-        "bytes": wb * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + Rs * d + R * F + T * ns * Fs)}
+        "bytes": wb * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + Rs * d + Hs * (3 if train else 1))}
     m["gemm_fwd_down"] = {
         "flops": 2.0 * (R * F * d + T * ns * Fs * d),
-        "bytes": wb * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + R * F + T * ns * Fs + Rs * d)}
+        "bytes": wb * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Hs + Rs * d)}
     m["combine"] = {"flops": 0.0, "bytes": wb * (Rs * d + T * d) + 8.0 * R}
     layer_flops = T * (2.0 * d * E + (k * 6.0 * d * F) + ns * 6.0 * d * Fs)
+    if train:
+        m["gather2"] = {"flops": 0.0, "bytes": 2.0 * wb * (T * d + R * d) + 4.0 * R}
+        m["gemm_bwd_da"] = {  # a = dY Wd^T; reads G, U; writes dG, dU, w*h
+            "flops": 2.0 * (R * F * d + T * ns * Fs * d),
+            "bytes": wb * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Rs * d + 5.0 * Hs) + 4.0 * R * 16}
+        m["router_bwd"] = {"flops": 0.0, "bytes": 4.0 * T * E + wb * T * E + 4.0 * R * 16}
+        m["gemm_bwd_dx"] = {  # dX = dG Wg^T + dU Wu^T (+ dl Wr^T)
+            "flops": 2.0 * (R * 2 * F * d + T * ns * 2 * Fs * d + T * E * d),
+            "bytes": wb * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + 2.0 * Hs + Rs * d + T * E)}
+        m["gemm_bwd_dw"] = {  # dWg, dWu, dWd (written for every expert) and x^T dl
+            "flops": 2.0 * (3.0 * (R * F * d + T * ns * Fs * d) + T * d * E),
+            "bytes": wb * (3.0 * (E * d * F + ns * d * Fs) + 2.0 * Rs * d + 3.0 * Hs + d * E)}
+        layer_flops = 3.0 * layer_flops
     return m, layer_flops, e_act
 
 
@@ -254,47 +269,45 @@ def cpu_baseline(L, shape, pool_tokens=2, budget_s=12.0, max_steps=64):
 
 
 # ------------------------------------------------------------------ the GB300 arm
-def run_mok(args, shape, rank, world, local_rank):
+def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
+    """Times `steps` whole-layer steps of `shape` (forward, plus backward for training
+    workloads).  Returns the measurement and the layer inputs."""
     import torch
 
     import mixture_experts_layer_14_gb300 as mok
     from mixture_experts_layer_14_gb300.synthetic import make_layer
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    peaks = load_peaks()
-    L = make_layer(shape, dev, with_dy=shape.backward)
+    if L is None:
+        L = make_layer(shape, dev, with_dy=shape.backward)
     D = mok.dims(shape.T, shape.d, shape.E, shape.k, shape.F, shape.F_shared, shape.n_shared)
     layer = mok.MoELayer(D, L, dev)
     x = L["x"]
     torch.cuda.synchronize()
 
     def step():
-        y = layer.forward(x, training=shape.backward)
-        n = mok.last_launch_count()
-        n_route = 1
+        layer.forward(x, training=shape.backward)
+        n = 1 + 3 + mok.last_launch_count()  # route, dispatch (3), expert forward
         if shape.backward:
             layer.backward(x, L["dY"])
             n += mok.last_launch_count()
-        return y, n + n_route + 3  # route (1) + dispatch (3) + forward/backward launches
+        return n
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     counts = layer.routing["counts"].cpu().tolist()
 
     stream = torch.cuda.current_stream()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local_rank)
+    sampler = ClockSampler(dev.index or 0)
     dist_barrier(world)
     torch.cuda.synchronize()
     sampler.start()
     mok.timing_enable(True)
     ev0.record(stream)
     launches = 0
-    for _ in range(args.steps):
-        _, n = step()
-        launches += n
+    for _ in range(steps):
+        launches += step()
     ev1.record(stream)
     torch.cuda.synchronize()
     mok.timing_enable(False)
@@ -302,9 +315,9 @@ def run_mok(args, shape, rank, world, local_rank):
     dist_barrier(world)
     ms = ev0.elapsed_time(ev1)
     kern = mok.timing_collect()
-    status = mok.read_status(layer.ws)
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed region")
+    for ws in (layer.ws, layer._ws_bwd):
+        if ws is not None and mok.read_status(ws) != 0:
+            raise RuntimeError(f"device status {mok.read_status(ws)} after the timed region")
     ms_max = dist_max(ms, world)
 
     model, layer_flops, e_act = work_model(shape, counts)
@@ -319,39 +332,77 @@ def run_mok(args, shape, rank, world, local_rank):
     dominant = max((n for n in kern if n in model), key=lambda n: kern[n][1])
     dn, dms = kern[dominant]
     roof = roofline_of(dominant, model, dms / dn, peaks)
-    roof.update({"kernel": dominant, "traffic": profiled_traffic(dominant, e_act + shape.n_shared),
-                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
-                 if peaks["source"] == "measured" else "fallback"})
-
-    tokens = world * shape.T * args.steps
-    value = tokens / (ms_max / 1e3)
-    tflops = layer_flops * args.steps / (ms / 1e3) / 1e12
-
-    e2e = None
-    if not args.no_e2e and not shape.backward:
-        e2e = run_e2e(args, mok, D, L, shape, dev, world)
-
-    line = {
-        "metric": "MoE-layer forward tokens/s" if not shape.backward else "MoE-layer fwd+bwd tokens/s",
-        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) activations, N(0,1/sqrt(fan_in)) bf16 weights, random init)",
-        "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E, "k": shape.k,
-                   "F": shape.F, "F_shared": shape.F_shared, "n_shared": shape.n_shared,
-                   "router_bias": shape.bias, "active_experts": e_act,
-                   "global_batch_tokens": world * shape.T, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2: every step streams >22 GB of expert weights"},
+    roof.update({"kernel": dominant, "traffic": profiled_traffic(dominant, e_act + shape.n_shared)
+                 if not shape.backward else None,
+                 "peak_source": "measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+                 else "fallback"})
+    tflops = layer_flops * steps / (ms / 1e3) / 1e12
+    out = {
+        "value": round(world * shape.T * steps / (ms_max / 1e3), 1),
+        "ms_per_step": round(ms_max / steps, 4),
         "tflops": round(tflops, 2),
         "tflops_frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
         "roofline": {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in roof.items()},
-        "kernels": kernels,
-        "gpu_launches": launches,
-        "clocks": clocks,
-        "e2e": e2e,
+        "kernels": kernels, "gpu_launches": launches, "clocks": clocks,
+        "active_experts": e_act, "max_expert_rows": max(counts), "empty_experts": counts.count(0),
+    }
+    del layer
+    return out, L
+
+
+def config_of(shape, world, e_act):
+    return {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E, "k": shape.k,
+            "F": shape.F, "F_shared": shape.F_shared, "n_shared": shape.n_shared,
+            "router_bias": shape.bias, "active_experts": e_act,
+            "global_batch_tokens": world * shape.T, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2: every step streams >22 GB of expert weights"}
+
+
+def run_mok(args, shape, rank, world, local_rank):
+    import torch
+
+    import mixture_experts_layer_14_gb300 as mok
+    from mixture_experts_layer_14_gb300.synthetic import WORKLOADS
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks = load_peaks()
+    res, L = measure(args, shape, args.steps, args.warmup, dev, world, peaks)
+    D = mok.dims(shape.T, shape.d, shape.E, shape.k, shape.F, shape.F_shared, shape.n_shared)
+    e2e = None
+    if not args.no_e2e and not shape.backward:
+        e2e = run_e2e(args, mok, D, L, shape, dev, world)
+    line = {
+        "metric": "MoE-layer forward tokens/s" if not shape.backward else "MoE-layer fwd+bwd tokens/s",
+        "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/sqrt(fan_in)) bf16 weights, random init)",
+        "config": config_of(shape, world, res["active_experts"]),
+        "tflops": res["tflops"], "tflops_frac_of_bf16_peak": res["tflops_frac_of_bf16_peak"],
+        "roofline": res["roofline"], "kernels": res["kernels"], "gpu_launches": res["gpu_launches"],
+        "clocks": res["clocks"], "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(L, shape, budget_s=args.cpu_seconds)
+    del L
+    torch.cuda.empty_cache()
+    if not args.no_extra:
+        extra = {}
+        for name in args.extra.split(","):
+            if not name or name == shape.name:
+                continue
+            try:
+                r, Lx = measure(args, WORKLOADS[name], min(args.steps, args.extra_steps), 3, dev, world, peaks)
+                del Lx
+                torch.cuda.empty_cache()
+                r["metric"] = ("MoE-layer fwd+bwd tokens/s" if WORKLOADS[name].backward
+                               else "MoE-layer forward tokens/s")
+                r["kernels"] = {k2: v for k2, v in list(r["kernels"].items())[:6]}
+                extra[name] = r
+            except Exception as exc:  # report, do not hide the headline
+                extra[name] = {"error": repr(exc)[:300]}
+        line["workloads"] = extra
     return line
 
 
@@ -431,6 +482,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--extra", default="dsv3_bf16_train,kimi_skew_bf16_fwd")
+    ap.add_argument("--extra-steps", type=int, default=30)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

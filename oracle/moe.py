@@ -192,11 +192,9 @@ def moe_backward(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_exp
     E = Wr.shape[1]
     k = idx.shape[1]
     w = weights_for_selection(logits, idx)
-    F = Wg[0].shape[1]
     dX = np.zeros_like(x)
-    dWg = np.zeros((E, d, F))
-    dWu = np.zeros((E, d, F))
-    dWd = np.zeros((E, F, d))
+    # per-expert gradients; stacked into [E, ...] arrays unless only some experts are asked for
+    dWg, dWu, dWd = {}, {}, {}
     dw = np.zeros((T, k))
 
     def ffn_backward(X, dYr, wr, Wge, Wue, Wde):
@@ -236,6 +234,13 @@ def moe_backward(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_exp
     np.put_along_axis(dl, idx, w * (dw - inner), axis=1)
     dX += dl @ Wr.T
     dWr = x.T @ dl
+    if only_experts is None:
+        Wg0 = np.asarray(Wg[0])
+        zg = np.zeros(Wg0.shape)
+        zd = np.zeros(Wg0.shape[::-1])
+        dWg = np.stack([dWg.get(e, zg) for e in range(E)])
+        dWu = np.stack([dWu.get(e, zg) for e in range(E)])
+        dWd = np.stack([dWd.get(e, zd) for e in range(E)])
     return {
         "dX": dX, "dW_gate": dWg, "dW_up": dWu, "dW_down": dWd,
         "dWs_gate": None if dWs is None else dWs[0],
