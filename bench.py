@@ -155,6 +155,16 @@ def work_model(shape, counts):
         "bytes": wb * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Hs + Rs * d)}
     m["combine"] = {"flops": 0.0, "bytes": wb * (Rs * d + T * d) + 8.0 * R}
     layer_flops = T * (2.0 * d * E + (k * 6.0 * d * F) + ns * 6.0 * d * Fs)
+    if shape.dtype == "mxfp8":
+        wq = 1.0 + 1.0 / 32  # E4M3 byte + one UE8M0 byte per 32
+        m["mx_quantize"] = {"flops": 0.0, "bytes": T * d * (wb + wq)}
+        m["gather_bytes"] = {"flops": 0.0, "bytes": wq * (T * d + R * d) + 4.0 * R}
+        m["gemm_fwd_gate_up_mx"] = {
+            "flops": m["gemm_fwd_gate_up"]["flops"], "dtype": "fp8",
+            "bytes": wq * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + Rs * d + Hs)}
+        m["gemm_fwd_down_mx"] = {
+            "flops": m["gemm_fwd_down"]["flops"], "dtype": "fp8",
+            "bytes": wq * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Hs) + wb * Rs * d}
     if train:
         m["gather2"] = {"flops": 0.0, "bytes": 2.0 * wb * (T * d + R * d) + 4.0 * R}
         m["gemm_bwd_da"] = {  # a = dY Wd^T; reads G, U; writes dG, dU, w*h
@@ -194,14 +204,16 @@ def profiled_traffic(name, weight_sets):
 
 def roofline_of(name, model, ms_per_launch, peaks):
     w = model[name]
-    t_flop = w["flops"] / (peaks["bf16_tflops"] * 1e12) if w["flops"] else 0.0
+    # an FP8 contraction takes the measured bf16 peak times the nominal fp8/bf16 ratio (2)
+    tpeak = peaks["bf16_tflops"] * (2.0 if w.get("dtype") == "fp8" else 1.0)
+    t_flop = w["flops"] / (tpeak * 1e12) if w["flops"] else 0.0
     t_byte = w["bytes"] / (peaks["hbm_gbs"] * 1e9)
     secs = ms_per_launch / 1e3
     if t_flop > t_byte:
         achieved = w["flops"] / secs / 1e12
-        return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "algorithmic_per_launch": w["flops"]}
+        return {"bound": "tensor", "achieved": achieved, "peak": tpeak,
+                "unit": "TFLOP/s", "frac": achieved / tpeak, "algorithmic_per_launch": w["flops"],
+                "peak_dtype": w.get("dtype", "bf16")}
     achieved = w["bytes"] / secs / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "algorithmic_per_launch": w["bytes"]}
@@ -279,7 +291,11 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
 
     if L is None:
         L = make_layer(shape, dev, with_dy=shape.backward)
-    D = mok.dims(shape.T, shape.d, shape.E, shape.k, shape.F, shape.F_shared, shape.n_shared)
+    mx = shape.dtype == "mxfp8"
+    D = mok.dims(shape.T, shape.d, shape.E, shape.k, shape.F, shape.F_shared, shape.n_shared,
+                 mok.MOK_MXFP8 if mx else mok.MOK_BF16)
+    if mx:  # weights are quantised once, outside the timed region
+        L["prepared"] = mok.prepare_weights(D, L)
     layer = mok.MoELayer(D, L, dev)
     x = L["x"]
     torch.cuda.synchronize()
@@ -337,11 +353,14 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
                  "peak_source": "measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
                  else "fallback"})
     tflops = layer_flops * steps / (ms / 1e3) / 1e12
+    tpeak = peaks["bf16_tflops"] * (2.0 if mx else 1.0)
     out = {
         "value": round(world * shape.T * steps / (ms_max / 1e3), 1),
         "ms_per_step": round(ms_max / steps, 4),
         "tflops": round(tflops, 2),
         "tflops_frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
+        "tflops_frac_of_dtype_peak": round(tflops / tpeak, 4),
+        "dtype": "mxfp8 (e4m3 + ue8m0/32)" if mx else "bf16",
         "roofline": {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in roof.items()},
         "kernels": kernels, "gpu_launches": launches, "clocks": clocks,
         "active_experts": e_act, "max_expert_rows": max(counts), "empty_experts": counts.count(0),
@@ -483,7 +502,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
-    ap.add_argument("--extra", default="dsv3_bf16_train,kimi_skew_bf16_fwd")
+    ap.add_argument("--extra", default="dsv3_bf16_train,kimi_skew_bf16_fwd,dsv3_mxfp8_fwd")
     ap.add_argument("--extra-steps", type=int, default=30)
     args = ap.parse_args(argv)
     if args.warmup < 3:

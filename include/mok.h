@@ -98,9 +98,23 @@ size_t mok_saved_size(const mok_dims *dims);
 size_t mok_prepared_size(const mok_dims *dims);
 
 /* MXFP8: quantise the routed and shared expert weights once into `prepared` (E4M3 values and
- * UE8M0 scales, blocks of 32 along each weight's reduction dimension).  No-op for MOK_BF16. */
+ * UE8M0 scales, blocks of 32 along each weight's reduction dimension, same rule as
+ * mok_mx_quantize_rows), transposed to K-major, in this order (each region 1 KB aligned):
+ * W_gate codes [E][F][d], scales [E][F][d/32]; W_up likewise; W_down codes [E][d][F], scales
+ * [E][d][F/32]; then the shared expert's three the same way.  No-op for MOK_BF16.
+ * MXFP8 needs d % 256 == 0 and is forward only (mok_moe_backward returns MOK_ERR_UNSUPPORTED). */
 int mok_prepare_weights(const mok_dims *dims, const mok_weights *w, void *prepared,
                         mok_stream_t stream);
+
+/* MXFP8 quantiser of activations: src[rows,K] bf16 -> q[rows,K] E4M3 codes and
+ * scales[rows,K/32] UE8M0 bytes, one block per 32 consecutive elements of a row: scale 2^s with
+ * s the smallest integer such that amax <= 448 * 2^s (amax / 448 rounded up to a power of two),
+ * s in [-127,127] (an all-zero block gets 0x00), codes = round-to-nearest-even E4M3 of v * 2^-s
+ * with saturation to +-448.  K % 128 == 0.  The MXFP8 format of the layer (page
+ * "Mixture-of-Kittens; MoE megakernel", key points); the scale rule as read for the MXFP8
+ * workload of the layer. */
+int mok_mx_quantize_rows(int64_t rows, int K, const void *src, void *q, void *scales,
+                         mok_stream_t stream);
 
 /* Router: logits = x W_router + bias in fp32 (bf16 tensor-core products, fp32 accumulation),
  * top-k by (logit descending, index ascending), weights = softmax over all experts

@@ -31,6 +31,7 @@ EXPORTED_SYMBOLS = [
     "mok_layer_host_extra_size", "mok_layer_forward_host", "mok_status_string",
     "mok_read_device_status", "mok_clear_device_status", "mok_last_launch_count",
     "mok_timing_enable", "mok_timing_collect", "mok_dispatch_index_noalloc",
+    "mok_mx_quantize_rows",
 ]
 
 
@@ -85,6 +86,7 @@ def lib():
             "mok_clear_device_status": (ctypes.c_int, [_VP, _VP]),
             "mok_last_launch_count": (ctypes.c_int, []),
             "mok_timing_enable": (ctypes.c_int, [ctypes.c_int]),
+            "mok_mx_quantize_rows": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int, _VP, _VP, _VP, _VP]),
             "mok_dispatch_index_noalloc": (ctypes.c_int, [_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
             "mok_timing_collect": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int),
                                                   ctypes.POINTER(ctypes.c_double), ctypes.c_int,
@@ -239,6 +241,36 @@ def dispatch_index_noalloc(D, topk_idx, topk_w, out):
         ctypes.byref(D), _ptr(topk_idx), _ptr(topk_w), _ptr(out["counts"]), _ptr(out["offsets"]),
         _ptr(out["sorted_tok"]), _ptr(out["sorted_w"]), _ptr(out["inv_pos"]), _stream()))
     return out
+
+
+def mx_quantize_rows(src):
+    """MXFP8 quantisation of a [rows, K] bf16 CUDA tensor along K: (codes uint8 [rows, K],
+    UE8M0 scale bytes uint8 [rows, K/32])."""
+    if src.dtype != torch.bfloat16 or not src.is_cuda or not src.is_contiguous() or src.dim() != 2:
+        raise ValueError("src must be a contiguous 2-D bf16 CUDA tensor")
+    rows, K = src.shape
+    q = torch.empty((rows, K), dtype=torch.uint8, device=src.device)
+    sc = torch.empty((rows, K // 32), dtype=torch.uint8, device=src.device)
+    _check(lib().mok_mx_quantize_rows(rows, K, _ptr(src), _ptr(q), _ptr(sc), _stream()))
+    return q, sc
+
+
+def prepared_size(D):
+    return lib().mok_prepared_size(ctypes.byref(D))
+
+
+def prepare_weights(D, W):
+    """MXFP8: quantised, K-major copy of the expert weights (uint8 CUDA tensor); returns None for
+    bf16.  Pass it as W["prepared"]."""
+    n = prepared_size(D)
+    if n == 0:
+        return None
+    buf = torch.empty(n, dtype=torch.uint8, device=W["W_gate"].device)
+    Wd = dict(W)
+    Wd["prepared"] = None
+    st = _weights_struct(D, Wd)
+    _check(lib().mok_prepare_weights(ctypes.byref(D), ctypes.byref(st), _ptr(buf), _stream()))
+    return buf
 
 
 def moe_forward(D, W, x, routing, ws, saved=None, y=None):

@@ -39,33 +39,35 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor of `rank` dims (innermost first), 128-byte swizzle, zero fill out of bounds.
+// bf16 (esize 2) or byte (esize 1) tensor of `rank` dims (innermost first), 128-byte swizzle,
+// zero fill out of bounds.
 static bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
-                     const uint64_t* strides_bytes, const uint32_t* box) {
+                     const uint64_t* strides_bytes, const uint32_t* box, int esize = 2) {
   auto fn = encode_fn();
   if (!fn) return false;
   const uint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims,
+  CUresult r = fn(m, esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  rank, const_cast<void*>(ptr), dims,
                   strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
-// 2D row-major [rows, cols] bf16, box {bc, br}
+// 2D row-major [rows, cols], box {bc, br}
 static bool map2d(CUtensorMap* m, const void* p, uint64_t rows, uint64_t cols, uint32_t bc,
-                  uint32_t br) {
+                  uint32_t br, int esize = 2) {
   const uint64_t dims[2] = {cols, rows};
-  const uint64_t str[1] = {cols * 2};
+  const uint64_t str[1] = {cols * esize};
   const uint32_t box[2] = {bc, br};
-  return make_map(m, p, 2, dims, str, box);
+  return make_map(m, p, 2, dims, str, box, esize);
 }
-// 3D row-major [n, rows, cols] bf16, box {bc, br, 1}
+// 3D row-major [n, rows, cols], box {bc, br, 1}
 static bool map3d(CUtensorMap* m, const void* p, uint64_t n, uint64_t rows, uint64_t cols,
-                  uint32_t bc, uint32_t br) {
+                  uint32_t bc, uint32_t br, int esize = 2) {
   const uint64_t dims[3] = {cols, rows, n};
-  const uint64_t str[2] = {cols * 2, rows * cols * 2};
+  const uint64_t str[2] = {cols * esize, rows * cols * esize};
   const uint32_t box[3] = {bc, br, 1};
-  return make_map(m, p, 3, dims, str, box);
+  return make_map(m, p, 3, dims, str, box, esize);
 }
 
 // ------------------------------------------------------------------ checks and layouts
@@ -80,7 +82,7 @@ static int check_dims(const mok_dims* d) {
   if (d->n_shared == 1 && (d->F_shared <= 0 || d->F_shared % 128)) return MOK_ERR_UNSUPPORTED;
   if (d->k < 1 || d->k > kMaxK || d->E < d->k || d->E > kMaxE || d->E % 8) return MOK_ERR_UNSUPPORTED;
   if (d->dtype != MOK_BF16 && d->dtype != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
-  if (d->dtype == MOK_MXFP8) return MOK_ERR_UNSUPPORTED;
+  if (d->dtype == MOK_MXFP8 && d->d % 256) return MOK_ERR_UNSUPPORTED;  // 256-wide down tiles
   return MOK_OK;
 }
 
@@ -90,7 +92,14 @@ struct Layout {
 };
 static size_t al(size_t x) { return (x + 1023) & ~size_t(1023); }
 
-enum FwdSlot { FW_STATUS, FW_HIST, FW_XS, FW_H, FW_HSH, FW_YS, FW_YSH, FW_N };
+enum FwdSlot {
+  FW_STATUS, FW_HIST, FW_XS, FW_H, FW_HSH, FW_YS, FW_YSH,
+  // MXFP8 only: E4M3 codes and UE8M0 scale rows of x, x_sorted, h, h_sh
+  FW_XQ, FW_XSC, FW_XQS, FW_XSCS, FW_HQ, FW_HSC, FW_HQSH, FW_HSCSH, FW_N
+};
+enum PrepSlot {  // MXFP8 prepared weights: K-major codes [n][N][K] and scales [n][N][K/32]
+  PR_GQ, PR_GS, PR_UQ, PR_US, PR_DQ, PR_DS, PR_SGQ, PR_SGS, PR_SUQ, PR_SUS, PR_SDQ, PR_SDS, PR_N
+};
 enum BwdSlot {
   BW_STATUS, BW_XS, BW_DYS, BW_DG, BW_DU, BW_HW, BW_DGSH, BW_DUSH, BW_HWSH, BW_P, BW_DL,
   BW_DXS, BW_DXSH, BW_N
@@ -112,6 +121,19 @@ static Layout layout_fwd(const mok_dims* d) {
   sz[FW_HSH] = 2ull * T * Fs;
   sz[FW_YS] = 2ull * R * d->d;
   sz[FW_YSH] = 2ull * T * d->d * d->n_shared;
+  if (d->dtype == MOK_MXFP8) {
+    sz[FW_XS] = 0;
+    sz[FW_H] = 0;
+    sz[FW_HSH] = 0;
+    sz[FW_XQ] = 1ull * T * d->d;
+    sz[FW_XSC] = 1ull * T * d->d / 32;
+    sz[FW_XQS] = 1ull * R * d->d;
+    sz[FW_XSCS] = 1ull * R * d->d / 32;
+    sz[FW_HQ] = 1ull * R * d->F;
+    sz[FW_HSC] = 1ull * R * d->F / 32;
+    sz[FW_HQSH] = 1ull * T * Fs;
+    sz[FW_HSCSH] = 1ull * T * Fs / 32;
+  }
   Layout L{};
   size_t o = 0;
   for (int i = 0; i < FW_N; ++i) { L.off[i] = o; o += al(sz[i]); }
@@ -139,6 +161,17 @@ static Layout layout_bwd(const mok_dims* d) {
   Layout L{};
   size_t o = 0;
   for (int i = 0; i < BW_N; ++i) { L.off[i] = o; o += al(sz[i]); }
+  L.total = o;
+  return L;
+}
+
+static Layout layout_prepared(const mok_dims* d) {
+  const uint64_t E = d->E, dd = d->d, F = d->F, Fs = d->n_shared ? d->F_shared : 0;
+  size_t sz[PR_N] = {E * F * dd, E * F * dd / 32, E * F * dd, E * F * dd / 32, E * dd * F, E * dd * F / 32,
+                     Fs * dd, Fs * dd / 32, Fs * dd, Fs * dd / 32, dd * Fs, dd * Fs / 32};
+  Layout L{};
+  size_t o = 0;
+  for (int i = 0; i < PR_N; ++i) { L.off[i] = o; o += al(sz[i]); }
   L.total = o;
   return L;
 }
@@ -192,7 +225,7 @@ size_t mok_saved_size(const mok_dims* dims) {
 
 size_t mok_prepared_size(const mok_dims* dims) {
   if (check_dims(dims) != MOK_OK) return 0;
-  return 0;
+  return dims->dtype == MOK_MXFP8 ? layout_prepared(dims).total : 0;
 }
 
 size_t mok_layer_host_extra_size(const mok_dims* dims) {
@@ -202,13 +235,40 @@ size_t mok_layer_host_extra_size(const mok_dims* dims) {
 
 int mok_prepare_weights(const mok_dims* dims, const mok_weights* w, void* prepared,
                         mok_stream_t stream) {
-  (void)prepared;
-  (void)stream;
   int rc = check_dims(dims);
   if (rc != MOK_OK) return rc;
   if (!w) return MOK_ERR_INVALID_ARG;
   g_last_launches = 0;
+  if (dims->dtype != MOK_MXFP8) return MOK_OK;
+  if (!prepared || !w->W_gate || !w->W_up || !w->W_down) return MOK_ERR_INVALID_ARG;
+  if (dims->n_shared && (!w->Ws_gate || !w->Ws_up || !w->Ws_down)) return MOK_ERR_INVALID_ARG;
+  if (!aligned16(prepared)) return MOK_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Layout P = layout_prepared(dims);
+  const int d = dims->d, F = dims->F, Fs = dims->F_shared, E = dims->E;
+  auto q = [&](int i) { return static_cast<char*>(prepared) + P.off[i]; };
+  // gate/up [E][d][F] -> [E][F][d] (K = d); down [E][F][d] -> [E][d][F] (K = F)
+  cudaError_t e = launch_mx_quantize_transpose(w->W_gate, E, d, F, q(PR_GQ), q(PR_GS), s);
+  if (e == cudaSuccess) e = launch_mx_quantize_transpose(w->W_up, E, d, F, q(PR_UQ), q(PR_US), s);
+  if (e == cudaSuccess) e = launch_mx_quantize_transpose(w->W_down, E, F, d, q(PR_DQ), q(PR_DS), s);
+  if (dims->n_shared) {
+    if (e == cudaSuccess) e = launch_mx_quantize_transpose(w->Ws_gate, 1, d, Fs, q(PR_SGQ), q(PR_SGS), s);
+    if (e == cudaSuccess) e = launch_mx_quantize_transpose(w->Ws_up, 1, d, Fs, q(PR_SUQ), q(PR_SUS), s);
+    if (e == cudaSuccess) e = launch_mx_quantize_transpose(w->Ws_down, 1, Fs, d, q(PR_SDQ), q(PR_SDS), s);
+  }
+  if (e != cudaSuccess) return MOK_ERR_CUDA;
+  g_last_launches = dims->n_shared ? 6 : 3;
   return MOK_OK;
+}
+
+int mok_mx_quantize_rows(int64_t rows, int K, const void* src, void* q, void* scales,
+                         mok_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 128) return MOK_ERR_UNSUPPORTED;
+  if (rows > 0 && (!src || !q || !scales)) return MOK_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(q) || !aligned16(scales)) return MOK_ERR_UNSUPPORTED;
+  g_last_launches = rows > 0 ? 1 : 0;
+  return cuda_status(
+      launch_mx_quantize_rows(src, rows, K, q, scales, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 const char* mok_status_string(int s) {
@@ -320,9 +380,117 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
   void* Ysh = at<void*>(ws, L.off[FW_YSH]);
   const Layout S = layout_saved(dims);
   int launches = 0;
+  const int grid_cap0 = num_sms();
+
+  if (dims->dtype == MOK_MXFP8) {
+    // MXFP8 path: x quantised once (E4M3 + UE8M0 per 32 along d), its codes and scale rows
+    // pulled into expert order, block-scaled gate/up GEMM whose epilogue quantises h along F,
+    // block-scaled down GEMM with the router weight, and the same bf16 combine.
+    if (!w->prepared || !aligned16(w->prepared)) return MOK_ERR_INVALID_ARG;
+    if (saved) return MOK_ERR_UNSUPPORTED;  // the MXFP8 path is forward only
+    const Layout P = layout_prepared(dims);
+    auto pw = [&](int i) { return static_cast<const char*>(w->prepared) + P.off[i]; };
+    void* xq = at<void*>(ws, L.off[FW_XQ]);
+    uint8_t* xsc = at<uint8_t*>(ws, L.off[FW_XSC]);
+    void* xqs = at<void*>(ws, L.off[FW_XQS]);
+    uint8_t* xscs = at<uint8_t*>(ws, L.off[FW_XSCS]);
+    void* hq = at<void*>(ws, L.off[FW_HQ]);
+    uint8_t* hsc = at<uint8_t*>(ws, L.off[FW_HSC]);
+    void* hqsh = at<void*>(ws, L.off[FW_HQSH]);
+    uint8_t* hscsh = at<uint8_t*>(ws, L.off[FW_HSCSH]);
+    rc = cuda_status(launch_mx_quantize_rows(x, T, d, xq, xsc, s));
+    if (rc == MOK_OK) rc = cuda_status(launch_gather_bytes(xq, sorted_tok, R, T, d, xqs, s));
+    if (rc == MOK_OK) rc = cuda_status(launch_gather_bytes(xsc, sorted_tok, R, T, d / 32, xscs, s));
+    if (rc != MOK_OK) return rc;
+    launches += 3;
+    {
+      GemmParams p{};
+      bool ok = true;
+      if (sh) {
+        ok &= map2d(&p.maps[MS_A0], xq, T, d, 128, 128, 1);
+        ok &= map3d(&p.maps[MS_B0], pw(PR_SGQ), 1, Fs, d, 128, 128, 1);
+        ok &= map3d(&p.maps[MS_B1], pw(PR_SUQ), 1, Fs, d, 128, 128, 1);
+      }
+      ok &= map2d(&p.maps[MS_A3], xqs, R, d, 128, 128, 1);
+      ok &= map3d(&p.maps[MS_B3], pw(PR_GQ), E, F, d, 128, 128, 1);
+      ok &= map3d(&p.maps[MS_B4], pw(PR_UQ), E, F, d, 128, 128, 1);
+      if (!ok) return MOK_ERR_CUDA;
+      p.offsets = offsets;
+      p.E = E;
+      p.has_shared = sh;
+      p.T = (int)T;
+      p.d = d;
+      p.F = F;
+      p.Fs = Fs;
+      p.nt[0] = Fs / 128;
+      p.nt[1] = F / 128;
+      p.out0[0] = hqsh;
+      p.out1[0] = hscsh;
+      p.out0[1] = hq;
+      p.out1[1] = hsc;
+      p.sfa[0] = xsc;
+      p.sfa_rows[0] = T;
+      p.sfa[1] = xscs;
+      p.sfa_rows[1] = R;
+      p.sfb[0][0] = reinterpret_cast<const uint8_t*>(pw(PR_SGS));
+      p.sfb[0][1] = reinterpret_cast<const uint8_t*>(pw(PR_SUS));
+      p.sfb[1][0] = reinterpret_cast<const uint8_t*>(pw(PR_GS));
+      p.sfb[1][1] = reinterpret_cast<const uint8_t*>(pw(PR_US));
+      p.sfb_estride[0] = 0;
+      p.sfb_estride[1] = (int64_t)F * (d / 32);
+      p.sf_ld[0] = p.sf_ld[1] = d / 32;
+      p.status = static_cast<int*>(ws);
+      const int64_t bound = (sh ? (T + BM - 1) / BM * p.nt[0] : 0) + ((R + BM - 1) / BM + E) * p.nt[1];
+      rc = cuda_status(launch_gemm(G_FWD_GU_MX, 256, p, (int)std::min<int64_t>(grid_cap0, bound), s));
+      if (rc != MOK_OK) return rc;
+      ++launches;
+    }
+    {
+      GemmParams p{};
+      bool ok = true;
+      if (sh) {
+        ok &= map2d(&p.maps[MS_A0], hqsh, T, Fs, 128, 128, 1);
+        ok &= map3d(&p.maps[MS_B0], pw(PR_SDQ), 1, d, Fs, 128, 256, 1);
+      }
+      ok &= map2d(&p.maps[MS_A3], hq, R, F, 128, 128, 1);
+      ok &= map3d(&p.maps[MS_B3], pw(PR_DQ), E, d, F, 128, 256, 1);
+      if (!ok) return MOK_ERR_CUDA;
+      p.offsets = offsets;
+      p.E = E;
+      p.has_shared = sh;
+      p.T = (int)T;
+      p.d = d;
+      p.F = F;
+      p.Fs = Fs;
+      p.nt[0] = d / 256;
+      p.nt[1] = d / 256;
+      p.out0[0] = Ysh;
+      p.out0[1] = Ys;
+      p.row_w = sorted_w;
+      p.sfa[0] = hscsh;
+      p.sfa_rows[0] = T;
+      p.sfa[1] = hsc;
+      p.sfa_rows[1] = R;
+      p.sfb[0][0] = reinterpret_cast<const uint8_t*>(pw(PR_SDS));
+      p.sfb[1][0] = reinterpret_cast<const uint8_t*>(pw(PR_DS));
+      p.sfb_estride[0] = 0;
+      p.sfb_estride[1] = (int64_t)d * (F / 32);
+      p.sf_ld[0] = Fs / 32;
+      p.sf_ld[1] = F / 32;
+      p.status = static_cast<int*>(ws);
+      const int64_t bound = (sh ? (T + BM - 1) / BM * p.nt[0] : 0) + ((R + BM - 1) / BM + E) * p.nt[1];
+      rc = cuda_status(launch_gemm(G_FWD_DOWN_MX, 256, p, (int)std::min<int64_t>(grid_cap0, bound), s));
+      if (rc != MOK_OK) return rc;
+      ++launches;
+    }
+    rc = cuda_status(launch_combine(T, d, dims->k, topk_idx, inv_pos, Ys, sh ? Ysh : nullptr, y, s));
+    if (rc != MOK_OK) return rc;
+    g_last_launches = launches + 1;
+    return MOK_OK;
+  }
 
   // 1. pull-gather of every expert's token rows
-  rc = cuda_status(launch_gather_rows(x, sorted_tok, R, d, xs, s));
+  rc = cuda_status(launch_gather_rows(x, sorted_tok, R, T, d, xs, s));
   if (rc != MOK_OK) return rc;
   ++launches;
 
@@ -416,6 +584,7 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
                       !sorted_w || !inv_pos || !dX || !dlogits))
     return MOK_ERR_INVALID_ARG;
   if (!w->W_router || !w->W_gate || !w->W_up || !w->W_down) return MOK_ERR_INVALID_ARG;
+  if (dims->dtype == MOK_MXFP8) return MOK_ERR_UNSUPPORTED;  // MXFP8 is forward only
   const bool sh = dims->n_shared == 1;
   if (sh && (!w->Ws_gate || !w->Ws_up || !w->Ws_down || !dWs_gate || !dWs_up || !dWs_down))
     return MOK_ERR_INVALID_ARG;
@@ -459,7 +628,7 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
   const int grid_cap = num_sms();
 
   // 1. gather x and dY rows into each expert's region
-  rc = cuda_status(launch_gather_rows2(x, dY, sorted_tok, R, d, xs, dys, s));
+  rc = cuda_status(launch_gather_rows2(x, dY, sorted_tok, R, T, d, xs, dys, s));
   if (rc != MOK_OK) return rc;
   ++launches;
   // 2. a = dY W_down^T; epilogue: dG, dU, w*h and the router partials <a, h>
@@ -561,9 +730,18 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
     ok &= map2d(&p.maps[MS_B3], dG, R, F, 64, 64);
     ok &= map2d(&p.maps[MS_B4], dU, R, F, 64, 64);
     ok &= map2d(&p.maps[MS_B5], dys, R, d, 64, 64);
+    if (sh) {
+      ok &= map3d(&p.omaps[OM_G0], dWs_gate, 1, d, Fs, 64, 32);
+      ok &= map3d(&p.omaps[OM_U0], dWs_up, 1, d, Fs, 64, 32);
+      ok &= map3d(&p.omaps[OM_D0], dWs_down, 1, Fs, d, 64, 32);
+    }
+    ok &= map3d(&p.omaps[OM_G1], dW_gate, E, d, F, 64, 32);
+    ok &= map3d(&p.omaps[OM_U1], dW_up, E, d, F, 64, 32);
+    ok &= map3d(&p.omaps[OM_D1], dW_down, E, F, d, 64, 32);
     if (dW_router) {
       ok &= map2d(&p.maps[MS_R_A], x, T, d, 64, 64);
       ok &= map2d(&p.maps[MS_R_B], dl, T, ldl, 64, 64);
+      ok &= map3d(&p.omaps[OM_R], dW_router, 1, d, E, 64, 32);
       p.router_tiles = (d / BM) * ((E + bn - 1) / bn);
       p.E_cols = E;
       p.out_router = dW_router;

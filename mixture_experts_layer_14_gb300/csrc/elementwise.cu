@@ -24,31 +24,73 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(
   for (int64_t r = wglobal; r < nrows; r += nwarps) {
     const int64_t t = rows[r];
     const bool ok = (t >= 0 && t < nsrc);
-    const uint4* s0 = src0 + t * vec_per_row;
     uint4* d0 = dst0 + r * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) d0[v] = ok ? s0[v] : make_uint4(0, 0, 0, 0);
+    uint4* d1 = src1 ? dst1 + r * vec_per_row : nullptr;
+    if (!ok) {
+      for (int v = lane; v < vec_per_row; v += 32) {
+        d0[v] = make_uint4(0, 0, 0, 0);
+        if (d1) d1[v] = make_uint4(0, 0, 0, 0);
+      }
+      continue;
+    }
+    const uint4* s0 = src0 + t * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) d0[v] = s0[v];
     if (src1) {
       const uint4* s1 = src1 + t * vec_per_row;
-      uint4* d1 = dst1 + r * vec_per_row;
-      for (int v = lane; v < vec_per_row; v += 32) d1[v] = ok ? s1[v] : make_uint4(0, 0, 0, 0);
+      for (int v = lane; v < vec_per_row; v += 32) d1[v] = s1[v];
     }
   }
 }
 
-cudaError_t launch_gather_rows(const void* src, const int32_t* rows, int64_t nrows, int d,
-                               void* dst, cudaStream_t s) {
-  return launch_gather_rows2(src, nullptr, rows, nrows, d, dst, nullptr, s);
+cudaError_t launch_gather_rows(const void* src, const int32_t* rows, int64_t nrows, int64_t nsrc,
+                               int d, void* dst, cudaStream_t s) {
+  return launch_gather_rows2(src, nullptr, rows, nrows, nsrc, d, dst, nullptr, s);
 }
 
 cudaError_t launch_gather_rows2(const void* src0, const void* src1, const int32_t* rows,
-                                int64_t nrows, int d, void* dst0, void* dst1, cudaStream_t s) {
+                                int64_t nrows, int64_t nsrc, int d, void* dst0, void* dst1,
+                                cudaStream_t s) {
   if (nrows == 0) return cudaSuccess;
-  // the number of source rows is not needed for addressing; bound the check by INT32 range of
-  // the token ids written by the dispatch (tokens are < T <= 2^31)
   prof_begin(src1 ? "gather2" : "gather", s);
   gather_rows_kernel<<<rows_grid(nrows), kRowThreads, 0, s>>>(
-      static_cast<const uint4*>(src0), static_cast<const uint4*>(src1), rows, nrows,
-      (int64_t)0x7fffffff, d / 8, static_cast<uint4*>(dst0), static_cast<uint4*>(dst1));
+      static_cast<const uint4*>(src0), static_cast<const uint4*>(src1), rows, nrows, nsrc, d / 8,
+      static_cast<uint4*>(dst0), static_cast<uint4*>(dst1));
+  prof_end(s);
+  return cudaGetLastError();
+}
+
+// Byte rows (row_bytes a multiple of 4): dst[r] = src[rows[r]] — the pull gather of E4M3 rows
+// and of their UE8M0 scale rows in the MXFP8 path.
+__global__ void __launch_bounds__(kRowThreads) gather_bytes_kernel(
+    const uint32_t* __restrict__ src, const int32_t* __restrict__ rows, int64_t nrows, int64_t nsrc,
+    int words, uint32_t* __restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wglobal = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = wglobal; r < nrows; r += nwarps) {
+    const int64_t t = rows[r];
+    uint32_t* d = dst + r * words;
+    if (t < 0 || t >= nsrc) {
+      for (int v = lane; v < words; v += 32) d[v] = 0u;
+      continue;
+    }
+    const uint32_t* s = src + t * words;
+    if ((words & 3) == 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(s);
+      uint4* d4 = reinterpret_cast<uint4*>(d);
+      for (int v = lane; v < words / 4; v += 32) d4[v] = s4[v];
+    } else {
+      for (int v = lane; v < words; v += 32) d[v] = s[v];
+    }
+  }
+}
+
+cudaError_t launch_gather_bytes(const void* src, const int32_t* rows, int64_t nrows, int64_t nsrc,
+                                int row_bytes, void* dst, cudaStream_t s) {
+  if (nrows == 0) return cudaSuccess;
+  prof_begin("gather_bytes", s);
+  gather_bytes_kernel<<<rows_grid(nrows), kRowThreads, 0, s>>>(
+      static_cast<const uint32_t*>(src), rows, nrows, nsrc, row_bytes / 4, static_cast<uint32_t*>(dst));
   prof_end(s);
   return cudaGetLastError();
 }

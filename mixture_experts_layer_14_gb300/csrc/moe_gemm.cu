@@ -13,7 +13,7 @@
 // blocks pulled straight from it).  CTA c takes tiles c, c+grid, c+2*grid, ...  Every output
 // element is produced by exactly one CTA with a fixed K order, so results are bit-identical
 // from run to run.  No host synchronisation: the tile count is read on the device.
-#include "mok_device.cuh"
+#include "mok_mx.cuh"
 
 namespace mok {
 
@@ -30,14 +30,23 @@ struct Tile {
 
 template <int MODE, int BN>
 struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  // every stage row is 128 bytes: 64 bf16 or 128 E4M3 elements of K
+  static constexpr bool MX = (MODE == G_FWD_GU_MX || MODE == G_FWD_DOWN_MX);
+  static constexpr int KE = MX ? 128 : BK;            // K elements per stage
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int SF_BYTES = MX ? (BM + BN) * 4 : 0;  // UE8M0 atoms of A and B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+  // G_BWD_DW: the output tile is staged in shared memory (32 rows x BN per epilogue warp) and
+  // written with TMA tile stores; its K loops are short, so fewer stages suffice.
+  static constexpr int STAGING_BYTES = (MODE == G_BWD_DW) ? 4 * 32 * BN * 2 : 0;
+  static constexpr int STAGES = (MODE == G_BWD_DW) ? ((BN == 256) ? 3 : 5) : ((BN == 256) ? 4 : 6);
   static constexpr bool A_MN = (MODE == G_BWD_DW);
   static constexpr bool B_MN = (MODE == G_FWD_GU || MODE == G_FWD_DOWN || MODE == G_BWD_DW);
-  static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr uint32_t IDESC = make_idesc_bf16(BN, A_MN, B_MN);
+  static constexpr int NUM_ACC = MX ? 1 : 2;           // MXFP8: TMEM also holds scale factors
+  static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
+  static constexpr int SF_TMEM_COL = 256;              // MXFP8: 16 columns per stage from here
+  static constexpr uint32_t IDESC = MX ? make_idesc_mxf8(BN) : make_idesc_bf16(BN, A_MN, B_MN);
   static constexpr bool K_GROUPED = (MODE == G_BWD_DW);
 };
 
@@ -46,7 +55,8 @@ constexpr int kSchedBytes = 2 * (kMaxE + 1) * 4;     // expert row offsets + M-t
 
 template <int MODE, int BN>
 constexpr int smem_bytes_for() {
-  return Cfg<MODE, BN>::STAGES * Cfg<MODE, BN>::STAGE_BYTES + kAuxBytes + kSchedBytes + 1024;
+  return Cfg<MODE, BN>::STAGES * Cfg<MODE, BN>::STAGE_BYTES + Cfg<MODE, BN>::STAGING_BYTES +
+         kAuxBytes + kSchedBytes + 1024;
 }
 
 int gemm_smem_bytes(int bn, int /*E*/) {
@@ -91,6 +101,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
     int nkb;
     if constexpr (MODE == G_FWD_GU || MODE == G_BWD_DA) nkb = p.d / BK;
     else if constexpr (MODE == G_FWD_DOWN) nkb = (t.g ? p.F : p.Fs) / BK;
+    else if constexpr (MODE == G_FWD_GU_MX) nkb = p.d / 128;
+    else if constexpr (MODE == G_FWD_DOWN_MX) nkb = (t.g ? p.F : p.Fs) / 128;
     else nkb = p.segkb[t.g][0] + p.segkb[t.g][1] + p.segkb[t.g][2];
     t.nkb = nkb;
   } else {
@@ -183,6 +195,14 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, 
     const CUtensorMap* b = &M[t.g ? MS_B3 : MS_B0];
 #pragma unroll
     for (int i = 0; i < BN / 64; ++i) tma_load_3d(sB + i * 8192, b, bar, t.n * BN + 64 * i, kb * BK, t.e);
+  } else if constexpr (MODE == G_FWD_GU_MX) {
+    // E4M3 operands, both K-major: A = x rows, B = 128 gate rows then 128 up rows
+    tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * 128, t.row0);
+    tma_load_3d(sB, &M[t.g ? MS_B3 : MS_B0], bar, kb * 128, t.n * 128, t.e);
+    tma_load_3d(sB + 16384, &M[t.g ? MS_B4 : MS_B1], bar, kb * 128, t.n * 128, t.e);
+  } else if constexpr (MODE == G_FWD_DOWN_MX) {
+    tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * 128, t.row0);
+    tma_load_3d(sB, &M[t.g ? MS_B3 : MS_B0], bar, kb * 128, t.n * BN, t.e);
   } else if constexpr (MODE == G_BWD_DA) {
     tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
     tma_load_3d(sB, &M[t.g ? MS_B3 : MS_B0], bar, kb * BK, t.n * BN, t.e);
@@ -220,6 +240,56 @@ __device__ __forceinline__ void ld_row64(const void* src, uint32_t (&v)[16]) {
   }
 }
 
+// G_BWD_DW epilogue: the warp's 32 rows x BN columns go to its staging buffer in the 128-byte
+// swizzled layout of the store map (64-column boxes of 32 rows x 128 B; the 16-byte chunk j of
+// row r sits at chunk j ^ (r % 8)), then one lane issues the TMA tile stores.
+template <int BN>
+__device__ __forceinline__ void epilogue_dw_tma(const GemmParams& p, const Tile& t, uint32_t tacc,
+                                                uint32_t stg, int q, int lane) {
+  if (lane == 0) bulk_wait_read0();  // the previous tile's stores have read the staging buffer
+  __syncwarp();
+  const bool zero = (t.nkb == 0);    // an expert without tokens: its gradient is zero
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 64) {  // one 64-column box: two TMEM loads, one wait
+    uint32_t v[2][32];
+    if (!zero) {
+      tmem_ld32(tacc + c, v[0]);
+      tmem_ld32(tacc + c + 32, v[1]);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[0][i] = v[1][i] = 0u;
+    }
+    const uint32_t box = stg + (c / 64) * 4096 + lane * 128;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t* w = &v[i >> 2][8 * (i & 3)];
+      const uint32_t a = pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1]));
+      const uint32_t b = pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3]));
+      const uint32_t cc = pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5]));
+      const uint32_t d = pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7]));
+      const uint32_t addr = box + ((i ^ (lane & 7)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(cc),
+                   "r"(d)
+                   : "memory");
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    int om, e = 0;
+    if (t.g == 2) om = OM_R;
+    else {
+      om = (t.g ? OM_G1 : OM_G0) + t.sub;
+      e = t.e;
+    }
+#pragma unroll 1
+    for (int b = 0; b < BN / 64; ++b)
+      tma_store_3d(&p.omaps[om], stg + b * 4096, t.n * BN + 64 * b, t.m0 + 32 * q, e);
+    bulk_commit();
+  }
+}
+
 template <int MODE, int BN>
 __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uint32_t tacc,
                                          int r) {
@@ -252,11 +322,37 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
         if (U) st_row64(U + c, up);
       }
     }
-  } else if constexpr (MODE == G_FWD_DOWN || MODE == G_BWD_DX) {
+  } else if constexpr (MODE == G_FWD_GU_MX) {
+    // h = SiLU(g) * u quantised per 32 columns: E4M3 codes [rows][F] + UE8M0 bytes [rows][F/32]
+    const bool valid = r < t.rows;
+    const int ld = t.g ? p.F : p.Fs;
+    const int64_t row = t.row0 + r;
+    uint8_t* hq = static_cast<uint8_t*>(p.out0[t.g]) + row * ld + t.n * 128;
+    uint8_t* hs = static_cast<uint8_t*>(p.out1[t.g]) + row * (ld / 32) + t.n * 4;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      uint32_t gr[32], ur[32];
+      tmem_ld32(tacc + c, gr);
+      tmem_ld32(tacc + 128 + c, ur);
+      tmem_ld_wait();
+      if (valid) {
+        float hv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          hv[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+        uint32_t qq[8];
+        const uint32_t sb = mx_block32(hv, qq);
+        uint4* d = reinterpret_cast<uint4*>(hq + c);
+        d[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+        d[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+        hs[c / 32] = (uint8_t)sb;
+      }
+    }
+  } else if constexpr (MODE == G_FWD_DOWN || MODE == G_BWD_DX || MODE == G_FWD_DOWN_MX) {
     const bool valid = r < t.rows;
     const int64_t row = t.row0 + r;
     float s = 1.0f;
-    if (MODE == G_FWD_DOWN && t.g == 1 && valid) s = p.row_w[row];
+    if (MODE != G_BWD_DX && t.g == 1 && valid) s = p.row_w[row];
     bf16* o = static_cast<bf16*>(p.out0[t.g]) + row * p.d + t.n * BN;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
@@ -364,13 +460,49 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
   }
 }
 
+// ------------------------------------------------------------------ MXFP8 scale factors
+// Writes the stage's UE8M0 scale factors into shared memory in the layout tcgen05.cp
+// (32x128b, replicated to the four lane quarters) moves into TMEM: a 512-byte atom per 128 rows
+// in which row r = r0 + 32*r1 (r0 < 32, r1 < 4) keeps its four K-block scales (K elements
+// kb*128 + 32*j, j = 0..3, byte j) at offset 16*r0 + 4*r1.  Scale rows are row-major [rows][K/32]
+// in global memory, so the four bytes of a row are one aligned 32-bit word.
+template <int MODE, int BN>
+__device__ __forceinline__ void fill_scale_factors(const GemmParams& p, const Tile& t, int kb,
+                                                   uint32_t sf, int lane) {
+  const int ld = p.sf_ld[t.g];
+  // A: tile rows r = lane + 32 j (rows past the tensor end become zeros)
+  const uint8_t* sa = p.sfa[t.g];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int64_t gr = (int64_t)t.row0 + lane + 32 * j;
+    const bool in = gr < p.sfa_rows[t.g];
+    cp_async4(sf + 16 * lane + 4 * j, in ? sa + gr * ld + kb * 4 : sa, in ? 4u : 0u);
+  }
+  // B: tile rows n = lane + 32 j, atom n / 128
+#pragma unroll
+  for (int j = 0; j < BN / 32; ++j) {
+    const int n = lane + 32 * j;
+    const uint8_t* sb;
+    int64_t brow;
+    if constexpr (MODE == G_FWD_GU_MX) {  // 128 gate rows then 128 up rows of the h tile
+      sb = p.sfb[t.g][n >> 7];
+      brow = (int64_t)t.n * 128 + (n & 127);
+    } else {
+      sb = p.sfb[t.g][0];
+      brow = (int64_t)t.n * BN + n;
+    }
+    cp_async4(sf + 512 + 512 * (j >> 2) + 16 * lane + 4 * (j & 3),
+              sb + (int64_t)t.e * p.sfb_estride[t.g] + brow * ld + kb * 4, 4u);
+  }
+}
+
 // ------------------------------------------------------------------ K-tail masking
 // G_BWD_DW: the last k-block of a problem may hold rows of the next expert; zero them in both
 // operands (MN-major: K is the row index inside every 64-column box, 128 B per row, and the
 // 128-byte swizzle only permutes 16-byte chunks within a row).
 template <int BN>
 __device__ __forceinline__ void zero_k_tail(uint32_t sA, uint32_t sB, int valid, int lane) {
-  const int nrows = BK - valid;
+  const int nrows = ((valid + 15) & ~15) - valid;  // only the MMA K steps that are issued
   const int nboxes = 2 + BN / 64;
   const int per_box = nrows * 8;  // 16-byte chunks
   for (int i = lane; i < nboxes * per_box; i += 32) {
@@ -393,8 +525,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA0 = base;
   const uint32_t sB0 = base + C::STAGES * C::A_BYTES;
-  uint8_t* aux = gbase + C::STAGES * C::STAGE_BYTES;
-  const uint32_t aux_s = base + C::STAGES * C::STAGE_BYTES;
+  const uint32_t sSF0 = sB0 + C::STAGES * C::B_BYTES;  // MXFP8 scale-factor atoms
+  const uint32_t sSTG0 = sSF0 + C::STAGES * C::SF_BYTES;  // G_BWD_DW output staging
+  uint8_t* aux = gbase + C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES;
+  const uint32_t aux_s = base + C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES;
   // aux layout: full[S] empty[S] tfull[2] tempty[2] drain | tmem addr | abort
   const uint32_t bar_full = aux_s;
   const uint32_t bar_empty = aux_s + 8 * C::STAGES;
@@ -410,7 +544,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
 
   if (tid == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      // MXFP8: the TMA arrival plus one cp.async arrival per producer lane (scale factors)
+      mbar_init(bar_full + 8 * s, C::MX ? 33 : 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -466,7 +601,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   const uint32_t tmem_base = *s_tmem;
   const int ntiles = total_tiles<MODE, BN>(p, s_mt);
 
-  if (warp == 0) {
+  if (warp == 0 && C::MX) {
+    // MXFP8 producer: lane 0 issues the TMA loads, then every lane copies its share of the
+    // stage's scale-factor atoms with cp.async and arrives on the stage barrier when they land;
+    // the producer never waits for a scale load.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool run = true;
+    for (int tile = blockIdx.x; run && tile < ntiles && !*s_abort; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort) ? 1 : 0;
+          if (ok) {
+            mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_BYTES + C::B_BYTES);
+            issue_loads<MODE, BN>(p, t, kb, sA0 + stage * C::A_BYTES, sB0 + stage * C::B_BYTES,
+                                  bar_full + 8 * stage);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { run = false; break; }
+        fill_scale_factors<MODE, BN>(p, t, kb, sSF0 + stage * C::SF_BYTES, lane);
+        cp_async_arrive_noinc(bar_full + 8 * stage);
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -474,7 +635,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) break;
-          mbar_arrive_expect_tx(bar_full + 8 * stage, C::STAGE_BYTES);
+          mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_BYTES + C::B_BYTES);
           issue_loads<MODE, BN>(p, t, kb, sA0 + stage * C::A_BYTES, sB0 + stage * C::B_BYTES,
                                 bar_full + 8 * stage);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -487,8 +648,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x, ++it) {
       const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
-      const int buf = it & 1;
-      const uint32_t tph = (it >> 1) & 1;
+      const int buf = it % C::NUM_ACC;
+      const uint32_t tph = (it / C::NUM_ACC) & 1;
       if (!mbar_wait(bar_tempty + 8 * buf, tph ^ 1, p.status, s_abort)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
@@ -497,22 +658,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         if (!mbar_wait(bar_full + 8 * stage, phase, p.status, s_abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sA = sA0 + stage * C::A_BYTES, sB = sB0 + stage * C::B_BYTES;
+        int nk16 = BK / 16;  // MMA K steps of this stage
         if constexpr (C::K_GROUPED) {
+          // last k-block of a problem: issue only the K steps holding rows of this problem and
+          // zero the rows of the next problem inside the last step
           const int valid = t.rows - kb * BK;
           if (valid < BK) {
-            zero_k_tail<BN>(sA, sB, valid, lane);
-            fence_proxy_async_smem();
-            __syncwarp();
+            nk16 = (valid + 15) / 16;
+            if (valid & 15) {
+              zero_k_tail<BN>(sA, sB, valid, lane);
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
           }
         }
         if (lane == 0) {
+          if constexpr (C::MX) {
+            // scale factors of this stage: smem atoms -> TMEM (16 columns per stage), then four
+            // K = 32 block-scaled MMAs; MMA j reads byte j of each 32-bit scale word.
+            const uint32_t sf = sSF0 + stage * C::SF_BYTES;
+            // the scale atoms were written by cp.async (generic proxy); tcgen05.cp reads them
+            // through the async proxy
+            fence_proxy_async_smem();
+            const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL + 16 * stage;
+            const uint32_t sfb_t = sfa_t + 4;
+            tmem_cp_32x128b_x4(sfa_t, make_sdesc_noswz(sf, 16, 128));
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = C::A_MN ? make_sdesc(sA + k * 2048, 8192, 1024)
-                                        : make_sdesc(sA + k * 32, 16, 1024);
-            const uint64_t bd = C::B_MN ? make_sdesc(sB + k * 2048, 8192, 1024)
-                                        : make_sdesc(sB + k * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
+            for (int a = 0; a < BN / 128; ++a)
+              tmem_cp_32x128b_x4(sfb_t + 4 * a, make_sdesc_noswz(sf + 512 + 512 * a, 16, 128));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = make_sdesc(sA + k * 32, 16, 1024);
+              const uint64_t bd = make_sdesc(sB + k * 32, 16, 1024);
+              const uint32_t idesc = C::IDESC | (static_cast<uint32_t>(k) << 29) |
+                                     (static_cast<uint32_t>(k) << 4);
+              umma_mxf8(d_tmem, ad, bd, idesc, sfa_t, sfb_t, (kb | k) != 0);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              if (k < nk16) {
+                const uint64_t ad = C::A_MN ? make_sdesc(sA + k * 2048, 8192, 1024)
+                                            : make_sdesc(sA + k * 32, 16, 1024);
+                const uint64_t bd = C::B_MN ? make_sdesc(sB + k * 2048, 8192, 1024)
+                                            : make_sdesc(sB + k * 32, 16, 1024);
+                umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
+              }
+            }
           }
           umma_commit(bar_empty + 8 * stage);
         }
@@ -536,14 +728,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x, ++it) {
       const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
-      const int buf = it & 1;
-      const uint32_t tph = (it >> 1) & 1;
+      const int buf = it % C::NUM_ACC;
+      const uint32_t tph = (it / C::NUM_ACC) & 1;
       if (!mbar_wait(bar_tfull + 8 * buf, tph, p.status, s_abort)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
-      epilogue<MODE, BN>(p, t, tacc, r);
+      if constexpr (MODE == G_BWD_DW)
+        epilogue_dw_tma<BN>(p, t, tacc, sSTG0 + q * (32 * BN * 2), q, lane);
+      else
+        epilogue<MODE, BN>(p, t, tacc, r);
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * buf);
+    }
+    if constexpr (MODE == G_BWD_DW) {
+      if (lane == 0) bulk_wait0();  // every tile store of this warp has completed
+      __syncwarp();
     }
   }
   __syncthreads();
@@ -560,7 +759,7 @@ static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   static const char* kNames[] = {"gemm_fwd_gate_up", "gemm_fwd_down", "gemm_bwd_da", "gemm_bwd_dx",
-                                 "gemm_bwd_dw"};
+                                 "gemm_bwd_dw", "gemm_fwd_gate_up_mx", "gemm_fwd_down_mx"};
   prof_begin(kNames[MODE], s);
   k<<<grid, kGemmThreads, smem, s>>>(p);
   prof_end(s);
@@ -578,6 +777,8 @@ cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStr
       return bn == 256 ? launch_one<G_BWD_DX, 256>(p, grid, s) : launch_one<G_BWD_DX, 128>(p, grid, s);
     case G_BWD_DW:
       return bn == 256 ? launch_one<G_BWD_DW, 256>(p, grid, s) : launch_one<G_BWD_DW, 128>(p, grid, s);
+    case G_FWD_GU_MX: return launch_one<G_FWD_GU_MX, 256>(p, grid, s);
+    case G_FWD_DOWN_MX: return launch_one<G_FWD_DOWN_MX, 256>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

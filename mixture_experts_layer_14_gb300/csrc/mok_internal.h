@@ -24,6 +24,8 @@ enum GemmMode : int {
   G_BWD_DA = 2,    // a = dY Wd^T -> dG, dU, w*h, <a,h>    M-grouped, A K-major, B K-major
   G_BWD_DX = 3,    // dX = dG Wg^T + dU Wu^T (+ dl Wr^T)   M-grouped, A K-major, B K-major
   G_BWD_DW = 4,    // dW = X^T dG, X^T dU, (w h)^T dY, x^T dl  K-grouped, A and B MN-major
+  G_FWD_GU_MX = 5,   // MXFP8 gate/up: h quantised to E4M3 + UE8M0 in the epilogue
+  G_FWD_DOWN_MX = 6, // MXFP8 down: Y = w * (h Wd), bf16 out
 };
 
 // Tensor-map slots.  Group 0 is the shared expert (rows = tokens), group 1 the routed experts
@@ -38,8 +40,12 @@ enum MapSlot : int {
   MS_COUNT = 14
 };
 
+// Store maps of the weight-gradient GEMM (TMA tile stores of the dW tiles).
+enum OutSlot : int { OM_R = 0, OM_G0, OM_U0, OM_D0, OM_G1, OM_U1, OM_D1, OM_COUNT };
+
 struct GemmParams {
   CUtensorMap maps[MS_COUNT];
+  CUtensorMap omaps[OM_COUNT];  // G_BWD_DW outputs: box {64 cols, 32 rows}, 128-byte swizzle
   const int* offsets;   // routed row offsets [E+1] (device), NULL when E == 0
   int E;                // routed experts in this launch (0 = none)
   int has_shared;       // group 0 present
@@ -59,6 +65,12 @@ struct GemmParams {
   const void* in1[2];   // U (saved)
   const float* row_w;   // router weight of each routed row (sorted_w)
   float* partial;       // G_BWD_DA: <a,h> per (routed row, N tile), [R, nt[1]]
+  // MXFP8 scale factors (UE8M0 bytes, row-major [rows][K/32]); [group]
+  const uint8_t* sfa[2];       // A rows (x / x_sorted or h_sh / h)
+  int64_t sfa_rows[2];         // rows of the A scale tensor (bounds)
+  const uint8_t* sfb[2][2];    // B rows per expert: [group][gate/up or down]
+  int64_t sfb_estride[2];      // bytes between experts
+  int sf_ld[2];                // bytes per scale row (= K/32)
   int* status;
 };
 
@@ -86,10 +98,12 @@ cudaError_t launch_dispatch(int64_t T, int E, int k, const int32_t* topk_idx, co
                             cudaStream_t s, int* launches);
 
 // Elementwise (elementwise.cu)
-cudaError_t launch_gather_rows(const void* src, const int32_t* rows, int64_t nrows, int d,
-                               void* dst, cudaStream_t s);
+// Row gathers: dst[r] = src[rows[r]] for r < nrows; an index outside [0, nsrc) gives a zero row.
+cudaError_t launch_gather_rows(const void* src, const int32_t* rows, int64_t nrows, int64_t nsrc,
+                               int d, void* dst, cudaStream_t s);
 cudaError_t launch_gather_rows2(const void* src0, const void* src1, const int32_t* rows,
-                                int64_t nrows, int d, void* dst0, void* dst1, cudaStream_t s);
+                                int64_t nrows, int64_t nsrc, int d, void* dst0, void* dst1,
+                                cudaStream_t s);
 cudaError_t launch_combine(int64_t T, int d, int k, const int32_t* topk_idx,
                            const int32_t* inv_pos, const void* Ys, const void* Ysh, void* y,
                            cudaStream_t s);
@@ -99,6 +113,14 @@ cudaError_t launch_router_backward(int64_t T, int E, int k, int ldp, const int32
                                    cudaStream_t s);
 
 int num_sms();
+
+// MXFP8 quantisation (mx.cu)
+cudaError_t launch_mx_quantize_rows(const void* src, int64_t rows, int K, void* q, void* sc,
+                                    cudaStream_t s);
+cudaError_t launch_mx_quantize_transpose(const void* src, int64_t nmat, int K, int N, void* q,
+                                         void* sc, cudaStream_t s);
+cudaError_t launch_gather_bytes(const void* src, const int32_t* rows, int64_t nrows, int64_t nsrc,
+                                int row_bytes, void* dst, cudaStream_t s);
 
 // Optional per-launch CUDA-event timing (profile.cu); no-ops unless enabled on this thread.
 void prof_begin(const char* name, cudaStream_t s);

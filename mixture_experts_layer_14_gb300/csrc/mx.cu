@@ -1,0 +1,97 @@
+// MXFP8 block quantisation (the MXFP8 path of the layer; page "Mixture-of-Kittens; MoE
+// megakernel", key points: BF16 and MXFP8).  Format: E4M3 values with one UE8M0 power-of-two
+// scale per 32 contiguous elements along the reduction dimension; the scale of a block is 2^s
+// with s the smallest integer such that amax <= 448 * 2^s (amax / 448 rounded up to a power of
+// two), s in [-127, 127], an all-zero block takes s = -127.  Values are multiplied by 2^-s
+// (exact) and converted with cvt.rn.satfinite (round to nearest even, saturate to +-448).
+#include "mok_mx.cuh"
+
+namespace mok {
+
+// rows x K bf16 (row-major) -> codes [rows][K] and scale bytes [rows][K/32].  One warp per row,
+// one 32-element block per lane per iteration.
+__global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const __nv_bfloat16* __restrict__ src,
+                                                               int64_t rows, int K,
+                                                               uint8_t* __restrict__ q,
+                                                               uint8_t* __restrict__ sc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int nblk = K / 32;
+  for (int64_t r = w; r < rows; r += nw) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + r * K);
+    uint4* q4 = reinterpret_cast<uint4*>(q + r * K);
+    for (int b = lane; b < nblk; b += 32) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = s4[b * 4 + i];
+        const uint32_t x[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * i + 2 * j] = bf16_lo(x[j]);
+          v[8 * i + 2 * j + 1] = bf16_hi(x[j]);
+        }
+      }
+      uint32_t qq[8];
+      const uint32_t sb = mx_block32(v, qq);
+      q4[b * 2] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+      q4[b * 2 + 1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+      sc[r * nblk + b] = (uint8_t)sb;
+    }
+  }
+}
+
+// Weights: src [n][K][N] bf16 (row-major, the layer's x @ W layout) -> codes [n][N][K] (K-major,
+// the operand layout of the block-scaled MMA) and scales [n][N][K/32].  One thread per
+// (matrix, column, K block): 32 strided reads (coalesced across the warp), 32 contiguous bytes out.
+__global__ void __launch_bounds__(256) mx_quantize_transpose_kernel(
+    const __nv_bfloat16* __restrict__ src, int64_t nmat, int K, int N, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ sc) {
+  const int nblk = K / 32;
+  const int64_t total = nmat * (int64_t)nblk * N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int col = (int)(i % N);
+    const int64_t rest = i / N;
+    const int kb = (int)(rest % nblk);
+    const int64_t m = rest / nblk;
+    const __nv_bfloat16* s = src + (m * K + (int64_t)kb * 32) * N + col;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(s[(int64_t)j * N]);
+    uint32_t qq[8];
+    const uint32_t sb = mx_block32(v, qq);
+    uint4* d = reinterpret_cast<uint4*>(q + (m * N + col) * (int64_t)K + (int64_t)kb * 32);
+    d[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+    d[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+    sc[(m * N + col) * (int64_t)nblk + kb] = (uint8_t)sb;
+  }
+}
+
+cudaError_t launch_mx_quantize_rows(const void* src, int64_t rows, int K, void* q, void* sc,
+                                    cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 8);
+  prof_begin("mx_quantize", s);
+  mx_quantize_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows,
+                                                      K, static_cast<uint8_t*>(q),
+                                                      static_cast<uint8_t*>(sc));
+  prof_end(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quantize_transpose(const void* src, int64_t nmat, int K, int N, void* q,
+                                         void* sc, cudaStream_t s) {
+  const int64_t total = nmat * (int64_t)(K / 32) * N;
+  if (total == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 16);
+  prof_begin("mx_quantize_weights", s);
+  mx_quantize_transpose_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src),
+                                                           nmat, K, N, static_cast<uint8_t*>(q),
+                                                           static_cast<uint8_t*>(sc));
+  prof_end(s);
+  return cudaGetLastError();
+}
+
+}  // namespace mok

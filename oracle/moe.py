@@ -248,3 +248,47 @@ def moe_backward(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_exp
         "dWs_down": None if dWs is None else dWs[2],
         "dlogits": dl, "dW_router": dWr, "dw": dw,
     }
+
+
+# --------------------------------------------------------------------------------------
+# MXFP8 reading of the forward (page "Mixture-of-Kittens; MoE megakernel", key points: the kernel
+# supports BF16 and MXFP8).  x, every expert weight (blocks of 32 along its reduction
+# dimension) and h (along F) pass through E4M3/UE8M0 quantise-dequantise; the router, the
+# weighting and the combine stay in full precision; products and sums are float64.
+# --------------------------------------------------------------------------------------
+
+def _mx_qd(a):
+    from .mxfp8 import mx_dequantize, mx_quantize
+
+    q, sc = mx_quantize(a)
+    return mx_dequantize(q, sc)
+
+
+def _mx_weight(W):
+    """[K, N] weight quantised along K (its reduction dimension), returned as [K, N]."""
+    return _mx_qd(np.asarray(W, dtype=np.float64).T).T
+
+
+def moe_forward_mxfp8(x, Wg, Wu, Wd, shared, topk_idx, topk_w):
+    """Layer output with the MXFP8 quantisation points of the path.  A composition of the
+    pinned quantiser and FFN pieces; pinned further by: values exactly representable in MXFP8
+    are fixed points of the quantiser, zero down weights give a zero output, and the distance to
+    moe_forward on random data stays within a few E4M3 steps."""
+    x = np.asarray(x, dtype=np.float64)
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    w = np.asarray(topk_w, dtype=np.float64)
+    xq = _mx_qd(x)
+
+    def ffn(X, Wg_e, Wu_e, Wd_e):
+        g = X @ _mx_weight(Wg_e)
+        u = X @ _mx_weight(Wu_e)
+        h = _mx_qd(silu(g) * u)
+        return h @ _mx_weight(Wd_e)
+
+    y = np.zeros_like(x)
+    if shared is not None:
+        y += ffn(xq, *shared)
+    for e in _experts_used(idx):
+        rows, slots = np.nonzero(idx == e)
+        np.add.at(y, rows, w[rows, slots][:, None] * ffn(xq[rows], Wg[e], Wu[e], Wd[e]))
+    return y

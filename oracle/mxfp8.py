@@ -30,23 +30,28 @@ def e4m3_decode(codes):
     return np.where(s == 1, -mag, mag)
 
 
-_POS_CODES = np.arange(0, 127, dtype=np.uint8)          # 0x00 .. 0x7E: all finite positives
-_POS_VALS = e4m3_decode(_POS_CODES)                      # strictly increasing
-
-
 def e4m3_encode(v):
-    """Nearest E4M3 code of each float64 value (ties to even mantissa, saturating to +-448,
-    NaN -> 0x7F with the sign bit of the input)."""
+    """Nearest E4M3 code of each float64 value: round to nearest with ties to an even mantissa,
+    saturating to +-448 (NaN -> 0x7F with the sign bit of the input).
+
+    The E4M3 grid in the binade [2^(e-1), 2^e) has 8 steps of 2^(e-4) for e-1 >= -6 and steps of
+    2^-9 below 2^-6 (subnormals); the value is divided by its step (exact power of two), rounded
+    to an integer with ties to even (np.rint), and multiplied back.  An even step count is an even
+    mantissa, so ties go to the even code."""
     v = np.asarray(v, dtype=np.float64)
-    a = np.minimum(np.abs(v), E4M3_MAX)
-    hi = np.clip(np.searchsorted(_POS_VALS, a, side="left"), 0, 126)   # first value >= a
-    lo = np.clip(hi - 1, 0, 126)
-    dlo = a - _POS_VALS[lo]
-    dhi = _POS_VALS[hi] - a
-    pick_hi = (dhi < dlo) | ((dhi == dlo) & ((_POS_CODES[hi] & 1) == 0))
-    code = np.where(pick_hi, _POS_CODES[hi], _POS_CODES[lo]).astype(np.uint8)
-    code = np.where(a == _POS_VALS[hi], _POS_CODES[hi], code).astype(np.uint8)
-    code = np.where(np.isnan(v), np.uint8(0x7F), code).astype(np.uint8)
+    nan = np.isnan(v)
+    a = np.where(nan, 0.0, np.minimum(np.abs(v), E4M3_MAX))
+    _, e = np.frexp(a)                                   # a = m 2^e, m in [0.5, 1)
+    step = np.maximum(e - 1, -6) - 3                     # exponent of the grid step
+    q = np.rint(np.ldexp(a, -step))                      # steps, ties to even
+    val = np.ldexp(q, step)                              # the rounded magnitude (exact)
+    # fields of the rounded magnitude
+    m2, e2 = np.frexp(val)
+    normal = val >= 2.0 ** -6
+    E = np.where(normal, e2 + 6, 0)
+    M = np.where(normal, np.rint((2.0 * m2 - 1.0) * 8.0), np.rint(np.ldexp(val, 9)))
+    code = (E.astype(np.int64) << 3) | M.astype(np.int64)
+    code = np.where(nan, 0x7F, code).astype(np.uint8)
     return np.where(np.signbit(v), code | np.uint8(0x80), code).astype(np.uint8)
 
 
@@ -74,10 +79,13 @@ def mx_quantize(v):
     return q.reshape(v.shape), (s + 127).astype(np.uint8)
 
 
+_DECODE_TABLE = e4m3_decode(np.arange(256, dtype=np.uint8))  # the 256 code values, once
+
+
 def mx_dequantize(codes, scale_bytes):
     """codes[..., K] * 2^(scale_byte - 127) per block of 32, float64."""
     c = np.asarray(codes, dtype=np.uint8)
     K = c.shape[-1]
-    vals = e4m3_decode(c).reshape(c.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
+    vals = _DECODE_TABLE[c].reshape(c.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
     s = np.asarray(scale_bytes, dtype=np.int64) - 127
     return np.ldexp(vals, s[..., None]).reshape(c.shape)

@@ -83,3 +83,33 @@ def test_quantize_block_layout_and_error_bound():
             err = np.abs(deq[r, 32 * b:32 * b + 32] - blk)
             spacing = np.maximum(2.0 ** (np.floor(np.log2(np.maximum(np.abs(blk) / 2.0 ** s, 2.0 ** -6))) - 3), 2.0 ** -9)
             assert (err <= 0.5 * spacing * 2.0 ** s * (1 + 1e-12)).all()
+
+
+def _representable(rng, shape):
+    """Values exactly representable in MXFP8 blocks: small integers times a power of two."""
+    return rng.integers(-7, 8, size=shape).astype(np.float64) * 2.0 ** rng.integers(-3, 1)
+
+
+def test_mxfp8_forward_pins():
+    rng = np.random.default_rng(3)
+    T, d, E, k, F = 6, 64, 3, 2, 32
+    x = _representable(rng, (T, d))
+    Wg = np.stack([_representable(rng, (d, F)) * 0.125 for _ in range(E)])
+    Wu = np.stack([_representable(rng, (d, F)) * 0.125 for _ in range(E)])
+    Wd = np.zeros((E, F, d))
+    idx = np.array([[0, 1], [1, 2], [2, 0], [0, 2], [1, 0], [2, 1]], dtype=np.int32)
+    w = rng.random((T, k))
+    # representable inputs are not changed by the quantiser, so with a zero W_down only the
+    # shared expert remains; its gate/up products equal the float64 ones
+    sh = (_representable(rng, (d, F)) * 0.125, _representable(rng, (d, F)) * 0.125, np.zeros((F, d)))
+    assert (oracle.moe_forward_mxfp8(x, Wg, Wu, Wd, sh, idx, w) == 0).all()
+    assert (oracle.mx_dequantize(*oracle.mx_quantize(x)) == x).all()
+    # with random data the MXFP8 output stays within a few E4M3 steps of the float64 output
+    x = rng.standard_normal((T, d))
+    Wg, Wu = rng.standard_normal((E, d, F)) / 8, rng.standard_normal((E, d, F)) / 8
+    Wd = rng.standard_normal((E, F, d)) / 6
+    sh = (rng.standard_normal((d, F)) / 8, rng.standard_normal((d, F)) / 8, rng.standard_normal((F, d)) / 6)
+    y = oracle.moe_forward(x, Wg, Wu, Wd, sh, idx, w)
+    yq = oracle.moe_forward_mxfp8(x, Wg, Wu, Wd, sh, idx, w)
+    rel = np.abs(yq - y).max() / np.abs(y).max()
+    assert 1e-4 < rel < 0.1
