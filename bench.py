@@ -302,10 +302,10 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
 
     def step():
         layer.forward(x, training=shape.backward)
-        n = 1 + 3 + mok.last_launch_count()  # route, dispatch (3), expert forward
+        n = layer.last_launches  # router, dispatch and expert-forward kernels
         if shape.backward:
             layer.backward(x, L["dY"])
-            n += mok.last_launch_count()
+            n += layer.last_launches
         return n
 
     for _ in range(warmup):

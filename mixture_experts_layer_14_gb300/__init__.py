@@ -341,10 +341,13 @@ class MoELayer:
 
     def forward(self, x, training=False):
         idx, w, _ = route(self.D, x, self.W["W_router"], self.W.get("bias"), self.ws)
+        n = last_launch_count()
         routing = dispatch_index(self.D, idx, w, self.ws)
-        if training:
+        n += last_launch_count()
+        if training and self.saved is None:
             self.saved = torch.empty(saved_size(self.D), dtype=torch.uint8, device=x.device)
         y = moe_forward(self.D, self.W, x, routing, self.ws, saved=self.saved if training else None)
+        self.last_launches = n + last_launch_count()  # kernels this call enqueued
         self.routing = routing
         return y
 
@@ -352,4 +355,6 @@ class MoELayer:
         if self._ws_bwd is None:
             self._ws_bwd = torch.zeros(workspace_size(self.D, backward=True), dtype=torch.uint8,
                                        device=x.device)
-        return moe_backward(self.D, self.W, x, dY, self.saved, self.routing, self._ws_bwd)
+        g = moe_backward(self.D, self.W, x, dY, self.saved, self.routing, self._ws_bwd)
+        self.last_launches = last_launch_count()
+        return g

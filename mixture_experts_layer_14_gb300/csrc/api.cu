@@ -95,7 +95,9 @@ static size_t al(size_t x) { return (x + 1023) & ~size_t(1023); }
 enum FwdSlot {
   FW_STATUS, FW_HIST, FW_XS, FW_H, FW_HSH, FW_YS, FW_YSH,
   // MXFP8 only: E4M3 codes and UE8M0 scale rows of x, x_sorted, h, h_sh
-  FW_XQ, FW_XSC, FW_XQS, FW_XSCS, FW_HQ, FW_HSC, FW_HQSH, FW_HSCSH, FW_N
+  FW_XQ, FW_XSC, FW_XQS, FW_XSCS, FW_HQ, FW_HSC, FW_HQSH, FW_HSCSH,
+  FW_RPART,  // router: split-K partial logits
+  FW_N
 };
 enum PrepSlot {  // MXFP8 prepared weights: K-major codes [n][N][K] and scales [n][N][K/32]
   PR_GQ, PR_GS, PR_UQ, PR_US, PR_DQ, PR_DS, PR_SGQ, PR_SGS, PR_SUQ, PR_SUS, PR_SDQ, PR_SDS, PR_N
@@ -121,6 +123,7 @@ static Layout layout_fwd(const mok_dims* d) {
   sz[FW_HSH] = 2ull * T * Fs;
   sz[FW_YS] = 2ull * R * d->d;
   sz[FW_YSH] = 2ull * T * d->d * d->n_shared;
+  sz[FW_RPART] = 4ull * route_splits_bound(T, d->d) * T * d->E;
   if (d->dtype == MOK_MXFP8) {
     sz[FW_XS] = 0;
     sz[FW_H] = 0;
@@ -324,8 +327,11 @@ int mok_route(const mok_dims* dims, const void* x, const void* W_router, const f
   p.E = dims->E;
   p.k = dims->k;
   p.status = static_cast<int*>(ws);
+  const Layout L = layout_fwd(dims);
+  p.splits = std::min(route_splits(dims->T, dims->d), route_splits_bound(dims->T, dims->d));
+  p.partial = at<float*>(ws, L.off[FW_RPART]);
   rc = cuda_status(launch_route(p, reinterpret_cast<cudaStream_t>(stream)));
-  if (rc == MOK_OK) g_last_launches = 1;
+  if (rc == MOK_OK) g_last_launches = p.splits > 1 ? 2 : 1;
   return rc;
 }
 

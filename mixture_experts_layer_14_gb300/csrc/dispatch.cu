@@ -4,45 +4,59 @@
 // "Метод и эксперименты": each expert then pulls its own tokens, e.g. E2 <- [0,2,9,15]).
 //
 // Three launches, no atomics on global memory, no host synchronisation:
-//  1. histogram: block b counts, for every expert, the routes of tokens [64b, 64b+64);
+//  1. histogram: block b counts, for every expert, the routes of tokens [64b, 64b+64) (one
+//     thread per route; warp-level match gives per-warp counts);
 //  2. scan: one block turns the (expert, block) histogram, expert-major, into exclusive bases
 //     (in place), per-expert counts and region offsets;
-//  3. scatter: block b walks its routes in (token, slot) order and gives each route of expert
-//     e the next row of e's region, so tokens ascend inside every region.
+//  3. scatter: block b gives route i of expert e the row base(e, b) + (routes of e in earlier
+//     warps of the block) + (routes of e in lower lanes of its warp), i.e. routes keep their
+//     (token, slot) order inside every region, so tokens ascend.
 #include "mok_device.cuh"
 
 namespace mok {
 
-constexpr int kDispatchThreads = 256;
+constexpr int kMaxDispatchWarps = kDispatchChunk * kMaxK / 32;  // one thread per route
 
-__device__ __forceinline__ int load_chunk(const int32_t* idx, int64_t T, int E, int k, int b,
-                                          int* s_idx, int* status) {
+// Per-warp expert counts of a chunk's routes: thread i holds route i of the chunk (routes in
+// token-major order).  __match_any_sync groups the lanes of a warp that route to the same
+// expert; the lowest such lane writes the group size to s_cnt[warp][e], and every lane gets its
+// rank inside its group (the number of lower lanes with the same expert).  No atomics.
+__device__ __forceinline__ int warp_expert_rank(const int32_t* idx, int64_t T, int E, int k, int b,
+                                                int* s_cnt, int* status, int& e_out) {
   const int64_t t0 = (int64_t)b * kDispatchChunk;
   const int64_t rem = T - t0;
   const int ntok = (int)(rem < kDispatchChunk ? rem : kDispatchChunk);
   const int n = ntok * k;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    int e = idx[t0 * k + i];
+  const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
+  for (int j = i; j < kMaxDispatchWarps * E; j += blockDim.x) s_cnt[j] = 0;
+  __syncthreads();
+  int e = -1;
+  if (i < n) {
+    e = idx[t0 * k + i];
     if (e < 0 || e >= E) {
-      record_status(status, MOK_ERR_DEVICE_CHECK);
+      if (status) record_status(status, MOK_ERR_DEVICE_CHECK);
       e = -1;  // the route is dropped
     }
-    s_idx[i] = e;
   }
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (e >= 0 && rank == 0) s_cnt[warp * E + e] = __popc(peers);
   __syncthreads();
-  return n;
+  e_out = e;
+  return rank;
 }
 
-__global__ void __launch_bounds__(kDispatchThreads) dispatch_hist_kernel(
+__global__ void __launch_bounds__(kDispatchChunk * kMaxK) dispatch_hist_kernel(
     const int32_t* __restrict__ idx, int64_t T, int E, int k, int nblk, int32_t* __restrict__ hist,
     int* status) {
-  __shared__ int s_idx[kDispatchChunk * kMaxK];
-  const int b = blockIdx.x;
-  const int n = load_chunk(idx, T, E, k, b, s_idx, status);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int cnt = 0;
-    for (int i = 0; i < n; ++i) cnt += (s_idx[i] == e);
-    hist[(int64_t)e * nblk + b] = cnt;
+  __shared__ int s_cnt[kMaxDispatchWarps * kMaxE];
+  int e;
+  warp_expert_rank(idx, T, E, k, blockIdx.x, s_cnt, status, e);
+  const int nw = blockDim.x >> 5;
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < nw; ++w) c += s_cnt[w * E + x];
+    hist[(int64_t)x * nblk + blockIdx.x] = c;
   }
 }
 
@@ -95,29 +109,39 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict
   for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = offsets[e + 1] - offsets[e];
 }
 
-__global__ void __launch_bounds__(kDispatchThreads) dispatch_scatter_kernel(
+__global__ void __launch_bounds__(kDispatchChunk * kMaxK) dispatch_scatter_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ topk_w, int64_t T, int E, int k,
     int nblk, const int32_t* __restrict__ base, int32_t* __restrict__ sorted_tok,
-    float* __restrict__ sorted_w, int32_t* __restrict__ inv_pos, int* status) {
-  __shared__ int s_idx[kDispatchChunk * kMaxK];
-  const int b = blockIdx.x;
-  const int n = load_chunk(idx, T, E, k, b, s_idx, nullptr);
-  const int64_t r0 = (int64_t)b * kDispatchChunk * k;  // first route of the chunk
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int pos = base[(int64_t)e * nblk + b];
-    for (int i = 0; i < n; ++i) {
-      if (s_idx[i] == e) {
-        const int64_t r = r0 + i;
-        sorted_tok[pos] = (int32_t)(r / k);
-        sorted_w[pos] = topk_w[r];
-        inv_pos[r] = pos;
-        ++pos;
-      }
+    float* __restrict__ sorted_w, int32_t* __restrict__ inv_pos) {
+  __shared__ int s_cnt[kMaxDispatchWarps * kMaxE];
+  int e;
+  const int rank = warp_expert_rank(idx, T, E, k, blockIdx.x, s_cnt, nullptr, e);
+  // exclusive prefix over the warps of the block, per expert, on top of the chunk's base
+  const int nw = blockDim.x >> 5;
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    int run = base[(int64_t)x * nblk + blockIdx.x];
+    for (int w = 0; w < nw; ++w) {
+      const int c = s_cnt[w * E + x];
+      s_cnt[w * E + x] = run;
+      run += c;
     }
   }
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    if (s_idx[i] < 0) inv_pos[r0 + i] = -1;
-  (void)status;
+  __syncthreads();
+  const int64_t t0 = (int64_t)blockIdx.x * kDispatchChunk;
+  const int64_t rem = T - t0;
+  const int n = (int)(rem < kDispatchChunk ? rem : kDispatchChunk) * k;
+  const int i = threadIdx.x;
+  if (i < n) {
+    const int64_t r = t0 * k + i;
+    if (e >= 0) {
+      const int pos = s_cnt[(i >> 5) * E + e] + rank;
+      sorted_tok[pos] = (int32_t)(r / k);
+      sorted_w[pos] = topk_w[r];
+      inv_pos[r] = pos;
+    } else {
+      inv_pos[r] = -1;
+    }
+  }
 }
 
 cudaError_t launch_dispatch(int64_t T, int E, int k, const int32_t* topk_idx, const float* topk_w,
@@ -127,7 +151,7 @@ cudaError_t launch_dispatch(int64_t T, int E, int k, const int32_t* topk_idx, co
   const int nblk = (int)((T + kDispatchChunk - 1) / kDispatchChunk);
   if (nblk > 0) {
     prof_begin("dispatch_hist", s);
-    dispatch_hist_kernel<<<nblk, kDispatchThreads, 0, s>>>(topk_idx, T, E, k, nblk, hist, status);
+    dispatch_hist_kernel<<<nblk, kDispatchChunk * k, 0, s>>>(topk_idx, T, E, k, nblk, hist, status);
     prof_end(s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -140,8 +164,8 @@ cudaError_t launch_dispatch(int64_t T, int E, int k, const int32_t* topk_idx, co
   *launches += (nblk > 0) ? 2 : 1;
   if (nblk > 0) {
     prof_begin("dispatch_scatter", s);
-    dispatch_scatter_kernel<<<nblk, kDispatchThreads, 0, s>>>(topk_idx, topk_w, T, E, k, nblk, hist,
-                                                              sorted_tok, sorted_w, inv_pos, status);
+    dispatch_scatter_kernel<<<nblk, kDispatchChunk * k, 0, s>>>(topk_idx, topk_w, T, E, k, nblk,
+                                                                hist, sorted_tok, sorted_w, inv_pos);
     prof_end(s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -6,6 +6,7 @@
 namespace mok {
 
 constexpr int kRowThreads = 256;
+constexpr int kCombineSplit = 2;
 
 static int rows_grid(int64_t nrows) {
   const int64_t blocks = (nrows + (kRowThreads / 32) - 1) / (kRowThreads / 32);  // one warp per row
@@ -107,7 +108,13 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
   const int lane = threadIdx.x & 31;
   const int64_t wglobal = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t t = wglobal; t < T; t += nwarps) {
+  // kCombineSplit warps share a token row, each summing one contiguous part of it
+  for (int64_t wt = wglobal; wt < T * kCombineSplit; wt += nwarps) {
+    const int64_t t = wt / kCombineSplit;
+    const int part = (int)(wt % kCombineSplit);
+    const int per = (vec_per_row + kCombineSplit - 1) / kCombineSplit;
+    const int v_begin = part * per;
+    const int v_end = min(vec_per_row, v_begin + per);
     // order the token's routes by expert id (k <= 8, distinct experts)
     int pos[kMaxK];
     int ex[kMaxK];
@@ -128,7 +135,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
         pos[b] = sw ? p0 : p1;
       }
     }
-    for (int v = lane; v < vec_per_row; v += 32) {
+    for (int v = v_begin + lane; v < v_end; v += 32) {
       float acc[8];
       if (Ysh) {
         const uint4 q = Ysh[t * vec_per_row + v];
@@ -156,7 +163,7 @@ cudaError_t launch_combine(int64_t T, int d, int k, const int32_t* topk_idx, con
                            const void* Ys, const void* Ysh, void* y, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   prof_begin("combine", s);
-  combine_kernel<<<rows_grid(T), kRowThreads, 0, s>>>(T, d / 8, k, topk_idx, inv_pos,
+  combine_kernel<<<rows_grid(T * kCombineSplit), kRowThreads, 0, s>>>(T, d / 8, k, topk_idx, inv_pos,
                                                       static_cast<const uint4*>(Ys),
                                                       static_cast<const uint4*>(Ysh),
                                                       static_cast<uint4*>(y));

@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/mok.h"
+#include "mok.h"
 
 namespace mok {
 
@@ -87,8 +87,20 @@ struct RouteParams {
   float* topk_w;
   float* logits;
   int T, d, E, k;
+  int splits;          // K splits per 128-token tile (1 = top-k straight from TMEM)
+  float* partial;      // [splits][T][E] fp32 partial logits (splits > 1)
   int* status;
 };
+constexpr int kMaxRouteSplits = 8;
+int route_splits(int64_t T, int d);
+// Upper bound of route_splits on any GPU of up to 256 SMs (sizes the partial-logit workspace).
+inline int route_splits_bound(int64_t T, int d) {
+  const int64_t mt = (T + BM - 1) / BM;
+  int64_t b = (256 + mt - 1) / (mt > 0 ? mt : 1);
+  if (b > kMaxRouteSplits) b = kMaxRouteSplits;
+  if (b > d / BK) b = d / BK;
+  return b < 1 ? 1 : (int)b;
+}
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
 
 // Dispatch (dispatch.cu)

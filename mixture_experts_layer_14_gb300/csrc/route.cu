@@ -29,6 +29,31 @@ __device__ __forceinline__ void topk_insert(float (&tv)[kMaxK], int (&ti)[kMaxK]
   }
 }
 
+// w_j = softmax(l)[e_j] / sum_sel softmax(l)[e_i] = exp(l_j - l_0) / sum_i exp(l_i - l_0)
+__device__ __forceinline__ void write_route(const RouteParams& p, int t, const float (&tv)[kMaxK],
+                                            const int (&ti)[kMaxK]) {
+  float ex[kMaxK];
+  float den = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    ex[j] = (j < p.k) ? __expf(tv[j] - tv[0]) : 0.0f;
+    den += ex[j];
+  }
+  const float inv = 1.0f / den;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j < p.k) {
+      int e = ti[j];
+      if (e < 0) {  // only possible with NaN logits
+        record_status(p.status, MOK_ERR_DEVICE_CHECK);
+        e = 0;
+      }
+      p.topk_idx[(int64_t)t * p.k + j] = e;
+      p.topk_w[(int64_t)t * p.k + j] = ex[j] * inv;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_constant__ RouteParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -53,7 +78,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = blockIdx.x * BM;
-  const int nkb = p.d / BK;
+  const int nkb_all = p.d / BK;
+  const int kps = (nkb_all + p.splits - 1) / p.splits;  // k-blocks of this split
+  const int kb0 = blockIdx.y * kps;
+  const int nkb = max(0, min(nkb_all, kb0 + kps) - kb0);
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -81,9 +109,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) break;
         const uint32_t bar = bar_full + 8 * stage;
         mbar_arrive_expect_tx(bar, stage_bytes);
-        tma_load_2d(sA0 + stage * a_bytes, &p.map_x, bar, kb * BK, m0);
+        tma_load_2d(sA0 + stage * a_bytes, &p.map_x, bar, (kb0 + kb) * BK, m0);
         for (int i = 0; i < E_pad / 64; ++i)
-          tma_load_2d(sB0 + stage * b_bytes + i * 8192, &p.map_w, bar, 64 * i, kb * BK);
+          tma_load_2d(sB0 + stage * b_bytes + i * 8192, &p.map_w, bar, 64 * i, (kb0 + kb) * BK);
         if (++stage == stages) { stage = 0; phase ^= 1; }
       }
     }
@@ -121,12 +149,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
     const int t = m0 + r;
     const bool ok = mbar_wait(bar_acc, 0, p.status, s_abort);
     tc_fence_after();
-    if (ok) {
+    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    if (ok && p.splits == 1) {
       float tv[kMaxK];
       int ti[kMaxK];
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) { tv[j] = -INFINITY; ti[j] = -1; }
-      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       for (int c = 0; c < p.E; c += 32) {
         uint32_t v[32];
         tmem_ld32(tacc + c, v);
@@ -141,27 +169,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
           }
         }
       }
-      if (t < p.T) {
-        // w_j = softmax(l)[e_j] / sum_sel softmax(l)[e_i] = exp(l_j - l_0) / sum_i exp(l_i - l_0)
-        float ex[kMaxK];
-        float den = 0.0f;
+      if (t < p.T) write_route(p, t, tv, ti);
+    } else if (ok) {
+      // split K: store this split's partial logits; route_finish_kernel sums the splits
+      float* part = p.partial + ((int64_t)blockIdx.y * p.T + t) * p.E;
+      for (int c = 0; c < p.E; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tacc + c, v);
+        tmem_ld_wait();
+        if (t < p.T) {
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-          ex[j] = (j < p.k) ? __expf(tv[j] - tv[0]) : 0.0f;
-          den += ex[j];
-        }
-        const float inv = 1.0f / den;
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-          if (j < p.k) {
-            int e = ti[j];
-            if (e < 0) {  // only possible with NaN logits
-              record_status(p.status, MOK_ERR_DEVICE_CHECK);
-              e = 0;
-            }
-            p.topk_idx[(int64_t)t * p.k + j] = e;
-            p.topk_w[(int64_t)t * p.k + j] = ex[j] * inv;
-          }
+          for (int i = 0; i < 32; i += 4)
+            if (c + i < p.E)
+              *reinterpret_cast<float4*>(part + c + i) =
+                  make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                              __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
         }
       }
     }
@@ -174,6 +196,77 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
   }
 }
 
+// Split-K router finish, one warp per token: sums the splits' partial logits in split order
+// (bit-identical from run to run), adds the bias, then selects the top k with k rounds of a
+// warp-shuffle argmax (larger logit first, lower expert index on ties) and writes the
+// renormalised softmax weights.  Lane l holds experts l, l+32, ...; loads are coalesced.
+constexpr int kMaxPerLane = kMaxE / 32;
+
+__global__ void __launch_bounds__(256) route_finish_kernel(const __grid_constant__ RouteParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int per = (p.E + 31) / 32;
+  for (int64_t t = w; t < p.T; t += nw) {
+    float v[kMaxPerLane];
+    bool used[kMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      used[i] = true;
+      v[i] = -INFINITY;
+      if (i < per && e < p.E) {
+        float acc = __ldcg(p.partial + (int64_t)t * p.E + e);
+        for (int sp = 1; sp < p.splits; ++sp) acc += __ldcg(p.partial + ((int64_t)sp * p.T + t) * p.E + e);
+        v[i] = acc + (p.bias ? p.bias[e] : 0.0f);
+        used[i] = false;
+        if (p.logits) p.logits[t * p.E + e] = v[i];
+      }
+    }
+    float tv[kMaxK];
+    int ti[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      tv[j] = -INFINITY;
+      ti[j] = -1;
+      if (j < p.k) {
+        float best = -INFINITY;
+        int bidx = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) {
+          const int e = lane + 32 * i;
+          if (!used[i] && (v[i] > best || (v[i] == best && e < bidx))) { best = v[i]; bidx = e; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+          if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
+        }
+        if (bidx != 0x7fffffff && (bidx & 31) == lane) {
+#pragma unroll
+          for (int i = 0; i < kMaxPerLane; ++i)
+            if (i == (bidx >> 5)) used[i] = true;
+        }
+        tv[j] = best;
+        ti[j] = (bidx == 0x7fffffff) ? -1 : bidx;
+      }
+    }
+    if (lane == 0) write_route(p, (int)t, tv, ti);
+  }
+}
+
+// K splits so that the grid fills the GPU about once (T=4096 -> 4 splits of 28 k-blocks at
+// d=7168), at most route_splits_bound(); every split gets at least one k-block.
+int route_splits(int64_t T, int d) {
+  const int64_t mt = (T + BM - 1) / BM;
+  const int nkb = d / BK;
+  int sp = (int)std::max<int64_t>(1, num_sms() / std::max<int64_t>(mt, 1));
+  sp = std::min(sp, route_splits_bound(T, d));
+  const int kps = (nkb + sp - 1) / sp;
+  return (nkb + kps - 1) / kps;
+}
+
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
   const int E_pad = (p.E + 63) & ~63;
   const int stage_bytes = BM * BK * 2 + E_pad * BK * 2;
@@ -181,9 +274,15 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
   const int smem = stages * stage_bytes + 1024 + 1024;
   cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int grid = (p.T + BM - 1) / BM;
+  const dim3 grid((p.T + BM - 1) / BM, p.splits);
   prof_begin("route", s);
   route_kernel<<<grid, kGemmThreads, smem, s>>>(p);
+  prof_end(s);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1) return e;
+  const int64_t blocks = std::min<int64_t>((p.T + 7) / 8, (int64_t)num_sms() * 8);
+  prof_begin("route_finish", s);
+  route_finish_kernel<<<(int)blocks, 256, 0, s>>>(p);
   prof_end(s);
   return cudaGetLastError();
 }

@@ -54,6 +54,11 @@ WORKLOADS = {
     # experts, so that a full profiler capture holds a few GB on the device.
     "dsv3_slice_e32": LayerShape("dsv3_slice_e32", 512, 7168, 32, 8, 2048, 2048, 1, 0.0,
                                  "normal0.1", "bf16", False, 6),
+    # the same kind of slice for the training step (256 rows per expert) and for MXFP8
+    "dsv3_train_slice_e32": LayerShape("dsv3_train_slice_e32", 1024, 7168, 32, 8, 2048, 2048, 1,
+                                       0.0, "normal0.1", "bf16", True, 7),
+    "dsv3_mxfp8_slice_e32": LayerShape("dsv3_mxfp8_slice_e32", 1024, 7168, 32, 8, 2048, 2048, 1,
+                                       0.0, "normal0.1", "mxfp8", False, 8),
 }
 
 
