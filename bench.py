@@ -77,6 +77,11 @@ def dist_max(value, world):
     return float(t.item())
 
 
+def whole_job_value(world, tokens_per_rank, steps, ms_max):
+    """Tokens per second of the whole job: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (ms_max / 1e3)
+
+
 # ------------------------------------------------------------------ clocks during the timed region
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -185,8 +190,10 @@ def work_model(shape, counts):
 # streamed (routed experts with tokens + shared expert), valid only while the kernel source is
 # the one that was captured (sha1 prefix).  Source: profiles/gemm_fwd_gate_up_dsv3_slice_e32.md.
 PROFILED_TRAFFIC = {
-    "gemm_fwd_gate_up": ("7de49fbd3f37", (2.015228e9 + 19.432192e6) / 33,
+    "gemm_fwd_gate_up": ("7ff03900ea5f", (2.015325e9 + 19.891456e6) / 33,
                          "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"),
+    "gemm_fwd_down": ("7ff03900ea5f", (0.992675e9 + 60.270080e6) / 33,
+                      "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"),
 }
 
 
@@ -343,6 +350,8 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
                  "share": round(tms / max(ms, 1e-9), 4)}
         if name in model:
             r = roofline_of(name, model, tms / max(n, 1), peaks)
+            if not shape.backward:
+                r["traffic"] = profiled_traffic(name, e_act + shape.n_shared)
             entry["roofline"] = {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in r.items()}
         kernels[name] = entry
     dominant = max((n for n in kern if n in model), key=lambda n: kern[n][1])
@@ -355,7 +364,7 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
     tflops = layer_flops * steps / (ms / 1e3) / 1e12
     tpeak = peaks["bf16_tflops"] * (2.0 if mx else 1.0)
     out = {
-        "value": round(world * shape.T * steps / (ms_max / 1e3), 1),
+        "value": round(whole_job_value(world, shape.T, steps, ms_max), 1),
         "ms_per_step": round(ms_max / steps, 4),
         "tflops": round(tflops, 2),
         "tflops_frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),

@@ -207,6 +207,13 @@ int mok_dispatch_index_noalloc(const mok_dims *dims, const int32_t *topk_idx, co
                                int32_t *counts, int32_t *offsets, int32_t *sorted_tok,
                                float *sorted_w, int32_t *inv_pos, mok_stream_t stream);
 
+/* Failure-detection self-test: launches one block that waits, with the library's bounded-wait
+ * code and a budget of budget_ns (at most 2 s), on a barrier nothing arrives on.  The wait runs
+ * out, MOK_ERR_TIMEOUT is recorded in the status word of `ws` and the kernel returns normally,
+ * so the context stays usable.  It exercises the error path of the kernels' waits without
+ * faulting or hanging the GPU. */
+int mok_selftest_bounded_wait(void *ws, int64_t budget_ns, mok_stream_t stream);
+
 /* Kernel timing for benchmarks.  While enabled on the calling host thread, every entry point
  * records a CUDA event pair around each kernel it launches, on the launch stream (the events do
  * not change what the GPU executes).  enable = 0 stops recording. */

@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = [
     "mok_layer_host_extra_size", "mok_layer_forward_host", "mok_status_string",
     "mok_read_device_status", "mok_clear_device_status", "mok_last_launch_count",
     "mok_timing_enable", "mok_timing_collect", "mok_dispatch_index_noalloc",
-    "mok_mx_quantize_rows",
+    "mok_mx_quantize_rows", "mok_selftest_bounded_wait",
 ]
 
 
@@ -86,6 +86,7 @@ def lib():
             "mok_clear_device_status": (ctypes.c_int, [_VP, _VP]),
             "mok_last_launch_count": (ctypes.c_int, []),
             "mok_timing_enable": (ctypes.c_int, [ctypes.c_int]),
+            "mok_selftest_bounded_wait": (ctypes.c_int, [_VP, ctypes.c_int64, _VP]),
             "mok_mx_quantize_rows": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int, _VP, _VP, _VP, _VP]),
             "mok_dispatch_index_noalloc": (ctypes.c_int, [_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
             "mok_timing_collect": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int),
@@ -154,6 +155,12 @@ def clear_status(ws):
 
 def last_launch_count():
     return lib().mok_last_launch_count()
+
+
+def selftest_bounded_wait(ws, budget_ns=50_000_000):
+    """Runs a kernel whose bounded wait must run out; the status word of ws then reads
+    MOK_ERR_TIMEOUT (-5)."""
+    _check(lib().mok_selftest_bounded_wait(_ptr(ws), int(budget_ns), _stream()))
 
 
 def timing_enable(on=True):

@@ -58,13 +58,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits for the phase of `parity` to complete, for at most kWaitNs nanoseconds.  On timeout the
 // status word gets MOK_ERR_TIMEOUT, `*abort` is raised for the whole CTA and false is returned.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status,
-                                          volatile int* abort) {
+                                          volatile int* abort, uint64_t budget_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_ns() - t0 > kWaitNs) {
+    if (global_ns() - t0 > budget_ns) {
       record_status(status, MOK_ERR_TIMEOUT);
       *abort = 1;
       return false;

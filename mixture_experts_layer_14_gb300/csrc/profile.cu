@@ -3,7 +3,7 @@
 #include <string>
 #include <vector>
 
-#include "mok_internal.h"
+#include "mok_device.cuh"
 
 namespace mok {
 namespace {
@@ -41,9 +41,31 @@ void prof_end(cudaStream_t s) {
   cudaEventRecord(g_prof.recs.back().b, s);
 }
 
+// Failure-detection self-test: one CTA waits, with a bounded wait of `budget_ns`, on an mbarrier
+// that nothing ever arrives on.  The wait gives up, records MOK_ERR_TIMEOUT in the status word
+// and the kernel returns normally, leaving the context usable.
+__global__ void selftest_wait_kernel(int* status, uint64_t budget_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bar)), "r"(1) : "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, status, &abort_flag, budget_ns);
+  __syncthreads();
+}
+
 }  // namespace mok
 
 extern "C" {
+
+int mok_selftest_bounded_wait(void* ws, int64_t budget_ns, mok_stream_t stream) {
+  if (!ws || budget_ns <= 0 || budget_ns > (int64_t)mok::kWaitNs) return MOK_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mok::selftest_wait_kernel<<<1, 32, 0, s>>>(static_cast<int*>(ws), (uint64_t)budget_ns);
+  return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
+}
 
 int mok_timing_enable(int enable) {
   mok::g_prof.on = enable != 0;
