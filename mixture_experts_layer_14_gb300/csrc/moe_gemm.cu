@@ -37,10 +37,10 @@ struct Cfg {
   static constexpr int B_BYTES = BN * 128;
   static constexpr int SF_BYTES = MX ? (BM + BN) * 4 : 0;  // UE8M0 atoms of A and B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
-  // G_BWD_DW: the output tile is staged in shared memory (32 rows x BN per epilogue warp) and
-  // written with TMA tile stores; its K loops are short, so fewer stages suffice.
-  static constexpr int STAGING_BYTES = (MODE == G_BWD_DW) ? 4 * 32 * BN * 2 : 0;
-  static constexpr int STAGES = (MODE == G_BWD_DW) ? ((BN == 256) ? 3 : 5) : ((BN == 256) ? 4 : 6);
+  // G_BWD_DW: the output tile goes through shared memory one 64-column box (32 rows x 128 B)
+  // per epilogue warp at a time and is written with TMA tile stores.
+  static constexpr int STAGING_BYTES = (MODE == G_BWD_DW) ? 4 * 4096 : 0;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr bool A_MN = (MODE == G_BWD_DW);
   static constexpr bool B_MN = (MODE == G_FWD_GU || MODE == G_FWD_DOWN || MODE == G_BWD_DW);
   static constexpr int NUM_ACC = MX ? 1 : 2;           // MXFP8: TMEM also holds scale factors
@@ -240,15 +240,18 @@ __device__ __forceinline__ void ld_row64(const void* src, uint32_t (&v)[16]) {
   }
 }
 
-// G_BWD_DW epilogue: the warp's 32 rows x BN columns go to its staging buffer in the 128-byte
-// swizzled layout of the store map (64-column boxes of 32 rows x 128 B; the 16-byte chunk j of
-// row r sits at chunk j ^ (r % 8)), then one lane issues the TMA tile stores.
+// G_BWD_DW epilogue: each 64-column box of the warp's 32 rows goes to the warp's 4 KB staging
+// buffer in the 128-byte swizzled layout of the store map (the 16-byte chunk j of row r sits at
+// chunk j ^ (r % 8)), then one lane issues the TMA tile store of the box.
 template <int BN>
 __device__ __forceinline__ void epilogue_dw_tma(const GemmParams& p, const Tile& t, uint32_t tacc,
                                                 uint32_t stg, int q, int lane) {
-  if (lane == 0) bulk_wait_read0();  // the previous tile's stores have read the staging buffer
-  __syncwarp();
   const bool zero = (t.nkb == 0);    // an expert without tokens: its gradient is zero
+  int om = OM_R, e = 0;
+  if (t.g != 2) {
+    om = (t.g ? OM_G1 : OM_G0) + t.sub;
+    e = t.e;
+  }
 #pragma unroll 1
   for (int c = 0; c < BN; c += 64) {  // one 64-column box: two TMEM loads, one wait
     uint32_t v[2][32];
@@ -260,7 +263,9 @@ __device__ __forceinline__ void epilogue_dw_tma(const GemmParams& p, const Tile&
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[0][i] = v[1][i] = 0u;
     }
-    const uint32_t box = stg + (c / 64) * 4096 + lane * 128;
+    if (lane == 0) bulk_wait_read0();  // the previous box's store has read the staging buffer
+    __syncwarp();
+    const uint32_t box = stg + lane * 128;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t* w = &v[i >> 2][8 * (i & 3)];
@@ -273,20 +278,12 @@ __device__ __forceinline__ void epilogue_dw_tma(const GemmParams& p, const Tile&
                    "r"(d)
                    : "memory");
     }
-  }
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    int om, e = 0;
-    if (t.g == 2) om = OM_R;
-    else {
-      om = (t.g ? OM_G1 : OM_G0) + t.sub;
-      e = t.e;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(&p.omaps[om], stg, t.n * BN + c, t.m0 + 32 * q, e);
+      bulk_commit();
     }
-#pragma unroll 1
-    for (int b = 0; b < BN / 64; ++b)
-      tma_store_3d(&p.omaps[om], stg + b * 4096, t.n * BN + 64 * b, t.m0 + 32 * q, e);
-    bulk_commit();
   }
 }
 
@@ -734,7 +731,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       tc_fence_after();
       const uint32_t tacc = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (MODE == G_BWD_DW)
-        epilogue_dw_tma<BN>(p, t, tacc, sSTG0 + q * (32 * BN * 2), q, lane);
+        epilogue_dw_tma<BN>(p, t, tacc, sSTG0 + q * 4096, q, lane);
       else
         epilogue<MODE, BN>(p, t, tacc, r);
       tc_fence_before();
