@@ -34,11 +34,25 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(
       }
       continue;
     }
+    // four 16-byte loads in flight per lane before their stores
     const uint4* s0 = src0 + t * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) d0[v] = s0[v];
-    if (src1) {
-      const uint4* s1 = src1 + t * vec_per_row;
-      for (int v = lane; v < vec_per_row; v += 32) d1[v] = s1[v];
+    const uint4* s1 = src1 ? src1 + t * vec_per_row : nullptr;
+    for (int v = lane; v < vec_per_row; v += 128) {
+      uint4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v + 32 * u < vec_per_row) a[u] = s0[v + 32 * u];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v + 32 * u < vec_per_row) d0[v + 32 * u] = a[u];
+      if (s1) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v + 32 * u < vec_per_row) a[u] = s1[v + 32 * u];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v + 32 * u < vec_per_row) d1[v + 32 * u] = a[u];
+      }
     }
   }
 }
@@ -101,8 +115,11 @@ cudaError_t launch_gather_bytes(const void* src, const int32_t* rows, int64_t nr
 // applied in the down-projection epilogue).  Page "Mixture-of-Kittens: Nhân kernel MoE ...",
 // section "Chồng lấp tính toán ...": the layer combines shared and routed expert outputs with
 // the router weights; the fixed order keeps the result bit-identical across runs.
+// One instantiation per k, so that the K + 1 row loads of a vector are unconditional and all in
+// flight together; a dropped route (inv_pos = -1) reads row 0 and is multiplied by zero.
+template <int K>
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(
-    int64_t T, int vec_per_row, int k, const int32_t* __restrict__ topk_idx,
+    int64_t T, int vec_per_row, const int32_t* __restrict__ topk_idx,
     const int32_t* __restrict__ inv_pos, const uint4* __restrict__ Ys, const uint4* __restrict__ Ysh,
     uint4* __restrict__ y) {
   const int lane = threadIdx.x & 31;
@@ -115,18 +132,18 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     const int per = (vec_per_row + kCombineSplit - 1) / kCombineSplit;
     const int v_begin = part * per;
     const int v_end = min(vec_per_row, v_begin + per);
-    // order the token's routes by expert id (k <= 8, distinct experts)
-    int pos[kMaxK];
-    int ex[kMaxK];
+    // order the token's routes by expert id (distinct experts)
+    int pos[K];
+    int ex[K];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      ex[j] = (j < k) ? topk_idx[t * k + j] : 0x7fffffff;
-      pos[j] = (j < k) ? inv_pos[t * k + j] : -1;
+    for (int j = 0; j < K; ++j) {
+      ex[j] = topk_idx[t * K + j];
+      pos[j] = inv_pos[t * K + j];
     }
 #pragma unroll
-    for (int a = 1; a < kMaxK; ++a) {
+    for (int a = 1; a < K; ++a) {
 #pragma unroll
-      for (int b = kMaxK - 1; b >= a; --b) {
+      for (int b = K - 1; b >= a; --b) {
         const bool sw = ex[b] < ex[b - 1];
         const int e0 = ex[b - 1], e1 = ex[b], p0 = pos[b - 1], p1 = pos[b];
         ex[b - 1] = sw ? e1 : e0;
@@ -135,23 +152,28 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
         pos[b] = sw ? p0 : p1;
       }
     }
+    float mul[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      mul[j] = pos[j] >= 0 ? 1.0f : 0.0f;
+      pos[j] = max(pos[j], 0);
+    }
     for (int v = v_begin + lane; v < v_end; v += 32) {
+      uint4 q[K + 1];
+      q[0] = Ysh ? Ysh[t * vec_per_row + v] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < K; ++j) q[j + 1] = Ys[(int64_t)pos[j] * vec_per_row + v];
       float acc[8];
-      if (Ysh) {
-        const uint4 q = Ysh[t * vec_per_row + v];
-        acc[0] = bf16_lo(q.x); acc[1] = bf16_hi(q.x); acc[2] = bf16_lo(q.y); acc[3] = bf16_hi(q.y);
-        acc[4] = bf16_lo(q.z); acc[5] = bf16_hi(q.z); acc[6] = bf16_lo(q.w); acc[7] = bf16_hi(q.w);
-      } else {
+      acc[0] = bf16_lo(q[0].x); acc[1] = bf16_hi(q[0].x); acc[2] = bf16_lo(q[0].y); acc[3] = bf16_hi(q[0].y);
+      acc[4] = bf16_lo(q[0].z); acc[5] = bf16_hi(q[0].z); acc[6] = bf16_lo(q[0].w); acc[7] = bf16_hi(q[0].w);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-      }
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < k && pos[j] >= 0) {
-          const uint4 q = Ys[(int64_t)pos[j] * vec_per_row + v];
-          acc[0] += bf16_lo(q.x); acc[1] += bf16_hi(q.x); acc[2] += bf16_lo(q.y); acc[3] += bf16_hi(q.y);
-          acc[4] += bf16_lo(q.z); acc[5] += bf16_hi(q.z); acc[6] += bf16_lo(q.w); acc[7] += bf16_hi(q.w);
-        }
+      for (int j = 0; j < K; ++j) {
+        const uint4 u = q[j + 1];
+        const float m = mul[j];
+        acc[0] += m * bf16_lo(u.x); acc[1] += m * bf16_hi(u.x);
+        acc[2] += m * bf16_lo(u.y); acc[3] += m * bf16_hi(u.y);
+        acc[4] += m * bf16_lo(u.z); acc[5] += m * bf16_hi(u.z);
+        acc[6] += m * bf16_lo(u.w); acc[7] += m * bf16_hi(u.w);
       }
       y[t * vec_per_row + v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                                           pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
@@ -162,11 +184,21 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
 cudaError_t launch_combine(int64_t T, int d, int k, const int32_t* topk_idx, const int32_t* inv_pos,
                            const void* Ys, const void* Ysh, void* y, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  const auto ys = static_cast<const uint4*>(Ys);
+  const auto ysh = static_cast<const uint4*>(Ysh);
+  auto yo = static_cast<uint4*>(y);
+  const int grid = rows_grid(T * kCombineSplit);
   prof_begin("combine", s);
-  combine_kernel<<<rows_grid(T * kCombineSplit), kRowThreads, 0, s>>>(T, d / 8, k, topk_idx, inv_pos,
-                                                      static_cast<const uint4*>(Ys),
-                                                      static_cast<const uint4*>(Ysh),
-                                                      static_cast<uint4*>(y));
+  switch (k) {
+    case 1: combine_kernel<1><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
+    case 2: combine_kernel<2><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
+    case 3: combine_kernel<3><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
+    case 4: combine_kernel<4><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
+    case 5: combine_kernel<5><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
+    case 6: combine_kernel<6><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
+    case 7: combine_kernel<7><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
+    default: combine_kernel<8><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
+  }
   prof_end(s);
   return cudaGetLastError();
 }
