@@ -44,6 +44,10 @@ struct Cfg {
   static constexpr bool A_MN = (MODE == G_BWD_DW);
   static constexpr bool B_MN = (MODE == G_FWD_GU || MODE == G_FWD_DOWN || MODE == G_BWD_DW);
   static constexpr int NUM_ACC = MX ? 1 : 2;           // MXFP8: TMEM also holds scale factors
+  // epilogue warps: two per TMEM lane quarter (each taking half the columns) where the single
+  // accumulator leaves the epilogue exposed, one otherwise
+  static constexpr int EPI_WARPS = MX ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
   static constexpr int SF_TMEM_COL = 256;              // MXFP8: 16 columns per stage from here
   static constexpr uint32_t IDESC = MX ? make_idesc_mxf8(BN) : make_idesc_bf16(BN, A_MN, B_MN);
@@ -289,7 +293,7 @@ __device__ __forceinline__ void epilogue_dw_tma(const GemmParams& p, const Tile&
 
 template <int MODE, int BN>
 __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uint32_t tacc,
-                                         int r) {
+                                         int r, int half) {
   using bf16 = __nv_bfloat16;
   if constexpr (MODE == G_FWD_GU) {
     const bool valid = r < t.rows;
@@ -321,13 +325,14 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
     }
   } else if constexpr (MODE == G_FWD_GU_MX) {
     // h = SiLU(g) * u quantised per 32 columns: E4M3 codes [rows][F] + UE8M0 bytes [rows][F/32]
+    // (this warp: h columns 64*half .. 64*half+63 of the tile)
     const bool valid = r < t.rows;
     const int ld = t.g ? p.F : p.Fs;
     const int64_t row = t.row0 + r;
     uint8_t* hq = static_cast<uint8_t*>(p.out0[t.g]) + row * ld + t.n * 128;
     uint8_t* hs = static_cast<uint8_t*>(p.out1[t.g]) + row * (ld / 32) + t.n * 4;
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
+    for (int c = 64 * half; c < 64 * half + 64; c += 32) {
       uint32_t gr[32], ur[32];
       tmem_ld32(tacc + c, gr);
       tmem_ld32(tacc + 128 + c, ur);
@@ -351,8 +356,9 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
     float s = 1.0f;
     if (MODE != G_BWD_DX && t.g == 1 && valid) s = p.row_w[row];
     bf16* o = static_cast<bf16*>(p.out0[t.g]) + row * p.d + t.n * BN;
+    constexpr int cols = (Cfg<MODE, BN>::EPI_WARPS == 8) ? BN / 2 : BN;  // columns of this warp
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = cols * half; c < cols * half + cols; c += 32) {
       uint32_t v[32];
       tmem_ld32(tacc + c, v);
       tmem_ld_wait();
@@ -514,7 +520,7 @@ __device__ __forceinline__ void zero_k_tail(uint32_t sA, uint32_t sB, int valid,
 
 // ------------------------------------------------------------------ the kernel
 template <int MODE, int BN>
-__global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<MODE, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -547,7 +553,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
-      mbar_init(bar_tempty + 8 * b, 4 * 32);
+      mbar_init(bar_tempty + 8 * b, C::EPI_WARPS * 32);
     }
     mbar_init(bar_drain, 1);
     *s_abort = 0;
@@ -721,6 +727,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     __syncwarp();
   } else {
     const int q = warp & 3;  // TMEM lane quarter accessible to this warp
+    const int half = (warp - 2) / 4;  // 8 epilogue warps: which column half
     const int r = q * 32 + lane;
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x, ++it) {
@@ -733,7 +740,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       if constexpr (MODE == G_BWD_DW)
         epilogue_dw_tma<BN>(p, t, tacc, sSTG0 + q * 4096, q, lane);
       else
-        epilogue<MODE, BN>(p, t, tacc, r);
+        epilogue<MODE, BN>(p, t, tacc, r, half);
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * buf);
     }
@@ -758,7 +765,7 @@ static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
   static const char* kNames[] = {"gemm_fwd_gate_up", "gemm_fwd_down", "gemm_bwd_da", "gemm_bwd_dx",
                                  "gemm_bwd_dw", "gemm_fwd_gate_up_mx", "gemm_fwd_down_mx"};
   prof_begin(kNames[MODE], s);
-  k<<<grid, kGemmThreads, smem, s>>>(p);
+  k<<<grid, Cfg<MODE, BN>::THREADS, smem, s>>>(p);
   prof_end(s);
   return cudaGetLastError();
 }
