@@ -736,18 +736,9 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
     ok &= map2d(&p.maps[MS_B3], dG, R, F, 64, 64);
     ok &= map2d(&p.maps[MS_B4], dU, R, F, 64, 64);
     ok &= map2d(&p.maps[MS_B5], dys, R, d, 64, 64);
-    if (sh) {
-      ok &= map3d(&p.omaps[OM_G0], dWs_gate, 1, d, Fs, 64, 32);
-      ok &= map3d(&p.omaps[OM_U0], dWs_up, 1, d, Fs, 64, 32);
-      ok &= map3d(&p.omaps[OM_D0], dWs_down, 1, Fs, d, 64, 32);
-    }
-    ok &= map3d(&p.omaps[OM_G1], dW_gate, E, d, F, 64, 32);
-    ok &= map3d(&p.omaps[OM_U1], dW_up, E, d, F, 64, 32);
-    ok &= map3d(&p.omaps[OM_D1], dW_down, E, F, d, 64, 32);
     if (dW_router) {
       ok &= map2d(&p.maps[MS_R_A], x, T, d, 64, 64);
       ok &= map2d(&p.maps[MS_R_B], dl, T, ldl, 64, 64);
-      ok &= map3d(&p.omaps[OM_R], dW_router, 1, d, E, 64, 32);
       p.router_tiles = (d / BM) * ((E + bn - 1) / bn);
       p.E_cols = E;
       p.out_router = dW_router;

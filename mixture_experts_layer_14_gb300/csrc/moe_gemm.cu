@@ -38,7 +38,7 @@ struct Cfg {
   static constexpr int SF_BYTES = MX ? (BM + BN) * 4 : 0;  // UE8M0 atoms of A and B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
   // G_BWD_DW: the output tile goes through shared memory one 64-column box (32 rows x 128 B)
-  // per epilogue warp at a time and is written with TMA tile stores.
+  // per epilogue warp at a time and is written with coalesced row stores.
   static constexpr int STAGING_BYTES = (MODE == G_BWD_DW) ? 4 * 4096 : 0;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr bool A_MN = (MODE == G_BWD_DW);
@@ -244,50 +244,74 @@ __device__ __forceinline__ void ld_row64(const void* src, uint32_t (&v)[16]) {
   }
 }
 
-// G_BWD_DW epilogue: each 64-column box of the warp's 32 rows goes to the warp's 4 KB staging
-// buffer in the 128-byte swizzled layout of the store map (the 16-byte chunk j of row r sits at
-// chunk j ^ (r % 8)), then one lane issues the TMA tile store of the box.
-template <int BN>
-__device__ __forceinline__ void epilogue_dw_tma(const GemmParams& p, const Tile& t, uint32_t tacc,
-                                                uint32_t stg, int q, int lane) {
-  const bool zero = (t.nkb == 0);    // an expert without tokens: its gradient is zero
-  int om = OM_R, e = 0;
-  if (t.g != 2) {
-    om = (t.g ? OM_G1 : OM_G0) + t.sub;
-    e = t.e;
-  }
-#pragma unroll 1
-  for (int c = 0; c < BN; c += 64) {  // one 64-column box: two TMEM loads, one wait
-    uint32_t v[2][32];
-    if (!zero) {
-      tmem_ld32(tacc + c, v[0]);
-      tmem_ld32(tacc + c + 32, v[1]);
-      tmem_ld_wait();
-    } else {
+// G_BWD_DW epilogue: for each 64-column box of the warp's 32 rows, every thread writes its row
+// (128 B) into the warp's 4 KB staging buffer (16-byte chunk j of row r at chunk j ^ (r % 8), so
+// neither side conflicts on banks), then the warp reads it back by rows and stores four whole
+// 128-byte rows per instruction.  The TMEM loads of the next box are in flight meanwhile.
+__device__ __forceinline__ void dw_tmem_box(uint32_t taddr, bool zero, uint32_t (&v)[2][32]) {
+  if (!zero) {
+    tmem_ld32(taddr, v[0]);
+    tmem_ld32(taddr + 32, v[1]);
+  } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[0][i] = v[1][i] = 0u;
+    for (int i = 0; i < 32; ++i) v[0][i] = v[1][i] = 0u;
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void epilogue_dw(const GemmParams& p, const Tile& t, uint32_t tacc,
+                                            uint32_t stg, int q, int lane) {
+  using bf16 = __nv_bfloat16;
+  const bool zero = (t.nkb == 0);    // an expert without tokens: its gradient is zero
+  bf16* out;
+  int ld, ncols;
+  if (t.g == 2) {
+    out = static_cast<bf16*>(p.out_router);
+    ld = ncols = p.E_cols;
+  } else {
+    const int Fg = t.g ? p.F : p.Fs;
+    if (t.sub < 2) {
+      out = static_cast<bf16*>(t.sub ? p.out1[t.g] : p.out0[t.g]) + (int64_t)t.e * p.d * Fg;
+      ld = Fg;
+    } else {
+      out = static_cast<bf16*>(p.out2[t.g]) + (int64_t)t.e * Fg * p.d;
+      ld = p.d;
     }
-    if (lane == 0) bulk_wait_read0();  // the previous box's store has read the staging buffer
-    __syncwarp();
-    const uint32_t box = stg + lane * 128;
+    ncols = ld;
+  }
+  const int row0 = t.m0 + 32 * q;
+  uint32_t v[2][2][32];
+  dw_tmem_box(tacc, zero, v[0]);
+#pragma unroll
+  for (int b = 0; b < BN / 64; ++b) {
+    uint32_t(&cur)[2][32] = v[b & 1];
+    if (!zero) tmem_ld_wait();
+    const uint32_t mine = stg + lane * 128;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t* w = &v[i >> 2][8 * (i & 3)];
+      const uint32_t* w = &cur[i >> 2][8 * (i & 3)];
       const uint32_t a = pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1]));
-      const uint32_t b = pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3]));
+      const uint32_t bb = pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3]));
       const uint32_t cc = pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5]));
       const uint32_t d = pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7]));
-      const uint32_t addr = box + ((i ^ (lane & 7)) << 4);
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(cc),
-                   "r"(d)
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(mine + ((i ^ (lane & 7)) << 4)),
+                   "r"(a), "r"(bb), "r"(cc), "r"(d)
                    : "memory");
     }
-    fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) {
-      tma_store_3d(&p.omaps[om], stg, t.n * BN + c, t.m0 + 32 * q, e);
-      bulk_commit();
+    if (b + 1 < BN / 64) dw_tmem_box(tacc + 64 * (b + 1), zero, v[(b + 1) & 1]);
+    const int col = t.n * BN + 64 * b + 8 * (lane & 7);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + (lane >> 3);  // rows 4i..4i+3, eight 16-byte chunks each
+      uint32_t a, bb, cc, d;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(a), "=r"(bb), "=r"(cc), "=r"(d)
+                   : "r"(stg + r * 128 + (((lane & 7) ^ (r & 7)) << 4)));
+      if (col < ncols)
+        *reinterpret_cast<uint4*>(out + (int64_t)(row0 + r) * ld + col) = make_uint4(a, bb, cc, d);
     }
+    __syncwarp();
   }
 }
 
@@ -738,15 +762,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       tc_fence_after();
       const uint32_t tacc = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (MODE == G_BWD_DW)
-        epilogue_dw_tma<BN>(p, t, tacc, sSTG0 + q * 4096, q, lane);
+        epilogue_dw<BN>(p, t, tacc, sSTG0 + q * 4096, q, lane);
       else
         epilogue<MODE, BN>(p, t, tacc, r, half);
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * buf);
-    }
-    if constexpr (MODE == G_BWD_DW) {
-      if (lane == 0) bulk_wait0();  // every tile store of this warp has completed
-      __syncwarp();
     }
   }
   __syncthreads();

@@ -40,12 +40,8 @@ enum MapSlot : int {
   MS_COUNT = 14
 };
 
-// Store maps of the weight-gradient GEMM (TMA tile stores of the dW tiles).
-enum OutSlot : int { OM_R = 0, OM_G0, OM_U0, OM_D0, OM_G1, OM_U1, OM_D1, OM_COUNT };
-
 struct GemmParams {
   CUtensorMap maps[MS_COUNT];
-  CUtensorMap omaps[OM_COUNT];  // G_BWD_DW outputs: box {64 cols, 32 rows}, 128-byte swizzle
   const int* offsets;   // routed row offsets [E+1] (device), NULL when E == 0
   int E;                // routed experts in this launch (0 = none)
   int has_shared;       // group 0 present
