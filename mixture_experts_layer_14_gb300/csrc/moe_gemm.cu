@@ -37,9 +37,6 @@ struct Cfg {
   static constexpr int B_BYTES = BN * 128;
   static constexpr int SF_BYTES = MX ? (BM + BN) * 4 : 0;  // UE8M0 atoms of A and B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
-  // G_BWD_DW: the output tile goes through shared memory one 64-column box (32 rows x 128 B)
-  // per epilogue warp at a time and is written with coalesced row stores.
-  static constexpr int STAGING_BYTES = (MODE == G_BWD_DW) ? 4 * 4096 : 0;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr bool A_MN = (MODE == G_BWD_DW);
   static constexpr bool B_MN = (MODE == G_FWD_GU || MODE == G_FWD_DOWN || MODE == G_BWD_DW);
@@ -48,6 +45,11 @@ struct Cfg {
   // accumulator leaves the epilogue exposed, one otherwise
   static constexpr int EPI_WARPS = MX ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  // the output tile goes through shared memory and is written with coalesced row stores:
+  // G_BWD_DW one 64-column box (32 rows x 128 B) per epilogue warp at a time, the row-major
+  // outputs of G_FWD_DOWN / G_BWD_DX / G_FWD_DOWN_MX one 32-column chunk (32 rows x 64 B)
+  static constexpr bool ROW_STAGED = (MODE == G_FWD_DOWN || MODE == G_BWD_DX || MODE == G_FWD_DOWN_MX);
+  static constexpr int STAGING_BYTES = (MODE == G_BWD_DW) ? 4 * 4096 : ROW_STAGED ? EPI_WARPS * 2048 : 0;
   static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
   static constexpr int SF_TMEM_COL = 256;              // MXFP8: 16 columns per stage from here
   static constexpr uint32_t IDESC = MX ? make_idesc_mxf8(BN) : make_idesc_bf16(BN, A_MN, B_MN);
@@ -315,6 +317,59 @@ __device__ __forceinline__ void epilogue_dw(const GemmParams& p, const Tile& t, 
   }
 }
 
+// Row-major outputs with d columns (G_FWD_DOWN, G_FWD_DOWN_MX: Y_s = router weight x accumulator;
+// G_BWD_DX: dX_s = accumulator).  Per 32-column chunk each thread packs its row (64 B) into the
+// warp's 2 KB staging buffer (16-byte chunk i of row r at i ^ ((r / 2) % 4): conflict-free on
+// both sides), then the warp reads it back by rows and stores eight whole 64-byte row pieces per
+// instruction, skipping rows past the expert's last token.  The TMEM load of the next chunk is in
+// flight meanwhile.
+template <int MODE, int BN>
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, const Tile& t, uint32_t tacc,
+                                              uint32_t stg, int q, int half, int lane) {
+  using bf16 = __nv_bfloat16;
+  constexpr int cols = (Cfg<MODE, BN>::EPI_WARPS == 8) ? BN / 2 : BN;  // columns of this warp
+  constexpr int NCH = cols / 32;
+  const int nrows = t.rows - q * 32;  // valid rows among this warp's 32 (may be <= 0)
+  if (nrows <= 0) return;
+  float s = 1.0f;
+  if (MODE != G_BWD_DX && t.g == 1 && lane < nrows) s = p.row_w[t.row0 + q * 32 + lane];
+  bf16* o = static_cast<bf16*>(p.out0[t.g]) + (int64_t)(t.row0 + q * 32) * p.d + t.n * BN + cols * half;
+  const uint32_t tcol = tacc + cols * half;
+  uint32_t v[2][32];
+  tmem_ld32(tcol, v[0]);
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    uint32_t(&cur)[32] = v[c & 1];
+    tmem_ld_wait();
+    const uint32_t mine = stg + lane * 64;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t* w = &cur[8 * i];
+      const uint32_t a = pack_bf16x2(s * __uint_as_float(w[0]), s * __uint_as_float(w[1]));
+      const uint32_t b = pack_bf16x2(s * __uint_as_float(w[2]), s * __uint_as_float(w[3]));
+      const uint32_t cc = pack_bf16x2(s * __uint_as_float(w[4]), s * __uint_as_float(w[5]));
+      const uint32_t d = pack_bf16x2(s * __uint_as_float(w[6]), s * __uint_as_float(w[7]));
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(mine + ((i ^ ((lane >> 1) & 3)) << 4)),
+                   "r"(a), "r"(b), "r"(cc), "r"(d)
+                   : "memory");
+    }
+    __syncwarp();
+    if (c + 1 < NCH) tmem_ld32(tcol + 32 * (c + 1), v[(c + 1) & 1]);
+    const int ch = lane & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = 8 * j + (lane >> 2);  // rows 8j..8j+7, four 16-byte chunks each
+      uint32_t a, b, cc, d;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
+                   : "r"(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)));
+      if (r < nrows)
+        *reinterpret_cast<uint4*>(o + (int64_t)r * p.d + 32 * c + 8 * ch) = make_uint4(a, b, cc, d);
+    }
+    __syncwarp();
+  }
+}
+
 template <int MODE, int BN>
 __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uint32_t tacc,
                                          int r, int half) {
@@ -372,26 +427,6 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
         d[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
         d[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
         hs[c / 32] = (uint8_t)sb;
-      }
-    }
-  } else if constexpr (MODE == G_FWD_DOWN || MODE == G_BWD_DX || MODE == G_FWD_DOWN_MX) {
-    const bool valid = r < t.rows;
-    const int64_t row = t.row0 + r;
-    float s = 1.0f;
-    if (MODE != G_BWD_DX && t.g == 1 && valid) s = p.row_w[row];
-    bf16* o = static_cast<bf16*>(p.out0[t.g]) + row * p.d + t.n * BN;
-    constexpr int cols = (Cfg<MODE, BN>::EPI_WARPS == 8) ? BN / 2 : BN;  // columns of this warp
-#pragma unroll 1
-    for (int c = cols * half; c < cols * half + cols; c += 32) {
-      uint32_t v[32];
-      tmem_ld32(tacc + c, v);
-      tmem_ld_wait();
-      if (valid) {
-        uint32_t q[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          q[i] = pack_bf16x2(s * __uint_as_float(v[2 * i]), s * __uint_as_float(v[2 * i + 1]));
-        st_row64(o + c, q);
       }
     }
   } else if constexpr (MODE == G_BWD_DA) {
@@ -553,7 +588,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
   const uint32_t sA0 = base;
   const uint32_t sB0 = base + C::STAGES * C::A_BYTES;
   const uint32_t sSF0 = sB0 + C::STAGES * C::B_BYTES;  // MXFP8 scale-factor atoms
-  const uint32_t sSTG0 = sSF0 + C::STAGES * C::SF_BYTES;  // G_BWD_DW output staging
+  const uint32_t sSTG0 = sSF0 + C::STAGES * C::SF_BYTES;  // output staging of the epilogue warps
   uint8_t* aux = gbase + C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES;
   const uint32_t aux_s = base + C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES;
   // aux layout: full[S] empty[S] tfull[2] tempty[2] drain | tmem addr | abort
@@ -763,6 +798,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       const uint32_t tacc = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (MODE == G_BWD_DW)
         epilogue_dw<BN>(p, t, tacc, sSTG0 + q * 4096, q, lane);
+      else if constexpr (C::ROW_STAGED)
+        epilogue_rows<MODE, BN>(p, t, tacc, sSTG0 + (warp - 2) * 2048, q, half, lane);
       else
         epilogue<MODE, BN>(p, t, tacc, r, half);
       tc_fence_before();
@@ -779,6 +816,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
 template <int MODE, int BN>
 static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
   constexpr int smem = smem_bytes_for<MODE, BN>();
+  static_assert(smem <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
   auto k = moe_gemm_kernel<MODE, BN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
