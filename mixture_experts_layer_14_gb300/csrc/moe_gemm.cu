@@ -318,55 +318,89 @@ __device__ __forceinline__ void epilogue_dw(const GemmParams& p, const Tile& t, 
 }
 
 // Row-major outputs with d columns (G_FWD_DOWN, G_FWD_DOWN_MX: Y_s = router weight x accumulator;
-// G_BWD_DX: dX_s = accumulator).  Per 32-column chunk each thread packs its row (64 B) into the
-// warp's 2 KB staging buffer (16-byte chunk i of row r at i ^ ((r / 2) % 4): conflict-free on
+// G_BWD_DX: dX_s = accumulator).  Per 32-column chunk each thread's row (64 B of bf16) goes into
+// the warp's 2 KB staging buffer (16-byte chunk i of row r at i ^ ((r / 2) % 4): conflict-free on
 // both sides), then the warp reads it back by rows and stores eight whole 64-byte row pieces per
-// instruction, skipping rows past the expert's last token.  The TMEM load of the next chunk is in
-// flight meanwhile.
+// instruction, skipping rows past the expert's last token.  With a single accumulator the warp
+// first packs all its columns into registers and releases the accumulator (arrival on `release`)
+// so that the next tile's MMAs run under the stores; with two, the TMEM load of the next chunk is
+// in flight during the stores and the accumulator is released at the end.
+template <int MODE, int BN>
+__device__ __forceinline__ void rows_store_chunk(__nv_bfloat16* o, int ld, int nrows, uint32_t stg,
+                                                 int lane, const uint32_t (&P)[16]) {
+  const uint32_t mine = stg + lane * 64;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(mine + ((i ^ ((lane >> 1) & 3)) << 4)),
+                 "r"(P[4 * i]), "r"(P[4 * i + 1]), "r"(P[4 * i + 2]), "r"(P[4 * i + 3])
+                 : "memory");
+  __syncwarp();
+  const int ch = lane & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = 8 * j + (lane >> 2);  // rows 8j..8j+7, four 16-byte chunks each
+    uint32_t a, b, c, d;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)));
+    if (r < nrows) *reinterpret_cast<uint4*>(o + (int64_t)r * ld + 8 * ch) = make_uint4(a, b, c, d);
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void pack_scaled(const uint32_t (&v)[32], float s, uint32_t (&P)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    P[i] = pack_bf16x2(s * __uint_as_float(v[2 * i]), s * __uint_as_float(v[2 * i + 1]));
+}
+
 template <int MODE, int BN>
 __device__ __forceinline__ void epilogue_rows(const GemmParams& p, const Tile& t, uint32_t tacc,
-                                              uint32_t stg, int q, int half, int lane) {
+                                              uint32_t stg, int q, int half, int lane,
+                                              uint32_t release) {
   using bf16 = __nv_bfloat16;
-  constexpr int cols = (Cfg<MODE, BN>::EPI_WARPS == 8) ? BN / 2 : BN;  // columns of this warp
+  using C = Cfg<MODE, BN>;
+  constexpr int cols = (C::EPI_WARPS == 8) ? BN / 2 : BN;  // columns of this warp
   constexpr int NCH = cols / 32;
   const int nrows = t.rows - q * 32;  // valid rows among this warp's 32 (may be <= 0)
-  if (nrows <= 0) return;
+  if (nrows <= 0) {
+    tc_fence_before();
+    mbar_arrive(release);
+    return;
+  }
   float s = 1.0f;
   if (MODE != G_BWD_DX && t.g == 1 && lane < nrows) s = p.row_w[t.row0 + q * 32 + lane];
   bf16* o = static_cast<bf16*>(p.out0[t.g]) + (int64_t)(t.row0 + q * 32) * p.d + t.n * BN + cols * half;
   const uint32_t tcol = tacc + cols * half;
-  uint32_t v[2][32];
-  tmem_ld32(tcol, v[0]);
+  if constexpr (C::NUM_ACC == 1) {
+    static_assert(NCH % 2 == 0, "pairs of chunks");
+    uint32_t P[NCH][16];
 #pragma unroll
-  for (int c = 0; c < NCH; ++c) {
-    uint32_t(&cur)[32] = v[c & 1];
-    tmem_ld_wait();
-    const uint32_t mine = stg + lane * 64;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t* w = &cur[8 * i];
-      const uint32_t a = pack_bf16x2(s * __uint_as_float(w[0]), s * __uint_as_float(w[1]));
-      const uint32_t b = pack_bf16x2(s * __uint_as_float(w[2]), s * __uint_as_float(w[3]));
-      const uint32_t cc = pack_bf16x2(s * __uint_as_float(w[4]), s * __uint_as_float(w[5]));
-      const uint32_t d = pack_bf16x2(s * __uint_as_float(w[6]), s * __uint_as_float(w[7]));
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(mine + ((i ^ ((lane >> 1) & 3)) << 4)),
-                   "r"(a), "r"(b), "r"(cc), "r"(d)
-                   : "memory");
+    for (int c = 0; c < NCH; c += 2) {
+      uint32_t v[2][32];
+      tmem_ld32(tcol + 32 * c, v[0]);
+      tmem_ld32(tcol + 32 * c + 32, v[1]);
+      tmem_ld_wait();
+      pack_scaled(v[0], s, P[c]);
+      pack_scaled(v[1], s, P[c + 1]);
     }
-    __syncwarp();
-    if (c + 1 < NCH) tmem_ld32(tcol + 32 * (c + 1), v[(c + 1) & 1]);
-    const int ch = lane & 3;
+    tc_fence_before();
+    mbar_arrive(release);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int r = 8 * j + (lane >> 2);  // rows 8j..8j+7, four 16-byte chunks each
-      uint32_t a, b, cc, d;
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
-                   : "r"(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)));
-      if (r < nrows)
-        *reinterpret_cast<uint4*>(o + (int64_t)r * p.d + 32 * c + 8 * ch) = make_uint4(a, b, cc, d);
+    for (int c = 0; c < NCH; ++c) rows_store_chunk<MODE, BN>(o + 32 * c, p.d, nrows, stg, lane, P[c]);
+  } else {
+    uint32_t v[2][32];
+    tmem_ld32(tcol, v[0]);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      tmem_ld_wait();
+      uint32_t P[16];
+      pack_scaled(v[c & 1], s, P);
+      if (c + 1 < NCH) tmem_ld32(tcol + 32 * (c + 1), v[(c + 1) & 1]);
+      rows_store_chunk<MODE, BN>(o + 32 * c, p.d, nrows, stg, lane, P);
     }
-    __syncwarp();
+    tc_fence_before();
+    mbar_arrive(release);
   }
 }
 
@@ -796,14 +830,18 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       if (!mbar_wait(bar_tfull + 8 * buf, tph, p.status, s_abort)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
-      if constexpr (MODE == G_BWD_DW)
-        epilogue_dw<BN>(p, t, tacc, sSTG0 + q * 4096, q, lane);
-      else if constexpr (C::ROW_STAGED)
-        epilogue_rows<MODE, BN>(p, t, tacc, sSTG0 + (warp - 2) * 2048, q, half, lane);
-      else
-        epilogue<MODE, BN>(p, t, tacc, r, half);
-      tc_fence_before();
-      mbar_arrive(bar_tempty + 8 * buf);
+      if constexpr (C::ROW_STAGED) {
+        // releases the accumulator itself (before its stores when there is only one)
+        epilogue_rows<MODE, BN>(p, t, tacc, sSTG0 + (warp - 2) * 2048, q, half, lane,
+                                bar_tempty + 8 * buf);
+      } else {
+        if constexpr (MODE == G_BWD_DW)
+          epilogue_dw<BN>(p, t, tacc, sSTG0 + q * 4096, q, lane);
+        else
+          epilogue<MODE, BN>(p, t, tacc, r, half);
+        tc_fence_before();
+        mbar_arrive(bar_tempty + 8 * buf);
+      }
     }
   }
   __syncthreads();
