@@ -100,8 +100,11 @@ size_t mok_prepared_size(const mok_dims *dims);
 /* MXFP8: quantise the routed and shared expert weights once into `prepared` (E4M3 values and
  * UE8M0 scales, blocks of 32 along each weight's reduction dimension, same rule as
  * mok_mx_quantize_rows), transposed to K-major, in this order (each region 1 KB aligned):
- * W_gate codes [E][F][d], scales [E][F][d/32]; W_up likewise; W_down codes [E][d][F], scales
- * [E][d][F/32]; then the shared expert's three the same way.  No-op for MOK_BF16.
+ * W_gate codes [E][F][d] and scales; W_up likewise; W_down codes [E][d][F] and scales; then the
+ * shared expert's three the same way.  The scales of a K-major matrix [N][K] (N rows, K/32 scale
+ * bytes per row) are stored in 512-byte atoms [N/128][K/128]: the atom of row tile a and K block
+ * b holds row n = 128a + 32 r1 + r0 (r0 < 32, r1 < 4), block 4b + j at byte 16 r0 + 4 r1 + j,
+ * the shared-memory image the block-scaled MMA's scale copy reads.  No-op for MOK_BF16.
  * MXFP8 needs d % 256 == 0 and is forward only (mok_moe_backward returns MOK_ERR_UNSUPPORTED). */
 int mok_prepare_weights(const mok_dims *dims, const mok_weights *w, void *prepared,
                         mok_stream_t stream);

@@ -94,12 +94,12 @@ static size_t al(size_t x) { return (x + 1023) & ~size_t(1023); }
 
 enum FwdSlot {
   FW_STATUS, FW_HIST, FW_XS, FW_H, FW_HSH, FW_YS, FW_YSH,
-  // MXFP8 only: E4M3 codes and UE8M0 scale rows of x, x_sorted, h, h_sh
+  // MXFP8 only: E4M3 codes and UE8M0 scale atoms of x, x_sorted, h, h_sh
   FW_XQ, FW_XSC, FW_XQS, FW_XSCS, FW_HQ, FW_HSC, FW_HQSH, FW_HSCSH,
   FW_RPART,  // router: split-K partial logits
   FW_N
 };
-enum PrepSlot {  // MXFP8 prepared weights: K-major codes [n][N][K] and scales [n][N][K/32]
+enum PrepSlot {  // MXFP8 prepared weights: K-major codes [n][N][K] and scale atoms
   PR_GQ, PR_GS, PR_UQ, PR_US, PR_DQ, PR_DS, PR_SGQ, PR_SGS, PR_SUQ, PR_SUS, PR_SDQ, PR_SDS, PR_N
 };
 enum BwdSlot {
@@ -128,14 +128,17 @@ static Layout layout_fwd(const mok_dims* d) {
     sz[FW_XS] = 0;
     sz[FW_H] = 0;
     sz[FW_HSH] = 0;
+    // scale atoms: 4 bytes per row and K block of 128, rows padded to whole M tiles; the
+    // expert-ordered tensors hold at most ceil(R / 128) + E tiles
+    const int64_t mt_x = (T + BM - 1) / BM, mt_r = (R + BM - 1) / BM + d->E;
     sz[FW_XQ] = 1ull * T * d->d;
-    sz[FW_XSC] = 1ull * T * d->d / 32;
+    sz[FW_XSC] = 4ull * BM * mt_x * (d->d / 128);
     sz[FW_XQS] = 1ull * R * d->d;
-    sz[FW_XSCS] = 1ull * R * d->d / 32;
+    sz[FW_XSCS] = 4ull * BM * mt_r * (d->d / 128);
     sz[FW_HQ] = 1ull * R * d->F;
-    sz[FW_HSC] = 1ull * R * d->F / 32;
+    sz[FW_HSC] = 4ull * BM * mt_r * (d->F / 128);
     sz[FW_HQSH] = 1ull * T * Fs;
-    sz[FW_HSCSH] = 1ull * T * Fs / 32;
+    sz[FW_HSCSH] = 4ull * BM * mt_x * (Fs / 128);
   }
   Layout L{};
   size_t o = 0;
@@ -271,7 +274,7 @@ int mok_mx_quantize_rows(int64_t rows, int K, const void* src, void* q, void* sc
   if (!aligned16(src) || !aligned16(q) || !aligned16(scales)) return MOK_ERR_UNSUPPORTED;
   g_last_launches = rows > 0 ? 1 : 0;
   return cuda_status(
-      launch_mx_quantize_rows(src, rows, K, q, scales, reinterpret_cast<cudaStream_t>(stream)));
+      launch_mx_quantize_rows(src, rows, K, q, scales, false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 const char* mok_status_string(int s) {
@@ -404,9 +407,10 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
     uint8_t* hsc = at<uint8_t*>(ws, L.off[FW_HSC]);
     void* hqsh = at<void*>(ws, L.off[FW_HQSH]);
     uint8_t* hscsh = at<uint8_t*>(ws, L.off[FW_HSCSH]);
-    rc = cuda_status(launch_mx_quantize_rows(x, T, d, xq, xsc, s));
+    rc = cuda_status(launch_mx_quantize_rows(x, T, d, xq, xsc, true, s));
     if (rc == MOK_OK) rc = cuda_status(launch_gather_bytes(xq, sorted_tok, R, T, d, xqs, s));
-    if (rc == MOK_OK) rc = cuda_status(launch_gather_bytes(xsc, sorted_tok, R, T, d / 32, xscs, s));
+    if (rc == MOK_OK)
+      rc = cuda_status(launch_gather_scale_atoms(xsc, sorted_tok, offsets, E, T, R, d, xscs, s));
     if (rc != MOK_OK) return rc;
     launches += 3;
     {
@@ -435,16 +439,12 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
       p.out0[1] = hq;
       p.out1[1] = hsc;
       p.sfa[0] = xsc;
-      p.sfa_rows[0] = T;
       p.sfa[1] = xscs;
-      p.sfa_rows[1] = R;
       p.sfb[0][0] = reinterpret_cast<const uint8_t*>(pw(PR_SGS));
       p.sfb[0][1] = reinterpret_cast<const uint8_t*>(pw(PR_SUS));
       p.sfb[1][0] = reinterpret_cast<const uint8_t*>(pw(PR_GS));
       p.sfb[1][1] = reinterpret_cast<const uint8_t*>(pw(PR_US));
-      p.sfb_estride[0] = 0;
-      p.sfb_estride[1] = (int64_t)F * (d / 32);
-      p.sf_ld[0] = p.sf_ld[1] = d / 32;
+      p.sf_kb[0] = p.sf_kb[1] = d / 128;
       p.status = static_cast<int*>(ws);
       const int64_t bound = (sh ? (T + BM - 1) / BM * p.nt[0] : 0) + ((R + BM - 1) / BM + E) * p.nt[1];
       rc = cuda_status(launch_gemm(G_FWD_GU_MX, 256, p, (int)std::min<int64_t>(grid_cap0, bound), s));
@@ -474,15 +474,11 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
       p.out0[1] = Ys;
       p.row_w = sorted_w;
       p.sfa[0] = hscsh;
-      p.sfa_rows[0] = T;
       p.sfa[1] = hsc;
-      p.sfa_rows[1] = R;
       p.sfb[0][0] = reinterpret_cast<const uint8_t*>(pw(PR_SDS));
       p.sfb[1][0] = reinterpret_cast<const uint8_t*>(pw(PR_DS));
-      p.sfb_estride[0] = 0;
-      p.sfb_estride[1] = (int64_t)d * (F / 32);
-      p.sf_ld[0] = Fs / 32;
-      p.sf_ld[1] = F / 32;
+      p.sf_kb[0] = Fs / 128;
+      p.sf_kb[1] = F / 128;
       p.status = static_cast<int*>(ws);
       const int64_t bound = (sh ? (T + BM - 1) / BM * p.nt[0] : 0) + ((R + BM - 1) / BM + E) * p.nt[1];
       rc = cuda_status(launch_gemm(G_FWD_DOWN_MX, 256, p, (int)std::min<int64_t>(grid_cap0, bound), s));

@@ -26,6 +26,8 @@ struct Tile {
   int m0;    // K-grouped: first output row (element offset along M)
   int n;     // N tile index
   int nkb;   // k-blocks
+  int mt;    // M-grouped: index of the M tile in the decode order (shared tiles, then each
+             // expert's); MXFP8 A scale atoms are stored by it
 };
 
 template <int MODE, int BN>
@@ -45,11 +47,11 @@ struct Cfg {
   // accumulator leaves the epilogue exposed, one otherwise
   static constexpr int EPI_WARPS = MX ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  // the output tile goes through shared memory and is written with coalesced row stores:
-  // G_BWD_DW one 64-column box (32 rows x 128 B) per epilogue warp at a time, the row-major
-  // outputs of G_FWD_DOWN / G_BWD_DX / G_FWD_DOWN_MX one 32-column chunk (32 rows x 64 B)
-  static constexpr bool ROW_STAGED = (MODE == G_FWD_DOWN || MODE == G_BWD_DX || MODE == G_FWD_DOWN_MX);
-  static constexpr int STAGING_BYTES = (MODE == G_BWD_DW) ? 4 * 4096 : ROW_STAGED ? EPI_WARPS * 2048 : 0;
+  // plain row-major outputs go through shared memory one 32-column chunk (32 rows x 64 B) per
+  // epilogue warp at a time and are written with coalesced row stores
+  static constexpr bool ROW_STAGED = (MODE == G_FWD_DOWN || MODE == G_BWD_DX ||
+                                      MODE == G_FWD_DOWN_MX || MODE == G_BWD_DW);
+  static constexpr int STAGING_BYTES = ROW_STAGED ? EPI_WARPS * 2048 : 0;
   static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
   static constexpr int SF_TMEM_COL = 256;              // MXFP8: 16 columns per stage from here
   static constexpr uint32_t IDESC = MX ? make_idesc_mxf8(BN) : make_idesc_bf16(BN, A_MN, B_MN);
@@ -76,6 +78,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
   Tile t;
   t.sub = 0;
   t.m0 = 0;
+  t.mt = 0;
   if constexpr (!Cfg<MODE, BN>::K_GROUPED) {
     const int mt0 = p.has_shared ? (p.T + BM - 1) / BM : 0;
     const int tiles0 = mt0 * p.nt[0];
@@ -86,6 +89,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
       t.row0 = m * BM;
       t.rows = min(BM, p.T - m * BM);
       t.n = n;
+      t.mt = m;
     } else {
       const int l = tile - tiles0;
       const int nt = p.nt[1];
@@ -103,6 +107,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
       t.row0 = s_off[e] + m * BM;
       t.rows = min(BM, s_off[e + 1] - s_off[e] - m * BM);
       t.n = n;
+      t.mt = s_mt[e] + m;
     }
     int nkb;
     if constexpr (MODE == G_FWD_GU || MODE == G_BWD_DA) nkb = p.d / BK;
@@ -246,25 +251,126 @@ __device__ __forceinline__ void ld_row64(const void* src, uint32_t (&v)[16]) {
   }
 }
 
-// G_BWD_DW epilogue: for each 64-column box of the warp's 32 rows, every thread writes its row
-// (128 B) into the warp's 4 KB staging buffer (16-byte chunk j of row r at chunk j ^ (r % 8), so
-// neither side conflicts on banks), then the warp reads it back by rows and stores four whole
-// 128-byte rows per instruction.  The TMEM loads of the next box are in flight meanwhile.
-__device__ __forceinline__ void dw_tmem_box(uint32_t taddr, bool zero, uint32_t (&v)[2][32]) {
-  if (!zero) {
-    tmem_ld32(taddr, v[0]);
-    tmem_ld32(taddr + 32, v[1]);
-  } else {
+// Staged row stores shared by the epilogues with plain row-major bf16 outputs.  Per 32-column
+// chunk each thread's row (64 B) goes into the warp's 2 KB staging buffer (16-byte chunk i of row
+// r at i ^ ((r / 2) % 4): conflict-free on both sides), then the warp reads it back by rows and
+// stores eight whole 64-byte row pieces per instruction, skipping rows at or past `nrows` and
+// columns at or past `ncols` (both counted from `o`, the warp's first row and column).
+__device__ __forceinline__ void rows_store_chunk(__nv_bfloat16* o, int64_t ld, int nrows, int ncols,
+                                                 uint32_t stg, int lane, const uint32_t (&P)[16]) {
+  const uint32_t mine = stg + lane * 64;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[0][i] = v[1][i] = 0u;
+  for (int i = 0; i < 4; ++i)
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(mine + ((i ^ ((lane >> 1) & 3)) << 4)),
+                 "r"(P[4 * i]), "r"(P[4 * i + 1]), "r"(P[4 * i + 2]), "r"(P[4 * i + 3])
+                 : "memory");
+  __syncwarp();
+  const int ch = lane & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = 8 * j + (lane >> 2);  // rows 8j..8j+7, four 16-byte chunks each
+    uint32_t a, b, c, d;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)));
+    if (r < nrows && 8 * ch < ncols) *reinterpret_cast<uint4*>(o + r * ld + 8 * ch) = make_uint4(a, b, c, d);
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void pack_scaled(const uint32_t (&v)[32], float s, uint32_t (&P)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    P[i] = pack_bf16x2(s * __uint_as_float(v[2 * i]), s * __uint_as_float(v[2 * i + 1]));
+}
+
+// One warp's NCH x 32 accumulator columns (its TMEM lane quarter, from column `tcol`) times `s`
+// (per thread: its row's factor) to bf16 rows through rows_store_chunk; `zero` writes zeros
+// without reading TMEM.  The warp arrives on `release` once it no longer needs the accumulator:
+// with EARLY, after packing every column into registers (the next tile's MMAs then run under the
+// stores); otherwise at the end, with the TMEM load of the next chunk in flight during each
+// chunk's stores.
+template <int NCH, bool EARLY>
+__device__ __forceinline__ void store_acc_rows(__nv_bfloat16* o, int64_t ld, int nrows, int ncols,
+                                               uint32_t tcol, bool zero, float s, uint32_t stg,
+                                               int lane, uint32_t release) {
+  if (nrows <= 0 || ncols <= 0) {
+    tc_fence_before();
+    mbar_arrive(release);
+    return;
+  }
+  if constexpr (EARLY) {
+    static_assert(NCH % 2 == 0, "pairs of chunks");
+    uint32_t P[NCH][16];
+#pragma unroll
+    for (int c = 0; c < NCH; c += 2) {
+      uint32_t v[2][32];
+      if (!zero) {
+        tmem_ld32(tcol + 32 * c, v[0]);
+        tmem_ld32(tcol + 32 * c + 32, v[1]);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[0][i] = v[1][i] = 0u;
+      }
+      pack_scaled(v[0], s, P[c]);
+      pack_scaled(v[1], s, P[c + 1]);
+    }
+    tc_fence_before();
+    mbar_arrive(release);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c)
+      rows_store_chunk(o + 32 * c, ld, nrows, ncols - 32 * c, stg, lane, P[c]);
+  } else {
+    uint32_t v[2][32];
+    if (!zero) tmem_ld32(tcol, v[0]);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      uint32_t P[16];
+      if (!zero) {
+        tmem_ld_wait();
+        pack_scaled(v[c & 1], s, P);
+        if (c + 1 < NCH) tmem_ld32(tcol + 32 * (c + 1), v[(c + 1) & 1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) P[i] = 0u;
+      }
+      rows_store_chunk(o + 32 * c, ld, nrows, ncols - 32 * c, stg, lane, P);
+    }
+    tc_fence_before();
+    mbar_arrive(release);
   }
 }
 
+// Columns of one epilogue warp: all BN with four epilogue warps, half with eight.
+template <int MODE, int BN>
+constexpr int warp_cols() { return Cfg<MODE, BN>::EPI_WARPS == 8 ? BN / 2 : BN; }
+
+// G_FWD_DOWN, G_FWD_DOWN_MX (Y_s = router weight x accumulator; the shared expert's rows take
+// weight 1) and G_BWD_DX (dX_s = accumulator): row-major outputs with d columns, rows past the
+// expert's last token skipped.
+template <int MODE, int BN>
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, const Tile& t, uint32_t tacc,
+                                              uint32_t stg, int q, int half, int lane,
+                                              uint32_t release) {
+  constexpr int cols = warp_cols<MODE, BN>();
+  const int nrows = t.rows - q * 32;  // valid rows among this warp's 32 (may be <= 0)
+  float s = 1.0f;
+  if (MODE != G_BWD_DX && t.g == 1 && lane < nrows) s = p.row_w[t.row0 + q * 32 + lane];
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out0[t.g]) + (int64_t)(t.row0 + q * 32) * p.d +
+                     t.n * BN + cols * half;
+  store_acc_rows<cols / 32, Cfg<MODE, BN>::NUM_ACC == 1>(o, p.d, nrows, cols, tacc + cols * half,
+                                                         false, s, stg, lane, release);
+}
+
+// G_BWD_DW: weight gradients [d x F] (dW_gate, dW_up), [F x d] (dW_down) or [d x E] (router);
+// an expert without tokens gets zeros.
 template <int BN>
 __device__ __forceinline__ void epilogue_dw(const GemmParams& p, const Tile& t, uint32_t tacc,
-                                            uint32_t stg, int q, int lane) {
+                                            uint32_t stg, int q, int half, int lane,
+                                            uint32_t release) {
   using bf16 = __nv_bfloat16;
-  const bool zero = (t.nkb == 0);    // an expert without tokens: its gradient is zero
+  constexpr int cols = warp_cols<G_BWD_DW, BN>();
   bf16* out;
   int ld, ncols;
   if (t.g == 2) {
@@ -281,127 +387,9 @@ __device__ __forceinline__ void epilogue_dw(const GemmParams& p, const Tile& t, 
     }
     ncols = ld;
   }
-  const int row0 = t.m0 + 32 * q;
-  uint32_t v[2][2][32];
-  dw_tmem_box(tacc, zero, v[0]);
-#pragma unroll
-  for (int b = 0; b < BN / 64; ++b) {
-    uint32_t(&cur)[2][32] = v[b & 1];
-    if (!zero) tmem_ld_wait();
-    const uint32_t mine = stg + lane * 128;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t* w = &cur[i >> 2][8 * (i & 3)];
-      const uint32_t a = pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1]));
-      const uint32_t bb = pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3]));
-      const uint32_t cc = pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5]));
-      const uint32_t d = pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7]));
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(mine + ((i ^ (lane & 7)) << 4)),
-                   "r"(a), "r"(bb), "r"(cc), "r"(d)
-                   : "memory");
-    }
-    __syncwarp();
-    if (b + 1 < BN / 64) dw_tmem_box(tacc + 64 * (b + 1), zero, v[(b + 1) & 1]);
-    const int col = t.n * BN + 64 * b + 8 * (lane & 7);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = 4 * i + (lane >> 3);  // rows 4i..4i+3, eight 16-byte chunks each
-      uint32_t a, bb, cc, d;
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(a), "=r"(bb), "=r"(cc), "=r"(d)
-                   : "r"(stg + r * 128 + (((lane & 7) ^ (r & 7)) << 4)));
-      if (col < ncols)
-        *reinterpret_cast<uint4*>(out + (int64_t)(row0 + r) * ld + col) = make_uint4(a, bb, cc, d);
-    }
-    __syncwarp();
-  }
-}
-
-// Row-major outputs with d columns (G_FWD_DOWN, G_FWD_DOWN_MX: Y_s = router weight x accumulator;
-// G_BWD_DX: dX_s = accumulator).  Per 32-column chunk each thread's row (64 B of bf16) goes into
-// the warp's 2 KB staging buffer (16-byte chunk i of row r at i ^ ((r / 2) % 4): conflict-free on
-// both sides), then the warp reads it back by rows and stores eight whole 64-byte row pieces per
-// instruction, skipping rows past the expert's last token.  With a single accumulator the warp
-// first packs all its columns into registers and releases the accumulator (arrival on `release`)
-// so that the next tile's MMAs run under the stores; with two, the TMEM load of the next chunk is
-// in flight during the stores and the accumulator is released at the end.
-template <int MODE, int BN>
-__device__ __forceinline__ void rows_store_chunk(__nv_bfloat16* o, int ld, int nrows, uint32_t stg,
-                                                 int lane, const uint32_t (&P)[16]) {
-  const uint32_t mine = stg + lane * 64;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(mine + ((i ^ ((lane >> 1) & 3)) << 4)),
-                 "r"(P[4 * i]), "r"(P[4 * i + 1]), "r"(P[4 * i + 2]), "r"(P[4 * i + 3])
-                 : "memory");
-  __syncwarp();
-  const int ch = lane & 3;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int r = 8 * j + (lane >> 2);  // rows 8j..8j+7, four 16-byte chunks each
-    uint32_t a, b, c, d;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-                 : "r"(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)));
-    if (r < nrows) *reinterpret_cast<uint4*>(o + (int64_t)r * ld + 8 * ch) = make_uint4(a, b, c, d);
-  }
-  __syncwarp();
-}
-
-__device__ __forceinline__ void pack_scaled(const uint32_t (&v)[32], float s, uint32_t (&P)[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    P[i] = pack_bf16x2(s * __uint_as_float(v[2 * i]), s * __uint_as_float(v[2 * i + 1]));
-}
-
-template <int MODE, int BN>
-__device__ __forceinline__ void epilogue_rows(const GemmParams& p, const Tile& t, uint32_t tacc,
-                                              uint32_t stg, int q, int half, int lane,
-                                              uint32_t release) {
-  using bf16 = __nv_bfloat16;
-  using C = Cfg<MODE, BN>;
-  constexpr int cols = (C::EPI_WARPS == 8) ? BN / 2 : BN;  // columns of this warp
-  constexpr int NCH = cols / 32;
-  const int nrows = t.rows - q * 32;  // valid rows among this warp's 32 (may be <= 0)
-  if (nrows <= 0) {
-    tc_fence_before();
-    mbar_arrive(release);
-    return;
-  }
-  float s = 1.0f;
-  if (MODE != G_BWD_DX && t.g == 1 && lane < nrows) s = p.row_w[t.row0 + q * 32 + lane];
-  bf16* o = static_cast<bf16*>(p.out0[t.g]) + (int64_t)(t.row0 + q * 32) * p.d + t.n * BN + cols * half;
-  const uint32_t tcol = tacc + cols * half;
-  if constexpr (C::NUM_ACC == 1) {
-    static_assert(NCH % 2 == 0, "pairs of chunks");
-    uint32_t P[NCH][16];
-#pragma unroll
-    for (int c = 0; c < NCH; c += 2) {
-      uint32_t v[2][32];
-      tmem_ld32(tcol + 32 * c, v[0]);
-      tmem_ld32(tcol + 32 * c + 32, v[1]);
-      tmem_ld_wait();
-      pack_scaled(v[0], s, P[c]);
-      pack_scaled(v[1], s, P[c + 1]);
-    }
-    tc_fence_before();
-    mbar_arrive(release);
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) rows_store_chunk<MODE, BN>(o + 32 * c, p.d, nrows, stg, lane, P[c]);
-  } else {
-    uint32_t v[2][32];
-    tmem_ld32(tcol, v[0]);
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      tmem_ld_wait();
-      uint32_t P[16];
-      pack_scaled(v[c & 1], s, P);
-      if (c + 1 < NCH) tmem_ld32(tcol + 32 * (c + 1), v[(c + 1) & 1]);
-      rows_store_chunk<MODE, BN>(o + 32 * c, p.d, nrows, stg, lane, P);
-    }
-    tc_fence_before();
-    mbar_arrive(release);
-  }
+  const int col0 = t.n * BN + cols * half;
+  store_acc_rows<cols / 32, false>(out + (int64_t)(t.m0 + 32 * q) * ld + col0, ld, 32, ncols - col0,
+                                   tacc + cols * half, t.nkb == 0, 1.0f, stg, lane, release);
 }
 
 template <int MODE, int BN>
@@ -437,13 +425,14 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
       }
     }
   } else if constexpr (MODE == G_FWD_GU_MX) {
-    // h = SiLU(g) * u quantised per 32 columns: E4M3 codes [rows][F] + UE8M0 bytes [rows][F/32]
-    // (this warp: h columns 64*half .. 64*half+63 of the tile)
+    // h = SiLU(g) * u quantised per 32 columns: E4M3 codes [rows][F] and UE8M0 scale atoms by
+    // M tile; the tile's 128 h columns are K block t.n of the down projection (this warp: h
+    // columns 64*half .. 64*half+63 of the tile)
     const bool valid = r < t.rows;
     const int ld = t.g ? p.F : p.Fs;
     const int64_t row = t.row0 + r;
     uint8_t* hq = static_cast<uint8_t*>(p.out0[t.g]) + row * ld + t.n * 128;
-    uint8_t* hs = static_cast<uint8_t*>(p.out1[t.g]) + row * (ld / 32) + t.n * 4;
+    uint8_t* hs = static_cast<uint8_t*>(p.out1[t.g]) + sf_atom_word(t.mt, t.n, ld / 128, r);
 #pragma unroll 1
     for (int c = 64 * half; c < 64 * half + 64; c += 32) {
       uint32_t gr[32], ur[32];
@@ -510,49 +499,6 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
       }
     }
     if (valid && t.g == 1) p.partial[row * p.nt[1] + t.n] = pacc;
-  } else {  // G_BWD_DW
-    bf16* o;
-    int ld, ncols;
-    if (t.g == 2) {
-      o = static_cast<bf16*>(p.out_router);
-      ld = p.E_cols;
-      ncols = p.E_cols;
-    } else {
-      const int Fg = t.g ? p.F : p.Fs;
-      if (t.sub < 2) {
-        o = static_cast<bf16*>(t.sub ? p.out1[t.g] : p.out0[t.g]) + (int64_t)t.e * p.d * Fg;
-        ld = Fg;
-      } else {
-        o = static_cast<bf16*>(p.out2[t.g]) + (int64_t)t.e * Fg * p.d;
-        ld = p.d;
-      }
-      ncols = ld;
-    }
-    o += (int64_t)(t.m0 + r) * ld;
-    const bool zero = (t.nkb == 0);
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t v[32];
-      if (!zero) {
-        tmem_ld32(tacc + c, v);
-        tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0u;
-      }
-      const int col = t.n * BN + c;
-      if (col + 32 <= ncols) {
-        uint32_t q[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          q[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-        st_row64(o + col, q);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (col + i < ncols) o[col + i] = __float2bfloat16_rn(__uint_as_float(v[i]));
-      }
-    }
   }
 }
 
@@ -562,33 +508,22 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
 // in which row r = r0 + 32*r1 (r0 < 32, r1 < 4) keeps its four K-block scales (K elements
 // kb*128 + 32*j, j = 0..3, byte j) at offset 16*r0 + 4*r1.  Scale rows are row-major [rows][K/32]
 // in global memory, so the four bytes of a row are one aligned 32-bit word.
+// MXFP8: the stage's scale atoms (the A tile's, then one per 128 B rows) by bulk copies on the
+// stage barrier.  Gate/up: B rows 0-127 are gate rows, 128-255 up rows of the h tile; down: B rows
+// are 256 consecutive rows of W_down (two atoms).
 template <int MODE, int BN>
-__device__ __forceinline__ void fill_scale_factors(const GemmParams& p, const Tile& t, int kb,
-                                                   uint32_t sf, int lane) {
-  const int ld = p.sf_ld[t.g];
-  // A: tile rows r = lane + 32 j (rows past the tensor end become zeros)
-  const uint8_t* sa = p.sfa[t.g];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int64_t gr = (int64_t)t.row0 + lane + 32 * j;
-    const bool in = gr < p.sfa_rows[t.g];
-    cp_async4(sf + 16 * lane + 4 * j, in ? sa + gr * ld + kb * 4 : sa, in ? 4u : 0u);
-  }
-  // B: tile rows n = lane + 32 j, atom n / 128
-#pragma unroll
-  for (int j = 0; j < BN / 32; ++j) {
-    const int n = lane + 32 * j;
-    const uint8_t* sb;
-    int64_t brow;
-    if constexpr (MODE == G_FWD_GU_MX) {  // 128 gate rows then 128 up rows of the h tile
-      sb = p.sfb[t.g][n >> 7];
-      brow = (int64_t)t.n * 128 + (n & 127);
-    } else {
-      sb = p.sfb[t.g][0];
-      brow = (int64_t)t.n * BN + n;
-    }
-    cp_async4(sf + 512 + 512 * (j >> 2) + 16 * lane + 4 * (j & 3),
-              sb + (int64_t)t.e * p.sfb_estride[t.g] + brow * ld + kb * 4, 4u);
+__device__ __forceinline__ void load_scale_atoms(const GemmParams& p, const Tile& t, int kb,
+                                                 uint32_t sf, uint32_t bar) {
+  const int nkb = p.sf_kb[t.g];
+  bulk_load(sf, p.sfa[t.g] + sf_atom_word(t.mt, kb, nkb, 0), 512, bar);
+  if constexpr (MODE == G_FWD_GU_MX) {
+    const int64_t tile = (int64_t)t.e * p.nt[t.g] + t.n;  // 128-row tile of gate / up
+    bulk_load(sf + 512, p.sfb[t.g][0] + sf_atom_word(tile, kb, nkb, 0), 512, bar);
+    bulk_load(sf + 1024, p.sfb[t.g][1] + sf_atom_word(tile, kb, nkb, 0), 512, bar);
+  } else {
+    const int64_t tile = ((int64_t)t.e * p.nt[t.g] + t.n) * 2;  // two 128-row tiles of W_down
+    bulk_load(sf + 512, p.sfb[t.g][0] + sf_atom_word(tile, kb, nkb, 0), 512, bar);
+    bulk_load(sf + 1024, p.sfb[t.g][0] + sf_atom_word(tile + 1, kb, nkb, 0), 512, bar);
   }
 }
 
@@ -640,8 +575,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
 
   if (tid == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      // MXFP8: the TMA arrival plus one cp.async arrival per producer lane (scale factors)
-      mbar_init(bar_full + 8 * s, C::MX ? 33 : 1);
+      mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -697,33 +631,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
   const uint32_t tmem_base = *s_tmem;
   const int ntiles = total_tiles<MODE, BN>(p, s_mt);
 
-  if (warp == 0 && C::MX) {
-    // MXFP8 producer: lane 0 issues the TMA loads, then every lane copies its share of the
-    // stage's scale-factor atoms with cp.async and arrives on the stage barrier when they land;
-    // the producer never waits for a scale load.
-    int stage = 0;
-    uint32_t phase = 0;
-    bool run = true;
-    for (int tile = blockIdx.x; run && tile < ntiles && !*s_abort; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
-      for (int kb = 0; kb < t.nkb; ++kb) {
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort) ? 1 : 0;
-          if (ok) {
-            mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_BYTES + C::B_BYTES);
-            issue_loads<MODE, BN>(p, t, kb, sA0 + stage * C::A_BYTES, sB0 + stage * C::B_BYTES,
-                                  bar_full + 8 * stage);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) { run = false; break; }
-        fill_scale_factors<MODE, BN>(p, t, kb, sSF0 + stage * C::SF_BYTES, lane);
-        cp_async_arrive_noinc(bar_full + 8 * stage);
-        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
-      }
-    }
-  } else if (warp == 0) {
+  if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -731,9 +639,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
         const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) break;
-          mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_BYTES + C::B_BYTES);
+          mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_BYTES + C::B_BYTES + C::SF_BYTES);
           issue_loads<MODE, BN>(p, t, kb, sA0 + stage * C::A_BYTES, sB0 + stage * C::B_BYTES,
                                 bar_full + 8 * stage);
+          if constexpr (C::MX)
+            load_scale_atoms<MODE, BN>(p, t, kb, sSF0 + stage * C::SF_BYTES, bar_full + 8 * stage);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       }
@@ -773,9 +683,6 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
             // scale factors of this stage: smem atoms -> TMEM (16 columns per stage), then four
             // K = 32 block-scaled MMAs; MMA j reads byte j of each 32-bit scale word.
             const uint32_t sf = sSF0 + stage * C::SF_BYTES;
-            // the scale atoms were written by cp.async (generic proxy); tcgen05.cp reads them
-            // through the async proxy
-            fence_proxy_async_smem();
             const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL + 16 * stage;
             const uint32_t sfb_t = sfa_t + 4;
             tmem_cp_32x128b_x4(sfa_t, make_sdesc_noswz(sf, 16, 128));
@@ -830,15 +737,15 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       if (!mbar_wait(bar_tfull + 8 * buf, tph, p.status, s_abort)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
-      if constexpr (C::ROW_STAGED) {
-        // releases the accumulator itself (before its stores when there is only one)
-        epilogue_rows<MODE, BN>(p, t, tacc, sSTG0 + (warp - 2) * 2048, q, half, lane,
-                                bar_tempty + 8 * buf);
+      // the staged epilogues release the accumulator themselves (before their stores when
+      // there is only one)
+      const uint32_t stg = sSTG0 + (warp - 2) * 2048;
+      if constexpr (MODE == G_BWD_DW) {
+        epilogue_dw<BN>(p, t, tacc, stg, q, half, lane, bar_tempty + 8 * buf);
+      } else if constexpr (C::ROW_STAGED) {
+        epilogue_rows<MODE, BN>(p, t, tacc, stg, q, half, lane, bar_tempty + 8 * buf);
       } else {
-        if constexpr (MODE == G_BWD_DW)
-          epilogue_dw<BN>(p, t, tacc, sSTG0 + q * 4096, q, lane);
-        else
-          epilogue<MODE, BN>(p, t, tacc, r, half);
+        epilogue<MODE, BN>(p, t, tacc, r, half);
         tc_fence_before();
         mbar_arrive(bar_tempty + 8 * buf);
       }

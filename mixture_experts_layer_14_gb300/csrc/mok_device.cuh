@@ -93,17 +93,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// ------------------------------------------------------------------ cp.async (4-byte)
-// Copies 4 bytes global -> shared asynchronously; src_bytes = 0 writes zeros without reading.
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared::cta.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-// One arrival on `bar` once every cp.async this thread issued so far has landed (the arrival
-// is one of the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+// ------------------------------------------------------------------ bulk copy (untiled)
+// Copies `bytes` global -> shared (both addresses 16-byte aligned, bytes a multiple of 16) and
+// completes them on `bar` like a TMA tile load.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05

@@ -61,12 +61,11 @@ struct GemmParams {
   const void* in1[2];   // U (saved)
   const float* row_w;   // router weight of each routed row (sorted_w)
   float* partial;       // G_BWD_DA: <a,h> per (routed row, N tile), [R, nt[1]]
-  // MXFP8 scale factors (UE8M0 bytes, row-major [rows][K/32]); [group]
-  const uint8_t* sfa[2];       // A rows (x / x_sorted or h_sh / h)
-  int64_t sfa_rows[2];         // rows of the A scale tensor (bounds)
-  const uint8_t* sfb[2][2];    // B rows per expert: [group][gate/up or down]
-  int64_t sfb_estride[2];      // bytes between experts
-  int sf_ld[2];                // bytes per scale row (= K/32)
+  // MXFP8 scale factors as scale atoms (mok_mx.cuh), [group]: A by M tile (the tile's index in
+  // the M-grouped decode), B by 128-row tile of each expert's K-major weight
+  const uint8_t* sfa[2];       // x / x_sorted (gate/up) or h_sh / h (down)
+  const uint8_t* sfb[2][2];    // [group][gate, up] or [group][down]
+  int sf_kb[2];                // K blocks of 128 (= K/128)
   int* status;
 };
 
@@ -122,9 +121,12 @@ cudaError_t launch_router_backward(int64_t T, int E, int k, int ldp, const int32
 
 int num_sms();
 
-// MXFP8 quantisation (mx.cu)
+// MXFP8 quantisation (mx.cu); scale atoms are described in mok_mx.cuh
 cudaError_t launch_mx_quantize_rows(const void* src, int64_t rows, int K, void* q, void* sc,
-                                    cudaStream_t s);
+                                    bool atoms, cudaStream_t s);
+cudaError_t launch_gather_scale_atoms(const void* src, const int32_t* sorted_tok,
+                                      const int32_t* offsets, int E, int64_t T, int64_t R, int K,
+                                      void* dst, cudaStream_t s);
 cudaError_t launch_mx_quantize_transpose(const void* src, int64_t nmat, int K, int N, void* q,
                                          void* sc, cudaStream_t s);
 cudaError_t launch_gather_bytes(const void* src, const int32_t* rows, int64_t nrows, int64_t nsrc,

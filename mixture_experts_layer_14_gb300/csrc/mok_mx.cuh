@@ -8,6 +8,16 @@
 
 namespace mok {
 
+// Scale-factor atoms.  The UE8M0 scales of 128 rows x one 128-element K block (4 bytes per row,
+// one per 32 elements) are kept as 512 contiguous bytes with row r at byte 16 (r % 32) + 4 (r / 32)
+// and block j of the 128 at + j: the shared-memory image that tcgen05.cp (32x128b, warpx4) moves
+// into TMEM for the block-scaled MMA, so that a GEMM stage fetches each operand's scales with one
+// bulk copy.  A scale tensor of rows x K/32 bytes is stored as [row tiles][K/128] atoms.
+// Byte offset of the 4-byte word of row r (0..127) of row tile `tile` in K block kb of nkb.
+__host__ __device__ __forceinline__ int64_t sf_atom_word(int64_t tile, int kb, int nkb, int r) {
+  return (tile * nkb + kb) * 512 + 16 * (r & 31) + 4 * (r >> 5);
+}
+
 // Scale exponent of a block from its amax (fp32, finite, >= 0), by exact bit inspection:
 // with amax = m 2^E, m in [1,2), the smallest s with amax <= 448 * 2^s = 1.75 * 2^(s+8) is
 // E - 8 when m <= 1.75 and E - 7 otherwise.

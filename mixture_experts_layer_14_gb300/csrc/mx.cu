@@ -8,8 +8,10 @@
 
 namespace mok {
 
-// rows x K bf16 (row-major) -> codes [rows][K] and scale bytes [rows][K/32].  One warp per row,
-// one 32-element block per lane per iteration.
+// rows x K bf16 (row-major) -> codes [rows][K] and scale bytes, [rows][K/32] or (ATOMS, K a
+// multiple of 128) scale atoms by 128-row tile.  One warp per row, one 32-element block per lane
+// per iteration.
+template <bool ATOMS>
 __global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const __nv_bfloat16* __restrict__ src,
                                                                int64_t rows, int K,
                                                                uint8_t* __restrict__ q,
@@ -37,14 +39,18 @@ __global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const __nv_bfloat
       const uint32_t sb = mx_block32(v, qq);
       q4[b * 2] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
       q4[b * 2 + 1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
-      sc[r * nblk + b] = (uint8_t)sb;
+      if (ATOMS)
+        sc[sf_atom_word(r >> 7, b >> 2, nblk >> 2, (int)(r & 127)) + (b & 3)] = (uint8_t)sb;
+      else
+        sc[r * nblk + b] = (uint8_t)sb;
     }
   }
 }
 
 // Weights: src [n][K][N] bf16 (row-major, the layer's x @ W layout) -> codes [n][N][K] (K-major,
-// the operand layout of the block-scaled MMA) and scales [n][N][K/32].  One thread per
-// (matrix, column, K block): 32 strided reads (coalesced across the warp), 32 contiguous bytes out.
+// the operand layout of the block-scaled MMA) and scale atoms of the [n][N][K/32] scales, by
+// 128-row tile of each matrix (N and K multiples of 128).  One thread per (matrix, column, K
+// block): 32 strided reads (coalesced across the warp), 32 contiguous bytes out.
 __global__ void __launch_bounds__(256) mx_quantize_transpose_kernel(
     const __nv_bfloat16* __restrict__ src, int64_t nmat, int K, int N, uint8_t* __restrict__ q,
     uint8_t* __restrict__ sc) {
@@ -65,18 +71,18 @@ __global__ void __launch_bounds__(256) mx_quantize_transpose_kernel(
     uint4* d = reinterpret_cast<uint4*>(q + (m * N + col) * (int64_t)K + (int64_t)kb * 32);
     d[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
     d[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
-    sc[(m * N + col) * (int64_t)nblk + kb] = (uint8_t)sb;
+    sc[sf_atom_word(m * (N / 128) + col / 128, kb >> 2, nblk >> 2, col & 127) + (kb & 3)] = (uint8_t)sb;
   }
 }
 
 cudaError_t launch_mx_quantize_rows(const void* src, int64_t rows, int K, void* q, void* sc,
-                                    cudaStream_t s) {
+                                    bool atoms, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 8);
   prof_begin("mx_quantize", s);
-  mx_quantize_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows,
-                                                      K, static_cast<uint8_t*>(q),
-                                                      static_cast<uint8_t*>(sc));
+  auto k = atoms ? mx_quantize_rows_kernel<true> : mx_quantize_rows_kernel<false>;
+  k<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, K,
+                                static_cast<uint8_t*>(q), static_cast<uint8_t*>(sc));
   prof_end(s);
   return cudaGetLastError();
 }
@@ -90,6 +96,73 @@ cudaError_t launch_mx_quantize_transpose(const void* src, int64_t nmat, int K, i
   mx_quantize_transpose_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src),
                                                            nmat, K, N, static_cast<uint8_t*>(q),
                                                            static_cast<uint8_t*>(sc));
+  prof_end(s);
+  return cudaGetLastError();
+}
+
+// Scale atoms of the pulled rows: sorted row i (expert e, i - offsets[e] = 128 m + r) takes the
+// scales of token sorted_tok[i] (atoms of x by 128-token tile) into row r of M tile s_mt[e] + m,
+// s_mt being the prefix over experts of ceil(rows / 128), the M-grouped GEMM's tile order.  One
+// 4-byte word (the row's four scales of one K block) per thread and (row, K block).
+__global__ void __launch_bounds__(256) gather_scale_atoms_kernel(
+    const uint8_t* __restrict__ src, const int32_t* __restrict__ sorted_tok,
+    const int32_t* __restrict__ offsets, int E, int64_t T, int nkb, uint8_t* __restrict__ dst) {
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_mt[kMaxE + 1];
+  if (threadIdx.x < 32) {  // one warp: offsets and the M-tile prefix
+    const int lane = threadIdx.x;
+    const int per = (E + 31) / 32;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) local += (offsets[e + 1] - offsets[e] + 127) / 128;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        s_off[e] = offsets[e];
+        s_mt[e] = run;
+        run += (offsets[e + 1] - offsets[e] + 127) / 128;
+      }
+    }
+    if (lane == 31) s_off[E] = offsets[E];
+  }
+  __syncthreads();
+  const int64_t R = s_off[E];
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < R * nkb;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int kb = (int)(i / R);
+    const int row = (int)(i - (int64_t)kb * R);
+    int lo = 0, hi = E;  // the expert holding sorted row `row`: largest e with s_off[e] <= row
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_off[mid] <= row) lo = mid; else hi = mid;
+    }
+    const int local = row - s_off[lo];
+    const int64_t tok = sorted_tok[row];
+    uint32_t w = 0u;
+    if (tok >= 0 && tok < T)
+      w = *reinterpret_cast<const uint32_t*>(src + sf_atom_word(tok >> 7, kb, nkb, (int)(tok & 127)));
+    *reinterpret_cast<uint32_t*>(dst + sf_atom_word(s_mt[lo] + local / 128, kb, nkb, local & 127)) = w;
+  }
+}
+
+cudaError_t launch_gather_scale_atoms(const void* src, const int32_t* sorted_tok,
+                                      const int32_t* offsets, int E, int64_t T, int64_t R, int K,
+                                      void* dst, cudaStream_t s) {
+  if (R == 0 || E == 0) return cudaSuccess;
+  const int nkb = K / 128;
+  const int64_t blocks = std::min<int64_t>((R * nkb + 255) / 256, (int64_t)num_sms() * 8);
+  prof_begin("gather_scale_atoms", s);
+  gather_scale_atoms_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint8_t*>(src), sorted_tok,
+                                                        offsets, E, T, nkb, static_cast<uint8_t*>(dst));
   prof_end(s);
   return cudaGetLastError();
 }

@@ -50,6 +50,30 @@ def _mx_shape(base, **kw):
     return base.with_(dtype="mxfp8", **kw)
 
 
+def scales_from_atoms(flat, n, N, K):
+    """[n][N][K/32] scale bytes from the 512-byte atoms [n][N/128][K/128] of mok.h: row
+    128a + 32 r1 + r0, block 4b + j at byte 16 r0 + 4 r1 + j of atom (a, b)."""
+    a = flat.reshape(n, N // 128, K // 128, 32, 4, 4)          # [n][a][b][r0][r1][j]
+    return a.transpose(0, 1, 4, 3, 2, 5).reshape(n, N, K // 32)  # [n][a][r1][r0][b][j]
+
+
+def test_atom_reader_on_a_known_layout():
+    """The atom reader places the byte written for (row, block) by the rule in mok.h back at
+    (row, block) (a layout check of the test's own reader, no GPU work)."""
+    n, N, K = 2, 256, 512
+    flat = np.zeros(n * N * K // 32, dtype=np.int64)
+    for m in range(n):
+        for row in range(N):
+            for blk in range(K // 32):
+                a, r = divmod(row, 128)
+                b, j = divmod(blk, 4)
+                off = ((m * (N // 128) + a) * (K // 128) + b) * 512 + 16 * (r % 32) + 4 * (r // 32) + j
+                flat[off] = (m * N + row) * 1000 + blk
+    got = scales_from_atoms(flat, n, N, K)
+    want = (np.arange(n)[:, None, None] * N + np.arange(N)[None, :, None]) * 1000 + np.arange(K // 32)
+    assert (got == want).all()
+
+
 def test_prepared_weights_bit_exact():
     ensure_lib()
     shape = _mx_shape(WORKLOADS["tiny"], F=256, F_shared=128)
@@ -72,7 +96,7 @@ def test_prepared_weights_bit_exact():
         Wt = np.swapaxes(f64(W), 1, 2)               # [n][N][K]: K-major
         q_ref, s_ref = oracle.mx_quantize(Wt)
         q = buf[offs[2 * i]:offs[2 * i] + n * N * K].reshape(n, N, K)
-        s = buf[offs[2 * i + 1]:offs[2 * i + 1] + n * N * K // 32].reshape(n, N, K // 32)
+        s = scales_from_atoms(buf[offs[2 * i + 1]:offs[2 * i + 1] + n * N * K // 32], n, N, K)
         assert (s == s_ref).all(), f"scales of matrix {i}"
         assert (q == q_ref).all(), f"codes of matrix {i}"
 
