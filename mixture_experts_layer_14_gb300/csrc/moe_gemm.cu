@@ -222,7 +222,8 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, 
     while (seg < 2 && kk >= p.segkb[t.g][seg]) { kk -= p.segkb[t.g][seg]; ++seg; }
     tma_load_2d(sA, &M[(t.g ? MS_A3 : MS_A0) + seg], bar, kk * BK, t.row0);
     tma_load_3d(sB, &M[(t.g ? MS_B3 : MS_B0) + seg], bar, kk * BK, t.n * BN, seg == 2 ? 0 : t.e);
-  } else {  // G_BWD_DW
+  } else {
+    static_assert(MODE == G_BWD_DW, "every mode has its loads");
     const int krow = t.row0 + kb * BK;
     int ia, ib;
     if (t.g == 2) { ia = MS_R_A; ib = MS_R_B; }
@@ -392,10 +393,48 @@ __device__ __forceinline__ void epilogue_dw(const GemmParams& p, const Tile& t, 
                                    tacc + cols * half, t.nkb == 0, 1.0f, stg, lane, release);
 }
 
+// G_FWD_GU_MX: h = SiLU(g) * u quantised per 32 columns into E4M3 codes [rows][F] and UE8M0
+// scale atoms by M tile; the tile's 128 h columns are K block t.n of the down projection.  This
+// warp takes h columns 64*half .. 64*half+63 of the tile: both 32-column blocks are computed and
+// quantised in registers, the accumulator is released (the next tile's MMAs then run under the
+// stores), then the codes and scale bytes are written.
+template <int BN>
+__device__ __forceinline__ void epilogue_gu_mx(const GemmParams& p, const Tile& t, uint32_t tacc,
+                                               int r, int half, uint32_t release) {
+  uint32_t qq[2][8], sb[2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const int c = 64 * half + 32 * b;
+    uint32_t gr[32], ur[32];
+    tmem_ld32(tacc + c, gr);
+    tmem_ld32(tacc + 128 + c, ur);
+    tmem_ld_wait();
+    float hv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) hv[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+    sb[b] = mx_block32(hv, qq[b]);
+  }
+  tc_fence_before();
+  mbar_arrive(release);
+  if (r < t.rows) {
+    const int ld = t.g ? p.F : p.Fs;
+    uint8_t* hq = static_cast<uint8_t*>(p.out0[t.g]) + (int64_t)(t.row0 + r) * ld + t.n * 128 + 64 * half;
+    uint4* d = reinterpret_cast<uint4*>(hq);
+    d[0] = make_uint4(qq[0][0], qq[0][1], qq[0][2], qq[0][3]);
+    d[1] = make_uint4(qq[0][4], qq[0][5], qq[0][6], qq[0][7]);
+    d[2] = make_uint4(qq[1][0], qq[1][1], qq[1][2], qq[1][3]);
+    d[3] = make_uint4(qq[1][4], qq[1][5], qq[1][6], qq[1][7]);
+    // scale bytes of blocks 2*half and 2*half+1: adjacent bytes of the row's atom word
+    uint8_t* hs = static_cast<uint8_t*>(p.out1[t.g]) + sf_atom_word(t.mt, t.n, ld / 128, r) + 2 * half;
+    *reinterpret_cast<uint16_t*>(hs) = (uint16_t)(sb[0] | (sb[1] << 8));
+  }
+}
+
 template <int MODE, int BN>
 __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uint32_t tacc,
                                          int r, int half) {
   using bf16 = __nv_bfloat16;
+  static_assert(MODE == G_FWD_GU || MODE == G_BWD_DA, "the other modes have their own epilogues");
   if constexpr (MODE == G_FWD_GU) {
     const bool valid = r < t.rows;
     const int ld = t.g ? p.F : p.Fs;
@@ -422,34 +461,6 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
         st_row64(h + c, hp);
         if (G) st_row64(G + c, gp);
         if (U) st_row64(U + c, up);
-      }
-    }
-  } else if constexpr (MODE == G_FWD_GU_MX) {
-    // h = SiLU(g) * u quantised per 32 columns: E4M3 codes [rows][F] and UE8M0 scale atoms by
-    // M tile; the tile's 128 h columns are K block t.n of the down projection (this warp: h
-    // columns 64*half .. 64*half+63 of the tile)
-    const bool valid = r < t.rows;
-    const int ld = t.g ? p.F : p.Fs;
-    const int64_t row = t.row0 + r;
-    uint8_t* hq = static_cast<uint8_t*>(p.out0[t.g]) + row * ld + t.n * 128;
-    uint8_t* hs = static_cast<uint8_t*>(p.out1[t.g]) + sf_atom_word(t.mt, t.n, ld / 128, r);
-#pragma unroll 1
-    for (int c = 64 * half; c < 64 * half + 64; c += 32) {
-      uint32_t gr[32], ur[32];
-      tmem_ld32(tacc + c, gr);
-      tmem_ld32(tacc + 128 + c, ur);
-      tmem_ld_wait();
-      if (valid) {
-        float hv[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          hv[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
-        uint32_t qq[8];
-        const uint32_t sb = mx_block32(hv, qq);
-        uint4* d = reinterpret_cast<uint4*>(hq + c);
-        d[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
-        d[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
-        hs[c / 32] = (uint8_t)sb;
       }
     }
   } else if constexpr (MODE == G_BWD_DA) {
@@ -737,13 +748,15 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       if (!mbar_wait(bar_tfull + 8 * buf, tph, p.status, s_abort)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
-      // the staged epilogues release the accumulator themselves (before their stores when
-      // there is only one)
+      // the staged and MXFP8 epilogues release the accumulator themselves (before their stores
+      // when there is only one)
       const uint32_t stg = sSTG0 + (warp - 2) * 2048;
       if constexpr (MODE == G_BWD_DW) {
         epilogue_dw<BN>(p, t, tacc, stg, q, half, lane, bar_tempty + 8 * buf);
       } else if constexpr (C::ROW_STAGED) {
         epilogue_rows<MODE, BN>(p, t, tacc, stg, q, half, lane, bar_tempty + 8 * buf);
+      } else if constexpr (MODE == G_FWD_GU_MX) {
+        epilogue_gu_mx<BN>(p, t, tacc, r, half, bar_tempty + 8 * buf);
       } else {
         epilogue<MODE, BN>(p, t, tacc, r, half);
         tc_fence_before();
