@@ -780,6 +780,7 @@ static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   static const char* kNames[] = {"gemm_fwd_gate_up", "gemm_fwd_down", "gemm_bwd_da", "gemm_bwd_dx",
                                  "gemm_bwd_dw", "gemm_fwd_gate_up_mx", "gemm_fwd_down_mx"};
+  if (grid <= 0) return cudaSuccess;
   prof_begin(kNames[MODE], s);
   k<<<grid, Cfg<MODE, BN>::THREADS, smem, s>>>(p);
   prof_end(s);

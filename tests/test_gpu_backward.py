@@ -17,6 +17,10 @@ CASES = {
     "tiny": WORKLOADS["tiny"].with_(backward=True),
     "ragged_skew": LayerShape("ragged_skew", 300, 384, 16, 4, 256, 384, 1, 0.0, "zipf", "bf16", True, 21),
     "noshared": LayerShape("noshared", 190, 256, 8, 3, 128, 0, 0, 0.05, "normal0.1", "bf16", True, 22),
+    # 256-column weight-gradient tiles (d, F, Fs multiples of 256) with several M and N tiles
+    # per problem; skewed routing leaves experts with few or no rows
+    "wide_tiles_skew": LayerShape("wide_tiles_skew", 260, 512, 8, 2, 512, 512, 1, 0.0, "zipf", "bf16", True, 23),
+    "wide_tiles_noshared": LayerShape("wide_tiles_noshared", 200, 256, 8, 3, 256, 0, 0, 0.0, "zipf", "bf16", True, 24),
 }
 
 
