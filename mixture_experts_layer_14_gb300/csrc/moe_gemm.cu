@@ -61,10 +61,25 @@ struct Cfg {
 constexpr int kAuxBytes = 1024;                      // barriers, TMEM address, abort flag
 constexpr int kSchedBytes = 2 * (kMaxE + 1) * 4;     // expert row offsets + M-tile prefix
 
-template <int MODE, int BN>
+// PAIR: CTA-pair tiles (two CTAs of a cluster, M = 256, tcgen05.mma.cta_group::2).  Each CTA
+// stages its own 128 A rows and half of the B columns, so a stage holds half the B bytes and six
+// stages fit.
+template <int MODE, int BN, bool PAIR>
+struct KCfg : Cfg<MODE, BN> {
+  using Base = Cfg<MODE, BN>;
+  static_assert(!PAIR || (!Base::MX && !Base::K_GROUPED && BN == 256), "pairs: bf16 M-grouped, N = 256");
+  static constexpr int B_BYTES = PAIR ? Base::B_BYTES / 2 : Base::B_BYTES;
+  static constexpr int STAGE_BYTES = Base::A_BYTES + B_BYTES + Base::SF_BYTES;
+  static constexpr int STAGES = PAIR ? 6 : Base::STAGES;
+  static constexpr int BMT = PAIR ? 2 * BM : BM;  // rows of an M tile
+  static constexpr uint32_t IDESC =
+      PAIR ? make_idesc_bf16(BN, Base::A_MN, Base::B_MN, 256) : Base::IDESC;
+};
+
+template <int MODE, int BN, bool PAIR = false>
 constexpr int smem_bytes_for() {
-  return Cfg<MODE, BN>::STAGES * Cfg<MODE, BN>::STAGE_BYTES + Cfg<MODE, BN>::STAGING_BYTES +
-         kAuxBytes + kSchedBytes + 1024;
+  using C = KCfg<MODE, BN, PAIR>;
+  return C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES + kAuxBytes + kSchedBytes + 1024;
 }
 
 int gemm_smem_bytes(int bn, int /*E*/) {
@@ -72,22 +87,25 @@ int gemm_smem_bytes(int bn, int /*E*/) {
 }
 
 // ------------------------------------------------------------------ tile decode
-template <int MODE, int BN>
+// PAIR: `tile` is a pair tile of 256 rows; CTA `rank` of the pair takes rows 128 rank ..
+// 128 rank + 127 of it (rows past the group's end: t.rows <= 0, nothing stored).
+template <int MODE, int BN, bool PAIR>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_off,
-                                            const int* s_mt, int tile) {
+                                            const int* s_mt, int tile, int rank) {
+  constexpr int BMT = KCfg<MODE, BN, PAIR>::BMT;
   Tile t;
   t.sub = 0;
   t.m0 = 0;
   t.mt = 0;
   if constexpr (!Cfg<MODE, BN>::K_GROUPED) {
-    const int mt0 = p.has_shared ? (p.T + BM - 1) / BM : 0;
+    const int mt0 = p.has_shared ? (p.T + BMT - 1) / BMT : 0;
     const int tiles0 = mt0 * p.nt[0];
     if (tile < tiles0) {
       const int n = tile / mt0, m = tile - n * mt0;
       t.g = 0;
       t.e = 0;
-      t.row0 = m * BM;
-      t.rows = min(BM, p.T - m * BM);
+      t.row0 = m * BMT + rank * BM;
+      t.rows = min(BM, p.T - t.row0);
       t.n = n;
       t.mt = m;
     } else {
@@ -104,8 +122,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
       const int n = l2 / mte, m = l2 - n * mte;
       t.g = 1;
       t.e = e;
-      t.row0 = s_off[e] + m * BM;
-      t.rows = min(BM, s_off[e + 1] - s_off[e] - m * BM);
+      t.row0 = s_off[e] + m * BMT + rank * BM;
+      t.rows = min(BM, s_off[e + 1] - t.row0);
       t.n = n;
       t.mt = s_mt[e] + m;
     }
@@ -168,10 +186,11 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
   return t;
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, bool PAIR>
 __device__ __forceinline__ int total_tiles(const GemmParams& p, const int* s_mt) {
   if constexpr (!Cfg<MODE, BN>::K_GROUPED) {
-    const int mt0 = p.has_shared ? (p.T + BM - 1) / BM : 0;
+    constexpr int BMT = KCfg<MODE, BN, PAIR>::BMT;
+    const int mt0 = p.has_shared ? (p.T + BMT - 1) / BMT : 0;
     return mt0 * p.nt[0] + (p.E > 0 ? s_mt[p.E] * p.nt[1] : 0);
   } else {
     const int tiles_sh =
@@ -188,11 +207,27 @@ __device__ __forceinline__ int total_tiles(const GemmParams& p, const int* s_mt)
 //  G_BWD_DA   A: dY / dY_sorted (K-major)          B: down weights (K-major view, 3D)
 //  G_BWD_DX   A: segments dG, dU (, dl)            B: gate, up (, router) weights (K-major view)
 //  G_BWD_DW   A: x / x_sorted, w*h (MN-major)      B: dG, dU, dY (MN-major); router x, dl
-template <int MODE, int BN>
-__device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, int kb,
+// PAIR: each CTA loads its A rows and its half of B (gate/up: the gate columns in the even CTA,
+// the up columns in the odd one; down: columns 128 rank .. 128 rank + 127 of the N tile), all
+// completing on the even CTA's barrier (`bar` is a cluster address).
+template <int MODE, int BN, bool PAIR>
+__device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, int kb, int rank,
                                             uint32_t sA, uint32_t sB, uint32_t bar) {
+  static_assert(!PAIR || MODE == G_FWD_GU || MODE == G_FWD_DOWN, "pair loads: gate/up and down");
   const CUtensorMap* M = p.maps;
-  if constexpr (MODE == G_FWD_GU) {
+  if constexpr (PAIR && MODE == G_FWD_GU) {
+    tma_load_2d_pair(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
+    const CUtensorMap* b = rank ? &M[t.g ? MS_B4 : MS_B1] : &M[t.g ? MS_B3 : MS_B0];
+    const int c0 = t.n * 128;
+    tma_load_3d_pair(sB, b, bar, c0, kb * BK, t.e);
+    tma_load_3d_pair(sB + 8192, b, bar, c0 + 64, kb * BK, t.e);
+  } else if constexpr (PAIR && MODE == G_FWD_DOWN) {
+    tma_load_2d_pair(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
+    const CUtensorMap* b = &M[t.g ? MS_B3 : MS_B0];
+    const int c0 = t.n * BN + 128 * rank;
+    tma_load_3d_pair(sB, b, bar, c0, kb * BK, t.e);
+    tma_load_3d_pair(sB + 8192, b, bar, c0 + 64, kb * BK, t.e);
+  } else if constexpr (MODE == G_FWD_GU) {
     tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
     const CUtensorMap* bg = &M[t.g ? MS_B3 : MS_B0];
     const CUtensorMap* bu = &M[t.g ? MS_B4 : MS_B1];
@@ -252,6 +287,14 @@ __device__ __forceinline__ void ld_row64(const void* src, uint32_t (&v)[16]) {
   }
 }
 
+// The warp no longer needs the accumulator: one arrival per warp on the accumulator-empty barrier
+// at cluster address `release` (this CTA's, or the even CTA's of a CTA pair).
+__device__ __forceinline__ void acc_release(uint32_t release, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive_cluster(release);
+}
+
 // Staged row stores shared by the epilogues with plain row-major bf16 outputs.  Per 32-column
 // chunk each thread's row (64 B) goes into the warp's 2 KB staging buffer (16-byte chunk i of row
 // r at i ^ ((r / 2) % 4): conflict-free on both sides), then the warp reads it back by rows and
@@ -296,8 +339,7 @@ __device__ __forceinline__ void store_acc_rows(__nv_bfloat16* o, int64_t ld, int
                                                uint32_t tcol, bool zero, float s, uint32_t stg,
                                                int lane, uint32_t release) {
   if (nrows <= 0 || ncols <= 0) {
-    tc_fence_before();
-    mbar_arrive(release);
+    acc_release(release, lane);
     return;
   }
   if constexpr (EARLY) {
@@ -317,8 +359,7 @@ __device__ __forceinline__ void store_acc_rows(__nv_bfloat16* o, int64_t ld, int
       pack_scaled(v[0], s, P[c]);
       pack_scaled(v[1], s, P[c + 1]);
     }
-    tc_fence_before();
-    mbar_arrive(release);
+    acc_release(release, lane);
 #pragma unroll
     for (int c = 0; c < NCH; ++c)
       rows_store_chunk(o + 32 * c, ld, nrows, ncols - 32 * c, stg, lane, P[c]);
@@ -338,8 +379,7 @@ __device__ __forceinline__ void store_acc_rows(__nv_bfloat16* o, int64_t ld, int
       }
       rows_store_chunk(o + 32 * c, ld, nrows, ncols - 32 * c, stg, lane, P);
     }
-    tc_fence_before();
-    mbar_arrive(release);
+    acc_release(release, lane);
   }
 }
 
@@ -414,8 +454,7 @@ __device__ __forceinline__ void epilogue_gu_mx(const GemmParams& p, const Tile& 
     for (int i = 0; i < 32; ++i) hv[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
     sb[b] = mx_block32(hv, qq[b]);
   }
-  tc_fence_before();
-  mbar_arrive(release);
+  acc_release(release, r & 31);
   if (r < t.rows) {
     const int ld = t.g ? p.F : p.Fs;
     uint8_t* hq = static_cast<uint8_t*>(p.out0[t.g]) + (int64_t)(t.row0 + r) * ld + t.n * 128 + 64 * half;
@@ -558,9 +597,13 @@ __device__ __forceinline__ void zero_k_tail(uint32_t sA, uint32_t sB, int valid,
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int MODE, int BN>
+// PAIR: launched in clusters of two CTAs; the pair takes one 256-row tile at a time.  The even
+// CTA issues the MMAs (cta_group::2) once both CTAs' stage has landed on its full barrier and
+// multicasts its commits to the empty and accumulator-full barriers of both CTAs; every
+// epilogue warp of both CTAs arrives on the even CTA's accumulator-empty barrier.
+template <int MODE, int BN, bool PAIR>
 __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = Cfg<MODE, BN>;
+  using C = KCfg<MODE, BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -591,7 +634,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
-      mbar_init(bar_tempty + 8 * b, C::EPI_WARPS * 32);
+      mbar_init(bar_tempty + 8 * b, C::EPI_WARPS * (PAIR ? 2 : 1));  // one arrival per warp
     }
     mbar_init(bar_drain, 1);
     *s_abort = 0;
@@ -601,8 +644,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
     for (int i = 0; i < MS_COUNT; ++i) tma_prefetch_desc(&p.maps[i]);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(s_tmem), C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(s_tmem), C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(s_tmem), C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   if (warp == 2 && p.E > 0) {
     // expert row offsets and (M-grouped) the prefix of M tiles per expert, one warp
@@ -614,7 +662,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       if (e < p.E) {
         const int o0 = p.offsets[e], o1 = p.offsets[e + 1];
         s_off[e] = o0;
-        local += (o1 - o0 + BM - 1) / BM;
+        local += (o1 - o0 + C::BMT - 1) / C::BMT;
       }
     }
     int incl = local;
@@ -628,7 +676,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       const int e = e0 + i;
       if (e < p.E) {
         s_mt[e] = run;
-        run += (p.offsets[e + 1] - p.offsets[e] + BM - 1) / BM;
+        run += (p.offsets[e + 1] - p.offsets[e] + C::BMT - 1) / C::BMT;
       }
     }
     if (lane == 31) {
@@ -638,36 +686,43 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
-  const int ntiles = total_tiles<MODE, BN>(p, s_mt);
+  const int ntiles = total_tiles<MODE, BN, PAIR>(p, s_mt);
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  const int first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // tile loop of this CTA
+  const int step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x) {
-        const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
+      for (int tile = first; tile < ntiles && !*s_abort; tile += step) {
+        const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) break;
-          mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_BYTES + C::B_BYTES + C::SF_BYTES);
-          issue_loads<MODE, BN>(p, t, kb, sA0 + stage * C::A_BYTES, sB0 + stage * C::B_BYTES,
-                                bar_full + 8 * stage);
+          if (!PAIR || rank == 0)  // a pair's stage: both CTAs' bytes on the even CTA's barrier
+            mbar_arrive_expect_tx(bar_full + 8 * stage,
+                                  (C::A_BYTES + C::B_BYTES + C::SF_BYTES) * (PAIR ? 2 : 1));
+          issue_loads<MODE, BN, PAIR>(p, t, kb, rank, sA0 + stage * C::A_BYTES,
+                                      sB0 + stage * C::B_BYTES,
+                                      PAIR ? mapa_shared(bar_full + 8 * stage, 0) : bar_full + 8 * stage);
           if constexpr (C::MX)
             load_scale_atoms<MODE, BN>(p, t, kb, sSF0 + stage * C::SF_BYTES, bar_full + 8 * stage);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && (!PAIR || rank == 0)) {
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
-    for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x, ++it) {
-      const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
+    for (int tile = first; tile < ntiles && !*s_abort; tile += step, ++it) {
+      const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
       const int buf = it % C::NUM_ACC;
       const uint32_t tph = (it / C::NUM_ACC) & 1;
-      if (!mbar_wait(bar_tempty + 8 * buf, tph ^ 1, p.status, s_abort)) break;
+      if (!mbar_wait<PAIR>(bar_tempty + 8 * buf, tph ^ 1, p.status, s_abort)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
       bool ok = true;
@@ -716,33 +771,47 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
                                             : make_sdesc(sA + k * 32, 16, 1024);
                 const uint64_t bd = C::B_MN ? make_sdesc(sB + k * 2048, 8192, 1024)
                                             : make_sdesc(sB + k * 32, 16, 1024);
-                umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
+                if constexpr (PAIR)
+                  umma_bf16_pair(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
+                else
+                  umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
               }
             }
           }
-          umma_commit(bar_empty + 8 * stage);
+          if constexpr (PAIR)
+            umma_commit_pair_mc(bar_empty + 8 * stage, 3);
+          else
+            umma_commit(bar_empty + 8 * stage);
         }
         __syncwarp();
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(bar_tfull + 8 * buf);
+      if (lane == 0) {
+        if constexpr (PAIR)
+          umma_commit_pair_mc(bar_tfull + 8 * buf, 3);
+        else
+          umma_commit(bar_tfull + 8 * buf);
+      }
       __syncwarp();
     }
     // every MMA issued by this CTA has completed before TMEM is released
     if (lane == 0) {
-      umma_commit(bar_drain);
+      if constexpr (PAIR)
+        umma_commit_pair(bar_drain);
+      else
+        umma_commit(bar_drain);
       volatile int no_abort = 0;
       mbar_wait(bar_drain, 0, p.status, &no_abort);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2) {
     const int q = warp & 3;  // TMEM lane quarter accessible to this warp
     const int half = (warp - 2) / 4;  // 8 epilogue warps: which column half
     const int r = q * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x, ++it) {
-      const Tile t = decode_tile<MODE, BN>(p, s_off, s_mt, tile);
+    for (int tile = first; tile < ntiles && !*s_abort; tile += step, ++it) {
+      const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
       const int buf = it % C::NUM_ACC;
       const uint32_t tph = (it / C::NUM_ACC) & 1;
       if (!mbar_wait(bar_tfull + 8 * buf, tph, p.status, s_abort)) break;
@@ -751,47 +820,80 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       // the staged and MXFP8 epilogues release the accumulator themselves (before their stores
       // when there is only one)
       const uint32_t stg = sSTG0 + (warp - 2) * 2048;
+      const uint32_t rel = PAIR ? mapa_shared(bar_tempty + 8 * buf, 0) : bar_tempty + 8 * buf;
       if constexpr (MODE == G_BWD_DW) {
-        epilogue_dw<BN>(p, t, tacc, stg, q, half, lane, bar_tempty + 8 * buf);
+        epilogue_dw<BN>(p, t, tacc, stg, q, half, lane, rel);
       } else if constexpr (C::ROW_STAGED) {
-        epilogue_rows<MODE, BN>(p, t, tacc, stg, q, half, lane, bar_tempty + 8 * buf);
+        epilogue_rows<MODE, BN>(p, t, tacc, stg, q, half, lane, rel);
       } else if constexpr (MODE == G_FWD_GU_MX) {
-        epilogue_gu_mx<BN>(p, t, tacc, r, half, bar_tempty + 8 * buf);
+        epilogue_gu_mx<BN>(p, t, tacc, r, half, rel);
       } else {
         epilogue<MODE, BN>(p, t, tacc, r, half);
-        tc_fence_before();
-        mbar_arrive(bar_tempty + 8 * buf);
+        acc_release(rel, lane);
       }
     }
   }
   __syncthreads();
+  // a pair: neither CTA frees TMEM or leaves while the other may still arrive on its barriers
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, bool PAIR = false>
 static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
-  constexpr int smem = smem_bytes_for<MODE, BN>();
+  constexpr int smem = smem_bytes_for<MODE, BN, PAIR>();
   static_assert(smem <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
-  auto k = moe_gemm_kernel<MODE, BN>;
+  auto k = moe_gemm_kernel<MODE, BN, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   static const char* kNames[] = {"gemm_fwd_gate_up", "gemm_fwd_down", "gemm_bwd_da", "gemm_bwd_dx",
                                  "gemm_bwd_dw", "gemm_fwd_gate_up_mx", "gemm_fwd_down_mx"};
-  if (grid <= 0) return cudaSuccess;
-  prof_begin(kNames[MODE], s);
-  k<<<grid, Cfg<MODE, BN>::THREADS, smem, s>>>(p);
-  prof_end(s);
-  return cudaGetLastError();
+  if constexpr (!PAIR) {
+    if (grid <= 0) return cudaSuccess;
+    prof_begin(kNames[MODE], s);
+    k<<<grid, Cfg<MODE, BN>::THREADS, smem, s>>>(p);
+    prof_end(s);
+    return cudaGetLastError();
+  } else {
+    // clusters of two CTAs; persistent: as many pairs as fit at once, at most one per pair tile
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(Cfg<MODE, BN>::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.gridDim = dim3(2);
+    int fit = 0;
+    e = cudaOccupancyMaxActiveClusters(&fit, k, &cfg);
+    if (e != cudaSuccess) return e;
+    const int pairs = std::min((grid + 1) / 2, fit);
+    if (pairs <= 0) return grid <= 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3(2 * pairs);
+    prof_begin(kNames[MODE], s);
+    e = cudaLaunchKernelEx(&cfg, k, p);
+    prof_end(s);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
 }
 
-cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s, bool pair) {
   switch (mode) {
-    case G_FWD_GU: return launch_one<G_FWD_GU, 256>(p, grid, s);
+    case G_FWD_GU:
+      return pair ? launch_one<G_FWD_GU, 256, true>(p, grid, s) : launch_one<G_FWD_GU, 256>(p, grid, s);
     case G_FWD_DOWN:
-      return bn == 256 ? launch_one<G_FWD_DOWN, 256>(p, grid, s) : launch_one<G_FWD_DOWN, 128>(p, grid, s);
+      if (bn != 256) return launch_one<G_FWD_DOWN, 128>(p, grid, s);
+      return pair ? launch_one<G_FWD_DOWN, 256, true>(p, grid, s) : launch_one<G_FWD_DOWN, 256>(p, grid, s);
     case G_BWD_DA:
       return bn == 256 ? launch_one<G_BWD_DA, 256>(p, grid, s) : launch_one<G_BWD_DA, 128>(p, grid, s);
     case G_BWD_DX:

@@ -70,7 +70,9 @@ struct GemmParams {
 };
 
 // Launches (moe_gemm.cu).  grid = persistent CTAs.
-cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s);
+// pair: bf16 gate/up and down (N tile 256) in CTA pairs of 256-row tiles (cluster launch).
+cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s,
+                        bool pair = false);
 int gemm_smem_bytes(int bn, int E);
 
 // Router (route.cu)

@@ -21,6 +21,8 @@ CASES = {
     # per problem; skewed routing leaves experts with few or no rows
     "wide_tiles_skew": LayerShape("wide_tiles_skew", 260, 512, 8, 2, 512, 512, 1, 0.0, "zipf", "bf16", True, 23),
     "wide_tiles_noshared": LayerShape("wide_tiles_noshared", 200, 256, 8, 3, 256, 0, 0, 0.0, "zipf", "bf16", True, 24),
+    # training forward in CTA pairs (at least 320 routed rows per expert)
+    "pairs_train": LayerShape("pairs_train", 880, 256, 8, 3, 256, 256, 1, 0.0, "zipf", "bf16", True, 25),
 }
 
 

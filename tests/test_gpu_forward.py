@@ -19,6 +19,11 @@ CASES = {
     "k_eq_E_noshared": LayerShape("k_eq_E_noshared", 129, 256, 8, 8, 128, 0, 0, 0.05, "none", "bf16", False, 12),
     "one_token": LayerShape("one_token", 1, 256, 16, 3, 256, 128, 1, 0.0, "normal0.1", "bf16", False, 13),
     "wide_E": LayerShape("wide_E", 200, 256, 384, 8, 128, 128, 1, 0.0, "normal0.1", "bf16", False, 14),
+    # at least 320 routed rows per expert: gate/up and down in CTA pairs of 256-row tiles, skewed
+    # so that experts span several pair tiles, end mid-tile or hold no rows
+    "pairs": LayerShape("pairs", 720, 256, 8, 4, 256, 256, 1, 0.0, "zipf", "bf16", False, 15),
+    # pairs for gate/up only (d not a multiple of 256: 128-column down tiles without pairs)
+    "pairs_gu_only": LayerShape("pairs_gu_only", 660, 384, 8, 4, 128, 0, 0, 0.0, "normal0.1", "bf16", False, 16),
 }
 
 
