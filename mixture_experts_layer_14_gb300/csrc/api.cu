@@ -104,7 +104,9 @@ enum PrepSlot {  // MXFP8 prepared weights: K-major codes [n][N][K] and scale at
 };
 enum BwdSlot {
   BW_STATUS, BW_XS, BW_DYS, BW_DG, BW_DU, BW_HW, BW_DGSH, BW_DUSH, BW_HWSH, BW_P, BW_DL,
-  BW_DXS, BW_DXSH, BW_N
+  BW_DXS, BW_DXSH,
+  BW_TMAP,  // weight-gradient GEMM: expert-bounded tensor-map copies
+  BW_N
 };
 enum SavedSlot { SV_G, SV_U, SV_GSH, SV_USH, SV_N };
 enum HostSlot { HS_X, HS_Y, HS_IDX, HS_W, HS_CNT, HS_OFF, HS_STOK, HS_SW, HS_INV, HS_N };
@@ -164,6 +166,7 @@ static Layout layout_bwd(const mok_dims* d) {
   sz[BW_DL] = 2ull * T * ldl;
   sz[BW_DXS] = 2ull * R * d->d;
   sz[BW_DXSH] = 2ull * T * d->d;
+  sz[BW_TMAP] = sizeof(CUtensorMap) * (size_t)kBoundMaps * d->E;
   Layout L{};
   size_t o = 0;
   for (int i = 0; i < BW_N; ++i) { L.off[i] = o; o += al(sz[i]); }
@@ -753,6 +756,26 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
     p.Fs = Fs;
     p.out0[0] = dWs_gate; p.out1[0] = dWs_up; p.out2[0] = dWs_down;
     p.out0[1] = dW_gate; p.out1[1] = dW_up; p.out2[1] = dW_down;
+    // the routed operands' maps bounded to each expert's rows
+    CUtensorMap* emaps = at<CUtensorMap*>(ws, L.off[BW_TMAP]);
+    {
+      BoundMapParams bp{};
+      const int slot[kBoundMaps] = {MS_A3, MS_A4, MS_B3, MS_B4, MS_B5};
+      const void* base[kBoundMaps] = {xs, hw, dG, dU, dys};
+      const int cols[kBoundMaps] = {d, F, F, F, d};
+      for (int j = 0; j < kBoundMaps; ++j) {
+        bp.templ[j] = p.maps[slot[j]];
+        bp.base[j] = base[j];
+        bp.cols[j] = cols[j];
+      }
+      bp.offsets = offsets;
+      bp.E = E;
+      bp.emaps = emaps;
+      rc = cuda_status(launch_dw_bound_maps(bp, s));
+      if (rc != MOK_OK) return rc;
+      ++launches;
+    }
+    p.emaps = emaps;
     p.status = static_cast<int*>(ws);
     const int64_t total = p.router_tiles +
                           (sh ? 2 * (d / BM) * (Fs / bn) + (Fs / BM) * (d / bn) : 0) +

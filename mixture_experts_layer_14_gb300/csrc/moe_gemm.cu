@@ -258,18 +258,28 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, 
     tma_load_2d(sA, &M[(t.g ? MS_A3 : MS_A0) + seg], bar, kk * BK, t.row0);
     tma_load_3d(sB, &M[(t.g ? MS_B3 : MS_B0) + seg], bar, kk * BK, t.n * BN, seg == 2 ? 0 : t.e);
   } else {
-    static_assert(MODE == G_BWD_DW, "every mode has its loads");
-    const int krow = t.row0 + kb * BK;
-    int ia, ib;
-    if (t.g == 2) { ia = MS_R_A; ib = MS_R_B; }
-    else if (t.sub == 0) { ia = t.g ? MS_A3 : MS_A0; ib = t.g ? MS_B3 : MS_B0; }
-    else if (t.sub == 1) { ia = t.g ? MS_A3 : MS_A0; ib = t.g ? MS_B4 : MS_B1; }
-    else { ia = t.g ? MS_A4 : MS_A1; ib = t.g ? MS_B5 : MS_B2; }
-    tma_load_2d(sA, &M[ia], bar, t.m0, krow);
-    tma_load_2d(sA + 8192, &M[ia], bar, t.m0 + 64, krow);
-#pragma unroll
-    for (int i = 0; i < BN / 64; ++i) tma_load_2d(sB + i * 8192, &M[ib], bar, t.n * BN + 64 * i, krow);
+    static_assert(MODE == -1, "every mode has its loads (G_BWD_DW: issue_loads_dw)");
   }
+}
+
+// G_BWD_DW: map slots of a tile's operands (g = 2: the router's x and dl).
+__device__ __forceinline__ void dw_slots(const Tile& t, int& ia, int& ib) {
+  if (t.g == 2) { ia = MS_R_A; ib = MS_R_B; }
+  else if (t.sub == 0) { ia = t.g ? MS_A3 : MS_A0; ib = t.g ? MS_B3 : MS_B0; }
+  else if (t.sub == 1) { ia = t.g ? MS_A3 : MS_A0; ib = t.g ? MS_B4 : MS_B1; }
+  else { ia = t.g ? MS_A4 : MS_A1; ib = t.g ? MS_B5 : MS_B2; }
+}
+
+// G_BWD_DW loads of one k-block: A = the tile's 128 M columns of the K-row-major operand (two
+// 64-column boxes), B = its BN N columns; `krow` = the block's first K row in the maps.
+template <int BN>
+__device__ __forceinline__ void issue_loads_dw(const CUtensorMap* ma, const CUtensorMap* mb,
+                                               const Tile& t, int krow, uint32_t sA, uint32_t sB,
+                                               uint32_t bar) {
+  tma_load_2d(sA, ma, bar, t.m0, krow);
+  tma_load_2d(sA + 8192, ma, bar, t.m0 + 64, krow);
+#pragma unroll
+  for (int i = 0; i < BN / 64; ++i) tma_load_2d(sB + i * 8192, mb, bar, t.n * BN + 64 * i, krow);
 }
 
 // ------------------------------------------------------------------ epilogues
@@ -581,20 +591,6 @@ __device__ __forceinline__ void load_scale_atoms(const GemmParams& p, const Tile
 // G_BWD_DW: the last k-block of a problem may hold rows of the next expert; zero them in both
 // operands (MN-major: K is the row index inside every 64-column box, 128 B per row, and the
 // 128-byte swizzle only permutes 16-byte chunks within a row).
-template <int BN>
-__device__ __forceinline__ void zero_k_tail(uint32_t sA, uint32_t sB, int valid, int lane) {
-  const int nrows = ((valid + 15) & ~15) - valid;  // only the MMA K steps that are issued
-  const int nboxes = 2 + BN / 64;
-  const int per_box = nrows * 8;  // 16-byte chunks
-  for (int i = lane; i < nboxes * per_box; i += 32) {
-    const int box = i / per_box;
-    const int j = i - box * per_box;
-    const int row = valid + (j >> 3);
-    const uint32_t base = (box < 2) ? sA + box * 8192 : sB + (box - 2) * 8192;
-    const uint32_t addr = base + row * 128 + (j & 7) * 16;
-    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
-  }
-}
 
 // ------------------------------------------------------------------ the kernel
 // PAIR: launched in clusters of two CTAs; the pair takes one 256-row tile at a time.  The even
@@ -695,7 +691,44 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
   const int step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if constexpr (MODE == G_BWD_DW) {
+      // A routed tile's K rows are one expert's rows: its loads go through that expert's copies
+      // of the A and B maps, bounded to its rows (dw_bound_maps_kernel), so the rows past its end
+      // arrive as zeros.  A map is acquired from the tensor-map proxy when it changes.
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        const CUtensorMap* last_a = nullptr;
+        const CUtensorMap* last_b = nullptr;
+        for (int tile = first; tile < ntiles && !*s_abort; tile += step) {
+          const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
+          if (t.nkb == 0) continue;
+          int ia, ib;
+          dw_slots(t, ia, ib);
+          const CUtensorMap* ma = &p.maps[ia];
+          const CUtensorMap* mb = &p.maps[ib];
+          int krow = t.row0;
+          if (t.g == 1) {
+            ma = p.emaps + (size_t)t.e * kBoundMaps + (ia == MS_A3 ? 0 : 1);
+            mb = p.emaps + (size_t)t.e * kBoundMaps + (ib - MS_B3 + 2);
+            if (ma != last_a) tmap_acquire(ma);
+            if (mb != last_b) tmap_acquire(mb);
+            last_a = ma;
+            last_b = mb;
+            krow = 0;
+          }
+          bool ok = true;
+          for (int kb = 0; kb < t.nkb; ++kb) {
+            if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_BYTES + C::B_BYTES);
+            issue_loads_dw<BN>(ma, mb, t, krow + kb * BK, sA0 + stage * C::A_BYTES,
+                               sB0 + stage * C::B_BYTES, bar_full + 8 * stage);
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+        }
+      }
+    } else if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = first; tile < ntiles && !*s_abort; tile += step) {
@@ -732,17 +765,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
         const uint32_t sA = sA0 + stage * C::A_BYTES, sB = sB0 + stage * C::B_BYTES;
         int nk16 = BK / 16;  // MMA K steps of this stage
         if constexpr (C::K_GROUPED) {
-          // last k-block of a problem: issue only the K steps holding rows of this problem and
-          // zero the rows of the next problem inside the last step
+          // last k-block of a problem: issue only the K steps holding rows of this problem (the
+          // rows past its end within the last step arrive as zeros: the loads are bounded to it)
           const int valid = t.rows - kb * BK;
-          if (valid < BK) {
-            nk16 = (valid + 15) / 16;
-            if (valid & 15) {
-              zero_k_tail<BN>(sA, sB, valid, lane);
-              fence_proxy_async_smem();
-              __syncwarp();
-            }
-          }
+          if (valid < BK) nk16 = (valid + 15) / 16;
         }
         if (lane == 0) {
           if constexpr (C::MX) {
@@ -843,6 +869,40 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
     else
       tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+}
+
+// One warp per (expert, routed weight-gradient operand): the operand's map with the base moved to
+// the expert's first row and the row extent cut to its rows (tensormap.replace on a shared-memory
+// copy), published to emaps[e * kBoundMaps + j] for the tensor-map proxy.  Experts without rows
+// are skipped (no tile loads them).
+__global__ void __launch_bounds__(256) dw_bound_maps_kernel(const __grid_constant__ BoundMapParams bp) {
+  __shared__ __align__(128) uint8_t smaps[8][128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 8 + warp;
+  if (i >= bp.E * kBoundMaps) return;
+  const int e = i / kBoundMaps, j = i - e * kBoundMaps;
+  const int r0 = bp.offsets[e], rows = bp.offsets[e + 1] - r0;
+  if (rows <= 0) return;
+  const uint32_t sm = smem_u32(smaps[warp]);
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(sm + 4 * lane),
+               "r"(reinterpret_cast<const uint32_t*>(&bp.templ[j])[lane])
+               : "memory");
+  __syncwarp();
+  if (lane == 0) {
+    tmap_replace_address(sm, static_cast<const char*>(bp.base[j]) + (int64_t)r0 * bp.cols[j] * 2);
+    tmap_replace_rows(sm, rows);
+  }
+  __syncwarp();
+  tmap_publish(bp.emaps + i, sm);
+}
+
+cudaError_t launch_dw_bound_maps(const BoundMapParams& bp, cudaStream_t s) {
+  const int n = bp.E * kBoundMaps;
+  if (n == 0) return cudaSuccess;
+  prof_begin("dw_bound_maps", s);
+  dw_bound_maps_kernel<<<(n + 7) / 8, 256, 0, s>>>(bp);
+  prof_end(s);
+  return cudaGetLastError();
 }
 
 template <int MODE, int BN, bool PAIR = false>

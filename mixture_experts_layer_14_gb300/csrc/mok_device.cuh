@@ -146,6 +146,34 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// ------------------------------------------------------------------ tensor-map copies
+// In-place edits of a tensor map held in shared memory (128-byte aligned).
+__device__ __forceinline__ void tmap_replace_address(uint32_t smem_map, const void* base) {
+  asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(smem_map),
+               "l"(reinterpret_cast<uint64_t>(base))
+               : "memory");
+}
+// Extent of dimension 1 (rows of a 2D map).
+__device__ __forceinline__ void tmap_replace_rows(uint32_t smem_map, int rows) {
+  asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 1, %1;" ::"r"(smem_map),
+               "r"(rows)
+               : "memory");
+}
+// Warp-wide: copies a 128-byte tensor map from shared to global memory and releases it to the
+// tensor-map proxy (GPU scope).
+__device__ __forceinline__ void tmap_publish(CUtensorMap* gmap, uint32_t smem_map) {
+  asm volatile(
+      "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned [%0], [%1], 128;" ::"l"(
+          reinterpret_cast<uint64_t>(gmap)),
+      "r"(smem_map)
+      : "memory");
+}
+// Acquire of a published map by the thread that issues loads with it.
+__device__ __forceinline__ void tmap_acquire(const CUtensorMap* gmap) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(gmap))
+               : "memory");
+}
+
 // ------------------------------------------------------------------ bulk copy (untiled)
 // Copies `bytes` global -> shared (both addresses 16-byte aligned, bytes a multiple of 16) and
 // completes them on `bar` like a TMA tile load.

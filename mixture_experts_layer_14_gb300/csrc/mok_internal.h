@@ -16,6 +16,7 @@ constexpr int kGemmThreads = 192;            // warp 0 TMA, warp 1 MMA/TMEM, war
 constexpr int kDispatchChunk = 64;           // tokens per histogram block of the counting sort
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 8;
+constexpr int kBoundMaps = 5;                   // G_BWD_DW: expert-bounded maps per expert
 
 // ------------------------------------------------------------------ grouped GEMM
 enum GemmMode : int {
@@ -66,8 +67,24 @@ struct GemmParams {
   const uint8_t* sfa[2];       // x / x_sorted (gate/up) or h_sh / h (down)
   const uint8_t* sfb[2][2];    // [group][gate, up] or [group][down]
   int sf_kb[2];                // K blocks of 128 (= K/128)
+  // G_BWD_DW: per expert, kBoundMaps copies of the routed operands' maps bounded to its rows
+  // (x_sorted, w*h, dG, dU, dY_sorted), from launch_dw_bound_maps
+  const CUtensorMap* emaps;
   int* status;
 };
+
+// Expert-bounded copies of the weight-gradient GEMM's routed operand maps (moe_gemm.cu):
+// templ[j] over the whole tensor base[j] (row-major, cols[j] bf16 per row), for j = x_sorted,
+// w*h, dG, dU, dY_sorted; emaps[e * kBoundMaps + j] gets the copy bounded to expert e's rows.
+struct BoundMapParams {
+  CUtensorMap templ[kBoundMaps];
+  const void* base[kBoundMaps];
+  int cols[kBoundMaps];
+  const int* offsets;
+  int E;
+  CUtensorMap* emaps;
+};
+cudaError_t launch_dw_bound_maps(const BoundMapParams& bp, cudaStream_t s);
 
 // Launches (moe_gemm.cu).  grid = persistent CTAs.
 // pair: bf16 gate/up and down (N tile 256) in CTA pairs of 256-row tiles (cluster launch).
