@@ -780,7 +780,10 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
     const int64_t total = p.router_tiles +
                           (sh ? 2 * (d / BM) * (Fs / bn) + (Fs / BM) * (d / bn) : 0) +
                           (int64_t)E * (2 * (d / BM) * (F / bn) + (F / BM) * (d / bn));
-    rc = cuda_status(launch_gemm(G_BWD_DW, bn, p, (int)std::min<int64_t>(grid_cap, total), s));
+    // CTA pairs (adjacent M tiles of one problem; each SM stages half the B columns) when every
+    // problem's M-tile count is even
+    const bool dw_pair = bn == 256 && (d / BM) % 2 == 0 && (F / BM) % 2 == 0 && (!sh || (Fs / BM) % 2 == 0);
+    rc = cuda_status(launch_gemm(G_BWD_DW, bn, p, (int)std::min<int64_t>(grid_cap, total), s, dw_pair));
     if (rc != MOK_OK) return rc;
     ++launches;
   }

@@ -67,11 +67,11 @@ constexpr int kSchedBytes = 2 * (kMaxE + 1) * 4;     // expert row offsets + M-t
 template <int MODE, int BN, bool PAIR>
 struct KCfg : Cfg<MODE, BN> {
   using Base = Cfg<MODE, BN>;
-  static_assert(!PAIR || (!Base::MX && !Base::K_GROUPED && BN == 256), "pairs: bf16 M-grouped, N = 256");
+  static_assert(!PAIR || (!Base::MX && BN == 256), "pairs: bf16, N = 256");
   static constexpr int B_BYTES = PAIR ? Base::B_BYTES / 2 : Base::B_BYTES;
   static constexpr int STAGE_BYTES = Base::A_BYTES + B_BYTES + Base::SF_BYTES;
   static constexpr int STAGES = PAIR ? 6 : Base::STAGES;
-  static constexpr int BMT = PAIR ? 2 * BM : BM;  // rows of an M tile
+  static constexpr int BMT = PAIR ? 2 * BM : BM;  // rows of an M tile (M-grouped)
   static constexpr uint32_t IDESC =
       PAIR ? make_idesc_bf16(BN, Base::A_MN, Base::B_MN, 256) : Base::IDESC;
 };
@@ -135,7 +135,9 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
     else nkb = p.segkb[t.g][0] + p.segkb[t.g][1] + p.segkb[t.g][2];
     t.nkb = nkb;
   } else {
-    int l = tile;
+    // pairs: the two CTAs take consecutive tiles, adjacent M tiles of one problem (every
+    // problem's M-tile count is even)
+    int l = PAIR ? 2 * tile + rank : tile;
     if (l < p.router_tiles) {
       const int mt = p.d / BM;
       t.g = 2;
@@ -196,7 +198,7 @@ __device__ __forceinline__ int total_tiles(const GemmParams& p, const int* s_mt)
     const int tiles_sh =
         p.has_shared ? 2 * (p.d / BM) * (p.Fs / BN) + (p.Fs / BM) * (p.d / BN) : 0;
     const int per = 2 * (p.d / BM) * (p.F / BN) + (p.F / BM) * (p.d / BN);
-    return p.router_tiles + tiles_sh + p.E * per;
+    return (p.router_tiles + tiles_sh + p.E * per) / (PAIR ? 2 : 1);
   }
 }
 
@@ -272,14 +274,23 @@ __device__ __forceinline__ void dw_slots(const Tile& t, int& ia, int& ib) {
 
 // G_BWD_DW loads of one k-block: A = the tile's 128 M columns of the K-row-major operand (two
 // 64-column boxes), B = its BN N columns; `krow` = the block's first K row in the maps.
-template <int BN>
+// PAIR: B columns 128 rank .. 128 rank + 127 of the tile only, on the even CTA's barrier.
+template <int BN, bool PAIR>
 __device__ __forceinline__ void issue_loads_dw(const CUtensorMap* ma, const CUtensorMap* mb,
-                                               const Tile& t, int krow, uint32_t sA, uint32_t sB,
-                                               uint32_t bar) {
-  tma_load_2d(sA, ma, bar, t.m0, krow);
-  tma_load_2d(sA + 8192, ma, bar, t.m0 + 64, krow);
+                                               const Tile& t, int krow, int rank, uint32_t sA,
+                                               uint32_t sB, uint32_t bar) {
+  if constexpr (PAIR) {
+    tma_load_2d_pair(sA, ma, bar, t.m0, krow);
+    tma_load_2d_pair(sA + 8192, ma, bar, t.m0 + 64, krow);
+    const int c0 = t.n * BN + 128 * rank;
+    tma_load_2d_pair(sB, mb, bar, c0, krow);
+    tma_load_2d_pair(sB + 8192, mb, bar, c0 + 64, krow);
+  } else {
+    tma_load_2d(sA, ma, bar, t.m0, krow);
+    tma_load_2d(sA + 8192, ma, bar, t.m0 + 64, krow);
 #pragma unroll
-  for (int i = 0; i < BN / 64; ++i) tma_load_2d(sB + i * 8192, mb, bar, t.n * BN + 64 * i, krow);
+    for (int i = 0; i < BN / 64; ++i) tma_load_2d(sB + i * 8192, mb, bar, t.n * BN + 64 * i, krow);
+  }
 }
 
 // ------------------------------------------------------------------ epilogues
@@ -720,9 +731,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
           bool ok = true;
           for (int kb = 0; kb < t.nkb; ++kb) {
             if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) { ok = false; break; }
-            mbar_arrive_expect_tx(bar_full + 8 * stage, C::A_BYTES + C::B_BYTES);
-            issue_loads_dw<BN>(ma, mb, t, krow + kb * BK, sA0 + stage * C::A_BYTES,
-                               sB0 + stage * C::B_BYTES, bar_full + 8 * stage);
+            if (!PAIR || rank == 0)
+              mbar_arrive_expect_tx(bar_full + 8 * stage, (C::A_BYTES + C::B_BYTES) * (PAIR ? 2 : 1));
+            issue_loads_dw<BN, PAIR>(ma, mb, t, krow + kb * BK, rank, sA0 + stage * C::A_BYTES,
+                                     sB0 + stage * C::B_BYTES,
+                                     PAIR ? mapa_shared(bar_full + 8 * stage, 0) : bar_full + 8 * stage);
             if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
           }
           if (!ok) break;
@@ -959,7 +972,8 @@ cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStr
     case G_BWD_DX:
       return bn == 256 ? launch_one<G_BWD_DX, 256>(p, grid, s) : launch_one<G_BWD_DX, 128>(p, grid, s);
     case G_BWD_DW:
-      return bn == 256 ? launch_one<G_BWD_DW, 256>(p, grid, s) : launch_one<G_BWD_DW, 128>(p, grid, s);
+      if (bn != 256) return launch_one<G_BWD_DW, 128>(p, grid, s);
+      return pair ? launch_one<G_BWD_DW, 256, true>(p, grid, s) : launch_one<G_BWD_DW, 256>(p, grid, s);
     case G_FWD_GU_MX: return launch_one<G_FWD_GU_MX, 256>(p, grid, s);
     case G_FWD_DOWN_MX: return launch_one<G_FWD_DOWN_MX, 256>(p, grid, s);
     default: return cudaErrorInvalidValue;

@@ -87,7 +87,8 @@ struct BoundMapParams {
 cudaError_t launch_dw_bound_maps(const BoundMapParams& bp, cudaStream_t s);
 
 // Launches (moe_gemm.cu).  grid = persistent CTAs.
-// pair: bf16 gate/up and down (N tile 256) in CTA pairs of 256-row tiles (cluster launch).
+// pair: bf16 gate/up and down (N tile 256) in CTA pairs of 256-row tiles, or the weight-gradient
+// GEMM in pairs of adjacent M tiles (cluster launch).
 cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s,
                         bool pair = false);
 int gemm_smem_bytes(int bn, int E);
