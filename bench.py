@@ -188,12 +188,14 @@ def work_model(shape, counts):
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures, per weight set
 # streamed (routed experts with tokens + shared expert), valid only while the kernel source is
-# the one that was captured (sha1 prefix).  Source: profiles/gemm_fwd_gate_up_dsv3_slice_e32.md.
+# the one that was captured (sha1 prefix).  Sources: profiles/gemm_fwd_gate_up_dsv3_slice_e32.md
+# and profiles/gemm_fwd_mxfp8_dsv3_mxfp8_slice_e32.md (32-expert slices: 33 weight sets).
+_GEMM_SRC = "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"
 PROFILED_TRAFFIC = {
-    "gemm_fwd_gate_up": ("7ff03900ea5f", (2.015325e9 + 19.891456e6) / 33,
-                         "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"),
-    "gemm_fwd_down": ("7ff03900ea5f", (0.992675e9 + 60.270080e6) / 33,
-                      "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"),
+    "gemm_fwd_gate_up": ("128babc61686", (2.015203e9 + 20.323328e6) / 33, _GEMM_SRC),
+    "gemm_fwd_down": ("128babc61686", (0.992527e9 + 61.174272e6) / 33, _GEMM_SRC),
+    "gemm_fwd_gate_up_mx": ("128babc61686", (1.083237e9 + 21.006336e6) / 33, _GEMM_SRC),
+    "gemm_fwd_down_mx": ("128babc61686", (0.519240e9 + 113.856e6) / 33, _GEMM_SRC),
 }
 
 
