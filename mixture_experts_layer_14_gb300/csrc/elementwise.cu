@@ -34,7 +34,8 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(
       }
       continue;
     }
-    // four 16-byte loads in flight per lane before their stores
+    // four 16-byte loads in flight per lane before their stores; the destination rows are
+    // written with evict-first stores so they do not push x out of L2
     const uint4* s0 = src0 + t * vec_per_row;
     const uint4* s1 = src1 ? src1 + t * vec_per_row : nullptr;
     for (int v = lane; v < vec_per_row; v += 128) {
@@ -44,14 +45,14 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(
         if (v + 32 * u < vec_per_row) a[u] = s0[v + 32 * u];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (v + 32 * u < vec_per_row) d0[v + 32 * u] = a[u];
+        if (v + 32 * u < vec_per_row) __stcs(d0 + v + 32 * u, a[u]);
       if (s1) {
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           if (v + 32 * u < vec_per_row) a[u] = s1[v + 32 * u];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          if (v + 32 * u < vec_per_row) d1[v + 32 * u] = a[u];
+          if (v + 32 * u < vec_per_row) __stcs(d1 + v + 32 * u, a[u]);
       }
     }
   }
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(kRowThreads) gather_bytes_kernel(
     if ((words & 3) == 0) {
       const uint4* s4 = reinterpret_cast<const uint4*>(s);
       uint4* d4 = reinterpret_cast<uint4*>(d);
-      for (int v = lane; v < words / 4; v += 32) d4[v] = s4[v];
+      for (int v = lane; v < words / 4; v += 32) __stcs(d4 + v, s4[v]);
     } else {
       for (int v = lane; v < words; v += 32) d[v] = s[v];
     }
