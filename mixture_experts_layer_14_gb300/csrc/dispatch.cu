@@ -3,14 +3,15 @@
 // its expert's region, giving per-expert counts, region offsets and the schedule table; page
 // "Метод и эксперименты": each expert then pulls its own tokens, e.g. E2 <- [0,2,9,15]).
 //
-// Three launches, no atomics on global memory, no host synchronisation:
+// Four launches, no atomics on global memory, no host synchronisation:
 //  1. histogram: block b counts, for every expert, the routes of tokens [64b, 64b+64) (one
 //     thread per route; warp-level match gives per-warp counts);
-//  2. scan: one block turns the (expert, block) histogram, expert-major, into exclusive bases
-//     (in place), per-expert counts and region offsets;
-//  3. scatter: block b gives route i of expert e the row base(e, b) + (routes of e in earlier
-//     warps of the block) + (routes of e in lower lanes of its warp), i.e. routes keep their
-//     (token, slot) order inside every region, so tokens ascend.
+//  2. scan: one block per expert turns its row of the (expert, block) histogram into exclusive
+//     bases within the expert (in place) and its count;
+//  3. offsets: one block scans the counts into region offsets;
+//  4. scatter: block b gives route i of expert e the row offset(e) + base(e, b) + (routes of e in
+//     earlier warps of the block) + (routes of e in lower lanes of its warp), i.e. routes keep
+//     their (token, slot) order inside every region, so tokens ascend.
 #include "mok_device.cuh"
 
 namespace mok {
@@ -60,66 +61,78 @@ __global__ void __launch_bounds__(kDispatchChunk * kMaxK) dispatch_hist_kernel(
   }
 }
 
-__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict__ hist, int E,
-                                                             int nblk, int32_t* __restrict__ counts,
-                                                             int32_t* __restrict__ offsets) {
-  __shared__ int s_warp[32];
-  const int N = E * nblk;
-  const int per = (N + blockDim.x - 1) / blockDim.x;
-  const int i0 = threadIdx.x * per;
-  const int i1 = min(N, i0 + per);
-  int local = 0;
-  for (int i = i0; i < i1; ++i) local += hist[i];
-  // block-wide exclusive scan of the per-thread sums (thread order = entry order)
+// Per expert (one block each, coalesced along its row of the histogram): the exclusive prefix of
+// its per-chunk route counts, in place, and its total.
+__global__ void __launch_bounds__(256) dispatch_scan_rows_kernel(int32_t* __restrict__ hist,
+                                                                 int nblk,
+                                                                 int32_t* __restrict__ counts) {
+  __shared__ int s_warp[8];
+  __shared__ int s_carry;
+  int32_t* row = hist + (int64_t)blockIdx.x * nblk;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = local;
+  if (threadIdx.x == 0) s_carry = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < nblk; c0 += 256) {
+    const int c = c0 + threadIdx.x;
+    const int v = c < nblk ? row[c] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int below = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int x = s_warp[w];
+      below += w < warp ? x : 0;
+      total += x;
+    }
+    const int carry = s_carry;
+    if (c < nblk) row[c] = carry + below + incl - v;
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry = carry + total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) counts[blockIdx.x] = s_carry;
+}
+
+// offsets[e] = routes of the experts before e, offsets[E] = all routes (one block, E <= 512).
+__global__ void __launch_bounds__(kMaxE) dispatch_offsets_kernel(const int32_t* __restrict__ counts,
+                                                                 int E,
+                                                                 int32_t* __restrict__ offsets) {
+  __shared__ int s_warp[kMaxE / 32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int v = t < E ? counts[t] : 0;
+  int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
   }
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    int v = lane < nw ? s_warp[lane] : 0;
-    int vi = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, vi, o);
-      if (lane >= o) vi += u;
-    }
-    if (lane < nw) s_warp[lane] = vi - v;  // exclusive warp base
-  }
-  __syncthreads();
-  int run = s_warp[warp] + incl - local;
-  for (int i = i0; i < i1; ++i) {
-    const int h = hist[i];
-    hist[i] = run;  // exclusive base of (expert, block), expert-major
-    run += h;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int start = nblk ? hist[(int64_t)e * nblk] : 0;
-    offsets[e] = start;
-  }
-  __syncthreads();
-  if (threadIdx.x == blockDim.x - 1) offsets[E] = run;  // the last thread ends at the total
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = offsets[e + 1] - offsets[e];
+  int below = 0;
+  for (int w = 0; w < warp; ++w) below += s_warp[w];
+  if (t < E) offsets[t] = below + incl - v;
+  if (t == E - 1) offsets[E] = below + incl;
 }
 
 __global__ void __launch_bounds__(kDispatchChunk * kMaxK) dispatch_scatter_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ topk_w, int64_t T, int E, int k,
-    int nblk, const int32_t* __restrict__ base, int32_t* __restrict__ sorted_tok,
+    int nblk, const int32_t* __restrict__ offsets, const int32_t* __restrict__ base,
+    int32_t* __restrict__ sorted_tok,
     float* __restrict__ sorted_w, int32_t* __restrict__ inv_pos) {
   __shared__ int s_cnt[kMaxDispatchWarps * kMaxE];
   int e;
   const int rank = warp_expert_rank(idx, T, E, k, blockIdx.x, s_cnt, nullptr, e);
-  // exclusive prefix over the warps of the block, per expert, on top of the chunk's base
+  // exclusive prefix over the warps of the block, per expert, on top of the chunk's base (the
+  // expert's offset plus the routes of its earlier chunks)
   const int nw = blockDim.x >> 5;
   for (int x = threadIdx.x; x < E; x += blockDim.x) {
-    int run = base[(int64_t)x * nblk + blockIdx.x];
+    int run = offsets[x] + base[(int64_t)x * nblk + blockIdx.x];
     for (int w = 0; w < nw; ++w) {
       const int c = s_cnt[w * E + x];
       s_cnt[w * E + x] = run;
@@ -157,15 +170,21 @@ cudaError_t launch_dispatch(int64_t T, int E, int k, const int32_t* topk_idx, co
     if (e != cudaSuccess) return e;
   }
   prof_begin("dispatch_scan", s);
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, E, nblk, counts, offsets);
+  dispatch_scan_rows_kernel<<<E, 256, 0, s>>>(hist, nblk, counts);
   prof_end(s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  *launches += (nblk > 0) ? 2 : 1;
+  prof_begin("dispatch_offsets", s);
+  dispatch_offsets_kernel<<<1, kMaxE, 0, s>>>(counts, E, offsets);
+  prof_end(s);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *launches += (nblk > 0) ? 3 : 2;
   if (nblk > 0) {
     prof_begin("dispatch_scatter", s);
     dispatch_scatter_kernel<<<nblk, kDispatchChunk * k, 0, s>>>(topk_idx, topk_w, T, E, k, nblk,
-                                                                hist, sorted_tok, sorted_w, inv_pos);
+                                                                offsets, hist, sorted_tok, sorted_w,
+                                                                inv_pos);
     prof_end(s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
