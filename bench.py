@@ -188,14 +188,19 @@ def work_model(shape, counts):
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures, per weight set
 # streamed (routed experts with tokens + shared expert), valid only while the kernel source is
-# the one that was captured (sha1 prefix).  Sources: profiles/gemm_fwd_gate_up_dsv3_slice_e32.md
-# and profiles/gemm_fwd_mxfp8_dsv3_mxfp8_slice_e32.md (32-expert slices: 33 weight sets).
+# the one that was captured (sha1 prefix).  Sources: profiles/gemm_fwd_gate_up_dsv3_slice_e32.md,
+# profiles/gemm_fwd_mxfp8_dsv3_mxfp8_slice_e32.md and profiles/gemm_bwd_dsv3_train_slice_e32.md
+# (32-expert slices: 33 weight sets).
 _GEMM_SRC = "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"
 PROFILED_TRAFFIC = {
     "gemm_fwd_gate_up": ("128babc61686", (2.015203e9 + 20.323328e6) / 33, _GEMM_SRC),
     "gemm_fwd_down": ("128babc61686", (0.992527e9 + 61.174272e6) / 33, _GEMM_SRC),
     "gemm_fwd_gate_up_mx": ("128babc61686", (1.083237e9 + 21.006336e6) / 33, _GEMM_SRC),
     "gemm_fwd_down_mx": ("128babc61686", (0.519240e9 + 113.856e6) / 33, _GEMM_SRC),
+    # profiles/gemm_bwd_dsv3_train_slice_e32.md
+    "gemm_bwd_da": ("128babc61686", (1.198957e9 + 0.102105e9) / 33, _GEMM_SRC),
+    "gemm_bwd_dx": ("128babc61686", (2.063618e9 + 0.127761e9) / 33, _GEMM_SRC),
+    "gemm_bwd_dw": ("128babc61686", (0.377721e9 + 2.851604e9) / 33, _GEMM_SRC),
 }
 
 
