@@ -171,8 +171,13 @@ int mok_moe_backward(const mok_dims *dims, const mok_weights *w, const void *x, 
 /* The whole layer forward (route, dispatch, expert forward) with x and y in HOST memory:
  * copies x_host[T,d] (bf16) to the workspace, runs the layer and copies y back to
  * y_host[T,d].  Pinned host memory makes the copies asynchronous; the call returns without
- * waiting (synchronise the stream before reading y_host).  Routing tensors live inside the
- * workspace (mok_workspace_size(dims, MOK_PASS_FORWARD) + mok_layer_host_extra_size(dims)). */
+ * waiting (synchronise the stream before reading y_host, or writing x_host again).  Routing
+ * tensors live inside the workspace (mok_workspace_size(dims, MOK_PASS_FORWARD) +
+ * mok_layer_host_extra_size(dims)).  The copy of x runs on a library-owned copy stream into one
+ * of two device buffers of the workspace, alternating per call, so that a call's copy overlaps
+ * the kernels of the previous call on the same workspace; `stream` waits for it before the
+ * layer runs, so synchronising `stream` still covers the whole call.  The library keeps one
+ * copy stream per device and two events per workspace (for the 16 most recent workspaces). */
 size_t mok_layer_host_extra_size(const mok_dims *dims);
 int mok_layer_forward_host(const mok_dims *dims, const mok_weights *w, const void *x_host,
                            void *y_host, void *ws, size_t ws_bytes, mok_stream_t stream);

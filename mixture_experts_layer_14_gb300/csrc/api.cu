@@ -198,7 +198,8 @@ static Layout layout_saved(const mok_dims* d) {
 
 static Layout layout_host(const mok_dims* d) {
   const int64_t T = d->T, R = T * d->k;
-  size_t sz[HS_N] = {2ull * T * d->d, 2ull * T * d->d, 4ull * R, 4ull * R, 4ull * d->E,
+  // x: two buffers, alternating per call (see mok_layer_forward_host)
+  size_t sz[HS_N] = {2 * al(2ull * T * d->d), 2ull * T * d->d, 4ull * R, 4ull * R, 4ull * d->E,
                      4ull * (d->E + 1), 4ull * R, 4ull * R, 4ull * R};
   Layout L{};
   size_t o = 0;
@@ -795,6 +796,76 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
   return MOK_OK;
 }
 
+}  // extern "C"
+
+// Per-workspace state of the host entry point: which of its two device x buffers the next call
+// fills, and per buffer the event of its copy landing and of the layer being done reading it.
+// A small table keyed by (device, workspace); its oldest entry is reused (after waiting for its
+// events) when a new workspace comes.
+struct HostPipe {
+  const void* ws = nullptr;
+  int device = -1;
+  cudaEvent_t ready[2] = {nullptr, nullptr};
+  cudaEvent_t freed[2] = {nullptr, nullptr};
+  int next = 0;
+  uint64_t last_use = 0;
+};
+constexpr int kHostPipes = 16;
+static std::mutex g_pipe_mu;
+static HostPipe g_pipes[kHostPipes];
+static uint64_t g_pipe_clock = 0;
+constexpr int kMaxDevices = 64;
+static cudaStream_t g_copy_stream[kMaxDevices] = {};
+
+static cudaError_t host_pipe(const void* ws, HostPipe** out, cudaStream_t* copy) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  if (!g_copy_stream[dev]) {
+    e = cudaStreamCreateWithFlags(&g_copy_stream[dev], cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+  }
+  *copy = g_copy_stream[dev];
+  HostPipe* hit = nullptr;
+  HostPipe* oldest = &g_pipes[0];
+  for (HostPipe& P : g_pipes) {
+    if (P.ws == ws && P.device == dev) hit = &P;
+    if (P.last_use < oldest->last_use) oldest = &P;
+  }
+  if (!hit) {
+    hit = oldest;
+    if (hit->ready[0]) {  // reused: its previous workspace's copies and readers are done first
+      for (int b = 0; b < 2; ++b) {
+        if ((e = cudaEventSynchronize(hit->ready[b])) != cudaSuccess) return e;
+        if ((e = cudaEventSynchronize(hit->freed[b])) != cudaSuccess) return e;
+      }
+      if (hit->device != dev) {
+        for (int b = 0; b < 2; ++b) {
+          cudaEventDestroy(hit->ready[b]);
+          cudaEventDestroy(hit->freed[b]);
+          hit->ready[b] = hit->freed[b] = nullptr;
+        }
+      }
+    }
+    if (!hit->ready[0]) {
+      for (int b = 0; b < 2; ++b) {
+        if ((e = cudaEventCreateWithFlags(&hit->ready[b], cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&hit->freed[b], cudaEventDisableTiming)) != cudaSuccess) return e;
+      }
+    }
+    hit->ws = ws;
+    hit->device = dev;
+    hit->next = 0;
+  }
+  hit->last_use = ++g_pipe_clock;
+  *out = hit;
+  return cudaSuccess;
+}
+
+extern "C" {
+
 int mok_layer_forward_host(const mok_dims* dims, const mok_weights* w, const void* x_host,
                            void* y_host, void* ws, size_t ws_bytes, mok_stream_t stream) {
   int rc = check_dims(dims);
@@ -806,7 +877,13 @@ int mok_layer_forward_host(const mok_dims* dims, const mok_weights* w, const voi
   if (dims->T == 0) return MOK_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ext = static_cast<char*>(ws) + fw;
-  void* x = ext + H.off[HS_X];
+  const size_t xbytes = 2ull * dims->T * dims->d;
+  HostPipe* P = nullptr;
+  cudaStream_t copy = nullptr;
+  if (host_pipe(ws, &P, &copy) != cudaSuccess) return MOK_ERR_CUDA;
+  const int b = P->next;
+  P->next ^= 1;
+  void* x = ext + H.off[HS_X] + b * al(xbytes);
   void* y = ext + H.off[HS_Y];
   int32_t* idx = reinterpret_cast<int32_t*>(ext + H.off[HS_IDX]);
   float* tw = reinterpret_cast<float*>(ext + H.off[HS_W]);
@@ -815,8 +892,12 @@ int mok_layer_forward_host(const mok_dims* dims, const mok_weights* w, const voi
   int32_t* stok = reinterpret_cast<int32_t*>(ext + H.off[HS_STOK]);
   float* sw = reinterpret_cast<float*>(ext + H.off[HS_SW]);
   int32_t* inv = reinterpret_cast<int32_t*>(ext + H.off[HS_INV]);
-  const size_t xbytes = 2ull * dims->T * dims->d;
-  if (cudaMemcpyAsync(x, x_host, xbytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOK_ERR_CUDA;
+  // the copy waits until the call two back (same buffer) is done reading it; the layer waits
+  // for the copy
+  if (cudaStreamWaitEvent(copy, P->freed[b], 0) != cudaSuccess) return MOK_ERR_CUDA;
+  if (cudaMemcpyAsync(x, x_host, xbytes, cudaMemcpyHostToDevice, copy) != cudaSuccess) return MOK_ERR_CUDA;
+  if (cudaEventRecord(P->ready[b], copy) != cudaSuccess) return MOK_ERR_CUDA;
+  if (cudaStreamWaitEvent(s, P->ready[b], 0) != cudaSuccess) return MOK_ERR_CUDA;
   int total = 0;
   rc = mok_route(dims, x, w->W_router, w->router_bias, idx, tw, nullptr, ws, fw, stream);
   if (rc != MOK_OK) return rc;
@@ -827,6 +908,7 @@ int mok_layer_forward_host(const mok_dims* dims, const mok_weights* w, const voi
   rc = mok_moe_forward(dims, w, x, idx, off, stok, sw, inv, y, nullptr, ws, fw, stream);
   if (rc != MOK_OK) return rc;
   total += g_last_launches;
+  if (cudaEventRecord(P->freed[b], s) != cudaSuccess) return MOK_ERR_CUDA;
   if (cudaMemcpyAsync(y_host, y, xbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOK_ERR_CUDA;
   g_last_launches = total;
   return MOK_OK;

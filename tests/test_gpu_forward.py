@@ -163,3 +163,29 @@ def test_host_buffer_entry_point_matches_device_path():
     mok.layer_forward_host(D, L, xh, yh, wsh)
     torch.cuda.synchronize()
     assert torch.equal(yh, y_dev.cpu())
+
+
+def test_host_entry_point_back_to_back_calls():
+    """Three host-buffer calls on one workspace with no synchronisation between them: each call's
+    copy of x goes to one of two device buffers in turn, so the third reuses the first one's
+    buffer while the layer may still run; every y must match its own device-path forward."""
+    ensure_lib()
+    shape = CASES["ragged_skew"]
+    L = to_dev(make_layer(shape, "cpu"))
+    D = dims_of(shape)
+    xs = [L["x"], (L["x"].float() * 0.5).to(torch.bfloat16), -L["x"]]
+    ws = torch.zeros(mok.workspace_size(D), dtype=torch.uint8, device="cuda")
+    y_dev = []
+    for x in xs:
+        idx, w, _ = mok.route(D, x, L["W_router"], L["bias"], ws)
+        y_dev.append(mok.moe_forward(D, L, x, mok.dispatch_index(D, idx, w, ws), ws).cpu())
+    torch.cuda.synchronize()
+    wsh = torch.zeros(mok.workspace_size(D) + mok.host_extra_size(D), dtype=torch.uint8, device="cuda")
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = [torch.empty_like(h).pin_memory() for h in xh]
+    for xi, yi in zip(xh, yh):
+        mok.layer_forward_host(D, L, xi, yi, wsh)
+    torch.cuda.synchronize()
+    assert mok.read_status(wsh) == 0
+    for i in range(3):
+        assert torch.equal(yh[i], y_dev[i]), i
