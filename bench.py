@@ -381,8 +381,39 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
         "kernels": kernels, "gpu_launches": launches, "clocks": clocks,
         "active_experts": e_act, "max_expert_rows": max(counts), "empty_experts": counts.count(0),
     }
+    if mx:  # context: the library's dense fp8 GEMM rate on this GPU (the roofline keeps 2 x bf16)
+        f8 = fp8_cublas_tflops(dev)
+        out["fp8_cublas_tflops_measured"] = f8
+        out["tflops_frac_of_measured_fp8_gemm"] = round(tflops / f8, 4) if f8 else None
     del layer
     return out, L
+
+
+def fp8_cublas_tflops(dev):
+    """Dense e4m3 x e4m3 -> bf16 GEMM throughput of the library routine (torch._scaled_mm at
+    8192^3, best of 10 CUDA-event-timed calls), reported beside the MXFP8 workload for context;
+    None where the routine is unavailable."""
+    import torch
+
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = None
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return round(2.0 * n ** 3 / (best / 1e3) / 1e12, 1)
+    except Exception:
+        return None
 
 
 def config_of(shape, world, e_act):

@@ -177,7 +177,9 @@ int mok_moe_backward(const mok_dims *dims, const mok_weights *w, const void *x, 
  * of two device buffers of the workspace, alternating per call, so that a call's copy overlaps
  * the kernels of the previous call on the same workspace; `stream` waits for it before the
  * layer runs, so synchronising `stream` still covers the whole call.  The library keeps one
- * copy stream per device and two events per workspace (for the 16 most recent workspaces). */
+ * copy stream per device and two events per workspace (for the 16 most recent workspaces).
+ * When y_host is pinned (mapped) host memory, the final combine writes y straight into it;
+ * otherwise y is combined in the workspace and copied back on `stream`. */
 size_t mok_layer_host_extra_size(const mok_dims *dims);
 int mok_layer_forward_host(const mok_dims *dims, const mok_weights *w, const void *x_host,
                            void *y_host, void *ws, size_t ws_bytes, mok_stream_t stream);

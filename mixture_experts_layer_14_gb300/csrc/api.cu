@@ -905,11 +905,22 @@ int mok_layer_forward_host(const mok_dims* dims, const mok_weights* w, const voi
   rc = mok_dispatch_index(dims, idx, tw, cnt, off, stok, sw, inv, ws, fw, stream);
   if (rc != MOK_OK) return rc;
   total += g_last_launches;
-  rc = mok_moe_forward(dims, w, x, idx, off, stok, sw, inv, y, nullptr, ws, fw, stream);
+  // pinned (mapped) y_host: the combine writes y straight into host memory; otherwise y is
+  // combined in the workspace and copied back
+  cudaPointerAttributes ya{};
+  void* y_out = y;
+  if (cudaPointerGetAttributes(&ya, y_host) == cudaSuccess && ya.type == cudaMemoryTypeHost &&
+      ya.devicePointer && aligned16(ya.devicePointer))
+    y_out = ya.devicePointer;
+  else
+    cudaGetLastError();  // pageable memory: not an error for this call
+  rc = mok_moe_forward(dims, w, x, idx, off, stok, sw, inv, y_out, nullptr, ws, fw, stream);
   if (rc != MOK_OK) return rc;
   total += g_last_launches;
   if (cudaEventRecord(P->freed[b], s) != cudaSuccess) return MOK_ERR_CUDA;
-  if (cudaMemcpyAsync(y_host, y, xbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOK_ERR_CUDA;
+  if (y_out == y &&
+      cudaMemcpyAsync(y_host, y, xbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOK_ERR_CUDA;
   g_last_launches = total;
   return MOK_OK;
 }

@@ -216,8 +216,15 @@ __global__ void __launch_bounds__(256) route_finish_kernel(const __grid_constant
       used[i] = true;
       v[i] = -INFINITY;
       if (i < per && e < p.E) {
-        float acc = __ldcg(p.partial + (int64_t)t * p.E + e);
-        for (int sp = 1; sp < p.splits; ++sp) acc += __ldcg(p.partial + ((int64_t)sp * p.T + t) * p.E + e);
+        // every split's partial in flight at once, then summed in split order
+        float part[kMaxRouteSplits];
+#pragma unroll
+        for (int sp = 0; sp < kMaxRouteSplits; ++sp)
+          part[sp] = sp < p.splits ? __ldcg(p.partial + ((int64_t)sp * p.T + t) * p.E + e) : 0.0f;
+        float acc = part[0];
+#pragma unroll
+        for (int sp = 1; sp < kMaxRouteSplits; ++sp)
+          if (sp < p.splits) acc += part[sp];
         v[i] = acc + (p.bias ? p.bias[e] : 0.0f);
         used[i] = false;
         if (p.logits) p.logits[t * p.E + e] = v[i];

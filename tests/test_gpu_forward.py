@@ -189,3 +189,22 @@ def test_host_entry_point_back_to_back_calls():
     assert mok.read_status(wsh) == 0
     for i in range(3):
         assert torch.equal(yh[i], y_dev[i]), i
+
+
+def test_host_entry_point_pageable_output():
+    """y_host in pageable memory: the layer combines into the workspace and copies y back (the
+    pinned case writes y straight into host memory); both give the device path's bytes."""
+    ensure_lib()
+    shape = CASES["tiny"]
+    L = to_dev(make_layer(shape, "cpu"))
+    D = dims_of(shape)
+    ws = torch.zeros(mok.workspace_size(D), dtype=torch.uint8, device="cuda")
+    idx, w, _ = mok.route(D, L["x"], L["W_router"], L["bias"], ws)
+    y_dev = mok.moe_forward(D, L, L["x"], mok.dispatch_index(D, idx, w, ws), ws).cpu()
+    wsh = torch.zeros(mok.workspace_size(D) + mok.host_extra_size(D), dtype=torch.uint8, device="cuda")
+    xh = L["x"].cpu().pin_memory()
+    yh = torch.empty_like(xh)          # pageable
+    assert not yh.is_pinned()
+    mok.layer_forward_host(D, L, xh, yh, wsh)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, y_dev)
