@@ -412,7 +412,8 @@ def fp8_cublas_tflops(dev):
             ms = e0.elapsed_time(e1)
             best = ms if best is None else min(best, ms)
         return round(2.0 * n ** 3 / (best / 1e3) / 1e12, 1)
-    except Exception:
+    except Exception as exc:
+        print(f"fp8 GEMM rate unavailable: {exc!r}"[:300], file=sys.stderr)
         return None
 
 
@@ -449,6 +450,9 @@ def run_mok(args, shape, rank, world, local_rank):
         "roofline": res["roofline"], "kernels": res["kernels"], "gpu_launches": res["gpu_launches"],
         "clocks": res["clocks"], "e2e": e2e,
     }
+    for key in ("fp8_cublas_tflops_measured", "tflops_frac_of_measured_fp8_gemm"):
+        if key in res:
+            line[key] = res[key]
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(L, shape, budget_s=args.cpu_seconds)
     del L

@@ -135,15 +135,20 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
     else nkb = p.segkb[t.g][0] + p.segkb[t.g][1] + p.segkb[t.g][2];
     t.nkb = nkb;
   } else {
-    // pairs: the two CTAs take consecutive tiles, adjacent M tiles of one problem (every
-    // problem's M-tile count is even)
+    // Inside a problem the N tiles run fastest, so the tiles in flight together write whole
+    // output rows.  Pairs: the two CTAs take adjacent M tiles of the same N tile (every
+    // problem's M-tile count is even).
+    constexpr int U = PAIR ? 2 : 1;
+    auto place = [&](int ls, int nt) {  // ls: tile index inside the problem, in single tiles
+      const int ps = ls / U;
+      t.n = ps % nt;
+      t.m0 = ((ps / nt) * U + ls % U) * BM;
+    };
     int l = PAIR ? 2 * tile + rank : tile;
     if (l < p.router_tiles) {
-      const int mt = p.d / BM;
       t.g = 2;
       t.e = 0;
-      t.m0 = (l % mt) * BM;
-      t.n = l / mt;
+      place(l, p.router_tiles / (p.d / BM));
       t.row0 = 0;
       t.rows = p.T;
     } else {
@@ -171,16 +176,10 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
       const int tg = (p.d / BM) * (Fg / BN);
       if (l < 2 * tg) {
         t.sub = l / tg;
-        l -= t.sub * tg;
-        const int mt = p.d / BM;
-        t.m0 = (l % mt) * BM;
-        t.n = l / mt;
+        place(l - t.sub * tg, Fg / BN);
       } else {
         t.sub = 2;
-        l -= 2 * tg;
-        const int mt = Fg / BM;
-        t.m0 = (l % mt) * BM;
-        t.n = l / mt;
+        place(l - 2 * tg, p.d / BN);
       }
     }
     t.nkb = (t.rows + BK - 1) / BK;
