@@ -15,29 +15,28 @@ static int rows_grid(int64_t nrows) {
 
 // dst[r] = src[rows[r]] for r < nrows (page "Метод и эксперименты": each expert pulls its
 // tokens; with the tokens of an expert ascending the reads walk x in order).  A row index
-// outside [0, nsrc) yields a zero row.
+// outside [0, nsrc) yields a zero row.  With a second source (the backward pulls x and dY with
+// the same schedule) the warps take the 2 nrows rows of both in one list.
 __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(
     const uint4* __restrict__ src0, const uint4* __restrict__ src1, const int32_t* __restrict__ rows,
     int64_t nrows, int64_t nsrc, int vec_per_row, uint4* __restrict__ dst0, uint4* __restrict__ dst1) {
   const int lane = threadIdx.x & 31;
   const int64_t wglobal = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t r = wglobal; r < nrows; r += nwarps) {
+  const int64_t total = src1 ? 2 * nrows : nrows;
+  for (int64_t rr = wglobal; rr < total; rr += nwarps) {
+    const bool second = rr >= nrows;
+    const int64_t r = second ? rr - nrows : rr;
+    const uint4* src = second ? src1 : src0;
+    uint4* d = (second ? dst1 : dst0) + r * vec_per_row;
     const int64_t t = rows[r];
-    const bool ok = (t >= 0 && t < nsrc);
-    uint4* d0 = dst0 + r * vec_per_row;
-    uint4* d1 = src1 ? dst1 + r * vec_per_row : nullptr;
-    if (!ok) {
-      for (int v = lane; v < vec_per_row; v += 32) {
-        d0[v] = make_uint4(0, 0, 0, 0);
-        if (d1) d1[v] = make_uint4(0, 0, 0, 0);
-      }
+    if (t < 0 || t >= nsrc) {
+      for (int v = lane; v < vec_per_row; v += 32) d[v] = make_uint4(0, 0, 0, 0);
       continue;
     }
     // four 16-byte loads in flight per lane before their stores; the destination rows are
-    // written with evict-first stores so they do not push x out of L2
-    const uint4* s0 = src0 + t * vec_per_row;
-    const uint4* s1 = src1 ? src1 + t * vec_per_row : nullptr;
+    // written with evict-first stores so they do not push the source out of L2
+    const uint4* s0 = src + t * vec_per_row;
     for (int v = lane; v < vec_per_row; v += 128) {
       uint4 a[4];
 #pragma unroll
@@ -45,15 +44,7 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(
         if (v + 32 * u < vec_per_row) a[u] = s0[v + 32 * u];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (v + 32 * u < vec_per_row) __stcs(d0 + v + 32 * u, a[u]);
-      if (s1) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (v + 32 * u < vec_per_row) a[u] = s1[v + 32 * u];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (v + 32 * u < vec_per_row) __stcs(d1 + v + 32 * u, a[u]);
-      }
+        if (v + 32 * u < vec_per_row) __stcs(d + v + 32 * u, a[u]);
     }
   }
 }
@@ -68,7 +59,7 @@ cudaError_t launch_gather_rows2(const void* src0, const void* src1, const int32_
                                 cudaStream_t s) {
   if (nrows == 0) return cudaSuccess;
   prof_begin(src1 ? "gather2" : "gather", s);
-  gather_rows_kernel<<<rows_grid(nrows), kRowThreads, 0, s>>>(
+  gather_rows_kernel<<<rows_grid(src1 ? 2 * nrows : nrows), kRowThreads, 0, s>>>(
       static_cast<const uint4*>(src0), static_cast<const uint4*>(src1), rows, nrows, nsrc, d / 8,
       static_cast<uint4*>(dst0), static_cast<uint4*>(dst1));
   prof_end(s);
