@@ -193,14 +193,14 @@ def work_model(shape, counts):
 # (32-expert slices: 33 weight sets).
 _GEMM_SRC = "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"
 PROFILED_TRAFFIC = {
-    "gemm_fwd_gate_up": ("128babc61686", (2.015203e9 + 20.323328e6) / 33, _GEMM_SRC),
-    "gemm_fwd_down": ("128babc61686", (0.992527e9 + 61.174272e6) / 33, _GEMM_SRC),
-    "gemm_fwd_gate_up_mx": ("128babc61686", (1.083237e9 + 21.006336e6) / 33, _GEMM_SRC),
-    "gemm_fwd_down_mx": ("128babc61686", (0.519240e9 + 113.856e6) / 33, _GEMM_SRC),
+    "gemm_fwd_gate_up": ("fd3e602e871f", (2.015002e9 + 20.1664e6) / 33, _GEMM_SRC),
+    "gemm_fwd_down": ("fd3e602e871f", (0.992624e9 + 61.2288e6) / 33, _GEMM_SRC),
+    "gemm_fwd_gate_up_mx": ("fd3e602e871f", (1.083484e9 + 21.151488e6) / 33, _GEMM_SRC),
+    "gemm_fwd_down_mx": ("fd3e602e871f", (0.519271e9 + 114.100992e6) / 33, _GEMM_SRC),
     # profiles/gemm_bwd_dsv3_train_slice_e32.md
-    "gemm_bwd_da": ("128babc61686", (1.198957e9 + 0.102105e9) / 33, _GEMM_SRC),
-    "gemm_bwd_dx": ("128babc61686", (2.063618e9 + 0.127761e9) / 33, _GEMM_SRC),
-    "gemm_bwd_dw": ("128babc61686", (0.377721e9 + 2.851604e9) / 33, _GEMM_SRC),
+    "gemm_bwd_da": ("fd3e602e871f", (1.199000e9 + 0.101744e9) / 33, _GEMM_SRC),
+    "gemm_bwd_dx": ("fd3e602e871f", (2.063276e9 + 0.127812e9) / 33, _GEMM_SRC),
+    "gemm_bwd_dw": ("fd3e602e871f", (0.378295e9 + 2.851484e9) / 33, _GEMM_SRC),
 }
 
 
