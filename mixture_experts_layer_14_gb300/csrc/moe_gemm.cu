@@ -82,10 +82,6 @@ constexpr int smem_bytes_for() {
   return C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES + kAuxBytes + kSchedBytes + 1024;
 }
 
-int gemm_smem_bytes(int bn, int /*E*/) {
-  return bn == 256 ? smem_bytes_for<G_FWD_GU, 256>() : smem_bytes_for<G_FWD_GU, 128>();
-}
-
 // ------------------------------------------------------------------ tile decode
 // PAIR: `tile` is a pair tile of 256 rows; CTA `rank` of the pair takes rows 128 rank ..
 // 128 rank + 127 of it (rows past the group's end: t.rows <= 0, nothing stored).

@@ -91,7 +91,6 @@ cudaError_t launch_dw_bound_maps(const BoundMapParams& bp, cudaStream_t s);
 // GEMM in pairs of adjacent M tiles (cluster launch).
 cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s,
                         bool pair = false);
-int gemm_smem_bytes(int bn, int E);
 
 // Router (route.cu)
 struct RouteParams {
