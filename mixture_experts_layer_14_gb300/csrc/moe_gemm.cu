@@ -942,9 +942,17 @@ static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.gridDim = dim3(2);
-    int fit = 0;
-    e = cudaOccupancyMaxActiveClusters(&fit, k, &cfg);
+    // pairs resident at once: a property of this kernel on this device, queried once per device
+    static int fit_of_device[64] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    int fit = (dev >= 0 && dev < 64) ? fit_of_device[dev] : 0;
+    if (fit == 0) {
+      e = cudaOccupancyMaxActiveClusters(&fit, k, &cfg);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) fit_of_device[dev] = fit;
+    }
     const int pairs = std::min((grid + 1) / 2, fit);
     if (pairs <= 0) return grid <= 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(2 * pairs);
