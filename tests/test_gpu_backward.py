@@ -23,6 +23,9 @@ CASES = {
     "wide_tiles_noshared": LayerShape("wide_tiles_noshared", 200, 256, 8, 3, 256, 0, 0, 0.0, "zipf", "bf16", True, 24),
     # training forward in CTA pairs (at least 320 routed rows per expert)
     "pairs_train": LayerShape("pairs_train", 880, 256, 8, 3, 256, 256, 1, 0.0, "zipf", "bf16", True, 25),
+    # the largest expert count and top-k the ABI accepts (E = 512, k = 8): the router GEMM's
+    # N = 512 and dW_router's two 256-column tiles
+    "max_E_k": LayerShape("max_E_k", 200, 256, 512, 8, 256, 256, 1, 0.0, "normal0.1", "bf16", True, 26),
 }
 
 

@@ -24,6 +24,8 @@ CASES = {
     "pairs": LayerShape("pairs", 720, 256, 8, 4, 256, 256, 1, 0.0, "zipf", "bf16", False, 15),
     # pairs for gate/up only (d not a multiple of 256: 128-column down tiles without pairs)
     "pairs_gu_only": LayerShape("pairs_gu_only", 660, 384, 8, 4, 128, 0, 0, 0.0, "normal0.1", "bf16", False, 16),
+    # the largest expert count and top-k the ABI accepts (E = 512, k = 8)
+    "max_E_k": LayerShape("max_E_k", 300, 256, 512, 8, 128, 128, 1, 0.0, "normal0.1", "bf16", False, 17),
 }
 
 
