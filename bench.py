@@ -295,6 +295,9 @@ def cpu_baseline(L, shape, pool_tokens=2, budget_s=12.0, max_steps=64):
 
 
 # ------------------------------------------------------------------ the GB300 arm
+TIMING_EVERY = 4  # per-launch event timing on every 4th timed step
+
+
 def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
     """Times `steps` whole-layer steps of `shape` (forward, plus backward for training
     workloads).  Returns the measurement and the layer inputs."""
@@ -333,10 +336,14 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
     dist_barrier(world)
     torch.cuda.synchronize()
     sampler.start()
-    mok.timing_enable(True)
+    # per-launch CUDA events on every TIMING_EVERY-th timed step (they cost about 1% of a step)
     ev0.record(stream)
     launches = 0
-    for _ in range(steps):
+    sampled = 0
+    for i in range(steps):
+        on = i % TIMING_EVERY == 0
+        mok.timing_enable(on)
+        sampled += on
         launches += step()
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -354,7 +361,7 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
     kernels = {}
     for name, (n, tms) in sorted(kern.items(), key=lambda kv: -kv[1][1]):
         entry = {"launches": n, "ms_total": round(tms, 4), "ms_per_launch": round(tms / max(n, 1), 5),
-                 "share": round(tms / max(ms, 1e-9), 4)}
+                 "share": round((tms / max(sampled, 1)) / max(ms / steps, 1e-9), 4)}
         if name in model:
             r = roofline_of(name, model, tms / max(n, 1), peaks)
             if not shape.backward:
@@ -378,7 +385,8 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
         "tflops_frac_of_dtype_peak": round(tflops / tpeak, 4),
         "dtype": "mxfp8 (e4m3 + ue8m0/32)" if mx else "bf16",
         "roofline": {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in roof.items()},
-        "kernels": kernels, "gpu_launches": launches, "clocks": clocks,
+        "kernels": kernels, "kernel_timing": f"CUDA events on {sampled} of the {steps} timed steps",
+        "gpu_launches": launches, "clocks": clocks,
         "active_experts": e_act, "max_expert_rows": max(counts), "empty_experts": counts.count(0),
     }
     if mx:  # context: the library's dense fp8 GEMM rate on this GPU (the roofline keeps 2 x bf16)
@@ -447,7 +455,8 @@ def run_mok(args, shape, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) activations, N(0,1/sqrt(fan_in)) bf16 weights, random init)",
         "config": config_of(shape, world, res["active_experts"]),
         "tflops": res["tflops"], "tflops_frac_of_bf16_peak": res["tflops_frac_of_bf16_peak"],
-        "roofline": res["roofline"], "kernels": res["kernels"], "gpu_launches": res["gpu_launches"],
+        "roofline": res["roofline"], "kernels": res["kernels"], "kernel_timing": res["kernel_timing"],
+        "gpu_launches": res["gpu_launches"],
         "clocks": res["clocks"], "e2e": e2e,
     }
     for key in ("fp8_cublas_tflops_measured", "tflops_frac_of_measured_fp8_gemm"):
