@@ -562,7 +562,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
-    ap.add_argument("--extra", default="dsv3_bf16_train,kimi_skew_bf16_fwd,dsv3_mxfp8_fwd")
+    ap.add_argument("--extra", default="dsv3_bf16_train,kimi_skew_bf16_fwd,dsv3_mxfp8_fwd,dsv3_decode_t64")
     ap.add_argument("--extra-steps", type=int, default=30)
     args = ap.parse_args(argv)
     if args.warmup < 3:

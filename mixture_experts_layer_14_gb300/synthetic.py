@@ -50,6 +50,10 @@ WORKLOADS = {
                                  "normal0.1", "mxfp8", False, 4),
     "dsv3_bf16_train": LayerShape("dsv3_bf16_train", 8192, 7168, 256, 8, 2048, 2048, 1, 0.0,
                                   "normal0.1", "bf16", True, 5),
+    # decode-sized batch of the same layer: 64 tokens (512 routes) still touch most experts, so
+    # the step streams nearly all the expert weights for few rows each
+    "dsv3_decode_t64": LayerShape("dsv3_decode_t64", 64, 7168, 256, 8, 2048, 2048, 1, 0.0,
+                                  "normal0.1", "bf16", False, 9),
     # A slice of the DeepSeek-V3 layer with the same rows per expert (T*k/E = 128) but 32
     # experts, so that a full profiler capture holds a few GB on the device.
     "dsv3_slice_e32": LayerShape("dsv3_slice_e32", 512, 7168, 32, 8, 2048, 2048, 1, 0.0,

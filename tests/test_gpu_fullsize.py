@@ -42,7 +42,8 @@ def _shared(L):
     return (f64(L["Ws_gate"]), f64(L["Ws_up"]), f64(L["Ws_down"]))
 
 
-@pytest.mark.parametrize("name,samples", [("dsv3_bf16_fwd", 4), ("kimi_skew_bf16_fwd", 4)])
+@pytest.mark.parametrize("name,samples", [("dsv3_bf16_fwd", 4), ("kimi_skew_bf16_fwd", 4),
+                                          ("dsv3_decode_t64", 4)])
 def test_fullsize_forward(name, samples):
     ensure_lib()
     shape = WORKLOADS[name]
