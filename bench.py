@@ -193,14 +193,14 @@ def work_model(shape, counts):
 # (32-expert slices: 33 weight sets).
 _GEMM_SRC = "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"
 PROFILED_TRAFFIC = {
-    "gemm_fwd_gate_up": ("fd3e602e871f", (2.015002e9 + 20.1664e6) / 33, _GEMM_SRC),
-    "gemm_fwd_down": ("fd3e602e871f", (0.992624e9 + 61.2288e6) / 33, _GEMM_SRC),
-    "gemm_fwd_gate_up_mx": ("fd3e602e871f", (1.083484e9 + 21.151488e6) / 33, _GEMM_SRC),
-    "gemm_fwd_down_mx": ("fd3e602e871f", (0.519271e9 + 114.100992e6) / 33, _GEMM_SRC),
+    "gemm_fwd_gate_up": ("9d0395352aa7", (2.015207e9 + 19.844864e6) / 33, _GEMM_SRC),
+    "gemm_fwd_down": ("9d0395352aa7", (0.992610e9 + 61.311744e6) / 33, _GEMM_SRC),
+    "gemm_fwd_gate_up_mx": ("9d0395352aa7", (1.081563e9 + 20.846848e6) / 33, _GEMM_SRC),
+    "gemm_fwd_down_mx": ("9d0395352aa7", (0.519242e9 + 114.017024e6) / 33, _GEMM_SRC),
     # profiles/gemm_bwd_dsv3_train_slice_e32.md
-    "gemm_bwd_da": ("fd3e602e871f", (1.199000e9 + 0.101744e9) / 33, _GEMM_SRC),
-    "gemm_bwd_dx": ("fd3e602e871f", (2.063276e9 + 0.127812e9) / 33, _GEMM_SRC),
-    "gemm_bwd_dw": ("fd3e602e871f", (0.378295e9 + 2.851484e9) / 33, _GEMM_SRC),
+    "gemm_bwd_da": ("9d0395352aa7", (1.198991e9 + 0.101332e9) / 33, _GEMM_SRC),
+    "gemm_bwd_dx": ("9d0395352aa7", (2.059321e9 + 0.127771e9) / 33, _GEMM_SRC),
+    "gemm_bwd_dw": ("9d0395352aa7", (0.378143e9 + 2.851202e9) / 33, _GEMM_SRC),
 }
 
 
