@@ -200,18 +200,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
 // (bit-identical from run to run), adds the bias, then selects the top k with k rounds of a
 // warp-shuffle argmax (larger logit first, lower expert index on ties) and writes the
 // renormalised softmax weights.  Lane l holds experts l, l+32, ...; loads are coalesced.
-constexpr int kMaxPerLane = kMaxE / 32;
 
+// PER: logits per lane (E <= 32 PER), a compile-time size so that the arrays stay in registers
+template <int PER>
 __global__ void __launch_bounds__(256) route_finish_kernel(const __grid_constant__ RouteParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int per = (p.E + 31) / 32;
   for (int64_t t = w; t < p.T; t += nw) {
-    float v[kMaxPerLane];
-    bool used[kMaxPerLane];
+    float v[PER];
+    bool used[PER];
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < PER; ++i) {
       const int e = lane + 32 * i;
       used[i] = true;
       v[i] = -INFINITY;
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(256) route_finish_kernel(const __grid_constant
         float best = -INFINITY;
         int bidx = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i) {
+        for (int i = 0; i < PER; ++i) {
           const int e = lane + 32 * i;
           if (!used[i] && (v[i] > best || (v[i] == best && e < bidx))) { best = v[i]; bidx = e; }
         }
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(256) route_finish_kernel(const __grid_constant
         }
         if (bidx != 0x7fffffff && (bidx & 31) == lane) {
 #pragma unroll
-          for (int i = 0; i < kMaxPerLane; ++i)
+          for (int i = 0; i < PER; ++i)
             if (i == (bidx >> 5)) used[i] = true;
         }
         tv[j] = best;
@@ -289,7 +290,11 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
   if (e != cudaSuccess || p.splits == 1) return e;
   const int64_t blocks = std::min<int64_t>((p.T + 7) / 8, (int64_t)num_sms() * 8);
   prof_begin("route_finish", s);
-  route_finish_kernel<<<(int)blocks, 256, 0, s>>>(p);
+  const int per = (p.E + 31) / 32;
+  if (per <= 2) route_finish_kernel<2><<<(int)blocks, 256, 0, s>>>(p);
+  else if (per <= 4) route_finish_kernel<4><<<(int)blocks, 256, 0, s>>>(p);
+  else if (per <= 8) route_finish_kernel<8><<<(int)blocks, 256, 0, s>>>(p);
+  else route_finish_kernel<kMaxE / 32><<<(int)blocks, 256, 0, s>>>(p);
   prof_end(s);
   return cudaGetLastError();
 }
