@@ -412,7 +412,9 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
     void* hqsh = at<void*>(ws, L.off[FW_HQSH]);
     uint8_t* hscsh = at<uint8_t*>(ws, L.off[FW_HSCSH]);
     rc = cuda_status(launch_mx_quantize_rows(x, T, d, xq, xsc, true, s));
-    if (rc == MOK_OK) rc = cuda_status(launch_gather_bytes(xq, sorted_tok, R, T, d, xqs, s));
+    if (rc == MOK_OK)
+      rc = cuda_status(launch_gather_rows("gather_bytes", xq, nullptr, inv_pos, T, dims->k, d, xqs,
+                                          nullptr, s));
     if (rc == MOK_OK)
       rc = cuda_status(launch_gather_scale_atoms(xsc, sorted_tok, offsets, E, T, R, d, xscs, s));
     if (rc != MOK_OK) return rc;
@@ -496,7 +498,7 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
   }
 
   // 1. pull-gather of every expert's token rows
-  rc = cuda_status(launch_gather_rows(x, sorted_tok, R, T, d, xs, s));
+  rc = cuda_status(launch_gather_rows("gather", x, nullptr, inv_pos, T, dims->k, 2 * d, xs, nullptr, s));
   if (rc != MOK_OK) return rc;
   ++launches;
 
@@ -638,7 +640,7 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
   const int grid_cap = num_sms();
 
   // 1. gather x and dY rows into each expert's region
-  rc = cuda_status(launch_gather_rows2(x, dY, sorted_tok, R, T, d, xs, dys, s));
+  rc = cuda_status(launch_gather_rows("gather2", x, dY, inv_pos, T, dims->k, 2 * d, xs, dys, s));
   if (rc != MOK_OK) return rc;
   ++launches;
   // 2. a = dY W_down^T; epilogue: dG, dU, w*h and the router partials <a, h>

@@ -13,91 +13,57 @@ static int rows_grid(int64_t nrows) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)num_sms() * 8));
 }
 
-// dst[r] = src[rows[r]] for r < nrows (page "Метод и эксперименты": each expert pulls its
-// tokens; with the tokens of an expert ascending the reads walk x in order).  A row index
-// outside [0, nsrc) yields a zero row.  With a second source (the backward pulls x and dY with
-// the same schedule) the warps take the 2 nrows rows of both in one list.
+// Pull gather (page "Метод и эксперименты": each expert pulls its tokens' rows into its region):
+// for every kept route (t, j), dst[inv_pos[t, j]] = src[t].  Token-major: each source row is read
+// once and written to its k destination rows, so a source larger than L2 is read from memory
+// once rather than once per route.  With a second source (the backward pulls x and dY with the
+// same schedule) the warps take both in one list.  Rows are handled as 16-byte vectors (bf16
+// rows and E4M3 code rows alike); destination rows that no kept route names are not written.
 __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(
-    const uint4* __restrict__ src0, const uint4* __restrict__ src1, const int32_t* __restrict__ rows,
-    int64_t nrows, int64_t nsrc, int vec_per_row, uint4* __restrict__ dst0, uint4* __restrict__ dst1) {
+    const uint4* __restrict__ src0, const uint4* __restrict__ src1,
+    const int32_t* __restrict__ inv_pos, int64_t T, int k, int vec_per_row,
+    uint4* __restrict__ dst0, uint4* __restrict__ dst1) {
   const int lane = threadIdx.x & 31;
   const int64_t wglobal = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t total = src1 ? 2 * nrows : nrows;
-  for (int64_t rr = wglobal; rr < total; rr += nwarps) {
-    const bool second = rr >= nrows;
-    const int64_t r = second ? rr - nrows : rr;
-    const uint4* src = second ? src1 : src0;
-    uint4* d = (second ? dst1 : dst0) + r * vec_per_row;
-    const int64_t t = rows[r];
-    if (t < 0 || t >= nsrc) {
-      for (int v = lane; v < vec_per_row; v += 32) d[v] = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    // four 16-byte loads in flight per lane before their stores; the destination rows are
-    // written with evict-first stores so they do not push the source out of L2
-    const uint4* s0 = src + t * vec_per_row;
+  const int64_t total = src1 ? 2 * T : T;
+  for (int64_t tt = wglobal; tt < total; tt += nwarps) {
+    const bool second = tt >= T;
+    const int64_t t = second ? tt - T : tt;
+    const uint4* s = (second ? src1 : src0) + t * vec_per_row;
+    uint4* dbase = second ? dst1 : dst0;
+    const int mine = lane < k ? inv_pos[t * k + lane] : -1;  // lane j: destination of route j
+    int dst_row[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) dst_row[j] = __shfl_sync(0xffffffffu, mine, j);
+    // four 16-byte loads in flight per lane, each stored to every destination row with
+    // evict-first stores (they are read back by the next kernel, not by this one)
     for (int v = lane; v < vec_per_row; v += 128) {
       uint4 a[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (v + 32 * u < vec_per_row) a[u] = s0[v + 32 * u];
+        if (v + 32 * u < vec_per_row) a[u] = s[v + 32 * u];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (v + 32 * u < vec_per_row) __stcs(d + v + 32 * u, a[u]);
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k && dst_row[j] >= 0) {
+          uint4* d = dbase + (int64_t)dst_row[j] * vec_per_row;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (v + 32 * u < vec_per_row) __stcs(d + v + 32 * u, a[u]);
+        }
+      }
     }
   }
 }
 
-cudaError_t launch_gather_rows(const void* src, const int32_t* rows, int64_t nrows, int64_t nsrc,
-                               int d, void* dst, cudaStream_t s) {
-  return launch_gather_rows2(src, nullptr, rows, nrows, nsrc, d, dst, nullptr, s);
-}
-
-cudaError_t launch_gather_rows2(const void* src0, const void* src1, const int32_t* rows,
-                                int64_t nrows, int64_t nsrc, int d, void* dst0, void* dst1,
-                                cudaStream_t s) {
-  if (nrows == 0) return cudaSuccess;
-  prof_begin(src1 ? "gather2" : "gather", s);
-  gather_rows_kernel<<<rows_grid(src1 ? 2 * nrows : nrows), kRowThreads, 0, s>>>(
-      static_cast<const uint4*>(src0), static_cast<const uint4*>(src1), rows, nrows, nsrc, d / 8,
-      static_cast<uint4*>(dst0), static_cast<uint4*>(dst1));
-  prof_end(s);
-  return cudaGetLastError();
-}
-
-// Byte rows (row_bytes a multiple of 4): dst[r] = src[rows[r]] — the pull gather of E4M3 rows
-// and of their UE8M0 scale rows in the MXFP8 path.
-__global__ void __launch_bounds__(kRowThreads) gather_bytes_kernel(
-    const uint32_t* __restrict__ src, const int32_t* __restrict__ rows, int64_t nrows, int64_t nsrc,
-    int words, uint32_t* __restrict__ dst) {
-  const int lane = threadIdx.x & 31;
-  const int64_t wglobal = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t r = wglobal; r < nrows; r += nwarps) {
-    const int64_t t = rows[r];
-    uint32_t* d = dst + r * words;
-    if (t < 0 || t >= nsrc) {
-      for (int v = lane; v < words; v += 32) d[v] = 0u;
-      continue;
-    }
-    const uint32_t* s = src + t * words;
-    if ((words & 3) == 0) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(s);
-      uint4* d4 = reinterpret_cast<uint4*>(d);
-      for (int v = lane; v < words / 4; v += 32) __stcs(d4 + v, s4[v]);
-    } else {
-      for (int v = lane; v < words; v += 32) d[v] = s[v];
-    }
-  }
-}
-
-cudaError_t launch_gather_bytes(const void* src, const int32_t* rows, int64_t nrows, int64_t nsrc,
-                                int row_bytes, void* dst, cudaStream_t s) {
-  if (nrows == 0) return cudaSuccess;
-  prof_begin("gather_bytes", s);
-  gather_bytes_kernel<<<rows_grid(nrows), kRowThreads, 0, s>>>(
-      static_cast<const uint32_t*>(src), rows, nrows, nsrc, row_bytes / 4, static_cast<uint32_t*>(dst));
+cudaError_t launch_gather_rows(const char* name, const void* src0, const void* src1,
+                               const int32_t* inv_pos, int64_t T, int k, int row_bytes,
+                               void* dst0, void* dst1, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  prof_begin(name, s);
+  gather_rows_kernel<<<rows_grid(src1 ? 2 * T : T), kRowThreads, 0, s>>>(
+      static_cast<const uint4*>(src0), static_cast<const uint4*>(src1), inv_pos, T, k,
+      row_bytes / 16, static_cast<uint4*>(dst0), static_cast<uint4*>(dst1));
   prof_end(s);
   return cudaGetLastError();
 }

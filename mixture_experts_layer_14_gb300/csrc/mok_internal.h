@@ -125,11 +125,11 @@ cudaError_t launch_dispatch(int64_t T, int E, int k, const int32_t* topk_idx, co
 
 // Elementwise (elementwise.cu)
 // Row gathers: dst[r] = src[rows[r]] for r < nrows; an index outside [0, nsrc) gives a zero row.
-cudaError_t launch_gather_rows(const void* src, const int32_t* rows, int64_t nrows, int64_t nsrc,
-                               int d, void* dst, cudaStream_t s);
-cudaError_t launch_gather_rows2(const void* src0, const void* src1, const int32_t* rows,
-                                int64_t nrows, int64_t nsrc, int d, void* dst0, void* dst1,
-                                cudaStream_t s);
+// Token-major pull gather: dst[inv_pos[t, j]] = src[t] for every kept route (rows of row_bytes,
+// a multiple of 16); a second source / destination pair (or NULL) moves the same way.
+cudaError_t launch_gather_rows(const char* name, const void* src0, const void* src1,
+                               const int32_t* inv_pos, int64_t T, int k, int row_bytes,
+                               void* dst0, void* dst1, cudaStream_t s);
 cudaError_t launch_combine(int64_t T, int d, int k, const int32_t* topk_idx,
                            const int32_t* inv_pos, const void* Ys, const void* Ysh, void* y,
                            cudaStream_t s);
@@ -148,9 +148,6 @@ cudaError_t launch_gather_scale_atoms(const void* src, const int32_t* sorted_tok
                                       void* dst, cudaStream_t s);
 cudaError_t launch_mx_quantize_transpose(const void* src, int64_t nmat, int K, int N, void* q,
                                          void* sc, cudaStream_t s);
-cudaError_t launch_gather_bytes(const void* src, const int32_t* rows, int64_t nrows, int64_t nsrc,
-                                int row_bytes, void* dst, cudaStream_t s);
-
 // Optional per-launch CUDA-event timing (profile.cu); no-ops unless enabled on this thread.
 void prof_begin(const char* name, cudaStream_t s);
 void prof_end(cudaStream_t s);
