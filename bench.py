@@ -171,7 +171,7 @@ def work_model(shape, counts):
             "flops": m["gemm_fwd_down"]["flops"], "dtype": "fp8",
             "bytes": wq * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Hs) + wb * Rs * d}
     if train:
-        m["gather2"] = {"flops": 0.0, "bytes": 2.0 * wb * (T * d + R * d) + 4.0 * R}
+        m["gather_dy"] = {"flops": 0.0, "bytes": wb * (T * d + R * d) + 4.0 * R}
         m["gemm_bwd_da"] = {  # a = dY Wd^T; reads G, U; writes dG, dU, w*h
             "flops": 2.0 * (R * F * d + T * ns * Fs * d),
             "bytes": wb * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Rs * d + 5.0 * Hs) + 4.0 * R * 16}

@@ -148,7 +148,8 @@ int mok_dispatch_index(const mok_dims *dims, const int32_t *topk_idx, const floa
  * the shared expert in one persistent launch per phase), then combines every token's rows in
  * ascending expert order on top of the shared-expert row (fp32 accumulation, one bf16
  * rounding).
- *   -> y[T,d] bf16.  `saved` (mok_saved_size bytes or NULL) receives G and U for backward. */
+ *   -> y[T,d] bf16.  `saved` (mok_saved_size bytes or NULL) receives what the backward needs:
+ *   G and U, and x in expert order. */
 int mok_moe_forward(const mok_dims *dims, const mok_weights *w, const void *x,
                     const int32_t *topk_idx, const int32_t *offsets, const int32_t *sorted_tok,
                     const float *sorted_w, const int32_t *inv_pos, void *y, void *saved,

@@ -103,12 +103,12 @@ enum PrepSlot {  // MXFP8 prepared weights: K-major codes [n][N][K] and scale at
   PR_GQ, PR_GS, PR_UQ, PR_US, PR_DQ, PR_DS, PR_SGQ, PR_SGS, PR_SUQ, PR_SUS, PR_SDQ, PR_SDS, PR_N
 };
 enum BwdSlot {
-  BW_STATUS, BW_XS, BW_DYS, BW_DG, BW_DU, BW_HW, BW_DGSH, BW_DUSH, BW_HWSH, BW_P, BW_DL,
+  BW_STATUS, BW_DYS, BW_DG, BW_DU, BW_HW, BW_DGSH, BW_DUSH, BW_HWSH, BW_P, BW_DL,
   BW_DXS, BW_DXSH,
   BW_TMAP,  // weight-gradient GEMM: expert-bounded tensor-map copies
   BW_N
 };
-enum SavedSlot { SV_G, SV_U, SV_GSH, SV_USH, SV_N };
+enum SavedSlot { SV_G, SV_U, SV_GSH, SV_USH, SV_XS, SV_N };
 enum HostSlot { HS_X, HS_Y, HS_IDX, HS_W, HS_CNT, HS_OFF, HS_STOK, HS_SW, HS_INV, HS_N };
 
 static int bn_for(int a, int b, int c) { return (a % 256 == 0 && b % 256 == 0 && c % 256 == 0) ? 256 : 128; }
@@ -158,7 +158,6 @@ static Layout layout_bwd(const mok_dims* d) {
   const int ntda = d->F / bwd_bn_da(d);
   size_t sz[BW_N] = {};
   sz[BW_STATUS] = 256;
-  sz[BW_XS] = 2ull * R * d->d;
   sz[BW_DYS] = 2ull * R * d->d;
   sz[BW_DG] = sz[BW_DU] = sz[BW_HW] = 2ull * R * d->F;
   sz[BW_DGSH] = sz[BW_DUSH] = sz[BW_HWSH] = 2ull * T * Fs;
@@ -188,7 +187,8 @@ static Layout layout_prepared(const mok_dims* d) {
 static Layout layout_saved(const mok_dims* d) {
   const int64_t T = d->T, R = T * d->k;
   const int Fs = d->n_shared ? d->F_shared : 0;
-  size_t sz[SV_N] = {2ull * R * d->F, 2ull * R * d->F, 2ull * T * Fs, 2ull * T * Fs};
+  size_t sz[SV_N] = {2ull * R * d->F, 2ull * R * d->F, 2ull * T * Fs, 2ull * T * Fs,
+                     2ull * R * d->d};  // G, U, their shared-expert copies, x in expert order
   Layout L{};
   size_t o = 0;
   for (int i = 0; i < SV_N; ++i) { L.off[i] = o; o += al(sz[i]); }
@@ -497,7 +497,8 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
     return MOK_OK;
   }
 
-  // 1. pull-gather of every expert's token rows
+  // 1. pull-gather of every expert's token rows (into `saved` when the backward will need them)
+  if (saved) xs = at<void*>(saved, S.off[SV_XS]);
   rc = cuda_status(launch_gather_rows("gather", x, nullptr, inv_pos, T, dims->k, 2 * d, xs, nullptr, s));
   if (rc != MOK_OK) return rc;
   ++launches;
@@ -624,7 +625,8 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
     return rc;
   }
   const Layout S = layout_saved(dims);
-  void* xs = at<void*>(ws, L.off[BW_XS]);
+  // x in expert order comes from the forward (`saved`); dY is pulled here
+  void* xs = at<void*>(const_cast<void*>(saved), S.off[SV_XS]);
   void* dys = at<void*>(ws, L.off[BW_DYS]);
   void* dG = at<void*>(ws, L.off[BW_DG]);
   void* dU = at<void*>(ws, L.off[BW_DU]);
@@ -639,8 +641,8 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
   const int ldl = (E + 63) & ~63;
   const int grid_cap = num_sms();
 
-  // 1. gather x and dY rows into each expert's region
-  rc = cuda_status(launch_gather_rows("gather2", x, dY, inv_pos, T, dims->k, 2 * d, xs, dys, s));
+  // 1. gather dY rows into each expert's region
+  rc = cuda_status(launch_gather_rows("gather_dy", dY, nullptr, inv_pos, T, dims->k, 2 * d, dys, nullptr, s));
   if (rc != MOK_OK) return rc;
   ++launches;
   // 2. a = dY W_down^T; epilogue: dG, dU, w*h and the router partials <a, h>

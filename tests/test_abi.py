@@ -44,8 +44,8 @@ def test_status_strings_and_size_queries():
     bw = mok.workspace_size(D, backward=True)
     R = 4096 * 8
     assert fw >= 2 * R * 7168 * 2 + R * 2048 * 2          # x_sorted, Y_s and h at least
-    assert bw >= 3 * R * 7168 * 2
-    assert mok.saved_size(D) >= 2 * R * 2048 * 2
+    assert bw >= 2 * R * 7168 * 2                          # dY_sorted and dX_s at least
+    assert mok.saved_size(D) >= 2 * R * 2048 * 2 + R * 7168 * 2   # G, U and x in expert order
     bad = [mok.dims(16, 100, 8, 2, 128), mok.dims(16, 128, 8, 9, 128), mok.dims(16, 128, 12, 2, 128),
            mok.dims(16, 128, 8, 2, 96), mok.dims(-1, 128, 8, 2, 128), mok.dims(16, 128, 1024, 2, 128)]
     for D in bad:
