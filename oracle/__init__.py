@@ -43,6 +43,7 @@ from .moe import (  # noqa: F401
     moe_forward_from_logits,
     moe_backward,
     moe_forward_mxfp8,
+    moe_backward_mxfp8,
 )
 from .mxfp8 import (  # noqa: F401
     E4M3_MAX,

@@ -292,3 +292,103 @@ def moe_forward_mxfp8(x, Wg, Wu, Wd, shared, topk_idx, topk_w):
         rows, slots = np.nonzero(idx == e)
         np.add.at(y, rows, w[rows, slots][:, None] * ffn(xq[rows], Wg[e], Wu[e], Wd[e]))
     return y
+
+
+# --------------------------------------------------------------------------------------
+# MXFP8 reading of the backward.  The pages give MXFP8 for the layer's kernel without saying
+# which GEMMs of a training step it covers; the plain extension of the forward reading above is
+# taken: every expert GEMM of the backward multiplies E4M3/UE8M0 operands, each quantised in
+# blocks of 32 along that GEMM's own reduction dimension, with exact products and sums:
+#   a       = q_d(dY) q_d(W_down)^T                       (reduction over d)
+#   dX_e    = q_F(dG) q_F(W_gate)^T + q_F(dU) q_F(W_up)^T    (over F)
+#   dW_gate = q_t(X)^T q_t(dG),  dW_up = q_t(X)^T q_t(dU),  dW_down = q_t(w h)^T q_t(dY)
+#             (over the expert's tokens, in token order, blocks of 32 from its first token)
+# The forward values being differentiated are those of the MXFP8 forward (g = q_d(x) q_d(W_gate),
+# u likewise).  The router terms (dl W_router^T, x^T dl), the SwiGLU derivative and the
+# router-weight gradient <a, h> stay unquantised.
+# --------------------------------------------------------------------------------------
+
+def _mx_qd_tokens(A):
+    """Quantise-dequantise A[n, C] along its first axis (tokens) in blocks of 32 rows from row 0;
+    a last partial block counts as padded with zeros (zeros do not change a block's amax)."""
+    A = np.asarray(A, dtype=np.float64)
+    n = A.shape[0]
+    pad = (-n) % 32
+    Ap = np.concatenate([A, np.zeros((pad,) + A.shape[1:])], axis=0)
+    return _mx_qd(Ap.T).T[:n]
+
+
+def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_experts=None):
+    """Gradients with the MXFP8 quantisation points above; same arguments and result keys as
+    moe_backward.  Pinned by: every gradient stays within a few E4M3 steps of moe_backward's
+    (itself pinned by finite differences) and differs from it; on inputs and weights exactly
+    representable in MXFP8 the router-weight gradients, dlogits and dW_router equal the float64
+    ones; the token-axis quantiser matches the pinned quantiser applied column by column."""
+    x = np.asarray(x, dtype=np.float64)
+    dY = np.asarray(dY, dtype=np.float64)
+    Wr = np.asarray(W_router, dtype=np.float64)
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    T, d = x.shape
+    E = Wr.shape[1]
+    k = idx.shape[1]
+    w = weights_for_selection(logits, idx)
+    xq = _mx_qd(x)
+    dYq = _mx_qd(dY)
+    dX = np.zeros_like(x)
+    dWg, dWu, dWd = {}, {}, {}
+    dw = np.zeros((T, k))
+
+    def ffn_backward(X, Xq, dYr, dYrq, wr, Wge, Wue, Wde):
+        Wge = np.asarray(Wge, dtype=np.float64)
+        Wue = np.asarray(Wue, dtype=np.float64)
+        Wde = np.asarray(Wde, dtype=np.float64)
+        g = Xq @ _mx_weight(Wge)                 # the MXFP8 forward's gate and up values
+        u = Xq @ _mx_weight(Wue)
+        s = 1.0 / (1.0 + np.exp(-g))
+        h = g * s * u
+        a = dYrq @ _mx_qd(Wde).T                 # W_down [F, d]: blocks along d
+        dwr = (a * h).sum(axis=1)
+        dh = wr[:, None] * a
+        dg = dh * u * s * (1.0 + g * (1.0 - s))
+        du = dh * g * s
+        dXr = _mx_qd(dg) @ _mx_qd(Wge).T + _mx_qd(du) @ _mx_qd(Wue).T   # W_gate [d, F]: along F
+        Xt = _mx_qd_tokens(X)
+        dWge = Xt.T @ _mx_qd_tokens(dg)
+        dWue = Xt.T @ _mx_qd_tokens(du)
+        dWde = _mx_qd_tokens(wr[:, None] * h).T @ _mx_qd_tokens(dYr)
+        return dXr, dWge, dWue, dWde, dwr
+
+    for e in (range(E) if only_experts is None else only_experts):
+        rows, slots = np.nonzero(idx == e)
+        if rows.size == 0:
+            continue
+        dXr, dWg[e], dWu[e], dWd[e], dwr = ffn_backward(
+            x[rows], xq[rows], dY[rows], dYq[rows], w[rows, slots], Wg[e], Wu[e], Wd[e])
+        np.add.at(dX, rows, dXr)
+        dw[rows, slots] = dwr
+
+    dWs = None
+    if shared is not None:
+        dXs, dWsg, dWsu, dWsd, _ = ffn_backward(x, xq, dY, dYq, np.ones(T), *shared)
+        dX += dXs
+        dWs = (dWsg, dWsu, dWsd)
+
+    dl = np.zeros((T, E))
+    inner = (w * dw).sum(axis=1, keepdims=True)
+    np.put_along_axis(dl, idx, w * (dw - inner), axis=1)
+    dX += dl @ Wr.T
+    dWr = x.T @ dl
+    if only_experts is None:
+        Wg0 = np.asarray(Wg[0])
+        zg = np.zeros(Wg0.shape)
+        zd = np.zeros(Wg0.shape[::-1])
+        dWg = np.stack([dWg.get(e, zg) for e in range(E)])
+        dWu = np.stack([dWu.get(e, zg) for e in range(E)])
+        dWd = np.stack([dWd.get(e, zd) for e in range(E)])
+    return {
+        "dX": dX, "dW_gate": dWg, "dW_up": dWu, "dW_down": dWd,
+        "dWs_gate": None if dWs is None else dWs[0],
+        "dWs_up": None if dWs is None else dWs[1],
+        "dWs_down": None if dWs is None else dWs[2],
+        "dlogits": dl, "dW_router": dWr, "dw": dw,
+    }

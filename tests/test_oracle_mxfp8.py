@@ -113,3 +113,78 @@ def test_mxfp8_forward_pins():
     yq = oracle.moe_forward_mxfp8(x, Wg, Wu, Wd, sh, idx, w)
     rel = np.abs(yq - y).max() / np.abs(y).max()
     assert 1e-4 < rel < 0.1
+
+
+def test_token_axis_quantiser_matches_columnwise_quantiser():
+    """The weight-gradient operands are quantised along tokens: each column of A[n, C] in blocks
+    of 32 rows from row 0, the last block zero-padded.  Checked column by column against the
+    pinned quantiser on a padded vector."""
+    from oracle.moe import _mx_qd_tokens
+
+    rng = np.random.default_rng(4)
+    A = rng.standard_normal((70, 5)) * np.exp2(rng.integers(-8, 8, size=(70, 1)))
+    got = _mx_qd_tokens(A)
+    for j in range(A.shape[1]):
+        col = np.concatenate([A[:, j], np.zeros(26)])
+        want = oracle.mx_dequantize(*oracle.mx_quantize(col[None, :]))[0, :70]
+        assert (got[:, j] == want).all()
+    # a large token in block 0 coarsens its block's other values but not block 1's
+    B = A.copy()
+    B[3, :] *= 2.0 ** 12
+    q = _mx_qd_tokens(B)
+    assert (q[32:64] == got[32:64]).all()
+    assert (q[[0, 1, 2, 4]] != got[[0, 1, 2, 4]]).any()
+
+
+def _small_backward_case(rng, representable):
+    T, d, E, k, F = 40, 64, 3, 2, 64
+    if representable:
+        x = _representable(rng, (T, d))
+        dY = _representable(rng, (T, d))
+        Wg = np.stack([_representable(rng, (d, F)) / 16 for _ in range(E)])
+        Wu = np.stack([_representable(rng, (d, F)) / 16 for _ in range(E)])
+        Wd = np.stack([_representable(rng, (F, d)) / 16 for _ in range(E)])
+        sh = tuple(_representable(rng, s) / 16 for s in ((d, F), (d, F), (F, d)))
+        Wr = _representable(rng, (d, E)) / 16
+    else:
+        x = rng.standard_normal((T, d))
+        dY = rng.standard_normal((T, d))
+        Wg, Wu = rng.standard_normal((E, d, F)) / 8, rng.standard_normal((E, d, F)) / 8
+        Wd = rng.standard_normal((E, F, d)) / 8
+        sh = (rng.standard_normal((d, F)) / 8, rng.standard_normal((d, F)) / 8,
+              rng.standard_normal((F, d)) / 8)
+        Wr = rng.standard_normal((d, E)) / 8
+    logits = x @ Wr
+    idx = np.argsort(-logits, axis=1, kind="stable")[:, :k].astype(np.int32)
+    return x, dY, Wr, Wg, Wu, Wd, sh, logits, idx
+
+
+def test_mxfp8_backward_within_e4m3_steps_of_float64():
+    """Every gradient of the MXFP8 reading is within a few E4M3 steps of the float64 backward
+    (pinned by finite differences) and not equal to it: a dropped or transposed term would be an
+    O(1) error, a missing quantisation point an exact match."""
+    rng = np.random.default_rng(5)
+    args = _small_backward_case(rng, representable=False)
+    ref = oracle.moe_backward(*args)
+    got = oracle.moe_backward_mxfp8(*args)
+    for key in ("dX", "dW_gate", "dW_up", "dW_down", "dWs_gate", "dWs_up", "dWs_down",
+                "dlogits", "dW_router"):
+        rel = np.abs(got[key] - ref[key]).max() / np.abs(ref[key]).max()
+        assert 1e-4 < rel < 0.15, (key, rel)
+
+
+def test_mxfp8_backward_router_path_exact_on_representable_inputs():
+    """With x, dY and every weight exactly representable in MXFP8, q_d(dY) q_d(W_down)^T and the
+    forward's gate/up products are the float64 ones, so the router-weight gradients <a, h>,
+    dlogits and dW_router equal the float64 backward's; the weight gradients do not (dG, dU and
+    w h are quantised)."""
+    rng = np.random.default_rng(6)
+    args = _small_backward_case(rng, representable=True)
+    ref = oracle.moe_backward(*args)
+    got = oracle.moe_backward_mxfp8(*args)
+    for key in ("dw", "dlogits", "dW_router"):
+        assert np.allclose(got[key], ref[key], rtol=1e-12, atol=1e-12 * np.abs(ref[key]).max()), key
+    assert not np.allclose(got["dW_gate"], ref["dW_gate"], rtol=1e-6, atol=0)
+    zero = oracle.moe_backward_mxfp8(args[0], np.zeros_like(args[1]), *args[2:])
+    for key in ("dX", "dW_gate", "dW_up", "dW_down", "dlogits"):
+        assert not zero[key].any(), key
