@@ -308,6 +308,16 @@ def moe_forward_mxfp8(x, Wg, Wu, Wd, shared, topk_idx, topk_w):
 # router-weight gradient <a, h> stay unquantised.
 # --------------------------------------------------------------------------------------
 
+def bf16_round(a):
+    """Round to bf16 the way a float32 value is stored as bf16 (round to nearest, ties to even):
+    float64 -> float32 first, then the 16 low bits rounded off.  Pinned against the library's
+    float32 -> bfloat16 conversion."""
+    f = np.asarray(a, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def _mx_qd_tokens(A):
     """Quantise-dequantise A[n, C] along its first axis (tokens) in blocks of 32 rows from row 0;
     a last partial block counts as padded with zeros (zeros do not change a block's amax)."""
@@ -318,12 +328,19 @@ def _mx_qd_tokens(A):
     return _mx_qd(Ap.T).T[:n]
 
 
-def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_experts=None):
+def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_experts=None,
+                       bf16_stored=False):
     """Gradients with the MXFP8 quantisation points above; same arguments and result keys as
     moe_backward.  Pinned by: every gradient stays within a few E4M3 steps of moe_backward's
     (itself pinned by finite differences) and differs from it; on inputs and weights exactly
     representable in MXFP8 the router-weight gradients, dlogits and dW_router equal the float64
-    ones; the token-axis quantiser matches the pinned quantiser applied column by column."""
+    ones; the token-axis quantiser matches the pinned quantiser applied column by column.
+
+    bf16_stored: the tensors a training step keeps in memory between its GEMMs are rounded to
+    bf16 where they are stored (bf16_round): G and U as the forward saves them, and dG, dU and
+    w h as the weight-gradient quantiser reads them.  E4M3 re-quantisation turns those roundings
+    into whole-step code changes for a few per cent of the elements, so this variant is the
+    closer reference for a path that stores them in bf16."""
     x = np.asarray(x, dtype=np.float64)
     dY = np.asarray(dY, dtype=np.float64)
     Wr = np.asarray(W_router, dtype=np.float64)
@@ -344,6 +361,8 @@ def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, on
         Wde = np.asarray(Wde, dtype=np.float64)
         g = Xq @ _mx_weight(Wge)                 # the MXFP8 forward's gate and up values
         u = Xq @ _mx_weight(Wue)
+        if bf16_stored:
+            g, u = bf16_round(g), bf16_round(u)
         s = 1.0 / (1.0 + np.exp(-g))
         h = g * s * u
         a = dYrq @ _mx_qd(Wde).T                 # W_down [F, d]: blocks along d
@@ -352,10 +371,13 @@ def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, on
         dg = dh * u * s * (1.0 + g * (1.0 - s))
         du = dh * g * s
         dXr = _mx_qd(dg) @ _mx_qd(Wge).T + _mx_qd(du) @ _mx_qd(Wue).T   # W_gate [d, F]: along F
+        hw = wr[:, None] * h
+        if bf16_stored:
+            dg, du, hw = bf16_round(dg), bf16_round(du), bf16_round(hw)
         Xt = _mx_qd_tokens(X)
         dWge = Xt.T @ _mx_qd_tokens(dg)
         dWue = Xt.T @ _mx_qd_tokens(du)
-        dWde = _mx_qd_tokens(wr[:, None] * h).T @ _mx_qd_tokens(dYr)
+        dWde = _mx_qd_tokens(hw).T @ _mx_qd_tokens(dYr)
         return dXr, dWge, dWue, dWde, dwr
 
     for e in (range(E) if only_experts is None else only_experts):
