@@ -182,6 +182,24 @@ def work_model(shape, counts):
         m["gemm_bwd_dw"] = {  # dWg, dWu, dWd (written for every expert) and x^T dl
             "flops": 2.0 * (3.0 * (R * F * d + T * ns * Fs * d) + T * d * E),
             "bytes": wb * (3.0 * (E * d * F + ns * d * Fs) + 2.0 * Rs * d + 3.0 * Hs + d * E)}
+        if shape.dtype == "mxfp8":
+            wq = 1.0 + 1.0 / 32
+            ops_t = 2.0 * Rs * d + 3.0 * Hs  # token-axis operands: x, dY, dG, dU, w*h
+            m["gemm_bwd_da_mx"] = {  # reads dY codes, W_down codes, G, U; writes dG, dU, w*h, codes
+                "flops": m["gemm_bwd_da"]["flops"], "dtype": "fp8",
+                "bytes": wq * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Rs * d + 2.0 * Hs)
+                + wb * 5.0 * Hs + 4.0 * R * (F // 128)}
+            m["gemm_bwd_dx_mx"] = {
+                "flops": 2.0 * (R * 2 * F * d + T * ns * 2 * Fs * d), "dtype": "fp8",
+                "bytes": wq * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + 2.0 * Hs) + wb * Rs * d}
+            m["gemm_bwd_dx"] = {"flops": 2.0 * T * E * d, "bytes": wb * (T * E + d * E + T * d)}
+            m["gemm_bwd_dw_mx"] = {
+                "flops": 2.0 * 3.0 * (R * F * d + T * ns * Fs * d), "dtype": "fp8",
+                "bytes": wb * 3.0 * (E * d * F + ns * d * Fs) + wq * ops_t}
+            m["gemm_bwd_dw"] = {"flops": 2.0 * T * d * E, "bytes": wb * (T * d + T * E + d * E)}
+            # per launch (two per group: x and dY, then dG, dU and w*h)
+            m["mx_quantize_tokens"] = {"flops": 0.0,
+                                       "bytes": (wb + wq) * ops_t / (2.0 * (1 + ns))}
         layer_flops = 3.0 * layer_flops
     return m, layer_flops, e_act
 
@@ -193,14 +211,14 @@ def work_model(shape, counts):
 # (32-expert slices: 33 weight sets).
 _GEMM_SRC = "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"
 PROFILED_TRAFFIC = {
-    "gemm_fwd_gate_up": ("9d0395352aa7", (2.015207e9 + 19.844864e6) / 33, _GEMM_SRC),
-    "gemm_fwd_down": ("9d0395352aa7", (0.992610e9 + 61.311744e6) / 33, _GEMM_SRC),
-    "gemm_fwd_gate_up_mx": ("9d0395352aa7", (1.081563e9 + 20.846848e6) / 33, _GEMM_SRC),
-    "gemm_fwd_down_mx": ("9d0395352aa7", (0.519242e9 + 114.017024e6) / 33, _GEMM_SRC),
+    "gemm_fwd_gate_up": ("9199640349bb", (2.015109e9 + 20.168960e6) / 33, _GEMM_SRC),
+    "gemm_fwd_down": ("9199640349bb", (0.992911e9 + 61.100800e6) / 33, _GEMM_SRC),
+    "gemm_fwd_gate_up_mx": ("9199640349bb", (1.083810e9 + 20.746496e6) / 33, _GEMM_SRC),
+    "gemm_fwd_down_mx": ("9199640349bb", (0.519240e9 + 114.256640e6) / 33, _GEMM_SRC),
     # profiles/gemm_bwd_dsv3_train_slice_e32.md
-    "gemm_bwd_da": ("9d0395352aa7", (1.198991e9 + 0.101332e9) / 33, _GEMM_SRC),
-    "gemm_bwd_dx": ("9d0395352aa7", (2.059321e9 + 0.127771e9) / 33, _GEMM_SRC),
-    "gemm_bwd_dw": ("9d0395352aa7", (0.378143e9 + 2.851202e9) / 33, _GEMM_SRC),
+    "gemm_bwd_da": ("9199640349bb", (1.198978e9 + 0.101969e9) / 33, _GEMM_SRC),
+    "gemm_bwd_dx": ("9199640349bb", (2.064511e9 + 0.127574e9) / 33, _GEMM_SRC),
+    "gemm_bwd_dw": ("9199640349bb", (0.378173e9 + 2.851676e9) / 33, _GEMM_SRC),
 }
 
 
@@ -313,6 +331,8 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
                  mok.MOK_MXFP8 if mx else mok.MOK_BF16)
     if mx:  # weights are quantised once, outside the timed region
         L["prepared"] = mok.prepare_weights(D, L)
+        if shape.backward:
+            L["prepared_bwd"] = mok.prepare_weights_bwd(D, L)
     layer = mok.MoELayer(D, L, dev)
     x = L["x"]
     torch.cuda.synchronize()
@@ -562,7 +582,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
-    ap.add_argument("--extra", default="dsv3_bf16_train,kimi_skew_bf16_fwd,dsv3_mxfp8_fwd,dsv3_decode_t64")
+    ap.add_argument("--extra", default="dsv3_bf16_train,kimi_skew_bf16_fwd,dsv3_mxfp8_fwd,"
+                    "dsv3_mxfp8_train,dsv3_decode_t64")
     ap.add_argument("--extra-steps", type=int, default=30)
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -72,7 +72,8 @@ typedef struct {
 } mok_dims;
 
 /* Layer weights (device, caller-owned). `prepared` is the output of mok_prepare_weights and is
- * required when dtype == MOK_MXFP8 (ignored for MOK_BF16). */
+ * required when dtype == MOK_MXFP8 (ignored for MOK_BF16); `prepared_bwd`, the output of
+ * mok_prepare_weights_bwd, is required by mok_moe_backward when dtype == MOK_MXFP8. */
 typedef struct {
   const void *W_router;     /* [d,E] bf16 */
   const float *router_bias; /* [E] fp32, or NULL */
@@ -83,6 +84,7 @@ typedef struct {
   const void *Ws_up;        /* [d,Fs] bf16 */
   const void *Ws_down;      /* [Fs,d] bf16 */
   const void *prepared;     /* mok_prepared_size() bytes, or NULL */
+  const void *prepared_bwd; /* mok_prepared_bwd_size() bytes, or NULL */
 } mok_weights;
 
 /* Bytes of device workspace needed by the entry points of `pass` (MOK_PASS_FORWARD covers
@@ -91,7 +93,7 @@ typedef struct {
 size_t mok_workspace_size(const mok_dims *dims, int pass);
 
 /* Bytes of the activations mok_moe_forward saves for mok_moe_backward (G and U, bf16, for the
- * routed rows and the shared expert). */
+ * routed rows and the shared expert; with MOK_BF16 also x in expert order). */
 size_t mok_saved_size(const mok_dims *dims);
 
 /* Bytes of the prepared-weights buffer for dims->dtype (0 for MOK_BF16). */
@@ -105,9 +107,21 @@ size_t mok_prepared_size(const mok_dims *dims);
  * bytes per row) are stored in 512-byte atoms [N/128][K/128]: the atom of row tile a and K block
  * b holds row n = 128a + 32 r1 + r0 (r0 < 32, r1 < 4), block 4b + j at byte 16 r0 + 4 r1 + j,
  * the shared-memory image the block-scaled MMA's scale copy reads.  No-op for MOK_BF16.
- * MXFP8 needs d % 256 == 0 and is forward only (mok_moe_backward returns MOK_ERR_UNSUPPORTED). */
+ * MXFP8 needs d % 256 == 0. */
 int mok_prepare_weights(const mok_dims *dims, const mok_weights *w, void *prepared,
                         mok_stream_t stream);
+
+/* MXFP8 backward: the expert weights quantised once more, along the reduction dimension of the
+ * backward GEMM that reads each (same rule and atom layout as mok_prepare_weights), in this order
+ * (each region 1 KB aligned): W_down codes [E][F][d] (blocks along d, for dY W_down^T) and
+ * scales; W_gate codes [E][d][F] (blocks along F, for dG W_gate^T) and scales; W_up likewise;
+ * then the shared expert's Ws_down [Fs][d], Ws_gate [d][Fs], Ws_up [d][Fs] the same way.  No
+ * transposes: each weight's rows are already along that K.  mok_prepared_bwd_size() bytes
+ * (0 for MOK_BF16, where this call is a no-op).  The MXFP8 backward needs F % 256 == 0 and
+ * Fs % 256 == 0 besides d % 256 == 0. */
+size_t mok_prepared_bwd_size(const mok_dims *dims);
+int mok_prepare_weights_bwd(const mok_dims *dims, const mok_weights *w, void *prepared_bwd,
+                            mok_stream_t stream);
 
 /* MXFP8 quantiser of activations: src[rows,K] bf16 -> q[rows,K] E4M3 codes and
  * scales[rows,K/32] UE8M0 bytes, one block per 32 consecutive elements of a row: scale 2^s with
@@ -149,7 +163,8 @@ int mok_dispatch_index(const mok_dims *dims, const int32_t *topk_idx, const floa
  * ascending expert order on top of the shared-expert row (fp32 accumulation, one bf16
  * rounding).
  *   -> y[T,d] bf16.  `saved` (mok_saved_size bytes or NULL) receives what the backward needs:
- *   G and U, and x in expert order. */
+ *   G and U (for MOK_MXFP8 the block-scaled products, in bf16), and for MOK_BF16 x in expert
+ *   order. */
 int mok_moe_forward(const mok_dims *dims, const mok_weights *w, const void *x,
                     const int32_t *topk_idx, const int32_t *offsets, const int32_t *sorted_tok,
                     const float *sorted_w, const int32_t *inv_pos, void *y, void *saved,
@@ -161,7 +176,13 @@ int mok_moe_forward(const mok_dims *dims, const mok_weights *w, const void *x,
  *   dX[T,d] (including the router path dlogits W_router^T), dW_gate/dW_up[E,d,F],
  *   dW_down[E,F,d] (experts with no token get zeros), dWs_gate/dWs_up[d,Fs], dWs_down[Fs,d]
  *   (NULL when n_shared == 0), dlogits[T,E] fp32 (zero off the selection),
- *   dW_router[d,E] (NULL to skip). */
+ *   dW_router[d,E] (NULL to skip).
+ * MOK_MXFP8 (the MXFP8 reading of the training step): every expert GEMM multiplies E4M3
+ * operands with UE8M0 scales per 32 along its own reduction dimension — dY and W_down along d,
+ * dG, dU, W_gate, W_up along F, and for the weight gradients x, dG, dU, w*h and dY along each
+ * expert's tokens (blocks of 32 from its first token, in token order) — with fp32 accumulation;
+ * the router terms dlogits W_router^T and x^T dlogits stay bf16.  Needs w->prepared_bwd and a
+ * `saved` from an MXFP8 forward; F % 256 == 0 and Fs % 256 == 0 (else MOK_ERR_UNSUPPORTED). */
 int mok_moe_backward(const mok_dims *dims, const mok_weights *w, const void *x, const void *dY,
                      const void *saved, const int32_t *topk_idx, const float *topk_w,
                      const int32_t *offsets, const int32_t *sorted_tok, const float *sorted_w,

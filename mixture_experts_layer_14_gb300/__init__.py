@@ -31,7 +31,8 @@ EXPORTED_SYMBOLS = [
     "mok_layer_host_extra_size", "mok_layer_forward_host", "mok_status_string",
     "mok_read_device_status", "mok_clear_device_status", "mok_last_launch_count",
     "mok_timing_enable", "mok_timing_collect", "mok_dispatch_index_noalloc",
-    "mok_mx_quantize_rows", "mok_selftest_bounded_wait",
+    "mok_mx_quantize_rows", "mok_selftest_bounded_wait", "mok_prepared_bwd_size",
+    "mok_prepare_weights_bwd",
 ]
 
 
@@ -48,7 +49,7 @@ class Dims(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "W_router", "router_bias", "W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down",
-        "prepared")]
+        "prepared", "prepared_bwd")]
 
 
 _LIB = None
@@ -74,6 +75,8 @@ def lib():
             "mok_workspace_size": (_SZ, [_DP, ctypes.c_int]),
             "mok_saved_size": (_SZ, [_DP]),
             "mok_prepared_size": (_SZ, [_DP]),
+            "mok_prepared_bwd_size": (_SZ, [_DP]),
+            "mok_prepare_weights_bwd": (ctypes.c_int, [_DP, _WP, _VP, _VP]),
             "mok_layer_host_extra_size": (_SZ, [_DP]),
             "mok_prepare_weights": (ctypes.c_int, [_DP, _WP, _VP, _VP]),
             "mok_route": (ctypes.c_int, [_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
@@ -201,7 +204,8 @@ def _weights_struct(D, W):
         W["Ws_gate"].data_ptr() if D.n_shared else None,
         W["Ws_up"].data_ptr() if D.n_shared else None,
         W["Ws_down"].data_ptr() if D.n_shared else None,
-        W["prepared"].data_ptr() if W.get("prepared") is not None else None)
+        W["prepared"].data_ptr() if W.get("prepared") is not None else None,
+        W["prepared_bwd"].data_ptr() if W.get("prepared_bwd") is not None else None)
 
 
 def route(D, x, W_router, bias, ws, want_logits=False):
@@ -275,8 +279,24 @@ def prepare_weights(D, W):
     buf = torch.empty(n, dtype=torch.uint8, device=W["W_gate"].device)
     Wd = dict(W)
     Wd["prepared"] = None
+    Wd["prepared_bwd"] = None
     st = _weights_struct(D, Wd)
     _check(lib().mok_prepare_weights(ctypes.byref(D), ctypes.byref(st), _ptr(buf), _stream()))
+    return buf
+
+
+def prepare_weights_bwd(D, W):
+    """MXFP8: the expert weights quantised along the backward GEMMs' reduction dimensions (uint8
+    CUDA tensor); returns None for bf16.  Pass it as W["prepared_bwd"] for the MXFP8 backward."""
+    n = lib().mok_prepared_bwd_size(ctypes.byref(D))
+    if n == 0:
+        return None
+    buf = torch.empty(n, dtype=torch.uint8, device=W["W_gate"].device)
+    Wd = dict(W)
+    Wd["prepared"] = None
+    Wd["prepared_bwd"] = None
+    st = _weights_struct(D, Wd)
+    _check(lib().mok_prepare_weights_bwd(ctypes.byref(D), ctypes.byref(st), _ptr(buf), _stream()))
     return buf
 
 

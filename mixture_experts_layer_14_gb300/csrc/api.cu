@@ -87,7 +87,7 @@ static int check_dims(const mok_dims* d) {
 }
 
 struct Layout {
-  size_t off[32];
+  size_t off[48];
   size_t total;
 };
 static size_t al(size_t x) { return (x + 1023) & ~size_t(1023); }
@@ -102,10 +102,25 @@ enum FwdSlot {
 enum PrepSlot {  // MXFP8 prepared weights: K-major codes [n][N][K] and scale atoms
   PR_GQ, PR_GS, PR_UQ, PR_US, PR_DQ, PR_DS, PR_SGQ, PR_SGS, PR_SUQ, PR_SUS, PR_SDQ, PR_SDS, PR_N
 };
+enum PrepBwdSlot {  // MXFP8 backward weights: codes quantised along the backward GEMMs' K
+  PB_DQ, PB_DS,    // W_down [E][F][d] along d (dY W_down^T)
+  PB_GQ, PB_GS,    // W_gate [E][d][F] along F (dG W_gate^T)
+  PB_UQ, PB_US,    // W_up
+  PB_SDQ, PB_SDS, PB_SGQ, PB_SGS, PB_SUQ, PB_SUS,  // the shared expert's, likewise
+  PB_N
+};
 enum BwdSlot {
   BW_STATUS, BW_DYS, BW_DG, BW_DU, BW_HW, BW_DGSH, BW_DUSH, BW_HWSH, BW_P, BW_DL,
   BW_DXS, BW_DXSH,
   BW_TMAP,  // weight-gradient GEMM: expert-bounded tensor-map copies
+  // MXFP8 only.  dY codes and atoms (token order, then expert order); dG, dU codes and atoms
+  // (routed, shared); the router term dl W_r^T of dX; the transposed token-axis operands of the
+  // weight gradients (routed [.][128 NKB1], shared [.][128 NKB0]) with their atoms.
+  BW_DYQ, BW_DYSC, BW_DYQS, BW_DYSCS,
+  BW_DGQ, BW_DGSC, BW_DUQ, BW_DUSC, BW_DGQSH, BW_DGSCSH, BW_DUQSH, BW_DUSCSH,
+  BW_DXR,
+  BW_XT, BW_XTS, BW_DYT, BW_DYTS, BW_DGT, BW_DGTS, BW_DUT, BW_DUTS, BW_HWT, BW_HWTS,
+  BW_XT0, BW_XTS0, BW_DYT0, BW_DYTS0, BW_DGT0, BW_DGTS0, BW_DUT0, BW_DUTS0, BW_HWT0, BW_HWTS0,
   BW_N
 };
 enum SavedSlot { SV_G, SV_U, SV_GSH, SV_USH, SV_XS, SV_N };
@@ -149,6 +164,11 @@ static Layout layout_fwd(const mok_dims* d) {
   return L;
 }
 
+// MXFP8 weight gradients: K blocks of 128 tokens in the transposed operands (row stride / 128).
+// Routed: every expert's tokens padded to whole blocks, at most ceil(R / 128) + E blocks.
+static int64_t mx_nkb_routed(const mok_dims* d) { return (d->T * d->k + 127) / 128 + d->E; }
+static int64_t mx_nkb_shared(const mok_dims* d) { return (d->T + 127) / 128; }
+
 static int bwd_bn_da(const mok_dims* d) { return bn_for(d->F, d->n_shared ? d->F_shared : 256, 256); }
 
 static Layout layout_bwd(const mok_dims* d) {
@@ -166,6 +186,28 @@ static Layout layout_bwd(const mok_dims* d) {
   sz[BW_DXS] = 2ull * R * d->d;
   sz[BW_DXSH] = 2ull * T * d->d;
   sz[BW_TMAP] = sizeof(CUtensorMap) * (size_t)kBoundMaps * d->E;
+  if (d->dtype == MOK_MXFP8) {
+    const int64_t mt_x = (T + BM - 1) / BM, mt_r = (R + BM - 1) / BM + d->E;
+    const int64_t k1 = 128 * mx_nkb_routed(d), k0 = 128 * mx_nkb_shared(d);
+    sz[BW_DYS] = 0;
+    sz[BW_TMAP] = 0;
+    sz[BW_P] = 4ull * R * (d->F / 128);
+    sz[BW_DYQ] = 1ull * T * d->d;
+    sz[BW_DYSC] = 4ull * BM * mt_x * (d->d / 128);
+    sz[BW_DYQS] = 1ull * R * d->d;
+    sz[BW_DYSCS] = 4ull * BM * mt_r * (d->d / 128);
+    sz[BW_DGQ] = sz[BW_DUQ] = 1ull * R * d->F;
+    sz[BW_DGSC] = sz[BW_DUSC] = 4ull * BM * mt_r * (d->F / 128);
+    sz[BW_DGQSH] = sz[BW_DUQSH] = 1ull * T * Fs;
+    sz[BW_DGSCSH] = sz[BW_DUSCSH] = 4ull * BM * mt_x * (Fs / 128);
+    sz[BW_DXR] = 2ull * T * d->d;
+    sz[BW_XT] = sz[BW_DYT] = 1ull * d->d * k1;
+    sz[BW_DGT] = sz[BW_DUT] = sz[BW_HWT] = 1ull * d->F * k1;
+    sz[BW_XT0] = sz[BW_DYT0] = 1ull * d->d * k0 * d->n_shared;
+    sz[BW_DGT0] = sz[BW_DUT0] = sz[BW_HWT0] = 1ull * Fs * k0;
+    for (int i : {BW_XT, BW_DYT, BW_DGT, BW_DUT, BW_HWT, BW_XT0, BW_DYT0, BW_DGT0, BW_DUT0, BW_HWT0})
+      sz[i + 1] = sz[i] / 32;  // scale atoms: one byte per 32 codes
+  }
   Layout L{};
   size_t o = 0;
   for (int i = 0; i < BW_N; ++i) { L.off[i] = o; o += al(sz[i]); }
@@ -184,11 +226,23 @@ static Layout layout_prepared(const mok_dims* d) {
   return L;
 }
 
+static Layout layout_prepared_bwd(const mok_dims* d) {
+  const uint64_t E = d->E, dd = d->d, F = d->F, Fs = d->n_shared ? d->F_shared : 0;
+  size_t sz[PB_N] = {E * F * dd, E * F * dd / 32, E * dd * F, E * dd * F / 32, E * dd * F, E * dd * F / 32,
+                     Fs * dd, Fs * dd / 32, dd * Fs, dd * Fs / 32, dd * Fs, dd * Fs / 32};
+  Layout L{};
+  size_t o = 0;
+  for (int i = 0; i < PB_N; ++i) { L.off[i] = o; o += al(sz[i]); }
+  L.total = o;
+  return L;
+}
+
 static Layout layout_saved(const mok_dims* d) {
   const int64_t T = d->T, R = T * d->k;
   const int Fs = d->n_shared ? d->F_shared : 0;
+  // G, U, their shared-expert copies, x in expert order (bf16 weight gradients only)
   size_t sz[SV_N] = {2ull * R * d->F, 2ull * R * d->F, 2ull * T * Fs, 2ull * T * Fs,
-                     2ull * R * d->d};  // G, U, their shared-expert copies, x in expert order
+                     d->dtype == MOK_MXFP8 ? 0 : 2ull * R * d->d};
   Layout L{};
   size_t o = 0;
   for (int i = 0; i < SV_N; ++i) { L.off[i] = o; o += al(sz[i]); }
@@ -214,6 +268,248 @@ static P at(void* base, size_t off) {
 }
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA; }
+
+// MXFP8 backward (the MXFP8 reading of the layer's training step): every expert GEMM takes E4M3
+// operands with UE8M0 scales along its own reduction dimension (dY and W_down along d; dG, dU,
+// W_gate, W_up along F; the weight gradients' operands along each expert's tokens); the router
+// terms dl W_router^T and x^T dl stay on the bf16 path.
+static int backward_mxfp8(const mok_dims* dims, const mok_weights* w, const void* x, const void* dY,
+                          const void* saved, const int32_t* topk_idx, const float* topk_w,
+                          const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
+                          const int32_t* inv_pos, void* dX, void* dW_gate, void* dW_up,
+                          void* dW_down, void* dWs_gate, void* dWs_up, void* dWs_down,
+                          float* dlogits, void* dW_router, void* ws, cudaStream_t s,
+                          int* launches) {
+  if (!w->prepared_bwd || !aligned16(w->prepared_bwd)) return MOK_ERR_INVALID_ARG;
+  const bool sh = dims->n_shared == 1;
+  const int64_t T = dims->T, R = T * dims->k;
+  const int d = dims->d, E = dims->E, F = dims->F, Fs = sh ? dims->F_shared : 0, k = dims->k;
+  const Layout L = layout_bwd(dims);
+  const Layout S = layout_saved(dims);
+  const Layout P = layout_prepared_bwd(dims);
+  auto pw = [&](int i) { return static_cast<const char*>(w->prepared_bwd) + P.off[i]; };
+  auto pu8 = [&](int i) { return reinterpret_cast<const uint8_t*>(pw(i)); };
+  auto W = [&](int i) { return at<void*>(ws, L.off[i]); };
+  auto W8 = [&](int i) { return at<uint8_t*>(ws, L.off[i]); };
+  auto SV = [&](int i) { return at<void*>(const_cast<void*>(saved), S.off[i]); };
+  const int grid_cap = num_sms();
+  const int64_t mt_x = (T + BM - 1) / BM, mt_rb = (R + BM - 1) / BM + E;  // M-tile bounds
+  const int nkb1 = (int)mx_nkb_routed(dims), nkb0 = (int)mx_nkb_shared(dims);
+  const int ldl = (E + 63) & ~63;
+  float* part = at<float*>(ws, L.off[BW_P]);
+  int rc;
+  // 1. dY quantised along d; its codes and scale atoms pulled into expert order
+  rc = cuda_status(launch_mx_quantize_rows(dY, T, d, W(BW_DYQ), W(BW_DYSC), true, s));
+  if (rc == MOK_OK)
+    rc = cuda_status(launch_gather_rows("gather_bytes", W(BW_DYQ), nullptr, inv_pos, T, k, d,
+                                        W(BW_DYQS), nullptr, s));
+  if (rc == MOK_OK)
+    rc = cuda_status(launch_gather_scale_atoms(W(BW_DYSC), sorted_tok, offsets, E, T, R, d,
+                                               W(BW_DYSCS), s));
+  if (rc != MOK_OK) return rc;
+  *launches += 3;
+  // 2. a = dY W_down^T; epilogue: dG, dU, w*h (bf16), dG and dU quantised along F, <a, h>
+  {
+    GemmParams p{};
+    bool ok = true;
+    if (sh) {
+      ok &= map2d(&p.maps[MS_A0], W(BW_DYQ), T, d, 128, 128, 1);
+      ok &= map3d(&p.maps[MS_B0], pw(PB_SDQ), 1, Fs, d, 128, 128, 1);
+    }
+    ok &= map2d(&p.maps[MS_A3], W(BW_DYQS), R, d, 128, 128, 1);
+    ok &= map3d(&p.maps[MS_B3], pw(PB_DQ), E, F, d, 128, 128, 1);
+    if (!ok) return MOK_ERR_CUDA;
+    p.offsets = offsets;
+    p.E = E;
+    p.has_shared = sh;
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.nt[0] = Fs / 128;  // 128-column N tiles: two accumulators, the epilogue overlaps the MMAs
+    p.nt[1] = F / 128;
+    p.in0[0] = SV(SV_GSH); p.in1[0] = SV(SV_USH);
+    p.in0[1] = SV(SV_G); p.in1[1] = SV(SV_U);
+    p.out0[0] = W(BW_DGSH); p.out1[0] = W(BW_DUSH); p.out2[0] = W(BW_HWSH);
+    p.out0[1] = W(BW_DG); p.out1[1] = W(BW_DU); p.out2[1] = W(BW_HW);
+    p.qout[0][0] = W(BW_DGQSH); p.qout[0][1] = W(BW_DUQSH);
+    p.qsc[0][0] = W8(BW_DGSCSH); p.qsc[0][1] = W8(BW_DUSCSH);
+    p.qout[1][0] = W(BW_DGQ); p.qout[1][1] = W(BW_DUQ);
+    p.qsc[1][0] = W8(BW_DGSC); p.qsc[1][1] = W8(BW_DUSC);
+    p.sfa[0][0] = W8(BW_DYSC);
+    p.sfa[1][0] = W8(BW_DYSCS);
+    p.sfb[0][0] = pu8(PB_SDS);
+    p.sfb[1][0] = pu8(PB_DS);
+    p.sf_kb[0] = p.sf_kb[1] = d / 128;
+    p.row_w = sorted_w;
+    p.partial = part;
+    p.status = static_cast<int*>(ws);
+    const int64_t bound = (sh ? mt_x * p.nt[0] : 0) + mt_rb * p.nt[1];
+    rc = cuda_status(launch_gemm(G_BWD_DA_MX, 128, p, (int)std::min<int64_t>(grid_cap, bound), s));
+    if (rc != MOK_OK) return rc;
+    ++*launches;
+  }
+  // 3. router backward: dw (128-column partials of <a, h>), dlogits, bf16 dl
+  rc = cuda_status(launch_router_backward(T, E, k, F / 128, topk_idx, topk_w, inv_pos, part,
+                                          dlogits, W(BW_DL), s));
+  if (rc != MOK_OK) return rc;
+  ++*launches;
+  // 4. dX_s = dG W_gate^T + dU W_up^T
+  {
+    GemmParams p{};
+    bool ok = true;
+    if (sh) {
+      ok &= map2d(&p.maps[MS_A0], W(BW_DGQSH), T, Fs, 128, 128, 1);
+      ok &= map2d(&p.maps[MS_A1], W(BW_DUQSH), T, Fs, 128, 128, 1);
+      ok &= map3d(&p.maps[MS_B0], pw(PB_SGQ), 1, d, Fs, 128, 256, 1);
+      ok &= map3d(&p.maps[MS_B1], pw(PB_SUQ), 1, d, Fs, 128, 256, 1);
+    }
+    ok &= map2d(&p.maps[MS_A3], W(BW_DGQ), R, F, 128, 128, 1);
+    ok &= map2d(&p.maps[MS_A4], W(BW_DUQ), R, F, 128, 128, 1);
+    ok &= map3d(&p.maps[MS_B3], pw(PB_GQ), E, d, F, 128, 256, 1);
+    ok &= map3d(&p.maps[MS_B4], pw(PB_UQ), E, d, F, 128, 256, 1);
+    if (!ok) return MOK_ERR_CUDA;
+    p.offsets = offsets;
+    p.E = E;
+    p.has_shared = sh;
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.nt[0] = p.nt[1] = d / 256;
+    p.sfa[0][0] = W8(BW_DGSCSH); p.sfa[0][1] = W8(BW_DUSCSH);
+    p.sfa[1][0] = W8(BW_DGSC); p.sfa[1][1] = W8(BW_DUSC);
+    p.sfb[0][0] = pu8(PB_SGS); p.sfb[0][1] = pu8(PB_SUS);
+    p.sfb[1][0] = pu8(PB_GS); p.sfb[1][1] = pu8(PB_US);
+    p.sf_kb[0] = Fs / 128;
+    p.sf_kb[1] = F / 128;
+    p.out0[0] = W(BW_DXSH);
+    p.out0[1] = W(BW_DXS);
+    p.status = static_cast<int*>(ws);
+    const int64_t bound = (sh ? mt_x * p.nt[0] : 0) + mt_rb * p.nt[1];
+    rc = cuda_status(launch_gemm(G_BWD_DX_MX, 256, p, (int)std::min<int64_t>(grid_cap, bound), s));
+    if (rc != MOK_OK) return rc;
+    ++*launches;
+  }
+  // 5. the router term of dX, dl W_router^T (bf16 GEMM, one K segment)
+  {
+    GemmParams p{};
+    bool ok = map2d(&p.maps[MS_A0], W(BW_DL), T, ldl, 64, 128);
+    ok &= map3d(&p.maps[MS_B0], w->W_router, 1, d, E, 64, 256);
+    if (!ok) return MOK_ERR_CUDA;
+    p.segkb[0][0] = ldl / BK;
+    p.has_shared = 1;
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.nt[0] = d / 256;
+    p.out0[0] = W(BW_DXR);
+    p.status = static_cast<int*>(ws);
+    rc = cuda_status(launch_gemm(G_BWD_DX, 256, p, (int)std::min<int64_t>(grid_cap, mt_x * p.nt[0]), s));
+    if (rc != MOK_OK) return rc;
+    ++*launches;
+  }
+  // 6. weight-gradient operands quantised along tokens, transposed: routed (x and dY pulled by
+  // sorted_tok; dG, dU, w*h in expert order), then the shared expert's (all tokens in order)
+  {
+    using bf = const __nv_bfloat16*;
+    auto tq = [&](bf a, bf b, bf c, int slot_a, int slot_b, int slot_c, int n, int C, int64_t nsrc,
+                  const int32_t* rows, const int32_t* offs, int nkb) {
+      TokQuantParams tp{};
+      const bf srcs[3] = {a, b, c};
+      const int slots[3] = {slot_a, slot_b, slot_c};
+      for (int i = 0; i < n; ++i) {
+        tp.src[i] = srcs[i];
+        tp.q[i] = W8(slots[i]);
+        tp.sc[i] = W8(slots[i] + 1);
+      }
+      tp.nops = n;
+      tp.C = C;
+      tp.nsrc = nsrc;
+      tp.rows_idx = rows;
+      tp.offsets = offs;
+      tp.E = E;
+      tp.nkb = nkb;
+      return cuda_status(launch_mx_quantize_tokens(tp, s));
+    };
+    const bf bx = static_cast<bf>(x), bdy = static_cast<bf>(dY);
+    rc = tq(bx, bdy, nullptr, BW_XT, BW_DYT, 0, 2, d, T, sorted_tok, offsets, nkb1);
+    if (rc == MOK_OK)
+      rc = tq(static_cast<bf>(W(BW_DG)), static_cast<bf>(W(BW_DU)), static_cast<bf>(W(BW_HW)),
+              BW_DGT, BW_DUT, BW_HWT, 3, F, R, nullptr, offsets, nkb1);
+    if (rc == MOK_OK && sh) rc = tq(bx, bdy, nullptr, BW_XT0, BW_DYT0, 0, 2, d, T, nullptr, nullptr, nkb0);
+    if (rc == MOK_OK && sh)
+      rc = tq(static_cast<bf>(W(BW_DGSH)), static_cast<bf>(W(BW_DUSH)), static_cast<bf>(W(BW_HWSH)),
+              BW_DGT0, BW_DUT0, BW_HWT0, 3, Fs, T, nullptr, nullptr, nkb0);
+    if (rc != MOK_OK) return rc;
+    *launches += sh ? 4 : 2;
+  }
+  // 7. weight gradients: dW_gate = X^T dG, dW_up = X^T dU, dW_down = (w h)^T dY, K = tokens
+  {
+    GemmParams p{};
+    bool ok = true;
+    const uint64_t k0 = 128ull * nkb0, k1 = 128ull * nkb1;
+    if (sh) {
+      ok &= map2d(&p.maps[MS_A0], W(BW_XT0), d, k0, 128, 128, 1);
+      ok &= map2d(&p.maps[MS_A1], W(BW_HWT0), Fs, k0, 128, 128, 1);
+      ok &= map2d(&p.maps[MS_B0], W(BW_DGT0), Fs, k0, 128, 256, 1);
+      ok &= map2d(&p.maps[MS_B1], W(BW_DUT0), Fs, k0, 128, 256, 1);
+      ok &= map2d(&p.maps[MS_B2], W(BW_DYT0), d, k0, 128, 256, 1);
+      p.sfa[0][0] = W8(BW_XTS0); p.sfa[0][1] = W8(BW_HWTS0);
+      p.sfb[0][0] = W8(BW_DGTS0); p.sfb[0][1] = W8(BW_DUTS0); p.sfb[0][2] = W8(BW_DYTS0);
+    }
+    ok &= map2d(&p.maps[MS_A3], W(BW_XT), d, k1, 128, 128, 1);
+    ok &= map2d(&p.maps[MS_A4], W(BW_HWT), F, k1, 128, 128, 1);
+    ok &= map2d(&p.maps[MS_B3], W(BW_DGT), F, k1, 128, 256, 1);
+    ok &= map2d(&p.maps[MS_B4], W(BW_DUT), F, k1, 128, 256, 1);
+    ok &= map2d(&p.maps[MS_B5], W(BW_DYT), d, k1, 128, 256, 1);
+    if (!ok) return MOK_ERR_CUDA;
+    p.sfa[1][0] = W8(BW_XTS); p.sfa[1][1] = W8(BW_HWTS);
+    p.sfb[1][0] = W8(BW_DGTS); p.sfb[1][1] = W8(BW_DUTS); p.sfb[1][2] = W8(BW_DYTS);
+    p.sf_kb[0] = nkb0;
+    p.sf_kb[1] = nkb1;
+    p.offsets = offsets;
+    p.E = E;
+    p.has_shared = sh;
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.out0[0] = dWs_gate; p.out1[0] = dWs_up; p.out2[0] = dWs_down;
+    p.out0[1] = dW_gate; p.out1[1] = dW_up; p.out2[1] = dW_down;
+    p.status = static_cast<int*>(ws);
+    const int64_t total = (sh ? 2 * (d / BM) * (Fs / 256) + (Fs / BM) * (d / 256) : 0) +
+                          (int64_t)E * (2 * (d / BM) * (F / 256) + (F / BM) * (d / 256));
+    rc = cuda_status(launch_gemm(G_BWD_DW_MX, 256, p, (int)std::min<int64_t>(grid_cap, total), s));
+    if (rc != MOK_OK) return rc;
+    ++*launches;
+  }
+  // 8. the router's weight gradient x^T dl (bf16 GEMM)
+  if (dW_router) {
+    GemmParams p{};
+    bool ok = map2d(&p.maps[MS_R_A], x, T, d, 64, 64);
+    ok &= map2d(&p.maps[MS_R_B], W(BW_DL), T, ldl, 64, 64);
+    if (!ok) return MOK_ERR_CUDA;
+    p.router_tiles = (d / BM) * ((E + 255) / 256);
+    p.E_cols = E;
+    p.out_router = dW_router;
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.status = static_cast<int*>(ws);
+    rc = cuda_status(launch_gemm(G_BWD_DW, 256, p, std::min(grid_cap, p.router_tiles), s));
+    if (rc != MOK_OK) return rc;
+    ++*launches;
+  }
+  // 9. dX = dX_shared + dl W_router^T + routed rows in ascending expert order
+  rc = cuda_status(launch_combine(T, d, k, topk_idx, inv_pos, W(BW_DXS), sh ? W(BW_DXSH) : nullptr,
+                                  dX, s, W(BW_DXR)));
+  if (rc != MOK_OK) return rc;
+  ++*launches;
+  return MOK_OK;
+}
 
 }  // namespace mok
 
@@ -265,6 +561,40 @@ int mok_prepare_weights(const mok_dims* dims, const mok_weights* w, void* prepar
     if (e == cudaSuccess) e = launch_mx_quantize_transpose(w->Ws_gate, 1, d, Fs, q(PR_SGQ), q(PR_SGS), s);
     if (e == cudaSuccess) e = launch_mx_quantize_transpose(w->Ws_up, 1, d, Fs, q(PR_SUQ), q(PR_SUS), s);
     if (e == cudaSuccess) e = launch_mx_quantize_transpose(w->Ws_down, 1, Fs, d, q(PR_SDQ), q(PR_SDS), s);
+  }
+  if (e != cudaSuccess) return MOK_ERR_CUDA;
+  g_last_launches = dims->n_shared ? 6 : 3;
+  return MOK_OK;
+}
+
+size_t mok_prepared_bwd_size(const mok_dims* dims) {
+  if (check_dims(dims) != MOK_OK) return 0;
+  return dims->dtype == MOK_MXFP8 ? layout_prepared_bwd(dims).total : 0;
+}
+
+int mok_prepare_weights_bwd(const mok_dims* dims, const mok_weights* w, void* prepared_bwd,
+                            mok_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != MOK_OK) return rc;
+  if (!w) return MOK_ERR_INVALID_ARG;
+  g_last_launches = 0;
+  if (dims->dtype != MOK_MXFP8) return MOK_OK;
+  if (!prepared_bwd || !w->W_gate || !w->W_up || !w->W_down) return MOK_ERR_INVALID_ARG;
+  if (dims->n_shared && (!w->Ws_gate || !w->Ws_up || !w->Ws_down)) return MOK_ERR_INVALID_ARG;
+  if (!aligned16(prepared_bwd)) return MOK_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Layout P = layout_prepared_bwd(dims);
+  const int64_t d = dims->d, F = dims->F, Fs = dims->F_shared, E = dims->E;
+  auto q = [&](int i) { return static_cast<char*>(prepared_bwd) + P.off[i]; };
+  // each weight's rows are already K-major for the backward GEMM that reads it:
+  // W_down [E][F][d] rows along d; W_gate, W_up [E][d][F] rows along F
+  cudaError_t e = launch_mx_quantize_rows(w->W_down, E * F, (int)d, q(PB_DQ), q(PB_DS), true, s);
+  if (e == cudaSuccess) e = launch_mx_quantize_rows(w->W_gate, E * d, (int)F, q(PB_GQ), q(PB_GS), true, s);
+  if (e == cudaSuccess) e = launch_mx_quantize_rows(w->W_up, E * d, (int)F, q(PB_UQ), q(PB_US), true, s);
+  if (dims->n_shared) {
+    if (e == cudaSuccess) e = launch_mx_quantize_rows(w->Ws_down, Fs, (int)d, q(PB_SDQ), q(PB_SDS), true, s);
+    if (e == cudaSuccess) e = launch_mx_quantize_rows(w->Ws_gate, d, (int)Fs, q(PB_SGQ), q(PB_SGS), true, s);
+    if (e == cudaSuccess) e = launch_mx_quantize_rows(w->Ws_up, d, (int)Fs, q(PB_SUQ), q(PB_SUS), true, s);
   }
   if (e != cudaSuccess) return MOK_ERR_CUDA;
   g_last_launches = dims->n_shared ? 6 : 3;
@@ -400,7 +730,6 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
     // pulled into expert order, block-scaled gate/up GEMM whose epilogue quantises h along F,
     // block-scaled down GEMM with the router weight, and the same bf16 combine.
     if (!w->prepared || !aligned16(w->prepared)) return MOK_ERR_INVALID_ARG;
-    if (saved) return MOK_ERR_UNSUPPORTED;  // the MXFP8 path is forward only
     const Layout P = layout_prepared(dims);
     auto pw = [&](int i) { return static_cast<const char*>(w->prepared) + P.off[i]; };
     void* xq = at<void*>(ws, L.off[FW_XQ]);
@@ -444,8 +773,14 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
       p.out1[0] = hscsh;
       p.out0[1] = hq;
       p.out1[1] = hsc;
-      p.sfa[0] = xsc;
-      p.sfa[1] = xscs;
+      if (saved) {  // training: G and U in bf16 for the backward
+        p.out2[0] = at<void*>(saved, S.off[SV_GSH]);
+        p.out3[0] = at<void*>(saved, S.off[SV_USH]);
+        p.out2[1] = at<void*>(saved, S.off[SV_G]);
+        p.out3[1] = at<void*>(saved, S.off[SV_U]);
+      }
+      p.sfa[0][0] = xsc;
+      p.sfa[1][0] = xscs;
       p.sfb[0][0] = reinterpret_cast<const uint8_t*>(pw(PR_SGS));
       p.sfb[0][1] = reinterpret_cast<const uint8_t*>(pw(PR_SUS));
       p.sfb[1][0] = reinterpret_cast<const uint8_t*>(pw(PR_GS));
@@ -479,8 +814,8 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
       p.out0[0] = Ysh;
       p.out0[1] = Ys;
       p.row_w = sorted_w;
-      p.sfa[0] = hscsh;
-      p.sfa[1] = hsc;
+      p.sfa[0][0] = hscsh;
+      p.sfa[1][0] = hsc;
       p.sfb[0][0] = reinterpret_cast<const uint8_t*>(pw(PR_SDS));
       p.sfb[1][0] = reinterpret_cast<const uint8_t*>(pw(PR_DS));
       p.sf_kb[0] = Fs / 128;
@@ -597,7 +932,6 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
                       !sorted_w || !inv_pos || !dX || !dlogits))
     return MOK_ERR_INVALID_ARG;
   if (!w->W_router || !w->W_gate || !w->W_up || !w->W_down) return MOK_ERR_INVALID_ARG;
-  if (dims->dtype == MOK_MXFP8) return MOK_ERR_UNSUPPORTED;  // MXFP8 is forward only
   const bool sh = dims->n_shared == 1;
   if (sh && (!w->Ws_gate || !w->Ws_up || !w->Ws_down || !dWs_gate || !dWs_up || !dWs_down))
     return MOK_ERR_INVALID_ARG;
@@ -622,6 +956,14 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
     if (rc == MOK_OK && sh) rc = cuda_status(cudaMemsetAsync(dWs_up, 0, 2ull * d * Fs, s));
     if (rc == MOK_OK && sh) rc = cuda_status(cudaMemsetAsync(dWs_down, 0, 2ull * d * Fs, s));
     if (rc == MOK_OK && dW_router) rc = cuda_status(cudaMemsetAsync(dW_router, 0, 2ull * d * E, s));
+    return rc;
+  }
+  if (dims->dtype == MOK_MXFP8) {
+    if (F % 256 || (sh && Fs % 256)) return MOK_ERR_UNSUPPORTED;  // 256-column tiles along F
+    rc = backward_mxfp8(dims, w, x, dY, saved, topk_idx, topk_w, offsets, sorted_tok, sorted_w,
+                        inv_pos, dX, dW_gate, dW_up, dW_down, dWs_gate, dWs_up, dWs_down, dlogits,
+                        dW_router, ws, s, &launches);
+    if (rc == MOK_OK) g_last_launches = launches;
     return rc;
   }
   const Layout S = layout_saved(dims);

@@ -68,8 +68,9 @@ cudaError_t launch_gather_rows(const char* name, const void* src0, const void* s
   return cudaGetLastError();
 }
 
-// y[t] = Ysh[t] + sum over the token's routes in ascending expert id of Ys[inv_pos[t,j]]
-// (fp32 accumulation, one bf16 rounding).  The router weight is already inside Ys (it is
+// y[t] = Ysh[t] (+ Ysh2[t]) + sum over the token's routes in ascending expert id of
+// Ys[inv_pos[t,j]] (fp32 accumulation, one bf16 rounding; Ysh2 is the router term dl W_r^T of
+// the MXFP8 backward's dX).  The router weight is already inside Ys (it is
 // applied in the down-projection epilogue).  Page "Mixture-of-Kittens: Nhân kernel MoE ...",
 // section "Chồng lấp tính toán ...": the layer combines shared and routed expert outputs with
 // the router weights; the fixed order keeps the result bit-identical across runs.
@@ -79,7 +80,7 @@ template <int K>
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     int64_t T, int vec_per_row, const int32_t* __restrict__ topk_idx,
     const int32_t* __restrict__ inv_pos, const uint4* __restrict__ Ys, const uint4* __restrict__ Ysh,
-    uint4* __restrict__ y) {
+    const uint4* __restrict__ Ysh2, uint4* __restrict__ y) {
   const int lane = threadIdx.x & 31;
   const int64_t wglobal = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -124,6 +125,11 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
       float acc[8];
       acc[0] = bf16_lo(q[0].x); acc[1] = bf16_hi(q[0].x); acc[2] = bf16_lo(q[0].y); acc[3] = bf16_hi(q[0].y);
       acc[4] = bf16_lo(q[0].z); acc[5] = bf16_hi(q[0].z); acc[6] = bf16_lo(q[0].w); acc[7] = bf16_hi(q[0].w);
+      if (Ysh2) {
+        const uint4 u = Ysh2[t * vec_per_row + v];
+        acc[0] += bf16_lo(u.x); acc[1] += bf16_hi(u.x); acc[2] += bf16_lo(u.y); acc[3] += bf16_hi(u.y);
+        acc[4] += bf16_lo(u.z); acc[5] += bf16_hi(u.z); acc[6] += bf16_lo(u.w); acc[7] += bf16_hi(u.w);
+      }
 #pragma unroll
       for (int j = 0; j < K; ++j) {
         const uint4 u = q[j + 1];
@@ -140,22 +146,24 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
 }
 
 cudaError_t launch_combine(int64_t T, int d, int k, const int32_t* topk_idx, const int32_t* inv_pos,
-                           const void* Ys, const void* Ysh, void* y, cudaStream_t s) {
+                           const void* Ys, const void* Ysh, void* y, cudaStream_t s,
+                           const void* Ysh2) {
   if (T == 0) return cudaSuccess;
   const auto ys = static_cast<const uint4*>(Ys);
   const auto ysh = static_cast<const uint4*>(Ysh);
+  const auto ysh2 = static_cast<const uint4*>(Ysh2);
   auto yo = static_cast<uint4*>(y);
   const int grid = rows_grid(T * kCombineSplit);
   prof_begin("combine", s);
   switch (k) {
-    case 1: combine_kernel<1><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
-    case 2: combine_kernel<2><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
-    case 3: combine_kernel<3><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
-    case 4: combine_kernel<4><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
-    case 5: combine_kernel<5><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
-    case 6: combine_kernel<6><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
-    case 7: combine_kernel<7><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
-    default: combine_kernel<8><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, yo); break;
+    case 1: combine_kernel<1><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
+    case 2: combine_kernel<2><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
+    case 3: combine_kernel<3><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
+    case 4: combine_kernel<4><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
+    case 5: combine_kernel<5><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
+    case 6: combine_kernel<6><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
+    case 7: combine_kernel<7><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
+    default: combine_kernel<8><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
   }
   prof_end(s);
   return cudaGetLastError();

@@ -33,7 +33,8 @@ struct Tile {
 template <int MODE, int BN>
 struct Cfg {
   // every stage row is 128 bytes: 64 bf16 or 128 E4M3 elements of K
-  static constexpr bool MX = (MODE == G_FWD_GU_MX || MODE == G_FWD_DOWN_MX);
+  static constexpr bool MX = (MODE == G_FWD_GU_MX || MODE == G_FWD_DOWN_MX || MODE == G_BWD_DA_MX ||
+                              MODE == G_BWD_DX_MX || MODE == G_BWD_DW_MX);
   static constexpr int KE = MX ? 128 : BK;            // K elements per stage
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
@@ -42,20 +43,23 @@ struct Cfg {
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr bool A_MN = (MODE == G_BWD_DW);
   static constexpr bool B_MN = (MODE == G_FWD_GU || MODE == G_FWD_DOWN || MODE == G_BWD_DW);
-  static constexpr int NUM_ACC = MX ? 1 : 2;           // MXFP8: TMEM also holds scale factors
+  // MXFP8: TMEM also holds the scale factors (from column 256), so one 256-column accumulator
+  // or two of 128 columns
+  static constexpr int NUM_ACC = (MX && BN == 256) ? 1 : 2;
   // epilogue warps: two per TMEM lane quarter (each taking half the columns) where the single
   // accumulator leaves the epilogue exposed, one otherwise
-  static constexpr int EPI_WARPS = MX ? 8 : 4;
+  static constexpr int EPI_WARPS = NUM_ACC == 1 ? 8 : 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   // plain row-major outputs go through shared memory one 32-column chunk (32 rows x 64 B) per
   // epilogue warp at a time and are written with coalesced row stores
   static constexpr bool ROW_STAGED = (MODE == G_FWD_DOWN || MODE == G_BWD_DX ||
-                                      MODE == G_FWD_DOWN_MX || MODE == G_BWD_DW);
+                                      MODE == G_FWD_DOWN_MX || MODE == G_BWD_DW ||
+                                      MODE == G_BWD_DX_MX || MODE == G_BWD_DW_MX);
   static constexpr int STAGING_BYTES = ROW_STAGED ? EPI_WARPS * 2048 : 0;
   static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
   static constexpr int SF_TMEM_COL = 256;              // MXFP8: 16 columns per stage from here
   static constexpr uint32_t IDESC = MX ? make_idesc_mxf8(BN) : make_idesc_bf16(BN, A_MN, B_MN);
-  static constexpr bool K_GROUPED = (MODE == G_BWD_DW);
+  static constexpr bool K_GROUPED = (MODE == G_BWD_DW || MODE == G_BWD_DW_MX);
 };
 
 constexpr int kAuxBytes = 1024;                      // barriers, TMEM address, abort flag
@@ -128,6 +132,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
     else if constexpr (MODE == G_FWD_DOWN) nkb = (t.g ? p.F : p.Fs) / BK;
     else if constexpr (MODE == G_FWD_GU_MX) nkb = p.d / 128;
     else if constexpr (MODE == G_FWD_DOWN_MX) nkb = (t.g ? p.F : p.Fs) / 128;
+    else if constexpr (MODE == G_BWD_DA_MX) nkb = p.d / 128;
+    else if constexpr (MODE == G_BWD_DX_MX) nkb = 2 * (t.g ? p.F : p.Fs) / 128;  // dG, then dU
     else nkb = p.segkb[t.g][0] + p.segkb[t.g][1] + p.segkb[t.g][2];
     t.nkb = nkb;
   } else {
@@ -178,7 +184,14 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
         place(l - 2 * tg, p.d / BN);
       }
     }
-    t.nkb = (t.rows + BK - 1) / BK;
+    if constexpr (MODE == G_BWD_DW_MX) {
+      // transposed operands quantised along tokens: expert e's tokens are columns from
+      // 128 s_mt[e] on, zero-padded to whole 128-column K blocks
+      if (t.g == 1) t.row0 = 128 * s_mt[t.e];
+      t.nkb = (t.rows + 127) / 128;
+    } else {
+      t.nkb = (t.rows + BK - 1) / BK;
+    }
   }
   return t;
 }
@@ -198,12 +211,23 @@ __device__ __forceinline__ int total_tiles(const GemmParams& p, const int* s_mt)
 }
 
 // ------------------------------------------------------------------ producer
+// G_BWD_DW, G_BWD_DW_MX: map slots of a tile's operands (g = 2: the router's x and dl).
+__device__ __forceinline__ void dw_slots(const Tile& t, int& ia, int& ib) {
+  if (t.g == 2) { ia = MS_R_A; ib = MS_R_B; }
+  else if (t.sub == 0) { ia = t.g ? MS_A3 : MS_A0; ib = t.g ? MS_B3 : MS_B0; }
+  else if (t.sub == 1) { ia = t.g ? MS_A3 : MS_A0; ib = t.g ? MS_B4 : MS_B1; }
+  else { ia = t.g ? MS_A4 : MS_A1; ib = t.g ? MS_B5 : MS_B2; }
+}
+
 // Map slots per mode (g = group):
 //  G_FWD_GU   A: x / x_sorted (K-major)            B: gate, up weights (MN-major, 3D)
 //  G_FWD_DOWN A: h_sh / h (K-major)                B: down weights (MN-major, 3D)
 //  G_BWD_DA   A: dY / dY_sorted (K-major)          B: down weights (K-major view, 3D)
 //  G_BWD_DX   A: segments dG, dU (, dl)            B: gate, up (, router) weights (K-major view)
 //  G_BWD_DW   A: x / x_sorted, w*h (MN-major)      B: dG, dU, dY (MN-major); router x, dl
+//  MXFP8 (E4M3 codes, both K-major): gate/up A x, B gate, up; down A h, B down; da A dY, B down
+//  quantised along d; dx A dG, dU, B gate, up quantised along F; dw A x^T, (w h)^T, B dG^T,
+//  dU^T, dY^T (transposed, quantised along tokens)
 // PAIR: each CTA loads its A rows and its half of B (gate/up: the gate columns in the even CTA,
 // the up columns in the odd one; down: columns 128 rank .. 128 rank + 127 of the N tile), all
 // completing on the even CTA's barrier (`bar` is a cluster address).
@@ -246,6 +270,23 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, 
   } else if constexpr (MODE == G_FWD_DOWN_MX) {
     tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * 128, t.row0);
     tma_load_3d(sB, &M[t.g ? MS_B3 : MS_B0], bar, kb * 128, t.n * BN, t.e);
+  } else if constexpr (MODE == G_BWD_DA_MX) {
+    // E4M3 dY rows (K = d) and 256 rows of W_down quantised along d
+    tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * 128, t.row0);
+    tma_load_3d(sB, &M[t.g ? MS_B3 : MS_B0], bar, kb * 128, t.n * BN, t.e);
+  } else if constexpr (MODE == G_BWD_DX_MX) {
+    // k-blocks 0 .. F/128 - 1: dG with W_gate; then dU with W_up (both quantised along F)
+    const int nseg = (t.g ? p.F : p.Fs) / 128;
+    const int seg = kb >= nseg ? 1 : 0, kk = kb - seg * nseg;
+    tma_load_2d(sA, &M[(t.g ? MS_A3 : MS_A0) + seg], bar, kk * 128, t.row0);
+    tma_load_3d(sB, &M[(t.g ? MS_B3 : MS_B0) + seg], bar, kk * 128, t.n * BN, t.e);
+  } else if constexpr (MODE == G_BWD_DW_MX) {
+    // transposed operands [rows][K columns]: A rows m0.., B rows n BN.., K columns from row0
+    int ia, ib;
+    dw_slots(t, ia, ib);
+    const int kc = t.row0 + kb * 128;
+    tma_load_2d(sA, &M[ia], bar, kc, t.m0);
+    tma_load_2d(sB, &M[ib], bar, kc, t.n * BN);
   } else if constexpr (MODE == G_BWD_DA) {
     tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
     tma_load_3d(sB, &M[t.g ? MS_B3 : MS_B0], bar, kb * BK, t.n * BN, t.e);
@@ -257,14 +298,6 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, 
   } else {
     static_assert(MODE == -1, "every mode has its loads (G_BWD_DW: issue_loads_dw)");
   }
-}
-
-// G_BWD_DW: map slots of a tile's operands (g = 2: the router's x and dl).
-__device__ __forceinline__ void dw_slots(const Tile& t, int& ia, int& ib) {
-  if (t.g == 2) { ia = MS_R_A; ib = MS_R_B; }
-  else if (t.sub == 0) { ia = t.g ? MS_A3 : MS_A0; ib = t.g ? MS_B3 : MS_B0; }
-  else if (t.sub == 1) { ia = t.g ? MS_A3 : MS_A0; ib = t.g ? MS_B4 : MS_B1; }
-  else { ia = t.g ? MS_A4 : MS_A1; ib = t.g ? MS_B5 : MS_B2; }
 }
 
 // G_BWD_DW loads of one k-block: A = the tile's 128 M columns of the K-row-major operand (two
@@ -404,30 +437,31 @@ template <int MODE, int BN>
 constexpr int warp_cols() { return Cfg<MODE, BN>::EPI_WARPS == 8 ? BN / 2 : BN; }
 
 // G_FWD_DOWN, G_FWD_DOWN_MX (Y_s = router weight x accumulator; the shared expert's rows take
-// weight 1) and G_BWD_DX (dX_s = accumulator): row-major outputs with d columns, rows past the
-// expert's last token skipped.
+// weight 1), G_BWD_DX and G_BWD_DX_MX (dX_s = accumulator): row-major outputs with d columns,
+// rows past the expert's last token skipped.
 template <int MODE, int BN>
 __device__ __forceinline__ void epilogue_rows(const GemmParams& p, const Tile& t, uint32_t tacc,
                                               uint32_t stg, int q, int half, int lane,
                                               uint32_t release) {
   constexpr int cols = warp_cols<MODE, BN>();
   const int nrows = t.rows - q * 32;  // valid rows among this warp's 32 (may be <= 0)
+  constexpr bool WEIGHTED = (MODE == G_FWD_DOWN || MODE == G_FWD_DOWN_MX);
   float s = 1.0f;
-  if (MODE != G_BWD_DX && t.g == 1 && lane < nrows) s = p.row_w[t.row0 + q * 32 + lane];
+  if (WEIGHTED && t.g == 1 && lane < nrows) s = p.row_w[t.row0 + q * 32 + lane];
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out0[t.g]) + (int64_t)(t.row0 + q * 32) * p.d +
                      t.n * BN + cols * half;
   store_acc_rows<cols / 32, Cfg<MODE, BN>::NUM_ACC == 1>(o, p.d, nrows, cols, tacc + cols * half,
                                                          false, s, stg, lane, release);
 }
 
-// G_BWD_DW: weight gradients [d x F] (dW_gate, dW_up), [F x d] (dW_down) or [d x E] (router);
-// an expert without tokens gets zeros.
-template <int BN>
+// G_BWD_DW, G_BWD_DW_MX: weight gradients [d x F] (dW_gate, dW_up), [F x d] (dW_down) or
+// [d x E] (router); an expert without tokens gets zeros.
+template <int MODE, int BN>
 __device__ __forceinline__ void epilogue_dw(const GemmParams& p, const Tile& t, uint32_t tacc,
                                             uint32_t stg, int q, int half, int lane,
                                             uint32_t release) {
   using bf16 = __nv_bfloat16;
-  constexpr int cols = warp_cols<G_BWD_DW, BN>();
+  constexpr int cols = warp_cols<MODE, BN>();
   bf16* out;
   int ld, ncols;
   if (t.g == 2) {
@@ -445,15 +479,17 @@ __device__ __forceinline__ void epilogue_dw(const GemmParams& p, const Tile& t, 
     ncols = ld;
   }
   const int col0 = t.n * BN + cols * half;
-  store_acc_rows<cols / 32, false>(out + (int64_t)(t.m0 + 32 * q) * ld + col0, ld, 32, ncols - col0,
-                                   tacc + cols * half, t.nkb == 0, 1.0f, stg, lane, release);
+  store_acc_rows<cols / 32, Cfg<MODE, BN>::NUM_ACC == 1>(out + (int64_t)(t.m0 + 32 * q) * ld + col0,
+                                                         ld, 32, ncols - col0, tacc + cols * half,
+                                                         t.nkb == 0, 1.0f, stg, lane, release);
 }
 
 // G_FWD_GU_MX: h = SiLU(g) * u quantised per 32 columns into E4M3 codes [rows][F] and UE8M0
 // scale atoms by M tile; the tile's 128 h columns are K block t.n of the down projection.  This
 // warp takes h columns 64*half .. 64*half+63 of the tile: both 32-column blocks are computed and
 // quantised in registers, the accumulator is released (the next tile's MMAs then run under the
-// stores), then the codes and scale bytes are written.
+// stores), then the codes and scale bytes are written.  Training (out2 set): g and u are also
+// stored in bf16 (out2, out3) for the backward.
 template <int BN>
 __device__ __forceinline__ void epilogue_gu_mx(const GemmParams& p, const Tile& t, uint32_t tacc,
                                                int r, int half, uint32_t release) {
@@ -469,6 +505,17 @@ __device__ __forceinline__ void epilogue_gu_mx(const GemmParams& p, const Tile& 
 #pragma unroll
     for (int i = 0; i < 32; ++i) hv[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
     sb[b] = mx_block32(hv, qq[b]);
+    if (p.out2[t.g] && r < t.rows) {
+      const int64_t o = (int64_t)(t.row0 + r) * (t.g ? p.F : p.Fs) + t.n * 128 + c;
+      uint32_t gp[16], up[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        gp[i] = pack_bf16x2(__uint_as_float(gr[2 * i]), __uint_as_float(gr[2 * i + 1]));
+        up[i] = pack_bf16x2(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1]));
+      }
+      st_row64(static_cast<__nv_bfloat16*>(p.out2[t.g]) + o, gp);
+      st_row64(static_cast<__nv_bfloat16*>(p.out3[t.g]) + o, up);
+    }
   }
   acc_release(release, r & 31);
   if (r < t.rows) {
@@ -482,6 +529,89 @@ __device__ __forceinline__ void epilogue_gu_mx(const GemmParams& p, const Tile& 
     // scale bytes of blocks 2*half and 2*half+1: adjacent bytes of the row's atom word
     uint8_t* hs = static_cast<uint8_t*>(p.out1[t.g]) + sf_atom_word(t.mt, t.n, ld / 128, r) + 2 * half;
     *reinterpret_cast<uint16_t*>(hs) = (uint16_t)(sb[0] | (sb[1] << 8));
+  }
+}
+
+// G_BWD_DA_MX: from a = dY W_down^T (the accumulator) and the saved G, U (bf16): dG, dU and w*h
+// in bf16 (inputs of the token-axis quantiser of the weight gradients), dG and dU quantised per
+// 32 columns (E4M3 codes [rows][F] and scale atoms by M tile: the A operands of the block-scaled
+// dX GEMM) and the router partial <a, h> per (routed row, 128-column block).  This warp takes
+// columns 128 half .. 128 half + 127 of the tile (N tile 128 with two accumulators and four
+// epilogue warps: half = 0): K block kb of F, whose four scale bytes per row are one atom word.
+template <int BN>
+__device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& t, uint32_t tacc,
+                                               int q, int half, int lane, uint32_t release) {
+  using bf16 = __nv_bfloat16;
+  const int r = q * 32 + lane;
+  const bool valid = r < t.rows;
+  const int ld = t.g ? p.F : p.Fs;
+  const int64_t row = t.row0 + r;
+  const float w = (t.g == 1 && valid) ? p.row_w[row] : 1.0f;
+  const int kb = t.n * (BN / 128) + half;
+  const int64_t off = row * ld + 128 * kb;
+  const bf16* Gs = static_cast<const bf16*>(p.in0[t.g]) + off;
+  const bf16* Us = static_cast<const bf16*>(p.in1[t.g]) + off;
+  bf16* dG = static_cast<bf16*>(p.out0[t.g]) + off;
+  bf16* dU = static_cast<bf16*>(p.out1[t.g]) + off;
+  bf16* hw = static_cast<bf16*>(p.out2[t.g]) + off;
+  uint8_t* dGq = static_cast<uint8_t*>(p.qout[t.g][0]) + off;
+  uint8_t* dUq = static_cast<uint8_t*>(p.qout[t.g][1]) + off;
+  float pacc = 0.0f;
+  uint32_t sg = 0u, su = 0u;
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 32) {
+    uint32_t v[32];
+    tmem_ld32(tacc + 128 * half + c, v);
+    tmem_ld_wait();
+    if (valid) {
+      uint32_t gq[16], uq[16];
+      ld_row64(Gs + c, gq);
+      ld_row64(Us + c, uq);
+      float fg[32], fu[32];
+      uint32_t o2[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float hv2[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const float g = h2 ? bf16_hi(gq[i]) : bf16_lo(gq[i]);
+          const float u = h2 ? bf16_hi(uq[i]) : bf16_lo(uq[i]);
+          const float a = __uint_as_float(v[2 * i + h2]);
+          const float sgm = sigmoid_f(g);
+          const float hv = g * sgm * u;
+          pacc += a * hv;
+          const float dh = w * a;
+          fg[2 * i + h2] = dh * u * sgm * (1.0f + g * (1.0f - sgm));
+          fu[2 * i + h2] = dh * g * sgm;
+          hv2[h2] = w * hv;
+        }
+        o2[i] = pack_bf16x2(hv2[0], hv2[1]);
+      }
+      uint32_t pg[16], pu[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        pg[i] = pack_bf16x2(fg[2 * i], fg[2 * i + 1]);
+        pu[i] = pack_bf16x2(fu[2 * i], fu[2 * i + 1]);
+      }
+      st_row64(dG + c, pg);
+      st_row64(dU + c, pu);
+      st_row64(hw + c, o2);
+      uint32_t qq[8];
+      sg |= mx_block32(fg, qq) << (c / 4);  // scale byte c / 32 of the row's atom word
+      uint4* dq = reinterpret_cast<uint4*>(dGq + c);
+      dq[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+      dq[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+      su |= mx_block32(fu, qq) << (c / 4);
+      dq = reinterpret_cast<uint4*>(dUq + c);
+      dq[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+      dq[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+    }
+  }
+  acc_release(release, lane);
+  if (valid) {
+    *reinterpret_cast<uint32_t*>(p.qsc[t.g][0] + sf_atom_word(t.mt, kb, ld / 128, r)) = sg;
+    *reinterpret_cast<uint32_t*>(p.qsc[t.g][1] + sf_atom_word(t.mt, kb, ld / 128, r)) = su;
+    if (t.g == 1) p.partial[row * (ld / 128) + kb] = pacc;
   }
 }
 
@@ -575,21 +705,39 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
 // kb*128 + 32*j, j = 0..3, byte j) at offset 16*r0 + 4*r1.  Scale rows are row-major [rows][K/32]
 // in global memory, so the four bytes of a row are one aligned 32-bit word.
 // MXFP8: the stage's scale atoms (the A tile's, then one per 128 B rows) by bulk copies on the
-// stage barrier.  Gate/up: B rows 0-127 are gate rows, 128-255 up rows of the h tile; down: B rows
-// are 256 consecutive rows of W_down (two atoms).
+// stage barrier.  Gate/up: B rows 0-127 are gate rows, 128-255 up rows of the h tile; down, da,
+// dx: B rows are 256 consecutive rows of the expert's K-major weight (two atoms); dw: A and B
+// rows are rows of the transposed operands, K block t.row0 / 128 + kb of the whole matrix.
 template <int MODE, int BN>
 __device__ __forceinline__ void load_scale_atoms(const GemmParams& p, const Tile& t, int kb,
                                                  uint32_t sf, uint32_t bar) {
   const int nkb = p.sf_kb[t.g];
-  bulk_load(sf, p.sfa[t.g] + sf_atom_word(t.mt, kb, nkb, 0), 512, bar);
   if constexpr (MODE == G_FWD_GU_MX) {
+    bulk_load(sf, p.sfa[t.g][0] + sf_atom_word(t.mt, kb, nkb, 0), 512, bar);
     const int64_t tile = (int64_t)t.e * p.nt[t.g] + t.n;  // 128-row tile of gate / up
     bulk_load(sf + 512, p.sfb[t.g][0] + sf_atom_word(tile, kb, nkb, 0), 512, bar);
     bulk_load(sf + 1024, p.sfb[t.g][1] + sf_atom_word(tile, kb, nkb, 0), 512, bar);
+  } else if constexpr (MODE == G_FWD_DOWN_MX || MODE == G_BWD_DA_MX || MODE == G_BWD_DX_MX) {
+    int seg = 0, kk = kb;
+    if constexpr (MODE == G_BWD_DX_MX) {  // dG with gate, then dU with up: nkb blocks each
+      seg = kb >= nkb ? 1 : 0;
+      kk = kb - seg * nkb;
+    }
+    bulk_load(sf, p.sfa[t.g][seg] + sf_atom_word(t.mt, kk, nkb, 0), 512, bar);
+    // the BN weight rows of the N tile: BN / 128 row tiles of the expert's K-major weight
+    const int64_t tile = ((int64_t)t.e * p.nt[t.g] + t.n) * (BN / 128);
+#pragma unroll
+    for (int a = 0; a < BN / 128; ++a)
+      bulk_load(sf + 512 * (1 + a), p.sfb[t.g][seg] + sf_atom_word(tile + a, kk, nkb, 0), 512, bar);
+  } else if constexpr (MODE == G_BWD_DW_MX) {
+    const int kg = t.row0 / 128 + kb;
+    const uint8_t* a = p.sfa[t.g][t.sub == 2 ? 1 : 0];
+    const uint8_t* b = p.sfb[t.g][t.sub];
+    bulk_load(sf, a + sf_atom_word(t.m0 / 128, kg, nkb, 0), 512, bar);
+    bulk_load(sf + 512, b + sf_atom_word(2 * t.n, kg, nkb, 0), 512, bar);
+    bulk_load(sf + 1024, b + sf_atom_word(2 * t.n + 1, kg, nkb, 0), 512, bar);
   } else {
-    const int64_t tile = ((int64_t)t.e * p.nt[t.g] + t.n) * 2;  // two 128-row tiles of W_down
-    bulk_load(sf + 512, p.sfb[t.g][0] + sf_atom_word(tile, kb, nkb, 0), 512, bar);
-    bulk_load(sf + 1024, p.sfb[t.g][0] + sf_atom_word(tile + 1, kb, nkb, 0), 512, bar);
+    static_assert(MODE == -1, "scale atoms of an MXFP8 mode");
   }
 }
 
@@ -855,12 +1003,14 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       // when there is only one)
       const uint32_t stg = sSTG0 + (warp - 2) * 2048;
       const uint32_t rel = PAIR ? mapa_shared(bar_tempty + 8 * buf, 0) : bar_tempty + 8 * buf;
-      if constexpr (MODE == G_BWD_DW) {
-        epilogue_dw<BN>(p, t, tacc, stg, q, half, lane, rel);
+      if constexpr (MODE == G_BWD_DW || MODE == G_BWD_DW_MX) {
+        epilogue_dw<MODE, BN>(p, t, tacc, stg, q, half, lane, rel);
       } else if constexpr (C::ROW_STAGED) {
         epilogue_rows<MODE, BN>(p, t, tacc, stg, q, half, lane, rel);
       } else if constexpr (MODE == G_FWD_GU_MX) {
         epilogue_gu_mx<BN>(p, t, tacc, r, half, rel);
+      } else if constexpr (MODE == G_BWD_DA_MX) {
+        epilogue_da_mx<BN>(p, t, tacc, q, half, lane, rel);
       } else {
         epilogue<MODE, BN>(p, t, tacc, r, half);
         acc_release(rel, lane);
@@ -920,8 +1070,10 @@ static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
   auto k = moe_gemm_kernel<MODE, BN, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  static const char* kNames[] = {"gemm_fwd_gate_up", "gemm_fwd_down", "gemm_bwd_da", "gemm_bwd_dx",
-                                 "gemm_bwd_dw", "gemm_fwd_gate_up_mx", "gemm_fwd_down_mx"};
+  static const char* kNames[] = {"gemm_fwd_gate_up", "gemm_fwd_down",      "gemm_bwd_da",
+                                 "gemm_bwd_dx",      "gemm_bwd_dw",        "gemm_fwd_gate_up_mx",
+                                 "gemm_fwd_down_mx", "gemm_bwd_da_mx",     "gemm_bwd_dx_mx",
+                                 "gemm_bwd_dw_mx"};
   if constexpr (!PAIR) {
     if (grid <= 0) return cudaSuccess;
     prof_begin(kNames[MODE], s);
@@ -979,6 +1131,9 @@ cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStr
       return pair ? launch_one<G_BWD_DW, 256, true>(p, grid, s) : launch_one<G_BWD_DW, 256>(p, grid, s);
     case G_FWD_GU_MX: return launch_one<G_FWD_GU_MX, 256>(p, grid, s);
     case G_FWD_DOWN_MX: return launch_one<G_FWD_DOWN_MX, 256>(p, grid, s);
+    case G_BWD_DA_MX: return launch_one<G_BWD_DA_MX, 128>(p, grid, s);  // two accumulators
+    case G_BWD_DX_MX: return launch_one<G_BWD_DX_MX, 256>(p, grid, s);
+    case G_BWD_DW_MX: return launch_one<G_BWD_DW_MX, 256>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 #include "mok.h"
@@ -27,6 +28,10 @@ enum GemmMode : int {
   G_BWD_DW = 4,    // dW = X^T dG, X^T dU, (w h)^T dY, x^T dl  K-grouped, A and B MN-major
   G_FWD_GU_MX = 5,   // MXFP8 gate/up: h quantised to E4M3 + UE8M0 in the epilogue
   G_FWD_DOWN_MX = 6, // MXFP8 down: Y = w * (h Wd), bf16 out
+  // MXFP8 backward (every operand E4M3 + UE8M0 along the GEMM's own K, both K-major):
+  G_BWD_DA_MX = 7,   // a = dY Wd^T -> dG, dU, w*h (bf16), dG and dU quantised along F, <a,h>
+  G_BWD_DX_MX = 8,   // dX = dG Wg^T + dU Wu^T                      M-grouped
+  G_BWD_DW_MX = 9,   // dW from operands quantised along tokens     K-grouped (transposed)
 };
 
 // Tensor-map slots.  Group 0 is the shared expert (rows = tokens), group 1 the routed experts
@@ -56,17 +61,24 @@ struct GemmParams {
   // epilogue pointers, [group]
   void* out0[2];        // h / Y / dG / dX / dW_gate
   void* out1[2];        // G (saved)      / dU / dW_up
-  void* out2[2];        // U (saved)      / w*h / dW_down
+  void* out2[2];        // U (saved)      / w*h / dW_down; G_FWD_GU_MX: G (saved) or NULL
+  void* out3[2];        // G_FWD_GU_MX: U (saved) or NULL
   void* out_router;     // dW_router [d,E]
   const void* in0[2];   // G (saved) for G_BWD_DA
   const void* in1[2];   // U (saved)
   const float* row_w;   // router weight of each routed row (sorted_w)
   float* partial;       // G_BWD_DA: <a,h> per (routed row, N tile), [R, nt[1]]
   // MXFP8 scale factors as scale atoms (mok_mx.cuh), [group]: A by M tile (the tile's index in
-  // the M-grouped decode), B by 128-row tile of each expert's K-major weight
-  const uint8_t* sfa[2];       // x / x_sorted (gate/up) or h_sh / h (down)
-  const uint8_t* sfb[2][2];    // [group][gate, up] or [group][down]
-  int sf_kb[2];                // K blocks of 128 (= K/128)
+  // the M-grouped decode), B by 128-row tile of each expert's K-major weight; the weight-gradient
+  // GEMM's transposed operands by 128-row tile and K block of the whole matrix.
+  //  gate/up: sfa x; sfb gate, up.  down: sfa h; sfb down.  da: sfa dY; sfb down.
+  //  dx: sfa dG, dU; sfb gate, up.  dw: sfa x^T, (w h)^T; sfb dG^T, dU^T, dY^T.
+  const uint8_t* sfa[2][2];
+  const uint8_t* sfb[2][3];
+  int sf_kb[2];                // K blocks of 128 per row of the scale atoms
+  // G_BWD_DA_MX: E4M3 codes [rows][F] and scale atoms (by M tile) of dG and dU, [group][dG, dU]
+  void* qout[2][2];
+  uint8_t* qsc[2][2];
   // G_BWD_DW: per expert, kBoundMaps copies of the routed operands' maps bounded to its rows
   // (x_sorted, w*h, dG, dU, dY_sorted), from launch_dw_bound_maps
   const CUtensorMap* emaps;
@@ -130,9 +142,10 @@ cudaError_t launch_dispatch(int64_t T, int E, int k, const int32_t* topk_idx, co
 cudaError_t launch_gather_rows(const char* name, const void* src0, const void* src1,
                                const int32_t* inv_pos, int64_t T, int k, int row_bytes,
                                void* dst0, void* dst1, cudaStream_t s);
+// y[t] = Ysh[t] (+ Ysh2[t]) + routed rows in ascending expert order; Ysh, Ysh2 may be NULL.
 cudaError_t launch_combine(int64_t T, int d, int k, const int32_t* topk_idx,
                            const int32_t* inv_pos, const void* Ys, const void* Ysh, void* y,
-                           cudaStream_t s);
+                           cudaStream_t s, const void* Ysh2 = nullptr);
 cudaError_t launch_router_backward(int64_t T, int E, int k, int ldp, const int32_t* topk_idx,
                                    const float* topk_w, const int32_t* inv_pos,
                                    const float* partial, float* dlogits, void* dl_bf16,
@@ -148,6 +161,24 @@ cudaError_t launch_gather_scale_atoms(const void* src, const int32_t* sorted_tok
                                       void* dst, cudaStream_t s);
 cudaError_t launch_mx_quantize_transpose(const void* src, int64_t nmat, int K, int N, void* q,
                                          void* sc, cudaStream_t s);
+// MXFP8 backward: rows of each expert (src rows rows_idx[offsets[e] + i], or offsets[e] + i
+// without rows_idx; one segment of nsrc rows when offsets is NULL) quantised along tokens into
+// the transposed codes q[C][128 nkb] (expert e at columns 128 s_mt[e], zero-padded to whole
+// 128-column blocks) and scale atoms [C/128][nkb]; up to three operands of the same rows and
+// width C (a multiple of 64) per launch.
+struct TokQuantParams {
+  const __nv_bfloat16* src[3];
+  uint8_t* q[3];
+  uint8_t* sc[3];
+  int nops;
+  int C;
+  int64_t nsrc;
+  const int32_t* rows_idx;
+  const int32_t* offsets;
+  int E;
+  int nkb;
+};
+cudaError_t launch_mx_quantize_tokens(const TokQuantParams& tp, cudaStream_t s);
 // Optional per-launch CUDA-event timing (profile.cu); no-ops unless enabled on this thread.
 void prof_begin(const char* name, cudaStream_t s);
 void prof_end(cudaStream_t s);

@@ -100,6 +100,139 @@ cudaError_t launch_mx_quantize_transpose(const void* src, int64_t nmat, int K, i
   return cudaGetLastError();
 }
 
+// Token-axis quantiser of the MXFP8 weight gradients (K = an expert's tokens): row i of expert e
+// (source row rows_idx[offsets[e] + i], or offsets[e] + i) is column 128 s_mt[e] + i of a
+// transposed code matrix q[C][128 nkb], s_mt being the prefix over experts of ceil(rows / 128);
+// columns up to the expert's next multiple of 128 are zeros, so every 128-column K block of the
+// GEMM holds one expert's tokens.  Blocks of 32 tokens start at the expert's first token.
+// Tiled through shared memory, one 128-token x 64-column tile at a time: coalesced 128-byte
+// row reads (gathered by rows_idx), one thread per (column, 32-token block) for the scale and
+// codes, coalesced 128-byte column writes of the codes, one 4-byte atom word per column.  Up to
+// three operands with the same rows and width go in one launch.
+constexpr int kTokTile = 128, kColTile = 64;
+
+__global__ void __launch_bounds__(256) mx_quantize_tokens_kernel(const __grid_constant__ TokQuantParams tp) {
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_mt[kMaxE + 1];
+  __shared__ uint32_t tile[kTokTile][kColTile / 2 + 1];  // bf16 pairs; odd pitch: no conflicts
+  __shared__ __align__(16) uint8_t codes[kColTile][kTokTile + 16];
+  __shared__ __align__(4) uint8_t sbytes[kColTile][4];
+  const int tid = threadIdx.x;
+  int E = tp.E;
+  if (tp.offsets == nullptr) {
+    if (tid == 0) {
+      s_off[0] = 0;
+      s_off[1] = (int)tp.nsrc;
+      s_mt[0] = 0;
+      s_mt[1] = (int)((tp.nsrc + 127) / 128);
+    }
+    E = 1;
+  } else if (tid < 32) {  // one warp: offsets and the 128-column block prefix
+    const int lane = tid;
+    const int per = (E + 31) / 32;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) local += (tp.offsets[e + 1] - tp.offsets[e] + 127) / 128;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        s_off[e] = tp.offsets[e];
+        s_mt[e] = run;
+        run += (tp.offsets[e + 1] - tp.offsets[e] + 127) / 128;
+      }
+    }
+    if (lane == 31) {
+      s_off[E] = tp.offsets[E];
+      s_mt[E] = incl;
+    }
+  }
+  __syncthreads();
+  const int C = tp.C;
+  const int64_t ld = 128 * (int64_t)tp.nkb;
+  const int ncolt = C / kColTile;
+  const int nkt = min(s_mt[E], tp.nkb);  // 128-token K blocks in use
+  const int64_t ntiles = (int64_t)tp.nops * nkt * ncolt;
+  for (int64_t id = blockIdx.x; id < ntiles; id += gridDim.x) {
+    // column tiles fastest: neighbouring blocks read the same source rows
+    const int op = (int)(id / ((int64_t)nkt * ncolt));
+    const int rest = (int)(id - (int64_t)op * nkt * ncolt);
+    const int kt = rest / ncolt, c0 = (rest - kt * ncolt) * kColTile;
+    int lo = 0, hi = E;  // the expert of K block kt: largest e with s_mt[e] <= kt
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_mt[mid] <= kt) lo = mid; else hi = mid;
+    }
+    const int li0 = (kt - s_mt[lo]) * kTokTile;
+    const int me = s_off[lo + 1] - s_off[lo];
+    const __nv_bfloat16* src = tp.src[op];
+    // 128 rows x 64 columns: 8 threads per row, 16 bytes each
+    const int ch = tid & 7;
+#pragma unroll
+    for (int j = 0; j < kTokTile / 32; ++j) {
+      const int r = (tid >> 3) + 32 * j;
+      const int li = li0 + r;
+      uint4 u = make_uint4(0u, 0u, 0u, 0u);
+      if (li < me) {
+        const int64_t row = s_off[lo] + li;
+        const int64_t sr = tp.rows_idx ? (int64_t)tp.rows_idx[row] : row;
+        if (sr >= 0 && sr < tp.nsrc) u = *reinterpret_cast<const uint4*>(src + sr * C + c0 + 8 * ch);
+      }
+      tile[r][4 * ch + 0] = u.x;
+      tile[r][4 * ch + 1] = u.y;
+      tile[r][4 * ch + 2] = u.z;
+      tile[r][4 * ch + 3] = u.w;
+    }
+    __syncthreads();
+    {  // thread: column cc, 32-token block b
+      const int cc = tid & (kColTile - 1), b = tid >> 6;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t w2 = tile[32 * b + i][cc >> 1];
+        v[i] = (cc & 1) ? bf16_hi(w2) : bf16_lo(w2);
+      }
+      uint32_t qq[8];
+      sbytes[cc][b] = (uint8_t)mx_block32(v, qq);
+      uint4* d = reinterpret_cast<uint4*>(&codes[cc][32 * b]);
+      d[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+      d[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+    }
+    __syncthreads();
+    uint8_t* q = tp.q[op];
+#pragma unroll
+    for (int pass = 0; pass < kColTile / 32; ++pass) {  // 8 threads per column: 128 bytes
+      const int cc = (tid >> 3) + 32 * pass;
+      *reinterpret_cast<uint4*>(q + (int64_t)(c0 + cc) * ld + (int64_t)kt * kTokTile + 16 * ch) =
+          *reinterpret_cast<const uint4*>(&codes[cc][16 * ch]);
+    }
+    if (tid < kColTile) {
+      const int c = c0 + tid;
+      *reinterpret_cast<uint32_t*>(tp.sc[op] + sf_atom_word(c >> 7, kt, tp.nkb, c & 127)) =
+          *reinterpret_cast<const uint32_t*>(&sbytes[tid][0]);
+    }
+    __syncthreads();  // the next tile reuses the shared buffers
+  }
+}
+
+cudaError_t launch_mx_quantize_tokens(const TokQuantParams& tp, cudaStream_t s) {
+  const int64_t bound = (int64_t)tp.nops * tp.nkb * (tp.C / kColTile);  // tiles, upper bound
+  if (bound == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>(bound, (int64_t)num_sms() * 8);
+  prof_begin("mx_quantize_tokens", s);
+  mx_quantize_tokens_kernel<<<(int)blocks, 256, 0, s>>>(tp);
+  prof_end(s);
+  return cudaGetLastError();
+}
+
 // Scale atoms of the pulled rows: sorted row i (expert e, i - offsets[e] = 128 m + r) takes the
 // scales of token sorted_tok[i] (atoms of x by 128-token tile) into row r of M tile s_mt[e] + m,
 // s_mt being the prefix over experts of ceil(rows / 128), the M-grouped GEMM's tile order.  One

@@ -50,6 +50,9 @@ WORKLOADS = {
                                  "normal0.1", "mxfp8", False, 4),
     "dsv3_bf16_train": LayerShape("dsv3_bf16_train", 8192, 7168, 256, 8, 2048, 2048, 1, 0.0,
                                   "normal0.1", "bf16", True, 5),
+    # the training step with every expert GEMM block-scaled (forward and backward)
+    "dsv3_mxfp8_train": LayerShape("dsv3_mxfp8_train", 8192, 7168, 256, 8, 2048, 2048, 1, 0.0,
+                                   "normal0.1", "mxfp8", True, 10),
     # decode-sized batch of the same layer: 64 tokens (512 routes) still touch most experts, so
     # the step streams nearly all the expert weights for few rows each
     "dsv3_decode_t64": LayerShape("dsv3_decode_t64", 64, 7168, 256, 8, 2048, 2048, 1, 0.0,
@@ -63,6 +66,8 @@ WORKLOADS = {
                                        0.0, "normal0.1", "bf16", True, 7),
     "dsv3_mxfp8_slice_e32": LayerShape("dsv3_mxfp8_slice_e32", 1024, 7168, 32, 8, 2048, 2048, 1,
                                        0.0, "normal0.1", "mxfp8", False, 8),
+    "dsv3_mxfp8_train_slice_e32": LayerShape("dsv3_mxfp8_train_slice_e32", 1024, 7168, 32, 8, 2048,
+                                             2048, 1, 0.0, "normal0.1", "mxfp8", True, 11),
 }
 
 

@@ -157,3 +157,154 @@ def test_fullsize_mxfp8_forward_sampled():
     Wg, Wu, Wd = LazyExperts(L["W_gate"]), LazyExperts(L["W_up"]), LazyExperts(L["W_down"])
     y_mx = oracle.moe_forward_mxfp8(x, Wg, Wu, Wd, sh, got[toks], wr)
     assert_close("y sampled vs MXFP8 reading", f64(y[toks]), y_mx, max_rel=MX_MAX_REL, mean_rel=1e-2)
+
+
+# The MXFP8 backward re-quantises dG, dU and w h, computed from G and U as the forward stores
+# them (bf16).  A relative change of about 2^-9 moves an E4M3 code by one step (6-12%) for a few
+# per cent of the elements, and now and then the scale of a whole 32-element block, so against
+# the oracle's reading that keeps those tensors in float64 the gradients sit about 1% (mean) and
+# up to 7% (max) away: the oracle's own bf16-stored variant lands 1.0-1.3% (mean) and 1.7-6.7%
+# (max) from it on these cases.  Bounds there: 2e-2 mean, 1e-1 max.  The bf16-stored variant
+# (the same roundings at the same points) is the tight reference.
+MX_BWD_MEAN_REL = 2e-2
+MX_BWD_MAX_REL = 1e-1
+MX_BWD_TIGHT = (3e-2, 5e-3)   # max, mean against the bf16-stored reading
+
+BWD_CASES = {
+    # skewed routing: experts with no token or fewer than 32 (a partial token block)
+    "mx_train_skew": LayerShape("mx_train_skew", 300, 256, 16, 4, 256, 256, 1, 0.0, "zipf", "mxfp8", True, 41),
+    "mx_train_noshared": LayerShape("mx_train_noshared", 130, 256, 8, 8, 256, 0, 0, 0.05, "none", "mxfp8", True, 42),
+    # several M and N tiles per weight-gradient problem; experts spanning several 128-token blocks
+    "mx_train_wide": LayerShape("mx_train_wide", 520, 512, 8, 2, 512, 512, 1, 0.0, "zipf", "mxfp8", True, 43),
+}
+
+
+@pytest.mark.parametrize("name", list(BWD_CASES))
+def test_mxfp8_backward_parity(name):
+    """MXFP8 training step (forward with saved G, U; block-scaled backward GEMMs) against the
+    oracle's MXFP8 reading of the backward with the GPU's selection: every gradient within
+    3e-2 max|ref| (mean 5e-3) of the bf16-stored reading, within 1e-1 (mean 2e-2) of the
+    float64-intermediate reading; the distance to the float64 backward bounded by the oracle's
+    own MXFP8-vs-float64 distance plus 2e-2; experts without tokens get exact zeros;
+    bit-identical reruns."""
+    ensure_lib()
+    shape = BWD_CASES[name]
+    L = make_layer(shape, "cpu", with_dy=True)
+    Ld = to_dev(L)
+    D = dims_of(shape, dtype=mok.MOK_MXFP8)
+    Ld["prepared"] = mok.prepare_weights(D, Ld)
+    Ld["prepared_bwd"] = mok.prepare_weights_bwd(D, Ld)
+    layer = mok.MoELayer(D, Ld)
+    layer.forward(Ld["x"], training=True)
+    g = layer.backward(Ld["x"], Ld["dY"])
+    torch.cuda.synchronize()
+    assert mok.read_status(layer.ws) == 0 and mok.read_status(layer._ws_bwd) == 0
+
+    idx = layer.routing["topk_idx"].cpu().numpy()
+    x, Wr = f64(L["x"]), f64(L["W_router"])
+    b = None if L["bias"] is None else f64(L["bias"])
+    logits = oracle.router_logits(x, Wr, b)
+    sh = None if not shape.n_shared else (f64(L["Ws_gate"]), f64(L["Ws_up"]), f64(L["Ws_down"]))
+    args = (x, f64(L["dY"]), Wr, f64(L["W_gate"]), f64(L["W_up"]), f64(L["W_down"]), sh, logits, idx)
+    ref_mx = oracle.moe_backward_mxfp8(*args)
+    ref_bf = oracle.moe_backward_mxfp8(*args, bf16_stored=True)
+    ref = oracle.moe_backward(*args)
+    keys = ["dX", "dW_gate", "dW_up", "dW_down", "dlogits", "dW_router"]
+    if shape.n_shared:
+        keys += ["dWs_gate", "dWs_up", "dWs_down"]
+    for key in keys:  # all distances first (printed), then the bounds
+        mb, nb = errors(f64(g[key]), ref_bf[key])
+        mx, mn = errors(f64(g[key]), ref_mx[key])
+        own_mx, own_mn = errors(ref_mx[key], ref[key])
+        mx2, mn2 = errors(f64(g[key]), ref[key])
+        print(f"{name} {key}: vs bf16-stored reading {mb:.2e} {nb:.2e}; vs MXFP8 reading "
+              f"{mx:.2e} {mn:.2e}; vs float64 {mx2:.2e} {mn2:.2e} (oracle {own_mx:.2e} {own_mn:.2e})")
+    for key in keys:
+        own_mx, own_mn = errors(ref_mx[key], ref[key])
+        assert_close(f"{key} vs bf16-stored reading", f64(g[key]), ref_bf[key],
+                     max_rel=MX_BWD_TIGHT[0], mean_rel=MX_BWD_TIGHT[1])
+        assert_close(f"{key} vs MXFP8 reading", f64(g[key]), ref_mx[key], max_rel=MX_BWD_MAX_REL,
+                     mean_rel=MX_BWD_MEAN_REL)
+        assert_close(f"{key} vs float64", f64(g[key]), ref[key], max_rel=own_mx + 2e-2,
+                     mean_rel=own_mn + 2e-2)
+    empty = np.nonzero(np.bincount(idx.ravel(), minlength=shape.E) == 0)[0]
+    for e in empty:
+        assert not g["dW_gate"][e].any() and not g["dW_up"][e].any() and not g["dW_down"][e].any()
+
+    g2 = layer.backward(Ld["x"], Ld["dY"])
+    torch.cuda.synchronize()
+    for key, v in g.items():
+        if v is not None:
+            assert torch.equal(v, g2[key]), key
+
+
+def test_mxfp8_backward_weights_bit_exact():
+    """mok_prepare_weights_bwd: the backward copies quantised along each GEMM's K, bit-exact
+    against the oracle's quantiser (rows of each weight, blocks along its last axis)."""
+    ensure_lib()
+    shape = _mx_shape(WORKLOADS["tiny"], F=256, F_shared=256)
+    L = to_dev(make_layer(shape, "cpu"))
+    D = dims_of(shape, dtype=mok.MOK_MXFP8)
+    prep = mok.prepare_weights_bwd(D, L)
+    torch.cuda.synchronize()
+    buf = prep.cpu().numpy()
+    E, d, F, Fs = shape.E, shape.d, shape.F, shape.F_shared
+
+    def al(n):
+        return (n + 1023) // 1024 * 1024
+
+    mats = [(L["W_down"], E, F, d), (L["W_gate"], E, d, F), (L["W_up"], E, d, F),
+            (L["Ws_down"][None], 1, Fs, d), (L["Ws_gate"][None], 1, d, Fs), (L["Ws_up"][None], 1, d, Fs)]
+    sizes = []
+    for _, n, N, K in mats:
+        sizes += [n * N * K, n * N * K // 32]
+    offs = np.cumsum([0] + [al(n) for n in sizes])
+    for i, (W, n, N, K) in enumerate(mats):
+        q_ref, s_ref = oracle.mx_quantize(f64(W))        # rows [n][N], blocks along K
+        q = buf[offs[2 * i]:offs[2 * i] + n * N * K].reshape(n, N, K)
+        s = scales_from_atoms(buf[offs[2 * i + 1]:offs[2 * i + 1] + n * N * K // 32], n, N, K)
+        assert (s == s_ref).all(), f"scales of matrix {i}"
+        assert (q == q_ref).all(), f"codes of matrix {i}"
+
+
+def test_fullsize_mxfp8_training_sampled():
+    """The full MXFP8 training workload (T=8192, E=256): dX and dlogits on sampled tokens, the
+    weight gradients of the busiest and the least busy expert in full (all their tokens, in
+    order, so the token blocks are the GPU's), the shared expert's over all tokens, against the
+    oracle's bf16-stored MXFP8 reading."""
+    ensure_lib()
+    shape = WORKLOADS["dsv3_mxfp8_train"]
+    L = make_layer(shape, "cuda", with_dy=True)
+    D = dims_of(shape, dtype=mok.MOK_MXFP8)
+    L["prepared"] = mok.prepare_weights(D, L)
+    L["prepared_bwd"] = mok.prepare_weights_bwd(D, L)
+    layer = mok.MoELayer(D, L)
+    layer.forward(L["x"], training=True)
+    g = layer.backward(L["x"], L["dY"])
+    torch.cuda.synchronize()
+    assert mok.read_status(layer.ws) == 0 and mok.read_status(layer._ws_bwd) == 0
+    got = layer.routing["topk_idx"].cpu().numpy()
+    counts = np.bincount(got.ravel(), minlength=shape.E)
+    x64, Wr = f64(L["x"]), f64(L["W_router"])
+    l64 = oracle.router_logits(x64, Wr, f64(L["bias"]))
+    dY = L["dY"]
+    Wg, Wu, Wd = LazyExperts(L["W_gate"]), LazyExperts(L["W_up"]), LazyExperts(L["W_down"])
+    sh = (f64(L["Ws_gate"]), f64(L["Ws_up"]), f64(L["Ws_down"]))
+    toks = [0, 1, shape.T - 1]
+    ref = oracle.moe_backward_mxfp8(x64[toks], f64(dY[toks]), Wr, Wg, Wu, Wd, sh, l64[toks],
+                                    got[toks], bf16_stored=True)
+    tmax, tmean = MX_BWD_TIGHT
+    assert_close("dX sampled", f64(g["dX"][toks]), ref["dX"], max_rel=tmax, mean_rel=tmean)
+    assert_close("dlogits sampled", f64(g["dlogits"][toks]), ref["dlogits"], max_rel=tmax,
+                 mean_rel=tmean)
+    for e in (int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))):
+        rows = np.nonzero((got == e).any(1))[0]
+        r = oracle.moe_backward_mxfp8(x64[rows], f64(dY[rows]), Wr, Wg, Wu, Wd, None, l64[rows],
+                                      got[rows], only_experts=[e], bf16_stored=True)
+        for key in ("dW_gate", "dW_up", "dW_down"):
+            assert_close(f"{key}[{e}]", f64(g[key][e]), r[key][e], max_rel=tmax, mean_rel=tmean)
+    rs = oracle.moe_backward_mxfp8(x64, f64(dY), Wr, Wg, Wu, Wd, sh, l64, got, only_experts=[],
+                                   bf16_stored=True)
+    for key in ("dWs_gate", "dWs_up", "dWs_down"):
+        assert_close(key, f64(g[key]), rs[key], max_rel=tmax, mean_rel=tmean)
+    assert_close("dW_router vs x^T dlogits", f64(g["dW_router"]), x64.T @ f64(g["dlogits"]))
