@@ -106,12 +106,13 @@ cudaError_t launch_mx_quantize_transpose(const void* src, int64_t nmat, int K, i
 // columns up to the expert's next multiple of 128 are zeros, so every 128-column K block of the
 // GEMM holds one expert's tokens.  Blocks of 32 tokens start at the expert's first token.
 // Tiled through shared memory, one 128-token x 64-column tile at a time: coalesced 128-byte
-// row reads (gathered by rows_idx), one thread per (column, 32-token block) for the scale and
-// codes, coalesced 128-byte column writes of the codes, one 4-byte atom word per column.  Up to
-// three operands with the same rows and width go in one launch.
+// row reads (gathered by rows_idx; the next tile's are issued before this one is quantised),
+// one thread per (column, 32-token block) for the scale and codes, coalesced 128-byte column
+// writes of the codes, one 4-byte atom word per column.  Up to three operands with the same
+// rows and width go in one launch.
 constexpr int kTokTile = 128, kColTile = 64;
 
-__global__ void __launch_bounds__(256) mx_quantize_tokens_kernel(const __grid_constant__ TokQuantParams tp) {
+__global__ void __launch_bounds__(256, 4) mx_quantize_tokens_kernel(const __grid_constant__ TokQuantParams tp) {
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_mt[kMaxE + 1];
   __shared__ uint32_t tile[kTokTile][kColTile / 2 + 1];  // bf16 pairs; odd pitch: no conflicts
@@ -161,11 +162,20 @@ __global__ void __launch_bounds__(256) mx_quantize_tokens_kernel(const __grid_co
   const int ncolt = C / kColTile;
   const int nkt = min(s_mt[E], tp.nkb);  // 128-token K blocks in use
   const int64_t ntiles = (int64_t)tp.nops * nkt * ncolt;
-  for (int64_t id = blockIdx.x; id < ntiles; id += gridDim.x) {
-    // column tiles fastest: neighbouring blocks read the same source rows
-    const int op = (int)(id / ((int64_t)nkt * ncolt));
+  const int ch = tid & 7;
+  // tile id -> operand, K block and first column (column tiles fastest: neighbouring blocks read
+  // the same source rows)
+  auto decode = [&](int64_t id, int& op, int& kt, int& c0) {
+    op = (int)(id / ((int64_t)nkt * ncolt));
     const int rest = (int)(id - (int64_t)op * nkt * ncolt);
-    const int kt = rest / ncolt, c0 = (rest - kt * ncolt) * kColTile;
+    kt = rest / ncolt;
+    c0 = (rest - kt * ncolt) * kColTile;
+  };
+  // the tile's global loads, 128 rows x 64 columns: 8 threads per row, 16 bytes each, rows
+  // tid / 8 + 32 j; rows past the expert's tokens are zeros
+  auto fetch = [&](int64_t id, uint4 (&u)[kTokTile / 32]) {
+    int op, kt, c0;
+    decode(id, op, kt, c0);
     int lo = 0, hi = E;  // the expert of K block kt: largest e with s_mt[e] <= kt
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -174,24 +184,33 @@ __global__ void __launch_bounds__(256) mx_quantize_tokens_kernel(const __grid_co
     const int li0 = (kt - s_mt[lo]) * kTokTile;
     const int me = s_off[lo + 1] - s_off[lo];
     const __nv_bfloat16* src = tp.src[op];
-    // 128 rows x 64 columns: 8 threads per row, 16 bytes each
-    const int ch = tid & 7;
 #pragma unroll
     for (int j = 0; j < kTokTile / 32; ++j) {
-      const int r = (tid >> 3) + 32 * j;
-      const int li = li0 + r;
-      uint4 u = make_uint4(0u, 0u, 0u, 0u);
+      const int li = li0 + (tid >> 3) + 32 * j;
+      u[j] = make_uint4(0u, 0u, 0u, 0u);
       if (li < me) {
         const int64_t row = s_off[lo] + li;
         const int64_t sr = tp.rows_idx ? (int64_t)tp.rows_idx[row] : row;
-        if (sr >= 0 && sr < tp.nsrc) u = *reinterpret_cast<const uint4*>(src + sr * C + c0 + 8 * ch);
+        if (sr >= 0 && sr < tp.nsrc) u[j] = *reinterpret_cast<const uint4*>(src + sr * C + c0 + 8 * ch);
       }
-      tile[r][4 * ch + 0] = u.x;
-      tile[r][4 * ch + 1] = u.y;
-      tile[r][4 * ch + 2] = u.z;
-      tile[r][4 * ch + 3] = u.w;
     }
-    __syncthreads();
+  };
+  uint4 u[kTokTile / 32];
+  if ((int64_t)blockIdx.x < ntiles) fetch(blockIdx.x, u);
+  // two barriers per tile: the next tile's loads are in flight while this one is quantised
+  for (int64_t id = blockIdx.x; id < ntiles; id += gridDim.x) {
+    int op, kt, c0;
+    decode(id, op, kt, c0);
+#pragma unroll
+    for (int j = 0; j < kTokTile / 32; ++j) {
+      const int r = (tid >> 3) + 32 * j;
+      tile[r][4 * ch + 0] = u[j].x;
+      tile[r][4 * ch + 1] = u[j].y;
+      tile[r][4 * ch + 2] = u[j].z;
+      tile[r][4 * ch + 3] = u[j].w;
+    }
+    __syncthreads();  // tile written; the previous tile's codes are out
+    if (id + gridDim.x < ntiles) fetch(id + gridDim.x, u);
     {  // thread: column cc, 32-token block b
       const int cc = tid & (kColTile - 1), b = tid >> 6;
       float v[32];
@@ -206,7 +225,7 @@ __global__ void __launch_bounds__(256) mx_quantize_tokens_kernel(const __grid_co
       d[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
       d[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
     }
-    __syncthreads();
+    __syncthreads();  // codes complete; the tile may be overwritten
     uint8_t* q = tp.q[op];
 #pragma unroll
     for (int pass = 0; pass < kColTile / 32; ++pass) {  // 8 threads per column: 128 bytes
@@ -219,14 +238,19 @@ __global__ void __launch_bounds__(256) mx_quantize_tokens_kernel(const __grid_co
       *reinterpret_cast<uint32_t*>(tp.sc[op] + sf_atom_word(c >> 7, kt, tp.nkb, c & 127)) =
           *reinterpret_cast<const uint32_t*>(&sbytes[tid][0]);
     }
-    __syncthreads();  // the next tile reuses the shared buffers
   }
 }
 
 cudaError_t launch_mx_quantize_tokens(const TokQuantParams& tp, cudaStream_t s) {
   const int64_t bound = (int64_t)tp.nops * tp.nkb * (tp.C / kColTile);  // tiles, upper bound
   if (bound == 0) return cudaSuccess;
-  const int64_t blocks = std::min<int64_t>(bound, (int64_t)num_sms() * 8);
+  // persistent: as many blocks as are resident at once (shared memory allows about seven per SM)
+  static int per_sm = 0;
+  if (per_sm == 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_quantize_tokens_kernel, 256, 0) !=
+          cudaSuccess)
+    per_sm = 4;
+  const int64_t blocks = std::min<int64_t>(bound, (int64_t)num_sms() * std::max(per_sm, 1));
   prof_begin("mx_quantize_tokens", s);
   mx_quantize_tokens_kernel<<<(int)blocks, 256, 0, s>>>(tp);
   prof_end(s);
