@@ -19,7 +19,7 @@ __all__ = [
     "MokError", "Dims", "Weights", "lib", "lib_path", "dims", "route", "dispatch_index",
     "moe_forward", "moe_backward", "layer_forward_host", "workspace_size", "saved_size",
     "read_status", "clear_status", "last_launch_count", "MoELayer", "EXPORTED_SYMBOLS",
-    "MOK_BF16", "MOK_MXFP8",
+    "MOK_BF16", "MOK_MXFP8", "prepare_weights", "prepare_weights_bwd", "mx_quantize_rows",
 ]
 
 MOK_BF16, MOK_MXFP8 = 0, 1
