@@ -185,10 +185,11 @@ def work_model(shape, counts):
         if shape.dtype == "mxfp8":
             wq = 1.0 + 1.0 / 32
             ops_t = 2.0 * Rs * d + 3.0 * Hs  # token-axis operands: x, dY, dG, dU, w*h
-            m["gemm_bwd_da_mx"] = {  # reads dY codes, W_down codes, G, U; writes dG, dU, w*h, codes
+            m["gemm_bwd_da_mx"] = {  # reads dY codes, W_down codes, G, U; writes the codes of
+                # dG, dU along F and of dG, dU, w*h along tokens
                 "flops": m["gemm_bwd_da"]["flops"], "dtype": "fp8",
-                "bytes": wq * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Rs * d + 2.0 * Hs)
-                + wb * 5.0 * Hs + 4.0 * R * (F // 128)}
+                "bytes": wq * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Rs * d + 5.0 * Hs)
+                + wb * 2.0 * Hs + 4.0 * R * (F // 128)}
             m["gemm_bwd_dx_mx"] = {
                 "flops": 2.0 * (R * 2 * F * d + T * ns * 2 * Fs * d), "dtype": "fp8",
                 "bytes": wq * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + 2.0 * Hs) + wb * Rs * d}
@@ -197,9 +198,9 @@ def work_model(shape, counts):
                 "flops": 2.0 * 3.0 * (R * F * d + T * ns * Fs * d), "dtype": "fp8",
                 "bytes": wb * 3.0 * (E * d * F + ns * d * Fs) + wq * ops_t}
             m["gemm_bwd_dw"] = {"flops": 2.0 * T * d * E, "bytes": wb * (T * d + T * E + d * E)}
-            # per launch (two per group: x and dY, then dG, dU and w*h)
+            # per launch (one per group: x and dY)
             m["mx_quantize_tokens"] = {"flops": 0.0,
-                                       "bytes": (wb + wq) * ops_t / (2.0 * (1 + ns))}
+                                       "bytes": (wb + wq) * 2.0 * Rs * d / (1.0 + ns)}
         layer_flops = 3.0 * layer_flops
     return m, layer_flops, e_act
 

@@ -191,6 +191,9 @@ static Layout layout_bwd(const mok_dims* d) {
     const int64_t k1 = 128 * mx_nkb_routed(d), k0 = 128 * mx_nkb_shared(d);
     sz[BW_DYS] = 0;
     sz[BW_TMAP] = 0;
+    // dG, dU, w*h go straight from the dA epilogue into codes (along F and along tokens)
+    sz[BW_DG] = sz[BW_DU] = sz[BW_HW] = 0;
+    sz[BW_DGSH] = sz[BW_DUSH] = sz[BW_HWSH] = 0;
     sz[BW_P] = 4ull * R * (d->F / 128);
     sz[BW_DYQ] = 1ull * T * d->d;
     sz[BW_DYSC] = 4ull * BM * mt_x * (d->d / 128);
@@ -308,7 +311,8 @@ static int backward_mxfp8(const mok_dims* dims, const mok_weights* w, const void
                                                W(BW_DYSCS), s));
   if (rc != MOK_OK) return rc;
   *launches += 3;
-  // 2. a = dY W_down^T; epilogue: dG, dU, w*h (bf16), dG and dU quantised along F, <a, h>
+  // 2. a = dY W_down^T; epilogue: dG and dU quantised along F (for dX), dG, dU and w*h along
+  // tokens (for the weight gradients), <a, h>
   {
     GemmParams p{};
     bool ok = true;
@@ -330,8 +334,12 @@ static int backward_mxfp8(const mok_dims* dims, const mok_weights* w, const void
     p.nt[1] = F / 128;
     p.in0[0] = SV(SV_GSH); p.in1[0] = SV(SV_USH);
     p.in0[1] = SV(SV_G); p.in1[1] = SV(SV_U);
-    p.out0[0] = W(BW_DGSH); p.out1[0] = W(BW_DUSH); p.out2[0] = W(BW_HWSH);
-    p.out0[1] = W(BW_DG); p.out1[1] = W(BW_DU); p.out2[1] = W(BW_HW);
+    p.tq[0][0] = W8(BW_DGT0); p.tq[0][1] = W8(BW_DUT0); p.tq[0][2] = W8(BW_HWT0);
+    p.tsc[0][0] = W8(BW_DGTS0); p.tsc[0][1] = W8(BW_DUTS0); p.tsc[0][2] = W8(BW_HWTS0);
+    p.tq[1][0] = W8(BW_DGT); p.tq[1][1] = W8(BW_DUT); p.tq[1][2] = W8(BW_HWT);
+    p.tsc[1][0] = W8(BW_DGTS); p.tsc[1][1] = W8(BW_DUTS); p.tsc[1][2] = W8(BW_HWTS);
+    p.tnkb[0] = nkb0;
+    p.tnkb[1] = nkb1;
     p.qout[0][0] = W(BW_DGQSH); p.qout[0][1] = W(BW_DUQSH);
     p.qsc[0][0] = W8(BW_DGSCSH); p.qsc[0][1] = W8(BW_DUSCSH);
     p.qout[1][0] = W(BW_DGQ); p.qout[1][1] = W(BW_DUQ);
@@ -410,8 +418,8 @@ static int backward_mxfp8(const mok_dims* dims, const mok_weights* w, const void
     if (rc != MOK_OK) return rc;
     ++*launches;
   }
-  // 6. weight-gradient operands quantised along tokens, transposed: routed (x and dY pulled by
-  // sorted_tok; dG, dU, w*h in expert order), then the shared expert's (all tokens in order)
+  // 6. x and dY quantised along tokens, transposed (dG, dU and w*h came from the dA epilogue):
+  // routed (rows pulled by sorted_tok), then the shared expert's (all tokens in order)
   {
     using bf = const __nv_bfloat16*;
     auto tq = [&](bf a, bf b, bf c, int slot_a, int slot_b, int slot_c, int n, int C, int64_t nsrc,
@@ -435,15 +443,9 @@ static int backward_mxfp8(const mok_dims* dims, const mok_weights* w, const void
     };
     const bf bx = static_cast<bf>(x), bdy = static_cast<bf>(dY);
     rc = tq(bx, bdy, nullptr, BW_XT, BW_DYT, 0, 2, d, T, sorted_tok, offsets, nkb1);
-    if (rc == MOK_OK)
-      rc = tq(static_cast<bf>(W(BW_DG)), static_cast<bf>(W(BW_DU)), static_cast<bf>(W(BW_HW)),
-              BW_DGT, BW_DUT, BW_HWT, 3, F, R, nullptr, offsets, nkb1);
     if (rc == MOK_OK && sh) rc = tq(bx, bdy, nullptr, BW_XT0, BW_DYT0, 0, 2, d, T, nullptr, nullptr, nkb0);
-    if (rc == MOK_OK && sh)
-      rc = tq(static_cast<bf>(W(BW_DGSH)), static_cast<bf>(W(BW_DUSH)), static_cast<bf>(W(BW_HWSH)),
-              BW_DGT0, BW_DUT0, BW_HWT0, 3, Fs, T, nullptr, nullptr, nkb0);
     if (rc != MOK_OK) return rc;
-    *launches += sh ? 4 : 2;
+    *launches += sh ? 2 : 1;
   }
   // 7. weight gradients: dW_gate = X^T dG, dW_up = X^T dU, dW_down = (w h)^T dY, K = tokens
   {

@@ -55,7 +55,9 @@ struct Cfg {
   static constexpr bool ROW_STAGED = (MODE == G_FWD_DOWN || MODE == G_BWD_DX ||
                                       MODE == G_FWD_DOWN_MX || MODE == G_BWD_DW ||
                                       MODE == G_BWD_DX_MX || MODE == G_BWD_DW_MX);
-  static constexpr int STAGING_BYTES = ROW_STAGED ? EPI_WARPS * 2048 : 0;
+  // per epilogue warp: a 2 KB row-staging buffer, or (dA MXFP8) a 32 x 36-float transpose buffer
+  static constexpr int STG_STRIDE = (MODE == G_BWD_DA_MX) ? 32 * 36 * 4 : 2048;
+  static constexpr int STAGING_BYTES = (ROW_STAGED || MODE == G_BWD_DA_MX) ? EPI_WARPS * STG_STRIDE : 0;
   static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
   static constexpr int SF_TMEM_COL = 256;              // MXFP8: 16 columns per stage from here
   static constexpr uint32_t IDESC = MX ? make_idesc_mxf8(BN) : make_idesc_bf16(BN, A_MN, B_MN);
@@ -532,15 +534,48 @@ __device__ __forceinline__ void epilogue_gu_mx(const GemmParams& p, const Tile& 
   }
 }
 
-// G_BWD_DA_MX: from a = dY W_down^T (the accumulator) and the saved G, U (bf16): dG, dU and w*h
-// in bf16 (inputs of the token-axis quantiser of the weight gradients), dG and dU quantised per
-// 32 columns (E4M3 codes [rows][F] and scale atoms by M tile: the A operands of the block-scaled
-// dX GEMM) and the router partial <a, h> per (routed row, 128-column block).  This warp takes
-// columns 128 half .. 128 half + 127 of the tile (N tile 128 with two accumulators and four
-// epilogue warps: half = 0): K block kb of F, whose four scale bytes per row are one atom word.
+// Token-axis MXFP8 quantisation of one 32-column chunk held by a warp whose 32 lanes are 32
+// consecutive tokens of one expert (one 32-token block): v[j] = the lane's value in column
+// c0 + j.  The chunk is transposed through the warp's shared-memory buffer (element (column j,
+// token i) at float 36 j + i: conflict-free writes, 16-byte reads), then lane j quantises column
+// c0 + j's 32 tokens and stores their codes as 32 consecutive bytes of that column's row of the
+// transposed matrix (`col0` points at column c0, token column of lane 0), and its scale byte as
+// block q of K block kg.
+__device__ __forceinline__ void quant_tokens_chunk(const float (&v)[32], uint32_t stg, uint8_t* col0,
+                                                   int64_t ld, uint8_t* atoms, int c0, int kg,
+                                                   int nkb, int q, int lane) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg + 4u * (36u * j + lane)), "f"(v[j]) : "memory");
+  __syncwarp();
+  float col[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(col[4 * i]), "=f"(col[4 * i + 1]), "=f"(col[4 * i + 2]), "=f"(col[4 * i + 3])
+                 : "r"(stg + 4u * (36u * lane + 4u * i)));
+  __syncwarp();  // the buffer is rewritten by the next chunk
+  uint32_t qq[8];
+  const uint32_t sb = mx_block32(col, qq);
+  uint4* d = reinterpret_cast<uint4*>(col0 + (int64_t)lane * ld);
+  d[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+  d[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+  const int c = c0 + lane;
+  atoms[sf_atom_word(c >> 7, kg, nkb, c & 127) + q] = (uint8_t)sb;
+}
+
+// G_BWD_DA_MX: from a = dY W_down^T (the accumulator) and the saved G, U (bf16): dG and dU
+// quantised per 32 columns (E4M3 codes [rows][F] and scale atoms by M tile: the A operands of the
+// block-scaled dX GEMM); dG, dU and w*h quantised along tokens (the warp's 32 rows are one
+// 32-token block of one expert) into the transposed operands of the weight-gradient GEMM; and
+// the router partial <a, h> per (routed row, 128-column block).  This warp takes columns
+// 128 half .. 128 half + 127 of the tile (N tile 128 with two accumulators and four epilogue
+// warps: half = 0): K block kb of F, whose four scale bytes per row are one atom word.  Rows past
+// the expert's last token count as zeros in the token blocks.
 template <int BN>
 __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& t, uint32_t tacc,
-                                               int q, int half, int lane, uint32_t release) {
+                                               uint32_t stg, int q, int half, int lane,
+                                               uint32_t release) {
   using bf16 = __nv_bfloat16;
   const int r = q * 32 + lane;
   const bool valid = r < t.rows;
@@ -551,60 +586,82 @@ __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& 
   const int64_t off = row * ld + 128 * kb;
   const bf16* Gs = static_cast<const bf16*>(p.in0[t.g]) + off;
   const bf16* Us = static_cast<const bf16*>(p.in1[t.g]) + off;
-  bf16* dG = static_cast<bf16*>(p.out0[t.g]) + off;
-  bf16* dU = static_cast<bf16*>(p.out1[t.g]) + off;
-  bf16* hw = static_cast<bf16*>(p.out2[t.g]) + off;
   uint8_t* dGq = static_cast<uint8_t*>(p.qout[t.g][0]) + off;
   uint8_t* dUq = static_cast<uint8_t*>(p.qout[t.g][1]) + off;
+  const int nkbt = p.tnkb[t.g];
+  const int64_t tld = 128 * (int64_t)nkbt;
+  const int64_t kpos = 128 * (int64_t)t.mt + 32 * q;  // the warp's token columns
   float pacc = 0.0f;
   uint32_t sg = 0u, su = 0u;
+  uint32_t gq[16], uq[16];  // G and U of the current chunk; the next chunk's load while it runs
+  if (valid) {
+    ld_row64(Gs, gq);
+    ld_row64(Us, uq);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) gq[i] = uq[i] = 0u;
+  }
 #pragma unroll 1
   for (int c = 0; c < 128; c += 32) {
     uint32_t v[32];
     tmem_ld32(tacc + 128 * half + c, v);
+    uint32_t gn[16], un[16];
+    if (valid && c + 32 < 128) {
+      ld_row64(Gs + c + 32, gn);
+      ld_row64(Us + c + 32, un);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) gn[i] = un[i] = 0u;
+    }
     tmem_ld_wait();
+    const int col0 = 128 * kb + c;
+    float f[32];
+    uint32_t qq[8];
+    // dG = w a u s (1 + g (1 - s)), s = sigmoid(g)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float g = (i & 1) ? bf16_hi(gq[i >> 1]) : bf16_lo(gq[i >> 1]);
+      const float u = (i & 1) ? bf16_hi(uq[i >> 1]) : bf16_lo(uq[i >> 1]);
+      const float sgm = sigmoid_f(g);
+      f[i] = valid ? w * __uint_as_float(v[i]) * u * sgm * (1.0f + g * (1.0f - sgm)) : 0.0f;
+    }
     if (valid) {
-      uint32_t gq[16], uq[16];
-      ld_row64(Gs + c, gq);
-      ld_row64(Us + c, uq);
-      float fg[32], fu[32];
-      uint32_t o2[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float hv2[2];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const float g = h2 ? bf16_hi(gq[i]) : bf16_lo(gq[i]);
-          const float u = h2 ? bf16_hi(uq[i]) : bf16_lo(uq[i]);
-          const float a = __uint_as_float(v[2 * i + h2]);
-          const float sgm = sigmoid_f(g);
-          const float hv = g * sgm * u;
-          pacc += a * hv;
-          const float dh = w * a;
-          fg[2 * i + h2] = dh * u * sgm * (1.0f + g * (1.0f - sgm));
-          fu[2 * i + h2] = dh * g * sgm;
-          hv2[h2] = w * hv;
-        }
-        o2[i] = pack_bf16x2(hv2[0], hv2[1]);
-      }
-      uint32_t pg[16], pu[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        pg[i] = pack_bf16x2(fg[2 * i], fg[2 * i + 1]);
-        pu[i] = pack_bf16x2(fu[2 * i], fu[2 * i + 1]);
-      }
-      st_row64(dG + c, pg);
-      st_row64(dU + c, pu);
-      st_row64(hw + c, o2);
-      uint32_t qq[8];
-      sg |= mx_block32(fg, qq) << (c / 4);  // scale byte c / 32 of the row's atom word
+      sg |= mx_block32(f, qq) << (c / 4);  // scale byte c / 32 of the row's atom word
       uint4* dq = reinterpret_cast<uint4*>(dGq + c);
       dq[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
       dq[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
-      su |= mx_block32(fu, qq) << (c / 4);
-      dq = reinterpret_cast<uint4*>(dUq + c);
+    }
+    quant_tokens_chunk(f, stg, p.tq[t.g][0] + (int64_t)col0 * tld + kpos, tld, p.tsc[t.g][0], col0,
+                       t.mt, nkbt, q, lane);
+    // dU = w a g s
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float g = (i & 1) ? bf16_hi(gq[i >> 1]) : bf16_lo(gq[i >> 1]);
+      f[i] = valid ? w * __uint_as_float(v[i]) * g * sigmoid_f(g) : 0.0f;
+    }
+    if (valid) {
+      su |= mx_block32(f, qq) << (c / 4);
+      uint4* dq = reinterpret_cast<uint4*>(dUq + c);
       dq[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
       dq[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+    }
+    quant_tokens_chunk(f, stg, p.tq[t.g][1] + (int64_t)col0 * tld + kpos, tld, p.tsc[t.g][1], col0,
+                       t.mt, nkbt, q, lane);
+    // w h, h = g s u, and the router partial <a, h>
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float g = (i & 1) ? bf16_hi(gq[i >> 1]) : bf16_lo(gq[i >> 1]);
+      const float u = (i & 1) ? bf16_hi(uq[i >> 1]) : bf16_lo(uq[i >> 1]);
+      const float hv = g * sigmoid_f(g) * u;
+      pacc += __uint_as_float(v[i]) * hv;  // zero on rows past the expert (g = u = 0)
+      f[i] = w * hv;
+    }
+    quant_tokens_chunk(f, stg, p.tq[t.g][2] + (int64_t)col0 * tld + kpos, tld, p.tsc[t.g][2], col0,
+                       t.mt, nkbt, q, lane);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      gq[i] = gn[i];
+      uq[i] = un[i];
     }
   }
   acc_release(release, lane);
@@ -1001,7 +1058,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       const uint32_t tacc = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       // the staged and MXFP8 epilogues release the accumulator themselves (before their stores
       // when there is only one)
-      const uint32_t stg = sSTG0 + (warp - 2) * 2048;
+      const uint32_t stg = sSTG0 + (warp - 2) * C::STG_STRIDE;
       const uint32_t rel = PAIR ? mapa_shared(bar_tempty + 8 * buf, 0) : bar_tempty + 8 * buf;
       if constexpr (MODE == G_BWD_DW || MODE == G_BWD_DW_MX) {
         epilogue_dw<MODE, BN>(p, t, tacc, stg, q, half, lane, rel);
@@ -1010,7 +1067,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       } else if constexpr (MODE == G_FWD_GU_MX) {
         epilogue_gu_mx<BN>(p, t, tacc, r, half, rel);
       } else if constexpr (MODE == G_BWD_DA_MX) {
-        epilogue_da_mx<BN>(p, t, tacc, q, half, lane, rel);
+        epilogue_da_mx<BN>(p, t, tacc, stg, q, half, lane, rel);
       } else {
         epilogue<MODE, BN>(p, t, tacc, r, half);
         acc_release(rel, lane);

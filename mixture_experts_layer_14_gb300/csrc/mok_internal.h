@@ -29,7 +29,7 @@ enum GemmMode : int {
   G_FWD_GU_MX = 5,   // MXFP8 gate/up: h quantised to E4M3 + UE8M0 in the epilogue
   G_FWD_DOWN_MX = 6, // MXFP8 down: Y = w * (h Wd), bf16 out
   // MXFP8 backward (every operand E4M3 + UE8M0 along the GEMM's own K, both K-major):
-  G_BWD_DA_MX = 7,   // a = dY Wd^T -> dG, dU, w*h (bf16), dG and dU quantised along F, <a,h>
+  G_BWD_DA_MX = 7,   // a = dY Wd^T -> dG, dU along F; dG, dU, w*h along tokens; <a,h>
   G_BWD_DX_MX = 8,   // dX = dG Wg^T + dU Wu^T                      M-grouped
   G_BWD_DW_MX = 9,   // dW from operands quantised along tokens     K-grouped (transposed)
 };
@@ -79,6 +79,11 @@ struct GemmParams {
   // G_BWD_DA_MX: E4M3 codes [rows][F] and scale atoms (by M tile) of dG and dU, [group][dG, dU]
   void* qout[2][2];
   uint8_t* qsc[2][2];
+  // G_BWD_DA_MX: dG, dU and w*h quantised along tokens for the weight gradients, transposed:
+  // codes [F][128 tnkb] (the M tile mt's rows are columns 128 mt ..), atoms [F/128][tnkb]
+  uint8_t* tq[2][3];
+  uint8_t* tsc[2][3];
+  int tnkb[2];
   // G_BWD_DW: per expert, kBoundMaps copies of the routed operands' maps bounded to its rows
   // (x_sorted, w*h, dG, dU, dY_sorted), from launch_dw_bound_maps
   const CUtensorMap* emaps;

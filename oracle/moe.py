@@ -336,11 +336,11 @@ def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, on
     representable in MXFP8 the router-weight gradients, dlogits and dW_router equal the float64
     ones; the token-axis quantiser matches the pinned quantiser applied column by column.
 
-    bf16_stored: the tensors a training step keeps in memory between its GEMMs are rounded to
-    bf16 where they are stored (bf16_round): G and U as the forward saves them, and dG, dU and
-    w h as the weight-gradient quantiser reads them.  E4M3 re-quantisation turns those roundings
-    into whole-step code changes for a few per cent of the elements, so this variant is the
-    closer reference for a path that stores them in bf16."""
+    bf16_stored: the activations a training step keeps in memory between the forward and the
+    backward, G and U, are rounded to bf16 where they are stored (bf16_round); dG, dU and w h
+    are quantised straight from their values.  E4M3 re-quantisation turns that rounding into
+    whole-step code changes for a few per cent of the elements, so this variant is the closer
+    reference for a path that stores G and U in bf16."""
     x = np.asarray(x, dtype=np.float64)
     dY = np.asarray(dY, dtype=np.float64)
     Wr = np.asarray(W_router, dtype=np.float64)
@@ -372,8 +372,6 @@ def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, on
         du = dh * g * s
         dXr = _mx_qd(dg) @ _mx_qd(Wge).T + _mx_qd(du) @ _mx_qd(Wue).T   # W_gate [d, F]: along F
         hw = wr[:, None] * h
-        if bf16_stored:
-            dg, du, hw = bf16_round(dg), bf16_round(du), bf16_round(hw)
         Xt = _mx_qd_tokens(X)
         dWge = Xt.T @ _mx_qd_tokens(dg)
         dWue = Xt.T @ _mx_qd_tokens(du)

@@ -206,9 +206,9 @@ def test_bf16_round_matches_library_conversion():
 
 
 def test_mxfp8_backward_bf16_stored_variant():
-    """The bf16-storage variant rounds only G, U, dG, dU and w h: the router-weight path keeps
-    the exact <a, h> up to those roundings, and every gradient moves by much less than the
-    MXFP8 quantisation itself."""
+    """The bf16-storage variant rounds only G and U: every gradient moves by much less than the
+    MXFP8 quantisation itself, and with G and U exactly representable in bf16 it changes
+    nothing."""
     rng = np.random.default_rng(8)
     args = _small_backward_case(rng, representable=False)
     a = oracle.moe_backward_mxfp8(*args)
@@ -218,3 +218,12 @@ def test_mxfp8_backward_bf16_stored_variant():
         moved = np.abs(b[key] - a[key]).max() / np.abs(a[key]).max()
         quant = np.abs(a[key] - ref[key]).max() / np.abs(ref[key]).max()
         assert 0 < moved < quant, (key, moved, quant)
+    # one power of two per row of x and weights of a few bits: G and U are exact in bf16
+    x, dY, Wr, Wg, Wu, Wd, sh, logits, idx = _small_backward_case(rng, representable=True)
+    T, d = x.shape
+    x = np.zeros((T, d))
+    x[np.arange(T), rng.integers(0, d, size=T)] = 2.0 ** rng.integers(-3, 3, size=T)
+    c = oracle.moe_backward_mxfp8(x, dY, Wr, Wg, Wu, Wd, sh, logits, idx)
+    d = oracle.moe_backward_mxfp8(x, dY, Wr, Wg, Wu, Wd, sh, logits, idx, bf16_stored=True)
+    for key in ("dX", "dW_gate", "dW_up", "dW_down", "dlogits"):
+        assert (c[key] == d[key]).all(), key
