@@ -74,3 +74,30 @@ def test_argument_errors_are_returned_not_raised():
     assert rc == -3
     with pytest.raises(mok.MokError):
         mok._check(-3)
+
+
+def test_mxfp8_backward_sizes_and_argument_errors():
+    """MXFP8 training sizes: the backward weight copies (codes + 1/32 scale bytes of the three
+    expert weights, routed and shared), the transposed token-axis operands in the backward
+    workspace, no x in expert order in `saved`; nothing for bf16; errors returned, not raised,
+    with no GPU work."""
+    L = ensure_lib()
+    T, d, E, k, F, Fs = 8192, 7168, 256, 8, 2048, 2048
+    D8 = mok.dims(T, d, E, k, F, Fs, 1, mok.MOK_MXFP8)
+    Db = mok.dims(T, d, E, k, F, Fs, 1)
+    weights = 3 * (E * d * F + d * Fs)
+    pb = L.mok_prepared_bwd_size(ctypes.byref(D8))
+    assert weights * (1 + 1 / 32) <= pb <= weights * (1 + 1 / 32) + 12 * 1024
+    assert L.mok_prepared_bwd_size(ctypes.byref(Db)) == 0
+    R = T * k
+    nkb = (R + 127) // 128 + E
+    assert mok.workspace_size(D8, backward=True) >= (2 * d + 3 * F) * 128 * nkb   # routed codes
+    assert mok.saved_size(D8) < mok.saved_size(Db)          # no bf16 x in expert order
+    null = None
+    rc = L.mok_prepare_weights_bwd(ctypes.byref(D8), null, null, null)
+    assert rc == -1
+    W = mok.Weights()
+    rc = L.mok_prepare_weights_bwd(ctypes.byref(D8), ctypes.byref(W), null, null)
+    assert rc == -1
+    rc = L.mok_prepare_weights_bwd(ctypes.byref(Db), ctypes.byref(W), null, null)
+    assert rc == 0                                           # bf16: nothing to prepare

@@ -176,6 +176,9 @@ BWD_CASES = {
     "mx_train_noshared": LayerShape("mx_train_noshared", 130, 256, 8, 8, 256, 0, 0, 0.05, "none", "mxfp8", True, 42),
     # several M and N tiles per weight-gradient problem; experts spanning several 128-token blocks
     "mx_train_wide": LayerShape("mx_train_wide", 520, 512, 8, 2, 512, 512, 1, 0.0, "zipf", "mxfp8", True, 43),
+    # the largest expert count and top-k: most experts hold a few tokens (one partial block each)
+    "mx_train_max_E_k": LayerShape("mx_train_max_E_k", 200, 256, 512, 8, 256, 256, 1, 0.0, "normal0.1",
+                                   "mxfp8", True, 44),
 }
 
 
@@ -308,3 +311,27 @@ def test_fullsize_mxfp8_training_sampled():
     for key in ("dWs_gate", "dWs_up", "dWs_down"):
         assert_close(key, f64(g[key]), rs[key], max_rel=tmax, mean_rel=tmean)
     assert_close("dW_router vs x^T dlogits", f64(g["dW_router"]), x64.T @ f64(g["dlogits"]))
+
+
+@pytest.mark.parametrize("dtype", [mok.MOK_BF16, mok.MOK_MXFP8])
+def test_backward_with_no_tokens_zeroes_the_weight_gradients(dtype):
+    """T = 0: no kernel runs; every weight gradient (and dW_router) is written as zeros."""
+    ensure_lib()
+    shape = _mx_shape(WORKLOADS["tiny"], F=256, F_shared=256).with_(T=0)
+    L = to_dev(make_layer(shape.with_(T=1), "cpu"))
+    D = dims_of(shape, dtype=dtype)
+    if dtype == mok.MOK_MXFP8:
+        L["prepared"] = mok.prepare_weights(D, L)
+        L["prepared_bwd"] = mok.prepare_weights_bwd(D, L)
+    x = torch.empty((0, shape.d), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(mok.workspace_size(D), dtype=torch.uint8, device="cuda")
+    idx, w, _ = mok.route(D, x, L["W_router"], L["bias"], ws)
+    r = mok.dispatch_index(D, idx, w, ws)
+    saved = torch.empty(max(mok.saved_size(D), 16), dtype=torch.uint8, device="cuda")
+    mok.moe_forward(D, L, x, r, ws, saved=saved)
+    wsb = torch.zeros(mok.workspace_size(D, backward=True), dtype=torch.uint8, device="cuda")
+    g = mok.moe_backward(D, L, x, x, saved, r, wsb)
+    torch.cuda.synchronize()
+    for key in ("dW_gate", "dW_up", "dW_down", "dWs_gate", "dWs_up", "dWs_down", "dW_router"):
+        assert not g[key].any(), key
+    assert g["dX"].shape == (0, shape.d)
