@@ -212,14 +212,14 @@ def work_model(shape, counts):
 # (32-expert slices: 33 weight sets).
 _GEMM_SRC = "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"
 PROFILED_TRAFFIC = {
-    "gemm_fwd_gate_up": ("9199640349bb", (2.015109e9 + 20.168960e6) / 33, _GEMM_SRC),
-    "gemm_fwd_down": ("9199640349bb", (0.992911e9 + 61.100800e6) / 33, _GEMM_SRC),
-    "gemm_fwd_gate_up_mx": ("9199640349bb", (1.083810e9 + 20.746496e6) / 33, _GEMM_SRC),
-    "gemm_fwd_down_mx": ("9199640349bb", (0.519240e9 + 114.256640e6) / 33, _GEMM_SRC),
+    "gemm_fwd_gate_up": ("f2054d2aed7b", (2.015065e9 + 19.827712e6) / 33, _GEMM_SRC),
+    "gemm_fwd_down": ("f2054d2aed7b", (0.992473e9 + 61.332736e6) / 33, _GEMM_SRC),
+    "gemm_fwd_gate_up_mx": ("f2054d2aed7b", (1.080146e9 + 20.816640e6) / 33, _GEMM_SRC),
+    "gemm_fwd_down_mx": ("f2054d2aed7b", (0.519241e9 + 114.185216e6) / 33, _GEMM_SRC),
     # profiles/gemm_bwd_dsv3_train_slice_e32.md
-    "gemm_bwd_da": ("9199640349bb", (1.198978e9 + 0.101969e9) / 33, _GEMM_SRC),
-    "gemm_bwd_dx": ("9199640349bb", (2.064511e9 + 0.127574e9) / 33, _GEMM_SRC),
-    "gemm_bwd_dw": ("9199640349bb", (0.378173e9 + 2.851676e9) / 33, _GEMM_SRC),
+    "gemm_bwd_da": ("f2054d2aed7b", (1.198966e9 + 0.101213e9) / 33, _GEMM_SRC),
+    "gemm_bwd_dx": ("f2054d2aed7b", (2.062313e9 + 0.127839e9) / 33, _GEMM_SRC),
+    "gemm_bwd_dw": ("f2054d2aed7b", (0.378002e9 + 2.851659e9) / 33, _GEMM_SRC),
 }
 
 
