@@ -468,6 +468,9 @@ def run_mok(args, shape, rank, world, local_rank):
     e2e = None
     if not args.no_e2e and not shape.backward:
         e2e = run_e2e(args, mok, D, L, shape, dev, world)
+    graph = None
+    if not shape.backward and shape.dtype == "bf16":
+        graph = run_graph(args, mok, D, L, shape, dev, world)
     line = {
         "metric": "MoE-layer forward tokens/s" if not shape.backward else "MoE-layer fwd+bwd tokens/s",
         "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -478,7 +481,7 @@ def run_mok(args, shape, rank, world, local_rank):
         "tflops": res["tflops"], "tflops_frac_of_bf16_peak": res["tflops_frac_of_bf16_peak"],
         "roofline": res["roofline"], "kernels": res["kernels"], "kernel_timing": res["kernel_timing"],
         "gpu_launches": res["gpu_launches"],
-        "clocks": res["clocks"], "e2e": e2e,
+        "clocks": res["clocks"], "e2e": e2e, "cuda_graph": graph,
     }
     for key in ("fp8_cublas_tflops_measured", "tflops_frac_of_measured_fp8_gemm"):
         if key in res:
@@ -504,6 +507,42 @@ def run_mok(args, shape, rank, world, local_rank):
                 extra[name] = {"error": repr(exc)[:300]}
         line["workloads"] = extra
     return line
+
+
+def run_graph(args, mok, D, L, shape, dev, world):
+    """The same device-resident step replayed from a CUDA graph (route, pull schedule and expert
+    forward captured once): the launch-overhead-free time of the layer."""
+    import torch
+
+    layer = mok.MoELayer(D, L, dev)
+    x = L["x"]
+    for _ in range(max(args.warmup, 1)):
+        layer.forward(x)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer.forward(x)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(x)
+    for _ in range(max(args.warmup, 1)):
+        graph.replay()
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist_max(e0.elapsed_time(e1), world)
+    if mok.read_status(layer.ws) != 0:
+        raise RuntimeError("device status after the graph replays")
+    del graph, layer
+    return {"value": round(world * shape.T * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+            "ms_per_step": round(ms / args.steps, 4)}
 
 
 def run_e2e(args, mok, D, L, shape, dev, world):

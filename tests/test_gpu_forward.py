@@ -210,3 +210,51 @@ def test_host_entry_point_pageable_output():
     mok.layer_forward_host(D, L, xh, yh, wsh)
     torch.cuda.synchronize()
     assert torch.equal(yh, y_dev)
+
+
+def test_layer_is_cuda_graph_capturable():
+    """The entry points allocate nothing, synchronise nothing and take their stream from the
+    caller, so a whole training step (route, pull schedule, forward, backward) can be captured in
+    a CUDA graph and replayed: replays give the eager results bit for bit, also after new inputs
+    are copied into the captured buffers."""
+    ensure_lib()
+    shape = CASES["ragged_skew"].with_(backward=True)
+    L = to_dev(make_layer(shape, "cpu", with_dy=True))
+    D = dims_of(shape)
+    layer = mok.MoELayer(D, L)
+    x = L["x"].clone()
+    dY = L["dY"].clone()
+
+    def step():
+        y = layer.forward(x, training=True)
+        g = layer.backward(x, dY)
+        return y, g
+
+    y0, g0 = step()                      # eager: also sets up the backward workspace
+    y0, g0 = y0.clone(), {k: (v.clone() if v is not None else None) for k, v in g0.items()}
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        y, g = step()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert mok.read_status(layer.ws) == 0 and mok.read_status(layer._ws_bwd) == 0
+    assert torch.equal(y, y0)
+    for k, v in g0.items():
+        if v is not None:
+            assert torch.equal(g[k], v), k
+    # new inputs through the captured buffers
+    x2 = make_layer(shape.with_(cid=shape.cid + 100), "cpu", with_dy=True)
+    x.copy_(x2["x"].cuda())
+    dY.copy_(x2["dY"].cuda())
+    graph.replay()
+    torch.cuda.synchronize()
+    y_replay, dX_replay = y.clone(), g["dX"].clone()
+    y_eager, g_eager = step()
+    torch.cuda.synchronize()
+    assert torch.equal(y_replay, y_eager)
+    assert torch.equal(dX_replay, g_eager["dX"])
