@@ -1,6 +1,8 @@
 // Bandwidth-bound kernels of the MoE layer: the pull gather of token rows into each expert's
 // region, the fixed-order combine, and the router-weight backward.  One warp per row, 16-byte
 // vector accesses, grid-stride loops over a grid of a few blocks per SM.
+#include <type_traits>
+
 #include "mok_device.cuh"
 
 namespace mok {
@@ -74,9 +76,10 @@ cudaError_t launch_gather_rows(const char* name, const void* src0, const void* s
 // applied in the down-projection epilogue).  Page "Mixture-of-Kittens: Nhân kernel MoE ...",
 // section "Chồng lấp tính toán ...": the layer combines shared and routed expert outputs with
 // the router weights; the fixed order keeps the result bit-identical across runs.
-// One instantiation per k, so that the K + 1 row loads of a vector are unconditional and all in
-// flight together; a dropped route (inv_pos = -1) reads row 0 and is multiplied by zero.
-template <int K>
+// One instantiation per k (and per presence of Ysh2), so that the row loads of a vector are
+// unconditional and all in flight together; a dropped route (inv_pos = -1) reads row 0 and is
+// multiplied by zero.
+template <int K, bool ADD2>
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     int64_t T, int vec_per_row, const int32_t* __restrict__ topk_idx,
     const int32_t* __restrict__ inv_pos, const uint4* __restrict__ Ys, const uint4* __restrict__ Ysh,
@@ -122,13 +125,14 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
       q[0] = Ysh ? Ysh[t * vec_per_row + v] : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int j = 0; j < K; ++j) q[j + 1] = Ys[(int64_t)pos[j] * vec_per_row + v];
+      uint4 q2 = make_uint4(0, 0, 0, 0);
+      if constexpr (ADD2) q2 = Ysh2[t * vec_per_row + v];
       float acc[8];
       acc[0] = bf16_lo(q[0].x); acc[1] = bf16_hi(q[0].x); acc[2] = bf16_lo(q[0].y); acc[3] = bf16_hi(q[0].y);
       acc[4] = bf16_lo(q[0].z); acc[5] = bf16_hi(q[0].z); acc[6] = bf16_lo(q[0].w); acc[7] = bf16_hi(q[0].w);
-      if (Ysh2) {
-        const uint4 u = Ysh2[t * vec_per_row + v];
-        acc[0] += bf16_lo(u.x); acc[1] += bf16_hi(u.x); acc[2] += bf16_lo(u.y); acc[3] += bf16_hi(u.y);
-        acc[4] += bf16_lo(u.z); acc[5] += bf16_hi(u.z); acc[6] += bf16_lo(u.w); acc[7] += bf16_hi(u.w);
+      if constexpr (ADD2) {
+        acc[0] += bf16_lo(q2.x); acc[1] += bf16_hi(q2.x); acc[2] += bf16_lo(q2.y); acc[3] += bf16_hi(q2.y);
+        acc[4] += bf16_lo(q2.z); acc[5] += bf16_hi(q2.z); acc[6] += bf16_lo(q2.w); acc[7] += bf16_hi(q2.w);
       }
 #pragma unroll
       for (int j = 0; j < K; ++j) {
@@ -155,15 +159,22 @@ cudaError_t launch_combine(int64_t T, int d, int k, const int32_t* topk_idx, con
   auto yo = static_cast<uint4*>(y);
   const int grid = rows_grid(T * kCombineSplit);
   prof_begin("combine", s);
+  auto launch = [&](auto kk) {
+    constexpr int K = decltype(kk)::value;
+    if (ysh2)
+      combine_kernel<K, true><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo);
+    else
+      combine_kernel<K, false><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo);
+  };
   switch (k) {
-    case 1: combine_kernel<1><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
-    case 2: combine_kernel<2><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
-    case 3: combine_kernel<3><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
-    case 4: combine_kernel<4><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
-    case 5: combine_kernel<5><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
-    case 6: combine_kernel<6><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
-    case 7: combine_kernel<7><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
-    default: combine_kernel<8><<<grid, kRowThreads, 0, s>>>(T, d / 8, topk_idx, inv_pos, ys, ysh, ysh2, yo); break;
+    case 1: launch(std::integral_constant<int, 1>{}); break;
+    case 2: launch(std::integral_constant<int, 2>{}); break;
+    case 3: launch(std::integral_constant<int, 3>{}); break;
+    case 4: launch(std::integral_constant<int, 4>{}); break;
+    case 5: launch(std::integral_constant<int, 5>{}); break;
+    case 6: launch(std::integral_constant<int, 6>{}); break;
+    case 7: launch(std::integral_constant<int, 7>{}); break;
+    default: launch(std::integral_constant<int, 8>{}); break;
   }
   prof_end(s);
   return cudaGetLastError();
