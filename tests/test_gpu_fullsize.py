@@ -100,3 +100,12 @@ def test_fullsize_training_backward():
         assert_close(key, f64(g[key]), rs[key])
     # dW_router = x^T dlogits: consistent with the GPU's own dlogits (property at full size)
     assert_close("dW_router vs x^T dlogits", f64(g["dW_router"]), x64.T @ f64(g["dlogits"]))
+    _assert_dlogit_rows_sum_to_zero(g["dlogits"])
+
+
+def _assert_dlogit_rows_sum_to_zero(dlogits):
+    """Every token's logit gradient sums to zero: dl_m = w_m (dw_m - sum_j w_j dw_j) over the
+    selection and sum_m w_m = 1 (the renormalised softmax), a property of all T tokens."""
+    dl = f64(dlogits)
+    scale = np.abs(dl).sum(axis=1)
+    assert (np.abs(dl.sum(axis=1)) <= 1e-4 * scale + 1e-30).all()

@@ -311,6 +311,9 @@ def test_fullsize_mxfp8_training_sampled():
     for key in ("dWs_gate", "dWs_up", "dWs_down"):
         assert_close(key, f64(g[key]), rs[key], max_rel=tmax, mean_rel=tmean)
     assert_close("dW_router vs x^T dlogits", f64(g["dW_router"]), x64.T @ f64(g["dlogits"]))
+    # every token's logit gradient sums to zero (the renormalised softmax), all 8192 tokens
+    dl = f64(g["dlogits"])
+    assert (np.abs(dl.sum(axis=1)) <= 1e-4 * np.abs(dl).sum(axis=1) + 1e-30).all()
 
 
 @pytest.mark.parametrize("dtype", [mok.MOK_BF16, mok.MOK_MXFP8])
