@@ -101,3 +101,29 @@ def test_mxfp8_backward_sizes_and_argument_errors():
     assert rc == -1
     rc = L.mok_prepare_weights_bwd(ctypes.byref(Db), ctypes.byref(W), null, null)
     assert rc == 0                                           # bf16: nothing to prepare
+
+
+def test_plain_c_program_uses_the_abi():
+    """tests/c/abi_check.c, a C99 program that includes only mok.h, compiles with -std=c99
+    -pedantic -Werror, links against libmok.so and runs its host-side checks (no GPU work)."""
+    import shutil
+    import subprocess
+    import tempfile
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    ensure_lib()
+    pkg = os.path.dirname(mok.lib_path())
+    cuda_libs = [p for p in ("/usr/local/cuda/lib64", "/usr/local/cuda/lib") if os.path.isdir(p)]
+    with tempfile.TemporaryDirectory() as tmp:
+        exe = os.path.join(tmp, "abi_check")
+        cmd = [gcc, "-std=c99", "-pedantic", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+               os.path.join(ROOT, "tests", "c", "abi_check.c"), "-o", exe, mok.lib_path(),
+               "-Wl,-rpath," + pkg, "-Wl,--allow-shlib-undefined"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+        env = dict(os.environ)
+        env["LD_LIBRARY_PATH"] = ":".join(cuda_libs + [pkg, env.get("LD_LIBRARY_PATH", "")])
+        r = subprocess.run([exe], capture_output=True, text=True, env=env, timeout=60)
+        assert r.returncode == 0 and "abi_check ok" in r.stdout, r.stdout + r.stderr
