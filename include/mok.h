@@ -182,7 +182,9 @@ int mok_moe_forward(const mok_dims *dims, const mok_weights *w, const void *x,
  * dG, dU, W_gate, W_up along F, and for the weight gradients x, dG, dU, w*h and dY along each
  * expert's tokens (blocks of 32 from its first token, in token order) — with fp32 accumulation;
  * the router terms dlogits W_router^T and x^T dlogits stay bf16.  Needs w->prepared_bwd and a
- * `saved` from an MXFP8 forward; F % 256 == 0 and Fs % 256 == 0 (else MOK_ERR_UNSUPPORTED). */
+ * `saved` from an MXFP8 forward; F % 256 == 0, Fs % 256 == 0 and
+ * 2 (ceil(T k / 128) + E) d / 64 < 2^31 (T below about 150M tokens at d = 7168, k = 8), else
+ * MOK_ERR_UNSUPPORTED. */
 int mok_moe_backward(const mok_dims *dims, const mok_weights *w, const void *x, const void *dY,
                      const void *saved, const int32_t *topk_idx, const float *topk_w,
                      const int32_t *offsets, const int32_t *sorted_tok, const float *sorted_w,

@@ -962,6 +962,8 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
   }
   if (dims->dtype == MOK_MXFP8) {
     if (F % 256 || (sh && Fs % 256)) return MOK_ERR_UNSUPPORTED;  // 256-column tiles along F
+    // the token-axis quantiser numbers its 128 x 64 tiles (x and dY) in an int
+    if (2 * mx_nkb_routed(dims) * (d / 64) > 0x7fffffffLL) return MOK_ERR_UNSUPPORTED;
     rc = backward_mxfp8(dims, w, x, dY, saved, topk_idx, topk_w, offsets, sorted_tok, sorted_w,
                         inv_pos, dX, dW_gate, dW_up, dW_down, dWs_gate, dWs_up, dWs_down, dlogits,
                         dW_router, ws, s, &launches);

@@ -161,19 +161,19 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_tokens_kernel(const __grid
   const int64_t ld = 128 * (int64_t)tp.nkb;
   const int ncolt = C / kColTile;
   const int nkt = min(s_mt[E], tp.nkb);  // 128-token K blocks in use
-  const int64_t ntiles = (int64_t)tp.nops * nkt * ncolt;
+  const int ntiles = tp.nops * nkt * ncolt;  // below 2^31: checked by the launcher
   const int ch = tid & 7;
   // tile id -> operand, K block and first column (column tiles fastest: neighbouring blocks read
   // the same source rows)
-  auto decode = [&](int64_t id, int& op, int& kt, int& c0) {
-    op = (int)(id / ((int64_t)nkt * ncolt));
-    const int rest = (int)(id - (int64_t)op * nkt * ncolt);
+  auto decode = [&](int id, int& op, int& kt, int& c0) {
+    op = id / (nkt * ncolt);
+    const int rest = id - op * nkt * ncolt;
     kt = rest / ncolt;
     c0 = (rest - kt * ncolt) * kColTile;
   };
   // the tile's global loads, 128 rows x 64 columns: 8 threads per row, 16 bytes each, rows
   // tid / 8 + 32 j; rows past the expert's tokens are zeros
-  auto fetch = [&](int64_t id, uint4 (&u)[kTokTile / 32]) {
+  auto fetch = [&](int id, uint4 (&u)[kTokTile / 32]) {
     int op, kt, c0;
     decode(id, op, kt, c0);
     int lo = 0, hi = E;  // the expert of K block kt: largest e with s_mt[e] <= kt
@@ -196,9 +196,9 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_tokens_kernel(const __grid
     }
   };
   uint4 u[kTokTile / 32];
-  if ((int64_t)blockIdx.x < ntiles) fetch(blockIdx.x, u);
+  if ((int)blockIdx.x < ntiles) fetch(blockIdx.x, u);
   // two barriers per tile: the next tile's loads are in flight while this one is quantised
-  for (int64_t id = blockIdx.x; id < ntiles; id += gridDim.x) {
+  for (int id = blockIdx.x; id < ntiles; id += gridDim.x) {
     int op, kt, c0;
     decode(id, op, kt, c0);
 #pragma unroll
@@ -210,15 +210,14 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_tokens_kernel(const __grid
       tile[r][4 * ch + 3] = u[j].w;
     }
     __syncthreads();  // tile written; the previous tile's codes are out
-    if (id + gridDim.x < ntiles) fetch(id + gridDim.x, u);
+    if (id + (int)gridDim.x < ntiles) fetch(id + gridDim.x, u);
     {  // thread: column cc, 32-token block b
       const int cc = tid & (kColTile - 1), b = tid >> 6;
+      // the column's bf16 half of each word moved to the top 16 bits: one byte permute
+      const uint32_t sel = (cc & 1) ? 0x3244u : 0x1044u;
       float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t w2 = tile[32 * b + i][cc >> 1];
-        v[i] = (cc & 1) ? bf16_hi(w2) : bf16_lo(w2);
-      }
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(__byte_perm(tile[32 * b + i][cc >> 1], 0u, sel));
       uint32_t qq[8];
       sbytes[cc][b] = (uint8_t)mx_block32(v, qq);
       uint4* d = reinterpret_cast<uint4*>(&codes[cc][32 * b]);
@@ -244,6 +243,7 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_tokens_kernel(const __grid
 cudaError_t launch_mx_quantize_tokens(const TokQuantParams& tp, cudaStream_t s) {
   const int64_t bound = (int64_t)tp.nops * tp.nkb * (tp.C / kColTile);  // tiles, upper bound
   if (bound == 0) return cudaSuccess;
+  if (bound > 0x7fffffffLL) return cudaErrorInvalidValue;  // the kernel numbers tiles in an int
   // persistent: as many blocks as are resident at once (shared memory allows about seven per SM)
   static int per_sm = 0;
   if (per_sm == 0 &&
