@@ -338,3 +338,23 @@ def test_backward_with_no_tokens_zeroes_the_weight_gradients(dtype):
     for key in ("dW_gate", "dW_up", "dW_down", "dWs_gate", "dWs_up", "dWs_down", "dW_router"):
         assert not g[key].any(), key
     assert g["dX"].shape == (0, shape.d)
+
+
+def test_mxfp8_host_entry_point_matches_device_path():
+    """The host-buffer entry point with MXFP8 dims (prepared weights passed through) gives the
+    device path's y bit for bit."""
+    ensure_lib()
+    shape = CASES["ragged_mx"]
+    L = to_dev(make_layer(shape, "cpu"))
+    D = dims_of(shape, dtype=mok.MOK_MXFP8)
+    L["prepared"] = mok.prepare_weights(D, L)
+    ws = torch.zeros(mok.workspace_size(D), dtype=torch.uint8, device="cuda")
+    idx, w, _ = mok.route(D, L["x"], L["W_router"], L["bias"], ws)
+    y_dev = mok.moe_forward(D, L, L["x"], mok.dispatch_index(D, idx, w, ws), ws)
+    wsh = torch.zeros(mok.workspace_size(D) + mok.host_extra_size(D), dtype=torch.uint8, device="cuda")
+    xh = L["x"].cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    mok.layer_forward_host(D, L, xh, yh, wsh)
+    torch.cuda.synchronize()
+    assert mok.read_status(wsh) == 0
+    assert torch.equal(yh, y_dev.cpu())
