@@ -9,7 +9,7 @@ import torch
 import mixture_experts_layer_14_gb300 as mok
 import oracle
 from mixture_experts_layer_14_gb300.synthetic import WORKLOADS, LayerShape, make_layer
-from tests._helpers import assert_close, dims_of, ensure_lib, f64, to_dev
+from tests._helpers import MAX_REL, assert_close, dims_of, ensure_lib, f64, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +26,16 @@ CASES = {
     # the largest expert count and top-k the ABI accepts (E = 512, k = 8): the router GEMM's
     # N = 512 and dW_router's two 256-column tiles
     "max_E_k": LayerShape("max_E_k", 200, 256, 512, 8, 256, 256, 1, 0.0, "normal0.1", "bf16", True, 26),
+    # one token: every weight-gradient problem has K = 1 (the bounded maps return zeros past it)
+    "one_token": LayerShape("one_token", 1, 256, 16, 3, 256, 128, 1, 0.0, "normal0.1", "bf16", True, 27),
 }
+
+# With one token the mean error of dlogits is that token's own: dl_m = w_m (dw_m - sum_j w_j dw_j)
+# subtracts nearly equal terms, so the bf16 rounding of the saved G and U inside dw (about 2^-8
+# relative) is not averaged over tokens (measured: 0.51% on its three values), and dW_router =
+# x^T dlogits is then one outer product that carries the same relative error (0.55%).  The max
+# bound still applies.
+MEAN_OVERRIDE = {("one_token", "dlogits"): MAX_REL, ("one_token", "dW_router"): MAX_REL}
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -50,7 +59,10 @@ def test_backward_parity_and_determinism(name):
     ref = oracle.moe_backward(x, f64(L["dY"]), Wr, f64(L["W_gate"]), f64(L["W_up"]),
                               f64(L["W_down"]), shared, logits, idx)
     for key in ("dX", "dW_gate", "dW_up", "dW_down", "dlogits", "dW_router"):
-        assert_close(key, f64(g[key]), ref[key])
+        if (name, key) in MEAN_OVERRIDE:
+            assert_close(key, f64(g[key]), ref[key], mean_rel=MEAN_OVERRIDE[(name, key)])
+        else:
+            assert_close(key, f64(g[key]), ref[key])
     if shape.n_shared:
         for key in ("dWs_gate", "dWs_up", "dWs_down"):
             assert_close(key, f64(g[key]), ref[key])

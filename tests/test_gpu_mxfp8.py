@@ -179,6 +179,9 @@ BWD_CASES = {
     # the largest expert count and top-k: most experts hold a few tokens (one partial block each)
     "mx_train_max_E_k": LayerShape("mx_train_max_E_k", 200, 256, 512, 8, 256, 256, 1, 0.0, "normal0.1",
                                    "mxfp8", True, 44),
+    # one token: eight experts with one row each (one zero-padded block per expert)
+    "mx_train_one_token": LayerShape("mx_train_one_token", 1, 256, 16, 8, 256, 256, 1, 0.0, "normal0.1",
+                                     "mxfp8", True, 45),
 }
 
 
