@@ -2,7 +2,7 @@
 
 * Quantiser (mok_mx_quantize_rows) and prepared weights (mok_prepare_weights): bit-exact codes
   and scale bytes against the oracle's quantiser on the same bf16 values.
-* Forward: within max|d| <= 6e-2 max|ref| (and a mean relative error <= 1e-2) of the oracle's
+* Forward: within max|d| <= 2e-2 max|ref| (and a mean relative error <= 5e-3) of the oracle's
   MXFP8 reading, which quantises x, the weights and h exactly where the method does and computes
   in float64; bit-identical reruns.  The distance to the unquantised float64 layer is reported
   and bounded by the oracle's own MXFP8-vs-float64 distance plus 1e-2: E4M3 rounding of random-
@@ -21,7 +21,12 @@ from tests._helpers import LazyExperts, assert_close, dims_of, ensure_lib, error
 
 pytestmark = pytest.mark.gpu
 
-MX_MAX_REL = 6e-2
+# Against the oracle's MXFP8 reading (quantisation where the path quantises, float64 sums) the
+# forward output sits 0.36-0.43% (max) and 0.20-0.22% (mean) away, full size included: h codes
+# differ where the GPU's fp32 h and the oracle's float64 h straddle a rounding point.  Bars: the
+# bf16 ones.
+MX_MAX_REL = 2e-2
+MX_MEAN_REL = 5e-3
 
 
 def _edge_rows():
@@ -132,7 +137,7 @@ def test_mxfp8_forward_parity(name):
     Wg, Wu, Wd = f64(L["W_gate"]), f64(L["W_up"]), f64(L["W_down"])
     y_ref = oracle.moe_forward(x, Wg, Wu, Wd, sh, got, wr)
     y_mx = oracle.moe_forward_mxfp8(x, Wg, Wu, Wd, sh, got, wr)
-    mx, mn = assert_close("y vs MXFP8 reading", f64(y), y_mx, max_rel=MX_MAX_REL, mean_rel=1e-2)
+    mx, mn = assert_close("y vs MXFP8 reading", f64(y), y_mx, max_rel=MX_MAX_REL, mean_rel=MX_MEAN_REL)
     own_mx, own_mn = errors(y_mx, y_ref)
     mx2, mn2 = assert_close("y vs float64", f64(y), y_ref, max_rel=own_mx + 1e-2, mean_rel=own_mn + 1e-2)
     print(f"{name}: vs MXFP8 reading max_rel {mx:.2e} mean_rel {mn:.2e}; vs float64 {mx2:.2e} "
@@ -156,7 +161,9 @@ def test_fullsize_mxfp8_forward_sampled():
     sh = (f64(L["Ws_gate"]), f64(L["Ws_up"]), f64(L["Ws_down"]))
     Wg, Wu, Wd = LazyExperts(L["W_gate"]), LazyExperts(L["W_up"]), LazyExperts(L["W_down"])
     y_mx = oracle.moe_forward_mxfp8(x, Wg, Wu, Wd, sh, got[toks], wr)
-    assert_close("y sampled vs MXFP8 reading", f64(y[toks]), y_mx, max_rel=MX_MAX_REL, mean_rel=1e-2)
+    mx, mn = assert_close("y sampled vs MXFP8 reading", f64(y[toks]), y_mx, max_rel=MX_MAX_REL,
+                          mean_rel=MX_MEAN_REL)
+    print(f"dsv3_mxfp8_fwd sampled: vs MXFP8 reading max_rel {mx:.2e} mean_rel {mn:.2e}")
 
 
 # The MXFP8 backward re-quantises dG, dU and w h, computed from G and U as the forward stores
