@@ -244,12 +244,18 @@ cudaError_t launch_mx_quantize_tokens(const TokQuantParams& tp, cudaStream_t s) 
   const int64_t bound = (int64_t)tp.nops * tp.nkb * (tp.C / kColTile);  // tiles, upper bound
   if (bound == 0) return cudaSuccess;
   if (bound > 0x7fffffffLL) return cudaErrorInvalidValue;  // the kernel numbers tiles in an int
-  // persistent: as many blocks as are resident at once (shared memory allows about seven per SM)
-  static int per_sm = 0;
-  if (per_sm == 0 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_quantize_tokens_kernel, 256, 0) !=
-          cudaSuccess)
-    per_sm = 4;
+  // persistent: as many blocks as are resident at once, a property of this kernel on this device
+  static int per_sm_of_device[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  int per_sm = per_sm_of_device[dev];
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_quantize_tokens_kernel, 256, 0) !=
+            cudaSuccess ||
+        per_sm <= 0)
+      per_sm = 4;
+    per_sm_of_device[dev] = per_sm;
+  }
   const int64_t blocks = std::min<int64_t>(bound, (int64_t)num_sms() * std::max(per_sm, 1));
   prof_begin("mx_quantize_tokens", s);
   mx_quantize_tokens_kernel<<<(int)blocks, 256, 0, s>>>(tp);
