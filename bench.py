@@ -1,13 +1,13 @@
 #!/usr/bin/env python
-"""Benchmark of the GB300 MoE layer (forward of a DeepSeek-V3-shaped layer by default).
+"""Benchmark of the GB300 MoE layer (forward of a Kimi-class layer with skewed routing by default).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl mok|reference]
 
 One step = one pass of the whole layer forward over one batch of T tokens: router GEMM + top-k,
 pull-schedule counting sort, pull gather, gate/up GEMM + SwiGLU, down GEMM + router weight,
 fixed-order combine (training workloads add the backward).  Inputs are synthetic, seeded, and
-resident in HBM before the timed region; the 22+ GB of expert weights read every step exceed the
-129 MB L2, so no explicit flush is needed.  Prints ONE JSON line on rank 0.
+resident in HBM before the timed region; the gigabytes of expert weights read every step exceed
+the 129 MB L2, so no explicit flush is needed.  Prints ONE JSON line on rank 0.
 
 --impl reference times the float64 CPU oracle (as it stands) on the host cores on a bounded
 sample of the same workload, one sampled token per step.
@@ -152,9 +152,11 @@ def work_model(shape, counts):
     m["route"] = {"flops": 2.0 * T * d * E, "bytes": wb * (T * d + d * E) + 8.0 * T * k}
     # x is read once (repeated rows of a token hit L2), every destination row written once
     m["gather"] = {"flops": 0.0, "bytes": wb * (T * d + R * d) + 4.0 * R}
+    # gate/up: the active weight sets, x once (the re-reads of a token's gathered rows are the
+    # kernel's own materialisation, not algorithmic), h written (and G, U saved for training)
     m["gemm_fwd_gate_up"] = {
         "flops": 2.0 * (R * 2 * F * d + T * ns * 2 * Fs * d),
-        "bytes": wb * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + Rs * d + Hs * (3 if train else 1))}
+        "bytes": wb * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + T * d + Hs * (3 if train else 1))}
     m["gemm_fwd_down"] = {
         "flops": 2.0 * (R * F * d + T * ns * Fs * d),
         "bytes": wb * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Hs + Rs * d)}
@@ -166,7 +168,7 @@ def work_model(shape, counts):
         m["gather_bytes"] = {"flops": 0.0, "bytes": wq * (T * d + R * d) + 4.0 * R}
         m["gemm_fwd_gate_up_mx"] = {
             "flops": m["gemm_fwd_gate_up"]["flops"], "dtype": "fp8",
-            "bytes": wq * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + Rs * d + Hs)}
+            "bytes": wq * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + T * d + Hs)}
         m["gemm_fwd_down_mx"] = {
             "flops": m["gemm_fwd_down"]["flops"], "dtype": "fp8",
             "bytes": wq * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Hs) + wb * Rs * d}
@@ -205,18 +207,16 @@ def work_model(shape, counts):
     return m, layer_flops, e_act
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures, per weight set
-# streamed (routed experts with tokens + shared expert), valid only while the kernel source is
-# the one that was captured (sha1 prefix).  Sources: profiles/gemm_fwd_gate_up_dsv3_slice_e32.md,
-# profiles/gemm_fwd_mxfp8_dsv3_mxfp8_slice_e32.md and profiles/gemm_bwd_dsv3_train_slice_e32.md
-# (32-expert slices: 33 weight sets).
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from ncu slice captures of the
+# DeepSeek-V3-shaped workloads (32-expert slices with the same rows per expert: 33 weight sets),
+# per weight set streamed (routed experts with tokens + shared expert), valid only while the
+# kernel source is the one that was captured (sha1 prefix).
 _GEMM_SRC = "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"
 PROFILED_TRAFFIC = {
     "gemm_fwd_gate_up": ("f2054d2aed7b", (2.015065e9 + 19.827712e6) / 33, _GEMM_SRC),
     "gemm_fwd_down": ("f2054d2aed7b", (0.992473e9 + 61.332736e6) / 33, _GEMM_SRC),
     "gemm_fwd_gate_up_mx": ("f2054d2aed7b", (1.080146e9 + 20.816640e6) / 33, _GEMM_SRC),
     "gemm_fwd_down_mx": ("f2054d2aed7b", (0.519241e9 + 114.185216e6) / 33, _GEMM_SRC),
-    # profiles/gemm_bwd_dsv3_train_slice_e32.md
     "gemm_bwd_da": ("f2054d2aed7b", (1.198966e9 + 0.101213e9) / 33, _GEMM_SRC),
     "gemm_bwd_dx": ("f2054d2aed7b", (2.062313e9 + 0.127839e9) / 33, _GEMM_SRC),
     "gemm_bwd_dw": ("f2054d2aed7b", (0.378002e9 + 2.851659e9) / 33, _GEMM_SRC),
@@ -235,6 +235,19 @@ def profiled_traffic(name, weight_sets):
     return per_set * weight_sets
 
 
+# What each forward kernel's algorithmic bytes count (a kernel's own re-reads of rows it
+# materialised, e.g. gathered token rows read once per N tile, are not counted).
+BYTE_BASIS = {
+    "gemm_fwd_gate_up": "active gate+up weight sets + x once (T d) + h written (+ G, U saved)",
+    "gemm_fwd_gate_up_mx": "active gate+up E4M3 weights and scales + x codes once + h codes written",
+    "gemm_fwd_down": "active down weight sets + h read + router-weighted rows Y_s written",
+    "gemm_fwd_down_mx": "active down E4M3 weights and scales + h codes read + Y_s written",
+    "combine": "(k + 1) rows read + one row written per token",
+    "gather": "x read once + every destination row written",
+    "route": "x read once + W_router + top-k written",
+}
+
+
 def roofline_of(name, model, ms_per_launch, peaks):
     w = model[name]
     # an FP8 contraction takes the measured bf16 peak times the nominal fp8/bf16 ratio (2)
@@ -248,8 +261,11 @@ def roofline_of(name, model, ms_per_launch, peaks):
                 "unit": "TFLOP/s", "frac": achieved / tpeak, "algorithmic_per_launch": w["flops"],
                 "peak_dtype": w.get("dtype", "bf16")}
     achieved = w["bytes"] / secs / 1e9
-    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "algorithmic_per_launch": w["bytes"]}
+    out = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": achieved / peaks["hbm_gbs"], "algorithmic_per_launch": w["bytes"]}
+    if name in BYTE_BASIS:
+        out["bytes_basis"] = BYTE_BASIS[name]
+    return out
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
@@ -446,12 +462,26 @@ def fp8_cublas_tflops(dev):
         return None
 
 
-def config_of(shape, world, e_act):
+def weight_bytes_per_step(shape, counts):
+    """Bytes of expert weights one forward streams: every active routed expert and the shared."""
+    b = 1.0 + 1.0 / 32 if shape.dtype == "mxfp8" else 2.0
+    e_act = sum(1 for c in counts if c > 0)
+    return b * 3.0 * shape.d * (e_act * shape.F + shape.n_shared * shape.F_shared)
+
+
+def config_of(shape, world):
+    """The workload definition (identical in both arms); routing statistics are reported apart."""
     return {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E, "k": shape.k,
             "F": shape.F, "F_shared": shape.F_shared, "n_shared": shape.n_shared,
-            "router_bias": shape.bias, "active_experts": e_act,
+            "router_bias": shape.bias, "pass": "fwd+bwd" if shape.backward else "fwd",
+            "expert_gemms": shape.dtype,
             "global_batch_tokens": world * shape.T, "parallelism": f"replicas x{world}",
-            "l2": "inputs larger than L2: every step streams >22 GB of expert weights"}
+            "l2": "inputs larger than L2: every step streams the active experts' weights "
+                  "(gigabytes) through the 129 MB L2, no flush needed"}
+
+
+def metric_of(shape):
+    return "MoE-layer fwd+bwd tokens/s" if shape.backward else "MoE-layer forward tokens/s"
 
 
 def run_mok(args, shape, rank, world, local_rank):
@@ -472,12 +502,14 @@ def run_mok(args, shape, rank, world, local_rank):
     if not shape.backward and shape.dtype == "bf16":
         graph = run_graph(args, mok, D, L, shape, dev, world)
     line = {
-        "metric": "MoE-layer forward tokens/s" if not shape.backward else "MoE-layer fwd+bwd tokens/s",
+        "metric": metric_of(shape),
         "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,1/sqrt(fan_in)) bf16 weights, random init)",
-        "config": config_of(shape, world, res["active_experts"]),
+        "config": config_of(shape, world),
+        "routing": {k2: res[k2] for k2 in ("active_experts", "max_expert_rows", "empty_experts",
+                                           "weight_gb_per_step")},
         "tflops": res["tflops"], "tflops_frac_of_bf16_peak": res["tflops_frac_of_bf16_peak"],
         "roofline": res["roofline"], "kernels": res["kernels"], "kernel_timing": res["kernel_timing"],
         "gpu_launches": res["gpu_launches"],
@@ -499,8 +531,7 @@ def run_mok(args, shape, rank, world, local_rank):
                 r, Lx = measure(args, WORKLOADS[name], min(args.steps, args.extra_steps), 3, dev, world, peaks)
                 del Lx
                 torch.cuda.empty_cache()
-                r["metric"] = ("MoE-layer fwd+bwd tokens/s" if WORKLOADS[name].backward
-                               else "MoE-layer forward tokens/s")
+                r["metric"] = metric_of(WORKLOADS[name])
                 r["kernels"] = {k2: v for k2, v in list(r["kernels"].items())[:6]}
                 extra[name] = r
             except Exception as exc:  # report, do not hide the headline
@@ -595,12 +626,11 @@ def run_reference(args, shape, rank, world, local_rank):
               f"(T={shape.T}): float64 router, pull schedule, {shape.k} routed experts + shared, "
               f"combine; weights converted to float64 once, untimed")
     return {
-        "metric": "MoE-layer forward tokens/s", "value": round(value, 3), "unit": "tokens/s",
+        "metric": metric_of(shape), "value": round(value, 3), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E, "k": shape.k,
-                   "F": shape.F, "F_shared": shape.F_shared},
+        "config": config_of(shape, world),
         "impl": "reference",
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": oracle_cores(),
                          "kind": "oracle", "sample": sample},
@@ -617,12 +647,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
-    ap.add_argument("--workload", default="dsv3_bf16_fwd", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="kimi_skew_bf16_fwd", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
-    ap.add_argument("--extra", default="dsv3_bf16_train,kimi_skew_bf16_fwd,dsv3_mxfp8_fwd,"
+    ap.add_argument("--extra", default="dsv3_bf16_fwd,dsv3_bf16_train,dsv3_mxfp8_fwd,"
                     "dsv3_mxfp8_train,dsv3_decode_t64")
     ap.add_argument("--extra-steps", type=int, default=30)
     args = ap.parse_args(argv)

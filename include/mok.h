@@ -222,21 +222,24 @@ int mok_clear_device_status(void *ws, mok_stream_t stream);
  * host thread (for launch accounting in benchmarks). */
 int mok_last_launch_count(void);
 
-/* Pull schedule without a workspace: same inputs, outputs and results as mok_dispatch_index,
- * but the scratch it needs (a status word and the per-chunk expert histogram) lives in a
- * 1 MiB device array owned by the library, so the call allocates nothing and takes no `ws`.
- * The pages describe no such variant; it exists for callers that may not allocate device
- * memory when they build the routing (a runtime that reserves all memory at start-up, or code
- * that must not trigger the device-wide synchronisation of cudaMalloc/cudaFree).
- *  - Limit: 64 + E * ceil(T / 64) int32 words must fit in 1 MiB (e.g. T <= 64K tokens at
- *    E = 256); larger sizes return MOK_ERR_WORKSPACE and enqueue nothing.
+/* Pull schedule without a workspace: same inputs as mok_dispatch_index and, for valid inputs,
+ * the same outputs, but the scratch it needs (a status word and the per-chunk expert histogram)
+ * lives in a device array owned by the library (a 256-byte header plus a 1 MiB histogram), so
+ * the call allocates nothing and takes no `ws`.  The pages describe no such variant; it exists
+ * for callers that may not allocate device memory when they build the routing (a runtime that
+ * reserves all memory at start-up, or code that must not trigger the device-wide
+ * synchronisation of cudaMalloc/cudaFree).
+ *  - Limit: E * ceil(T / 64) <= 262144 (T <= 65536 tokens at E = 256, T <= 32768 at E = 512);
+ *    larger sizes return MOK_ERR_WORKSPACE and enqueue nothing.
  *  - The first call on each device looks up the array's device address (with that device
  *    current) and caches it; make that first call before any stream capture.
  *  - Every device holds the array until the process exits.  All calls on a device share it
  *    and it keeps the last call's contents, so calls whose GPU work overlaps (different
  *    streams, no ordering between them) race; order them on one stream.
- *  - An expert index outside [0,E) drops that route (inv_pos = -1, offsets[E] < T*k); the
- *    status word of this variant is internal and is not reported. */
+ *  - Invalid routing is not reported: an expert index outside [0,E) drops that route
+ *    (inv_pos = -1, offsets[E] < T*k), where mok_dispatch_index would also set
+ *    MOK_ERR_DEVICE_CHECK in its workspace status word.  Callers that cannot vouch for their
+ *    indices can compare offsets[E] with T*k. */
 int mok_dispatch_index_noalloc(const mok_dims *dims, const int32_t *topk_idx, const float *topk_w,
                                int32_t *counts, int32_t *offsets, int32_t *sorted_tok,
                                float *sorted_w, int32_t *inv_pos, mok_stream_t stream);

@@ -117,14 +117,14 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def _want(t, name, shape, dtype, device):
+def _want(t, name, shape, dtype, device, check_device=True):
     if t is None:
         raise ValueError(f"{name} is required")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
     if t.dtype != dtype:
         raise ValueError(f"{name}: dtype {t.dtype} != {dtype}")
-    if not t.is_cuda or (device is not None and t.device != device):
+    if check_device and (not t.is_cuda or (device is not None and t.device != device)):
         raise ValueError(f"{name} must live on {device}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -247,7 +247,19 @@ def dispatch_index(D, topk_idx, topk_w, ws):
 def dispatch_index_noalloc(D, topk_idx, topk_w, out):
     """Pull schedule into the caller's preallocated tensors ``out`` (same keys as the dict of
     :func:`dispatch_index`) without a workspace: for callers that may not allocate device memory
-    while routing.  The library keeps its scratch in a fixed 1 MiB device array."""
+    while routing.  The library keeps its scratch in a fixed device array (1 MiB of histogram),
+    looked up for the current device, so every tensor must live there."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cuda"
+    R = D.T * D.k
+    specs = [(topk_idx, "topk_idx", (D.T, D.k), torch.int32), (topk_w, "topk_w", (D.T, D.k), torch.float32)]
+    for key, shape, dtype in (("counts", (D.E,), torch.int32), ("offsets", (D.E + 1,), torch.int32),
+                              ("sorted_tok", (R,), torch.int32), ("sorted_w", (R,), torch.float32),
+                              ("inv_pos", (D.T, D.k), torch.int32)):
+        specs.append((out.get(key), f"out[{key!r}]", shape, dtype))
+    for t, name, shape, dtype in specs:      # every shape and dtype first, then the devices
+        _want(t, name, shape, dtype, None, check_device=False)
+    for t, name, shape, dtype in specs:
+        _want(t, name, shape, dtype, dev)
     _check(lib().mok_dispatch_index_noalloc(
         ctypes.byref(D), _ptr(topk_idx), _ptr(topk_w), _ptr(out["counts"]), _ptr(out["offsets"]),
         _ptr(out["sorted_tok"]), _ptr(out["sorted_w"]), _ptr(out["inv_pos"]), _stream()))

@@ -12,11 +12,13 @@
 
 namespace mok {
 
-// Scratch of the no-allocation dispatch: word 0 is the status word of the call, the histogram
-// of (expert, token block) counts starts at word 64.  Every device that loads the library keeps
-// this array until the process exits.
-constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
-static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
+// Scratch of the no-allocation dispatch: a 256-byte header (word 0 is the status word of the
+// call) followed by a 1 MiB histogram of (expert, token block) counts, so that E * ceil(T / 64)
+// counts fit when that product is at most 262144 (T = 65536 at E = 256).  Every device that
+// loads the library keeps this array until the process exits.
+constexpr int kNoAllocHeaderWords = 64;
+constexpr size_t kNoAllocHistWords = size_t(1) << 18;
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocHeaderWords + kNoAllocHistWords];
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -54,8 +56,8 @@ extern "C" int mok_dispatch_index_noalloc(const mok_dims* dims, const int32_t* t
       (dims->T > 0 && (!topk_idx || !topk_w || !sorted_tok || !sorted_w || !inv_pos)))
     return MOK_ERR_INVALID_ARG;
   const int64_t nblk = (dims->T + kDispatchChunk - 1) / kDispatchChunk;
-  const int64_t words = 64 + (int64_t)dims->E * (nblk > 0 ? nblk : 1);
-  if ((size_t)words * sizeof(int32_t) > kNoAllocScratchBytes) return MOK_ERR_WORKSPACE;
+  const int64_t hist_words = (int64_t)dims->E * (nblk > 0 ? nblk : 1);
+  if ((size_t)hist_words > kNoAllocHistWords) return MOK_ERR_WORKSPACE;
 
   int32_t* scratch = scratch_on_current_device();
   if (!scratch) return MOK_ERR_CUDA;
@@ -65,6 +67,6 @@ extern "C" int mok_dispatch_index_noalloc(const mok_dims* dims, const int32_t* t
   int n = 0;
   const cudaError_t e =
       launch_dispatch(dims->T, dims->E, dims->k, topk_idx, topk_w, counts, offsets, sorted_tok,
-                      sorted_w, inv_pos, scratch + 64, scratch, s, &n);
+                      sorted_w, inv_pos, scratch + kNoAllocHeaderWords, scratch, s, &n);
   return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
 }

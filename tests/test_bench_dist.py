@@ -8,6 +8,7 @@ import pytest
 import torch.multiprocessing as mp
 
 import bench
+from mixture_experts_layer_14_gb300.synthetic import WORKLOADS
 
 
 def _free_port():
@@ -66,18 +67,22 @@ def test_reference_arm_prints_the_contract_line(capsys):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["config"]["workload"] == "tiny"
+    # the same workload definition as the GB300 arm's line, key for key
+    assert line["config"] == bench.config_of(WORKLOADS["tiny"], 1)
+    assert line["metric"] == bench.metric_of(WORKLOADS["tiny"])
 
 
 def test_work_model_matches_the_stated_algorithmic_bytes():
     """The algorithmic bytes and FLOPs behind the roofline fractions, for the DSV3 forward with
-    every expert active: gate/up 15.77 GB and 2.17 TFLOP, down 8.23 GB, combine 587 MB, gather
-    529 MB."""
-    from mixture_experts_layer_14_gb300.synthetic import WORKLOADS
+    every expert active: gate/up 15.30 GB (257 weight sets, x once, h written) and 2.17 TFLOP,
+    down 8.23 GB, combine 587 MB, gather 529 MB."""
 
     shape = WORKLOADS["dsv3_bf16_fwd"]
     m, flops, e_act = bench.work_model(shape, [128] * shape.E)
     assert e_act == 256
-    assert m["gemm_fwd_gate_up"]["bytes"] == pytest.approx(15.77e9, rel=2e-3)
+    assert m["gemm_fwd_gate_up"]["bytes"] == pytest.approx(
+        2 * (257 * 2 * 7168 * 2048 + 4096 * 7168 + 9 * 4096 * 2048), rel=1e-12)
+    assert m["gemm_fwd_gate_up"]["bytes"] == pytest.approx(15.30e9, rel=2e-3)
     assert m["gemm_fwd_gate_up"]["flops"] == pytest.approx(2.17e12, rel=5e-3)
     assert m["gemm_fwd_down"]["bytes"] == pytest.approx(8.23e9, rel=2e-3)
     assert m["combine"]["bytes"] == pytest.approx(587e6, rel=2e-3)
