@@ -166,9 +166,10 @@ def work_model(shape, counts):
         wq = 1.0 + 1.0 / 32  # E4M3 byte + one UE8M0 byte per 32
         m["mx_quantize"] = {"flops": 0.0, "bytes": T * d * (wb + wq)}
         m["gather_bytes"] = {"flops": 0.0, "bytes": wq * (T * d + R * d) + 4.0 * R}
-        m["gemm_fwd_gate_up_mx"] = {
+        m["gemm_fwd_gate_up_mx"] = {  # (training: G and U saved in fp32)
             "flops": m["gemm_fwd_gate_up"]["flops"], "dtype": "fp8",
-            "bytes": wq * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + T * d + Hs)}
+            "bytes": wq * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + T * d + Hs)
+            + (8.0 * Hs if train else 0.0)}
         m["gemm_fwd_down_mx"] = {
             "flops": m["gemm_fwd_down"]["flops"], "dtype": "fp8",
             "bytes": wq * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Hs) + wb * Rs * d}
@@ -187,11 +188,11 @@ def work_model(shape, counts):
         if shape.dtype == "mxfp8":
             wq = 1.0 + 1.0 / 32
             ops_t = 2.0 * Rs * d + 3.0 * Hs  # token-axis operands: x, dY, dG, dU, w*h
-            m["gemm_bwd_da_mx"] = {  # reads dY codes, W_down codes, G, U; writes the codes of
+            m["gemm_bwd_da_mx"] = {  # reads dY codes, W_down codes, fp32 G, U; writes the codes of
                 # dG, dU along F and of dG, dU, w*h along tokens
                 "flops": m["gemm_bwd_da"]["flops"], "dtype": "fp8",
                 "bytes": wq * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Rs * d + 5.0 * Hs)
-                + wb * 2.0 * Hs + 4.0 * R * (F // 128)}
+                + 4.0 * 2.0 * Hs + 4.0 * R * (F // 128)}
             m["gemm_bwd_dx_mx"] = {
                 "flops": 2.0 * (R * 2 * F * d + T * ns * 2 * Fs * d), "dtype": "fp8",
                 "bytes": wq * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs + 2.0 * Hs) + wb * Rs * d}
@@ -248,10 +249,15 @@ BYTE_BASIS = {
 }
 
 
-def roofline_of(name, model, ms_per_launch, peaks):
+SUSTAINED_AFTER_MS = 2000.0  # timed regions this long run under the power cap: sustained peak
+
+
+def roofline_of(name, model, ms_per_launch, peaks, sustained=False):
     w = model[name]
-    # an FP8 contraction takes the measured bf16 peak times the nominal fp8/bf16 ratio (2)
-    tpeak = peaks["bf16_tflops"] * (2.0 if w.get("dtype") == "fp8" else 1.0)
+    # the measured bf16 peak (burst for a short timed region, the seconds-long sustained figure
+    # for a long one); an FP8 contraction takes it times the nominal fp8/bf16 ratio (2)
+    base = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) if sustained else peaks["bf16_tflops"]
+    tpeak = base * (2.0 if w.get("dtype") == "fp8" else 1.0)
     t_flop = w["flops"] / (tpeak * 1e12) if w["flops"] else 0.0
     t_byte = w["bytes"] / (peaks["hbm_gbs"] * 1e9)
     secs = ms_per_launch / 1e3
@@ -259,7 +265,8 @@ def roofline_of(name, model, ms_per_launch, peaks):
         achieved = w["flops"] / secs / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": tpeak,
                 "unit": "TFLOP/s", "frac": achieved / tpeak, "algorithmic_per_launch": w["flops"],
-                "peak_dtype": w.get("dtype", "bf16")}
+                "peak_dtype": w.get("dtype", "bf16"),
+                "peak_kind": "sustained (power-capped loop)" if sustained else "burst"}
     achieved = w["bytes"] / secs / 1e9
     out = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
            "frac": achieved / peaks["hbm_gbs"], "algorithmic_per_launch": w["bytes"]}
@@ -395,19 +402,20 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
     ms_max = dist_max(ms, world)
 
     model, layer_flops, e_act = work_model(shape, counts)
+    sustained = ms >= SUSTAINED_AFTER_MS
     kernels = {}
     for name, (n, tms) in sorted(kern.items(), key=lambda kv: -kv[1][1]):
         entry = {"launches": n, "ms_total": round(tms, 4), "ms_per_launch": round(tms / max(n, 1), 5),
                  "share": round((tms / max(sampled, 1)) / max(ms / steps, 1e-9), 4)}
         if name in model:
-            r = roofline_of(name, model, tms / max(n, 1), peaks)
+            r = roofline_of(name, model, tms / max(n, 1), peaks, sustained)
             if not shape.backward:
                 r["traffic"] = profiled_traffic(name, e_act + shape.n_shared)
             entry["roofline"] = {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in r.items()}
         kernels[name] = entry
     dominant = max((n for n in kern if n in model), key=lambda n: kern[n][1])
     dn, dms = kern[dominant]
-    roof = roofline_of(dominant, model, dms / dn, peaks)
+    roof = roofline_of(dominant, model, dms / dn, peaks, sustained)
     roof.update({"kernel": dominant, "traffic": profiled_traffic(dominant, e_act + shape.n_shared)
                  if not shape.backward else None,
                  "peak_source": "measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
@@ -425,6 +433,7 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
         "kernels": kernels, "kernel_timing": f"CUDA events on {sampled} of the {steps} timed steps",
         "gpu_launches": launches, "clocks": clocks,
         "active_experts": e_act, "max_expert_rows": max(counts), "empty_experts": counts.count(0),
+        "weight_gb_per_step": round(weight_bytes_per_step(shape, counts) / 1e9, 3),
     }
     if mx:  # context: the library's dense fp8 GEMM rate on this GPU (the roofline keeps 2 x bf16)
         f8 = fp8_cublas_tflops(dev)

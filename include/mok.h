@@ -92,8 +92,9 @@ typedef struct {
  * mok_moe_backward).  Returns 0 for invalid dims. */
 size_t mok_workspace_size(const mok_dims *dims, int pass);
 
-/* Bytes of the activations mok_moe_forward saves for mok_moe_backward (G and U, bf16, for the
- * routed rows and the shared expert; with MOK_BF16 also x in expert order). */
+/* Bytes of the activations mok_moe_forward saves for mok_moe_backward: G and U for the routed
+ * rows and the shared expert (bf16 for MOK_BF16, fp32 for MOK_MXFP8, whose backward quantises
+ * dG, dU and w*h derived from them), and with MOK_BF16 also x in expert order. */
 size_t mok_saved_size(const mok_dims *dims);
 
 /* Bytes of the prepared-weights buffer for dims->dtype (0 for MOK_BF16). */
@@ -163,8 +164,8 @@ int mok_dispatch_index(const mok_dims *dims, const int32_t *topk_idx, const floa
  * ascending expert order on top of the shared-expert row (fp32 accumulation, one bf16
  * rounding).
  *   -> y[T,d] bf16.  `saved` (mok_saved_size bytes or NULL) receives what the backward needs:
- *   G and U (for MOK_MXFP8 the block-scaled products, in bf16), and for MOK_BF16 x in expert
- *   order. */
+ *   G and U (bf16; for MOK_MXFP8 the block-scaled products in fp32), and for MOK_BF16 x in
+ *   expert order. */
 int mok_moe_forward(const mok_dims *dims, const mok_weights *w, const void *x,
                     const int32_t *topk_idx, const int32_t *offsets, const int32_t *sorted_tok,
                     const float *sorted_w, const int32_t *inv_pos, void *y, void *saved,
@@ -207,6 +208,23 @@ int mok_moe_backward(const mok_dims *dims, const mok_weights *w, const void *x, 
 size_t mok_layer_host_extra_size(const mok_dims *dims);
 int mok_layer_forward_host(const mok_dims *dims, const mok_weights *w, const void *x_host,
                            void *y_host, void *ws, size_t ws_bytes, mok_stream_t stream);
+
+/* Schedule of the bf16 expert GEMMs of mok_moe_forward (process-wide; default
+ * MOK_SCHEDULE_TWO_LAUNCHES):
+ *  - MOK_SCHEDULE_TWO_LAUNCHES: gate/up + SwiGLU, then down + router weight, each one persistent
+ *    launch whose CTAs take the tiles c, c + grid, c + 2 grid, ...
+ *  - MOK_SCHEDULE_FUSED: both phases in one persistent launch.  CTAs claim tiles in order from a
+ *    device work counter (every gate/up tile before any down tile) and a down tile first waits,
+ *    bounded, until every gate/up tile of its M tile has written its h rows (a readiness counter
+ *    per M tile).  This is the fused, device-scheduled form of the layer's kernel (page
+ *    "Mixture-of-Kittens: Nhân kernel MoE ...", intro and section "Lập lịch"; page
+ *    "Mixture-of-Kittens; MoE megakernel", key points); on one GPU it measured about 1% slower
+ *    than two launches at the DeepSeek-V3 shape, hence not the default.
+ * Results are bit-identical under both.  Shapes run in CTA pairs (at least 320 routed rows per
+ * expert) or with d % 256 != 0 always use two launches.  Returns MOK_OK, or MOK_ERR_INVALID_ARG
+ * for another value; *previous (NULL to skip) receives the schedule before the call. */
+typedef enum { MOK_SCHEDULE_TWO_LAUNCHES = 0, MOK_SCHEDULE_FUSED = 1 } mok_schedule;
+int mok_set_forward_schedule(int schedule, int *previous);
 
 /* Human-readable name of a status code (static string). */
 const char *mok_status_string(int status);

@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = [
     "mok_read_device_status", "mok_clear_device_status", "mok_last_launch_count",
     "mok_timing_enable", "mok_timing_collect", "mok_dispatch_index_noalloc",
     "mok_mx_quantize_rows", "mok_selftest_bounded_wait", "mok_prepared_bwd_size",
-    "mok_prepare_weights_bwd",
+    "mok_prepare_weights_bwd", "mok_set_forward_schedule",
 ]
 
 
@@ -92,6 +92,7 @@ def lib():
             "mok_selftest_bounded_wait": (ctypes.c_int, [_VP, ctypes.c_int64, _VP]),
             "mok_mx_quantize_rows": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int, _VP, _VP, _VP, _VP]),
             "mok_dispatch_index_noalloc": (ctypes.c_int, [_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+            "mok_set_forward_schedule": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
             "mok_timing_collect": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int),
                                                   ctypes.POINTER(ctypes.c_double), ctypes.c_int,
                                                   ctypes.POINTER(ctypes.c_int)]),
@@ -164,6 +165,18 @@ def selftest_bounded_wait(ws, budget_ns=50_000_000):
     """Runs a kernel whose bounded wait must run out; the status word of ws then reads
     MOK_ERR_TIMEOUT (-5)."""
     _check(lib().mok_selftest_bounded_wait(_ptr(ws), int(budget_ns), _stream()))
+
+
+SCHEDULE_TWO_LAUNCHES, SCHEDULE_FUSED = 0, 1
+
+
+def set_forward_schedule(schedule):
+    """Process-wide schedule of the bf16 forward's expert GEMMs (SCHEDULE_TWO_LAUNCHES, the
+    default, or SCHEDULE_FUSED: one persistent launch fed by a device work counter); returns the
+    previous one.  Results are bit-identical under both."""
+    prev = ctypes.c_int(0)
+    _check(lib().mok_set_forward_schedule(int(schedule), ctypes.byref(prev)))
+    return prev.value
 
 
 def timing_enable(on=True):

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -12,6 +13,7 @@
 namespace mok {
 
 static thread_local int g_last_launches = 0;
+static std::atomic<int> g_forward_schedule{MOK_SCHEDULE_TWO_LAUNCHES};
 
 int num_sms() {
   int dev = 0;
@@ -94,9 +96,9 @@ static size_t al(size_t x) { return (x + 1023) & ~size_t(1023); }
 
 enum FwdSlot {
   FW_STATUS, FW_HIST, FW_XS, FW_H, FW_HSH, FW_YS, FW_YSH,
+  FW_SYNC,  // fused forward: work counter, then one readiness counter per M tile
   // MXFP8 only: E4M3 codes and UE8M0 scale atoms of x, x_sorted, h, h_sh
   FW_XQ, FW_XSC, FW_XQS, FW_XSCS, FW_HQ, FW_HSC, FW_HQSH, FW_HSCSH,
-  FW_RPART,  // router: split-K partial logits
   FW_N
 };
 enum PrepSlot {  // MXFP8 prepared weights: K-major codes [n][N][K] and scale atoms
@@ -140,7 +142,7 @@ static Layout layout_fwd(const mok_dims* d) {
   sz[FW_HSH] = 2ull * T * Fs;
   sz[FW_YS] = 2ull * R * d->d;
   sz[FW_YSH] = 2ull * T * d->d * d->n_shared;
-  sz[FW_RPART] = 4ull * route_splits_bound(T, d->d) * T * d->E;
+  sz[FW_SYNC] = 256 + 4ull * ((T + BM - 1) / BM + (R + BM - 1) / BM + d->E);
   if (d->dtype == MOK_MXFP8) {
     sz[FW_XS] = 0;
     sz[FW_H] = 0;
@@ -243,8 +245,10 @@ static Layout layout_prepared_bwd(const mok_dims* d) {
 static Layout layout_saved(const mok_dims* d) {
   const int64_t T = d->T, R = T * d->k;
   const int Fs = d->n_shared ? d->F_shared : 0;
-  // G, U, their shared-expert copies, x in expert order (bf16 weight gradients only)
-  size_t sz[SV_N] = {2ull * R * d->F, 2ull * R * d->F, 2ull * T * Fs, 2ull * T * Fs,
+  // G, U, their shared-expert copies (bf16; fp32 for MXFP8, whose backward requantises the
+  // values derived from them), x in expert order (bf16 weight gradients only)
+  const size_t gb = d->dtype == MOK_MXFP8 ? 4 : 2;
+  size_t sz[SV_N] = {gb * R * d->F, gb * R * d->F, gb * T * Fs, gb * T * Fs,
                      d->dtype == MOK_MXFP8 ? 0 : 2ull * R * d->d};
   Layout L{};
   size_t o = 0;
@@ -644,6 +648,13 @@ int mok_clear_device_status(void* ws, mok_stream_t stream) {
 
 int mok_last_launch_count(void) { return g_last_launches; }
 
+int mok_set_forward_schedule(int schedule, int* previous) {
+  if (schedule != MOK_SCHEDULE_TWO_LAUNCHES && schedule != MOK_SCHEDULE_FUSED) return MOK_ERR_INVALID_ARG;
+  const int old = g_forward_schedule.exchange(schedule);
+  if (previous) *previous = old;
+  return MOK_OK;
+}
+
 int mok_route(const mok_dims* dims, const void* x, const void* W_router, const float* bias,
               int32_t* topk_idx, float* topk_w, float* logits, void* ws, size_t ws_bytes,
               mok_stream_t stream) {
@@ -666,11 +677,9 @@ int mok_route(const mok_dims* dims, const void* x, const void* W_router, const f
   p.E = dims->E;
   p.k = dims->k;
   p.status = static_cast<int*>(ws);
-  const Layout L = layout_fwd(dims);
-  p.splits = std::min(route_splits(dims->T, dims->d), route_splits_bound(dims->T, dims->d));
-  p.partial = at<float*>(ws, L.off[FW_RPART]);
+  p.splits = route_splits(dims->T, dims->d);
   rc = cuda_status(launch_route(p, reinterpret_cast<cudaStream_t>(stream)));
-  if (rc == MOK_OK) g_last_launches = p.splits > 1 ? 2 : 1;
+  if (rc == MOK_OK) g_last_launches = 1;
   return rc;
 }
 
@@ -775,7 +784,7 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
       p.out1[0] = hscsh;
       p.out0[1] = hq;
       p.out1[1] = hsc;
-      if (saved) {  // training: G and U in bf16 for the backward
+      if (saved) {  // training: G and U in fp32 for the backward
         p.out2[0] = at<void*>(saved, S.off[SV_GSH]);
         p.out3[0] = at<void*>(saved, S.off[SV_USH]);
         p.out2[1] = at<void*>(saved, S.off[SV_G]);
@@ -845,6 +854,60 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
   // hold enough rows to fill them: measured faster at about 340 routed rows per expert, slower
   // (gate/up) at 256, where ragged experts leave many pair tiles half empty
   const bool pair = R >= 320 * (int64_t)E;
+  if (!pair && d % 256 == 0 && g_forward_schedule.load() == MOK_SCHEDULE_FUSED) {
+    // 2+3. gate/up and down in one persistent launch (work counter, per-M-tile readiness)
+    int* sync = at<int*>(ws, L.off[FW_SYNC]);
+    rc = cuda_status(cudaMemsetAsync(sync, 0, 256 + 4ull * ((T + BM - 1) / BM + (R + BM - 1) / BM + E), s));
+    if (rc != MOK_OK) return rc;
+    GemmParams p{};
+    bool ok = true;
+    if (sh) {
+      ok &= map2d(&p.maps[MS_A0], x, T, d, 64, 128);
+      ok &= map3d(&p.maps[MS_B0], w->Ws_gate, 1, d, Fs, 64, 64);
+      ok &= map3d(&p.maps[MS_B1], w->Ws_up, 1, d, Fs, 64, 64);
+      ok &= map2d(&p.maps[MS_A1], hsh, T, Fs, 64, 128);
+      ok &= map3d(&p.maps[MS_B2], w->Ws_down, 1, Fs, d, 64, 64);
+    }
+    ok &= map2d(&p.maps[MS_A3], xs, R, d, 64, 128);
+    ok &= map3d(&p.maps[MS_B3], w->W_gate, E, d, F, 64, 64);
+    ok &= map3d(&p.maps[MS_B4], w->W_up, E, d, F, 64, 64);
+    ok &= map2d(&p.maps[MS_A4], h, R, F, 64, 128);
+    ok &= map3d(&p.maps[MS_B5], w->W_down, E, F, d, 64, 64);
+    if (!ok) return MOK_ERR_CUDA;
+    p.offsets = offsets;
+    p.E = E;
+    p.has_shared = sh;
+    p.T = (int)T;
+    p.d = d;
+    p.F = F;
+    p.Fs = Fs;
+    p.nt[0] = Fs / 128;
+    p.nt[1] = F / 128;
+    p.ntb[0] = p.ntb[1] = d / 256;
+    p.out0[0] = hsh;
+    p.out0[1] = h;
+    if (saved) {
+      p.out1[0] = at<void*>(saved, S.off[SV_GSH]);
+      p.out2[0] = at<void*>(saved, S.off[SV_USH]);
+      p.out1[1] = at<void*>(saved, S.off[SV_G]);
+      p.out2[1] = at<void*>(saved, S.off[SV_U]);
+    }
+    p.out3[0] = Ysh;
+    p.out3[1] = Ys;
+    p.row_w = sorted_w;
+    p.work = sync;
+    p.ready = sync + 64;
+    p.status = static_cast<int*>(ws);
+    const int64_t mtb = (sh ? (T + BM - 1) / BM : 0) + (R + BM - 1) / BM + E;
+    const int grid = (int)std::min<int64_t>(grid_cap, mtb * (F / 128 + d / 256));
+    rc = cuda_status(launch_gemm(G_FWD_GUD, 256, p, grid, s));
+    if (rc != MOK_OK) return rc;
+    ++launches;
+    rc = cuda_status(launch_combine(T, d, dims->k, topk_idx, inv_pos, Ys, sh ? Ysh : nullptr, y, s));
+    if (rc != MOK_OK) return rc;
+    g_last_launches = launches + 1;
+    return MOK_OK;
+  }
   // 2. gate/up GEMM with SiLU(gate)*up fused in the epilogue
   {
     GemmParams p{};

@@ -42,7 +42,10 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr bool A_MN = (MODE == G_BWD_DW);
-  static constexpr bool B_MN = (MODE == G_FWD_GU || MODE == G_FWD_DOWN || MODE == G_BWD_DW);
+  static constexpr bool B_MN = (MODE == G_FWD_GU || MODE == G_FWD_DOWN || MODE == G_BWD_DW ||
+                                MODE == G_FWD_GUD);
+  // gate/up then down in one launch, tiles claimed from a device work counter
+  static constexpr bool FUSED = (MODE == G_FWD_GUD);
   // MXFP8: TMEM also holds the scale factors (from column 256), so one 256-column accumulator
   // or two of 128 columns
   static constexpr int NUM_ACC = (MX && BN == 256) ? 1 : 2;
@@ -54,7 +57,8 @@ struct Cfg {
   // epilogue warp at a time and are written with coalesced row stores
   static constexpr bool ROW_STAGED = (MODE == G_FWD_DOWN || MODE == G_BWD_DX ||
                                       MODE == G_FWD_DOWN_MX || MODE == G_BWD_DW ||
-                                      MODE == G_BWD_DX_MX || MODE == G_BWD_DW_MX);
+                                      MODE == G_BWD_DX_MX || MODE == G_BWD_DW_MX ||
+                                      MODE == G_FWD_GUD);
   // per epilogue warp: a 2 KB row-staging buffer, or (dA MXFP8) a 32 x 36-float transpose buffer
   static constexpr int STG_STRIDE = (MODE == G_BWD_DA_MX) ? 32 * 36 * 4 : 2048;
   static constexpr int STAGING_BYTES = (ROW_STAGED || MODE == G_BWD_DA_MX) ? EPI_WARPS * STG_STRIDE : 0;
@@ -64,7 +68,8 @@ struct Cfg {
   static constexpr bool K_GROUPED = (MODE == G_BWD_DW || MODE == G_BWD_DW_MX);
 };
 
-constexpr int kAuxBytes = 1024;                      // barriers, TMEM address, abort flag
+constexpr int kAuxBytes = 1024;                      // barriers, TMEM address, abort flag, tile ring
+constexpr int kRing = 4;                             // G_FWD_GUD: claimed tiles in flight per CTA
 constexpr int kSchedBytes = 2 * (kMaxE + 1) * 4;     // expert row offsets + M-tile prefix
 
 // PAIR: CTA-pair tiles (two CTAs of a cluster, M = 256, tcgen05.mma.cta_group::2).  Each CTA
@@ -74,6 +79,7 @@ template <int MODE, int BN, bool PAIR>
 struct KCfg : Cfg<MODE, BN> {
   using Base = Cfg<MODE, BN>;
   static_assert(!PAIR || (!Base::MX && BN == 256), "pairs: bf16, N = 256");
+  static_assert(!PAIR || !Base::FUSED, "the fused forward runs single CTAs");
   static constexpr int B_BYTES = PAIR ? Base::B_BYTES / 2 : Base::B_BYTES;
   static constexpr int STAGE_BYTES = Base::A_BYTES + B_BYTES + Base::SF_BYTES;
   static constexpr int STAGES = PAIR ? 6 : Base::STAGES;
@@ -101,7 +107,17 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
   t.mt = 0;
   if constexpr (!Cfg<MODE, BN>::K_GROUPED) {
     const int mt0 = p.has_shared ? (p.T + BMT - 1) / BMT : 0;
-    const int tiles0 = mt0 * p.nt[0];
+    int nt0 = p.nt[0], nt1 = p.nt[1];
+    if constexpr (Cfg<MODE, BN>::FUSED) {  // the down tiles follow every gate/up tile
+      const int tiles_a = mt0 * nt0 + (p.E > 0 ? s_mt[p.E] * nt1 : 0);
+      if (tile >= tiles_a) {
+        tile -= tiles_a;
+        nt0 = p.ntb[0];
+        nt1 = p.ntb[1];
+        t.sub = 1;
+      }
+    }
+    const int tiles0 = mt0 * nt0;
     if (tile < tiles0) {
       const int n = tile / mt0, m = tile - n * mt0;
       t.g = 0;
@@ -112,7 +128,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
       t.mt = m;
     } else {
       const int l = tile - tiles0;
-      const int nt = p.nt[1];
+      const int nt = nt1;
       int lo = 0, hi = p.E;  // largest e with s_mt[e]*nt <= l
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -130,7 +146,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
       t.mt = s_mt[e] + m;
     }
     int nkb;
-    if constexpr (MODE == G_FWD_GU || MODE == G_BWD_DA) nkb = p.d / BK;
+    if constexpr (MODE == G_FWD_GUD) nkb = t.sub ? (t.g ? p.F : p.Fs) / BK : p.d / BK;
+    else if constexpr (MODE == G_FWD_GU || MODE == G_BWD_DA) nkb = p.d / BK;
     else if constexpr (MODE == G_FWD_DOWN) nkb = (t.g ? p.F : p.Fs) / BK;
     else if constexpr (MODE == G_FWD_GU_MX) nkb = p.d / 128;
     else if constexpr (MODE == G_FWD_DOWN_MX) nkb = (t.g ? p.F : p.Fs) / 128;
@@ -203,7 +220,10 @@ __device__ __forceinline__ int total_tiles(const GemmParams& p, const int* s_mt)
   if constexpr (!Cfg<MODE, BN>::K_GROUPED) {
     constexpr int BMT = KCfg<MODE, BN, PAIR>::BMT;
     const int mt0 = p.has_shared ? (p.T + BMT - 1) / BMT : 0;
-    return mt0 * p.nt[0] + (p.E > 0 ? s_mt[p.E] * p.nt[1] : 0);
+    const int mte = p.E > 0 ? s_mt[p.E] : 0;
+    if constexpr (Cfg<MODE, BN>::FUSED)
+      return mt0 * (p.nt[0] + p.ntb[0]) + mte * (p.nt[1] + p.ntb[1]);
+    return mt0 * p.nt[0] + mte * p.nt[1];
   } else {
     const int tiles_sh =
         p.has_shared ? 2 * (p.d / BM) * (p.Fs / BN) + (p.Fs / BM) * (p.d / BN) : 0;
@@ -238,7 +258,23 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, 
                                             uint32_t sA, uint32_t sB, uint32_t bar) {
   static_assert(!PAIR || MODE == G_FWD_GU || MODE == G_FWD_DOWN, "pair loads: gate/up and down");
   const CUtensorMap* M = p.maps;
-  if constexpr (PAIR && MODE == G_FWD_GU) {
+  if constexpr (MODE == G_FWD_GUD) {
+    if (t.sub == 0) {  // gate/up: as G_FWD_GU
+      tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
+      const CUtensorMap* bg = &M[t.g ? MS_B3 : MS_B0];
+      const CUtensorMap* bu = &M[t.g ? MS_B4 : MS_B1];
+      const int c0 = t.n * 128;
+      tma_load_3d(sB + 0 * 8192, bg, bar, c0, kb * BK, t.e);
+      tma_load_3d(sB + 1 * 8192, bg, bar, c0 + 64, kb * BK, t.e);
+      tma_load_3d(sB + 2 * 8192, bu, bar, c0, kb * BK, t.e);
+      tma_load_3d(sB + 3 * 8192, bu, bar, c0 + 64, kb * BK, t.e);
+    } else {  // down: as G_FWD_DOWN, A = h (slots A1 / A4), B = down weights (B2 / B5)
+      tma_load_2d(sA, &M[t.g ? MS_A4 : MS_A1], bar, kb * BK, t.row0);
+      const CUtensorMap* b = &M[t.g ? MS_B5 : MS_B2];
+#pragma unroll
+      for (int i = 0; i < BN / 64; ++i) tma_load_3d(sB + i * 8192, b, bar, t.n * BN + 64 * i, kb * BK, t.e);
+    }
+  } else if constexpr (PAIR && MODE == G_FWD_GU) {
     tma_load_2d_pair(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
     const CUtensorMap* b = rank ? &M[t.g ? MS_B4 : MS_B1] : &M[t.g ? MS_B3 : MS_B0];
     const int c0 = t.n * 128;
@@ -442,15 +478,15 @@ constexpr int warp_cols() { return Cfg<MODE, BN>::EPI_WARPS == 8 ? BN / 2 : BN; 
 // weight 1), G_BWD_DX and G_BWD_DX_MX (dX_s = accumulator): row-major outputs with d columns,
 // rows past the expert's last token skipped.
 template <int MODE, int BN>
-__device__ __forceinline__ void epilogue_rows(const GemmParams& p, const Tile& t, uint32_t tacc,
-                                              uint32_t stg, int q, int half, int lane,
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, void* const (&outs)[2], const Tile& t,
+                                              uint32_t tacc, uint32_t stg, int q, int half, int lane,
                                               uint32_t release) {
   constexpr int cols = warp_cols<MODE, BN>();
   const int nrows = t.rows - q * 32;  // valid rows among this warp's 32 (may be <= 0)
   constexpr bool WEIGHTED = (MODE == G_FWD_DOWN || MODE == G_FWD_DOWN_MX);
   float s = 1.0f;
   if (WEIGHTED && t.g == 1 && lane < nrows) s = p.row_w[t.row0 + q * 32 + lane];
-  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out0[t.g]) + (int64_t)(t.row0 + q * 32) * p.d +
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(outs[t.g]) + (int64_t)(t.row0 + q * 32) * p.d +
                      t.n * BN + cols * half;
   store_acc_rows<cols / 32, Cfg<MODE, BN>::NUM_ACC == 1>(o, p.d, nrows, cols, tacc + cols * half,
                                                          false, s, stg, lane, release);
@@ -491,7 +527,7 @@ __device__ __forceinline__ void epilogue_dw(const GemmParams& p, const Tile& t, 
 // warp takes h columns 64*half .. 64*half+63 of the tile: both 32-column blocks are computed and
 // quantised in registers, the accumulator is released (the next tile's MMAs then run under the
 // stores), then the codes and scale bytes are written.  Training (out2 set): g and u are also
-// stored in bf16 (out2, out3) for the backward.
+// stored in fp32 (out2, out3), as accumulated, for the backward's requantisation.
 template <int BN>
 __device__ __forceinline__ void epilogue_gu_mx(const GemmParams& p, const Tile& t, uint32_t tacc,
                                                int r, int half, uint32_t release) {
@@ -509,14 +545,13 @@ __device__ __forceinline__ void epilogue_gu_mx(const GemmParams& p, const Tile& 
     sb[b] = mx_block32(hv, qq[b]);
     if (p.out2[t.g] && r < t.rows) {
       const int64_t o = (int64_t)(t.row0 + r) * (t.g ? p.F : p.Fs) + t.n * 128 + c;
-      uint32_t gp[16], up[16];
+      uint4* gd = reinterpret_cast<uint4*>(static_cast<float*>(p.out2[t.g]) + o);
+      uint4* ud = reinterpret_cast<uint4*>(static_cast<float*>(p.out3[t.g]) + o);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        gp[i] = pack_bf16x2(__uint_as_float(gr[2 * i]), __uint_as_float(gr[2 * i + 1]));
-        up[i] = pack_bf16x2(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1]));
+      for (int i = 0; i < 8; ++i) {
+        gd[i] = make_uint4(gr[4 * i], gr[4 * i + 1], gr[4 * i + 2], gr[4 * i + 3]);
+        ud[i] = make_uint4(ur[4 * i], ur[4 * i + 1], ur[4 * i + 2], ur[4 * i + 3]);
       }
-      st_row64(static_cast<__nv_bfloat16*>(p.out2[t.g]) + o, gp);
-      st_row64(static_cast<__nv_bfloat16*>(p.out3[t.g]) + o, up);
     }
   }
   acc_release(release, r & 31);
@@ -564,7 +599,7 @@ __device__ __forceinline__ void quant_tokens_chunk(const float (&v)[32], uint32_
   atoms[sf_atom_word(c >> 7, kg, nkb, c & 127) + q] = (uint8_t)sb;
 }
 
-// G_BWD_DA_MX: from a = dY W_down^T (the accumulator) and the saved G, U (bf16): dG and dU
+// G_BWD_DA_MX: from a = dY W_down^T (the accumulator) and the saved G, U (fp32): dG and dU
 // quantised per 32 columns (E4M3 codes [rows][F] and scale atoms by M tile: the A operands of the
 // block-scaled dX GEMM); dG, dU and w*h quantised along tokens (the warp's 32 rows are one
 // 32-token block of one expert) into the transposed operands of the weight-gradient GEMM; and
@@ -572,11 +607,19 @@ __device__ __forceinline__ void quant_tokens_chunk(const float (&v)[32], uint32_
 // 128 half .. 128 half + 127 of the tile (N tile 128 with two accumulators and four epilogue
 // warps: half = 0): K block kb of F, whose four scale bytes per row are one atom word.  Rows past
 // the expert's last token count as zeros in the token blocks.
+__device__ __forceinline__ void ld_row128(const float* src, float (&v)[32]) {
+  const float4* s = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 q = s[i];
+    v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+  }
+}
+
 template <int BN>
 __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& t, uint32_t tacc,
                                                uint32_t stg, int q, int half, int lane,
                                                uint32_t release) {
-  using bf16 = __nv_bfloat16;
   const int r = q * 32 + lane;
   const bool valid = r < t.rows;
   const int ld = t.g ? p.F : p.Fs;
@@ -584,8 +627,8 @@ __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& 
   const float w = (t.g == 1 && valid) ? p.row_w[row] : 1.0f;
   const int kb = t.n * (BN / 128) + half;
   const int64_t off = row * ld + 128 * kb;
-  const bf16* Gs = static_cast<const bf16*>(p.in0[t.g]) + off;
-  const bf16* Us = static_cast<const bf16*>(p.in1[t.g]) + off;
+  const float* Gs = static_cast<const float*>(p.in0[t.g]) + off;
+  const float* Us = static_cast<const float*>(p.in1[t.g]) + off;
   uint8_t* dGq = static_cast<uint8_t*>(p.qout[t.g][0]) + off;
   uint8_t* dUq = static_cast<uint8_t*>(p.qout[t.g][1]) + off;
   const int nkbt = p.tnkb[t.g];
@@ -593,26 +636,18 @@ __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& 
   const int64_t kpos = 128 * (int64_t)t.mt + 32 * q;  // the warp's token columns
   float pacc = 0.0f;
   uint32_t sg = 0u, su = 0u;
-  uint32_t gq[16], uq[16];  // G and U of the current chunk; the next chunk's load while it runs
-  if (valid) {
-    ld_row64(Gs, gq);
-    ld_row64(Us, uq);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) gq[i] = uq[i] = 0u;
-  }
 #pragma unroll 1
   for (int c = 0; c < 128; c += 32) {
-    uint32_t v[32];
-    tmem_ld32(tacc + 128 * half + c, v);
-    uint32_t gn[16], un[16];
-    if (valid && c + 32 < 128) {
-      ld_row64(Gs + c + 32, gn);
-      ld_row64(Us + c + 32, un);
+    float gq[32], uq[32];  // G and U of this chunk (their loads overlap the TMEM load)
+    if (valid) {
+      ld_row128(Gs + c, gq);
+      ld_row128(Us + c, uq);
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) gn[i] = un[i] = 0u;
+      for (int i = 0; i < 32; ++i) gq[i] = uq[i] = 0.0f;
     }
+    uint32_t v[32];
+    tmem_ld32(tacc + 128 * half + c, v);
     tmem_ld_wait();
     const int col0 = 128 * kb + c;
     float f[32];
@@ -620,8 +655,7 @@ __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& 
     // dG = w a u s (1 + g (1 - s)), s = sigmoid(g)
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float g = (i & 1) ? bf16_hi(gq[i >> 1]) : bf16_lo(gq[i >> 1]);
-      const float u = (i & 1) ? bf16_hi(uq[i >> 1]) : bf16_lo(uq[i >> 1]);
+      const float g = gq[i], u = uq[i];
       const float sgm = sigmoid_f(g);
       f[i] = valid ? w * __uint_as_float(v[i]) * u * sgm * (1.0f + g * (1.0f - sgm)) : 0.0f;
     }
@@ -636,7 +670,7 @@ __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& 
     // dU = w a g s
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float g = (i & 1) ? bf16_hi(gq[i >> 1]) : bf16_lo(gq[i >> 1]);
+      const float g = gq[i];
       f[i] = valid ? w * __uint_as_float(v[i]) * g * sigmoid_f(g) : 0.0f;
     }
     if (valid) {
@@ -650,19 +684,13 @@ __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& 
     // w h, h = g s u, and the router partial <a, h>
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float g = (i & 1) ? bf16_hi(gq[i >> 1]) : bf16_lo(gq[i >> 1]);
-      const float u = (i & 1) ? bf16_hi(uq[i >> 1]) : bf16_lo(uq[i >> 1]);
+      const float g = gq[i], u = uq[i];
       const float hv = g * sigmoid_f(g) * u;
       pacc += __uint_as_float(v[i]) * hv;  // zero on rows past the expert (g = u = 0)
       f[i] = w * hv;
     }
     quant_tokens_chunk(f, stg, p.tq[t.g][2] + (int64_t)col0 * tld + kpos, tld, p.tsc[t.g][2], col0,
                        t.mt, nkbt, q, lane);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      gq[i] = gn[i];
-      uq[i] = un[i];
-    }
   }
   acc_release(release, lane);
   if (valid) {
@@ -829,6 +857,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
   const uint32_t bar_drain = bar_tempty + 16;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(aux + 16 * C::STAGES + 40);
   volatile int* s_abort = reinterpret_cast<volatile int*>(aux + 16 * C::STAGES + 48);
+  // G_FWD_GUD: a ring of claimed tile indices (full: written by the producer; empty: taken by the
+  // MMA warp and every epilogue warp)
+  const uint32_t bar_rfull = aux_s + 16 * C::STAGES + 64;
+  const uint32_t bar_rempty = bar_rfull + 8 * kRing;
+  volatile int* s_ring = reinterpret_cast<volatile int*>(aux + 16 * C::STAGES + 64 + 16 * kRing);
   int* s_off = reinterpret_cast<int*>(aux + kAuxBytes);
   int* s_mt = s_off + (kMaxE + 1);
 
@@ -844,6 +877,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       mbar_init(bar_tempty + 8 * b, C::EPI_WARPS * (PAIR ? 2 : 1));  // one arrival per warp
     }
     mbar_init(bar_drain, 1);
+    if constexpr (C::FUSED) {
+      for (int i = 0; i < kRing; ++i) {
+        mbar_init(bar_rfull + 8 * i, 1);
+        mbar_init(bar_rempty + 8 * i, 1 + C::EPI_WARPS);
+      }
+    }
     *s_abort = 0;
     fence_barrier_init();
   }
@@ -944,10 +983,9 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
     } else if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int tile = first; tile < ntiles && !*s_abort; tile += step) {
-        const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
+      auto produce = [&](const Tile& t) {
         for (int kb = 0; kb < t.nkb; ++kb) {
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) break;
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) return;
           if (!PAIR || rank == 0)  // a pair's stage: both CTAs' bytes on the even CTA's barrier
             mbar_arrive_expect_tx(bar_full + 8 * stage,
                                   (C::A_BYTES + C::B_BYTES + C::SF_BYTES) * (PAIR ? 2 : 1));
@@ -958,17 +996,37 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
             load_scale_atoms<MODE, BN>(p, t, kb, sSF0 + stage * C::SF_BYTES, bar_full + 8 * stage);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
+      };
+      if constexpr (C::FUSED) {
+        // claim tiles in order from the work counter and hand each to the MMA and epilogue warps;
+        // a down tile first waits until every gate/up tile of its M tile has written its h rows
+        const int mt0 = p.has_shared ? (p.T + BM - 1) / BM : 0;
+        for (int it = 0;; ++it) {
+          const int slot = it % kRing;
+          if (!mbar_wait(bar_rempty + 8 * slot, ((it / kRing) & 1) ^ 1, p.status, s_abort)) break;
+          const int tile = *s_abort ? ntiles : atomicAdd(p.work, 1);
+          s_ring[slot] = tile;
+          mbar_arrive(bar_rfull + 8 * slot);
+          if (tile >= ntiles) break;
+          const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
+          if (t.sub == 1 && !wait_counter(p.ready + (t.g ? mt0 + t.mt : t.mt), p.nt[t.g] * C::EPI_WARPS,
+                                          p.status, s_abort))
+            break;
+          produce(t);
+        }
+      } else {
+        for (int tile = first; tile < ntiles && !*s_abort; tile += step)
+          produce(decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank));
       }
     }
   } else if (warp == 1 && (!PAIR || rank == 0)) {
     int stage = 0;
     uint32_t phase = 0;
-    int it = 0;
-    for (int tile = first; tile < ntiles && !*s_abort; tile += step, ++it) {
-      const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
+    // the MMAs of the it-th tile of this CTA; false when a bounded wait ran out
+    auto mma_tile = [&](const Tile& t, int it) -> bool {
       const int buf = it % C::NUM_ACC;
       const uint32_t tph = (it / C::NUM_ACC) & 1;
-      if (!mbar_wait<PAIR>(bar_tempty + 8 * buf, tph ^ 1, p.status, s_abort)) break;
+      if (!mbar_wait<PAIR>(bar_tempty + 8 * buf, tph ^ 1, p.status, s_abort)) return false;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
       bool ok = true;
@@ -1025,7 +1083,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
         __syncwarp();
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
       }
-      if (!ok) break;
+      if (!ok) return false;
       if (lane == 0) {
         if constexpr (PAIR)
           umma_commit_pair_mc(bar_tfull + 8 * buf, 3);
@@ -1033,6 +1091,22 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
           umma_commit(bar_tfull + 8 * buf);
       }
       __syncwarp();
+      return true;
+    };
+    if constexpr (C::FUSED) {
+      for (int it = 0;; ++it) {
+        const int slot = it % kRing;
+        if (!mbar_wait(bar_rfull + 8 * slot, (it / kRing) & 1, p.status, s_abort)) break;
+        const int tile = s_ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_rempty + 8 * slot);
+        if (tile >= ntiles) break;
+        if (!mma_tile(decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank), it)) break;
+      }
+    } else {
+      int it = 0;
+      for (int tile = first; tile < ntiles && !*s_abort; tile += step, ++it)
+        if (!mma_tile(decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank), it)) break;
     }
     // every MMA issued by this CTA has completed before TMEM is released
     if (lane == 0) {
@@ -1048,22 +1122,30 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
     const int q = warp & 3;  // TMEM lane quarter accessible to this warp
     const int half = (warp - 2) / 4;  // 8 epilogue warps: which column half
     const int r = q * 32 + lane;
-    int it = 0;
-    for (int tile = first; tile < ntiles && !*s_abort; tile += step, ++it) {
-      const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
+    // the epilogue of the it-th tile of this CTA; false when a bounded wait ran out
+    auto epi_tile = [&](const Tile& t, int it) -> bool {
       const int buf = it % C::NUM_ACC;
       const uint32_t tph = (it / C::NUM_ACC) & 1;
-      if (!mbar_wait(bar_tfull + 8 * buf, tph, p.status, s_abort)) break;
+      if (!mbar_wait(bar_tfull + 8 * buf, tph, p.status, s_abort)) return false;
       tc_fence_after();
       const uint32_t tacc = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       // the staged and MXFP8 epilogues release the accumulator themselves (before their stores
       // when there is only one)
       const uint32_t stg = sSTG0 + (warp - 2) * C::STG_STRIDE;
       const uint32_t rel = PAIR ? mapa_shared(bar_tempty + 8 * buf, 0) : bar_tempty + 8 * buf;
-      if constexpr (MODE == G_BWD_DW || MODE == G_BWD_DW_MX) {
+      if constexpr (MODE == G_FWD_GUD) {
+        if (t.sub == 0) {  // h (and G, U), then this warp's share of the M tile's readiness
+          epilogue<G_FWD_GU, BN>(p, t, tacc, r, half);
+          acc_release(rel, lane);
+          const int mt0 = p.has_shared ? (p.T + BM - 1) / BM : 0;
+          signal_counter(p.ready + (t.g ? mt0 + t.mt : t.mt), lane);
+        } else {  // Y = router weight x (h W_down) into out3
+          epilogue_rows<G_FWD_DOWN, BN>(p, p.out3, t, tacc, stg, q, half, lane, rel);
+        }
+      } else if constexpr (MODE == G_BWD_DW || MODE == G_BWD_DW_MX) {
         epilogue_dw<MODE, BN>(p, t, tacc, stg, q, half, lane, rel);
       } else if constexpr (C::ROW_STAGED) {
-        epilogue_rows<MODE, BN>(p, t, tacc, stg, q, half, lane, rel);
+        epilogue_rows<MODE, BN>(p, p.out0, t, tacc, stg, q, half, lane, rel);
       } else if constexpr (MODE == G_FWD_GU_MX) {
         epilogue_gu_mx<BN>(p, t, tacc, r, half, rel);
       } else if constexpr (MODE == G_BWD_DA_MX) {
@@ -1072,6 +1154,22 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
         epilogue<MODE, BN>(p, t, tacc, r, half);
         acc_release(rel, lane);
       }
+      return true;
+    };
+    if constexpr (C::FUSED) {
+      for (int it = 0;; ++it) {
+        const int slot = it % kRing;
+        if (!mbar_wait(bar_rfull + 8 * slot, (it / kRing) & 1, p.status, s_abort)) break;
+        const int tile = s_ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_rempty + 8 * slot);
+        if (tile >= ntiles) break;
+        if (!epi_tile(decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank), it)) break;
+      }
+    } else {
+      int it = 0;
+      for (int tile = first; tile < ntiles && !*s_abort; tile += step, ++it)
+        if (!epi_tile(decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank), it)) break;
     }
   }
   __syncthreads();
@@ -1130,7 +1228,7 @@ static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
   static const char* kNames[] = {"gemm_fwd_gate_up", "gemm_fwd_down",      "gemm_bwd_da",
                                  "gemm_bwd_dx",      "gemm_bwd_dw",        "gemm_fwd_gate_up_mx",
                                  "gemm_fwd_down_mx", "gemm_bwd_da_mx",     "gemm_bwd_dx_mx",
-                                 "gemm_bwd_dw_mx"};
+                                 "gemm_bwd_dw_mx",   "gemm_fwd_fused"};
   if constexpr (!PAIR) {
     if (grid <= 0) return cudaSuccess;
     prof_begin(kNames[MODE], s);
@@ -1191,6 +1289,7 @@ cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStr
     case G_BWD_DA_MX: return launch_one<G_BWD_DA_MX, 128>(p, grid, s);  // two accumulators
     case G_BWD_DX_MX: return launch_one<G_BWD_DX_MX, 256>(p, grid, s);
     case G_BWD_DW_MX: return launch_one<G_BWD_DW_MX, 256>(p, grid, s);
+    case G_FWD_GUD: return launch_one<G_FWD_GUD, 256>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -50,12 +50,24 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
+// 16 bytes from the shared memory of a CTA of the cluster (`addr` from mapa_shared).
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 // One arrival on the barrier at a cluster address (any CTA of the cluster, this one included),
 // with the default CTA-scope release: what it publishes to the other CTA is the end of this
 // warp's TMEM reads, ordered by tcgen05.wait::ld and tcgen05.fence::before_thread_sync; a
 // cluster-scope release would also wait for the warp's outstanding global stores.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -99,6 +111,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
       return false;
     }
   }
+}
+
+// ------------------------------------------------------------------ counters in global memory
+// One warp's share of a readiness counter: every lane's earlier global stores are made visible
+// at GPU scope, then lane 0 adds 1 with release semantics.
+__device__ __forceinline__ void signal_counter(int* ctr, int lane) {
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+// Waits (acquire, at most kWaitNs) until *ctr >= target, then orders the data it guards before
+// this thread's later TMA (async-proxy) reads.  On timeout: MOK_ERR_TIMEOUT, CTA abort, false.
+__device__ __forceinline__ bool wait_counter(const int* ctr, int target, int* status,
+                                             volatile int* abort) {
+  const uint64_t t0 = global_ns();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) break;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitNs) {
+      record_status(status, MOK_ERR_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
 }
 
 // ------------------------------------------------------------------ TMA

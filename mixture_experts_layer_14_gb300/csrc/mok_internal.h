@@ -32,6 +32,10 @@ enum GemmMode : int {
   G_BWD_DA_MX = 7,   // a = dY Wd^T -> dG, dU along F; dG, dU, w*h along tokens; <a,h>
   G_BWD_DX_MX = 8,   // dX = dG Wg^T + dU Wu^T                      M-grouped
   G_BWD_DW_MX = 9,   // dW from operands quantised along tokens     K-grouped (transposed)
+  // gate/up + SwiGLU, then down + router weight, in one persistent launch: CTAs claim tiles from
+  // a device work counter (every gate/up tile before any down tile), and a down tile waits for
+  // the readiness counter of its M tile (all its h columns written)
+  G_FWD_GUD = 10,
 };
 
 // Tensor-map slots.  Group 0 is the shared expert (rows = tokens), group 1 the routed experts
@@ -61,10 +65,10 @@ struct GemmParams {
   // epilogue pointers, [group]
   void* out0[2];        // h / Y / dG / dX / dW_gate
   void* out1[2];        // G (saved)      / dU / dW_up
-  void* out2[2];        // U (saved)      / w*h / dW_down; G_FWD_GU_MX: G (saved) or NULL
-  void* out3[2];        // G_FWD_GU_MX: U (saved) or NULL
+  void* out2[2];        // U (saved)      / w*h / dW_down; G_FWD_GU_MX: G (saved, fp32) or NULL
+  void* out3[2];        // G_FWD_GU_MX: U (saved, fp32) or NULL
   void* out_router;     // dW_router [d,E]
-  const void* in0[2];   // G (saved) for G_BWD_DA
+  const void* in0[2];   // G (saved) for G_BWD_DA (bf16) and G_BWD_DA_MX (fp32)
   const void* in1[2];   // U (saved)
   const float* row_w;   // router weight of each routed row (sorted_w)
   float* partial;       // G_BWD_DA: <a,h> per (routed row, N tile), [R, nt[1]]
@@ -87,6 +91,11 @@ struct GemmParams {
   // G_BWD_DW: per expert, kBoundMaps copies of the routed operands' maps bounded to its rows
   // (x_sorted, w*h, dG, dU, dY_sorted), from launch_dw_bound_maps
   const CUtensorMap* emaps;
+  // G_FWD_GUD: N tiles of the down phase per group; the work counter (work[0], zero at launch)
+  // and one readiness counter per M tile (shared expert's first, zero at launch)
+  int ntb[2];
+  int* work;
+  int* ready;
   int* status;
 };
 
@@ -118,20 +127,12 @@ struct RouteParams {
   float* topk_w;
   float* logits;
   int T, d, E, k;
-  int splits;          // K splits per 128-token tile (1 = top-k straight from TMEM)
-  float* partial;      // [splits][T][E] fp32 partial logits (splits > 1)
+  int splits;          // K splits per 128-token tile: a cluster of `splits` CTAs (power of two)
+  int chunk;           // splits > 1: logit columns reduced through shared memory per pass
   int* status;
 };
 constexpr int kMaxRouteSplits = 8;
 int route_splits(int64_t T, int d);
-// Upper bound of route_splits on any GPU of up to 256 SMs (sizes the partial-logit workspace).
-inline int route_splits_bound(int64_t T, int d) {
-  const int64_t mt = (T + BM - 1) / BM;
-  int64_t b = (256 + mt - 1) / (mt > 0 ? mt : 1);
-  if (b > kMaxRouteSplits) b = kMaxRouteSplits;
-  if (b > d / BK) b = d / BK;
-  return b < 1 ? 1 : (int)b;
-}
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
 
 // Dispatch (dispatch.cu)

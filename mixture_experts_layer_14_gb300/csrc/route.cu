@@ -1,13 +1,20 @@
 // Router of the MoE layer: logits = x W_router + b on the tensor cores (tcgen05, fp32 TMEM
-// accumulator), fused with the top-k selection and the renormalised softmax weights in the
-// epilogue.  Page "Mixture-of-Kittens: Nhân kernel MoE ...", section "Chồng lấp tính toán và
-// truyền tải trong MoE": the router projection picks the top-k routed experts of each token and
-// gives each a router weight.
+// accumulator), fused with the top-k selection and the renormalised softmax weights.  Page
+// "Mixture-of-Kittens: Nhân kernel MoE ...", section "Chồng lấp tính toán và truyền tải trong
+// MoE": the router projection picks the top-k routed experts of each token and gives each a
+// router weight.
 //
-// One CTA per 128-token tile.  Warp 0 issues TMA loads of the x tile (K-major) and of all E
-// columns of W_router (MN-major), warp 1 issues the UMMAs (N = E rounded up to 64, split into
-// MMAs of at most 256 columns), warps 2..5 run the epilogue: each thread owns one token row of
-// the accumulator, so top-k needs no cross-thread communication.
+// One CTA per (128-token tile, K split).  Warp 0 issues TMA loads of the x tile (K-major) and of
+// all E columns of W_router (MN-major), warp 1 issues the UMMAs (N = E rounded up to 64, split
+// into MMAs of at most 256 columns), warps 2..5 run the epilogue.
+//  - One split (the token tiles alone fill the GPU): each epilogue thread owns one token row of
+//    the accumulator and selects its top k straight from TMEM.
+//  - S > 1 splits (a power of two): the S CTAs of a tile form a thread-block cluster.  Each
+//    writes its partial logits to its own shared memory (reusing the drained stage buffers, a
+//    chunk of columns at a time), and CTA r reduces tile rows r 128/S .. (r+1) 128/S - 1: S
+//    threads per row each sum every CTA's partial of a quarter of the columns in rank order
+//    (distributed shared memory; the same fixed order on every run), keep their own top-k list,
+//    and merge the S lists with warp shuffles.  The partial logits never leave the chip.
 #include "mok_device.cuh"
 
 namespace mok {
@@ -54,6 +61,91 @@ __device__ __forceinline__ void write_route(const RouteParams& p, int t, const f
   }
 }
 
+// (v, i) ranks before (bv, bi): larger logit first, lower expert index among equal logits; an
+// empty entry (index -1) ranks last.
+__device__ __forceinline__ bool ranks_before(float v, int i, float bv, int bi) {
+  const unsigned ui = static_cast<unsigned>(i), ubi = static_cast<unsigned>(bi);
+  return v > bv || (v == bv && ui < ubi);
+}
+
+// Merge of the sorted top-k lists of the S lanes of a group (lanes S g .. S g + S - 1) into the
+// first k entries of (ov, oi), identical in every lane of the group.
+template <int S>
+__device__ __forceinline__ void merge_topk(int k, float (&tv)[kMaxK], int (&ti)[kMaxK],
+                                           float (&ov)[kMaxK], int (&oi)[kMaxK]) {
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    ov[j] = -INFINITY;
+    oi[j] = -1;
+    if (j < k) {
+      float bv = tv[0];
+      int bi = ti[0];
+#pragma unroll
+      for (int o = 1; o < S; o <<= 1) {
+        const float v = __shfl_xor_sync(0xffffffffu, bv, o, S);
+        const int i = __shfl_xor_sync(0xffffffffu, bi, o, S);
+        if (ranks_before(v, i, bv, bi)) { bv = v; bi = i; }
+      }
+      // expert indices are distinct, so exactly one lane of the group holds the winner
+      const bool mine = (bi == ti[0]) && (bi >= 0);
+#pragma unroll
+      for (int i = 0; i + 1 < kMaxK; ++i) {
+        tv[i] = mine ? tv[i + 1] : tv[i];
+        ti[i] = mine ? ti[i + 1] : ti[i];
+      }
+      if (mine) { tv[kMaxK - 1] = -INFINITY; ti[kMaxK - 1] = -1; }
+      ov[j] = bv;
+      oi[j] = bi;
+    }
+  }
+}
+
+// Splits > 1, one pass over logit columns c0 .. c0 + p.chunk - 1: thread `et` (0..127) of the
+// epilogue sums the S partials of its row's columns 4 (sub + S i) .. + 3 in cluster rank order,
+// adds the bias and inserts them into its top-k list.
+template <int S>
+__device__ __forceinline__ void reduce_chunk(const RouteParams& p, uint32_t part, uint32_t pstride,
+                                             int c0, int rank, int et, float (&tv)[kMaxK],
+                                             int (&ti)[kMaxK]) {
+  constexpr int RPC = BM / S;            // rows this CTA reduces
+  const int row = rank * RPC + et / S;   // row of the tile
+  const int sub = et % S;
+  const int t = blockIdx.x * BM + row;
+  const uint32_t mine = part + row * pstride;
+  uint32_t src[S];
+#pragma unroll
+  for (int r = 0; r < S; ++r) src[r] = mapa_shared(mine, r);
+  for (int j = sub; j < p.chunk / 4; j += S) {
+    float4 acc = ld_shared_cluster_v4(src[0] + 16 * j);
+#pragma unroll
+    for (int r = 1; r < S; ++r) {
+      const float4 v = ld_shared_cluster_v4(src[r] + 16 * j);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int e = c0 + 4 * j + c;
+      if (e < p.E) {
+        const float l = a4[c] + (p.bias ? p.bias[e] : 0.0f);
+        if (t < p.T && p.logits) p.logits[(int64_t)t * p.E + e] = l;
+        if (ranks_before(l, e, tv[kMaxK - 1], ti[kMaxK - 1])) topk_insert(tv, ti, l, e);
+      }
+    }
+  }
+}
+
+template <int S>
+__device__ __forceinline__ void finish_split(const RouteParams& p, int rank, int et,
+                                             float (&tv)[kMaxK], int (&ti)[kMaxK]) {
+  float ov[kMaxK];
+  int oi[kMaxK];
+  merge_topk<S>(p.k, tv, ti, ov, oi);
+  const int row = rank * (BM / S) + et / S;
+  const int t = blockIdx.x * BM + row;
+  if (et % S == 0 && t < p.T) write_route(p, t, ov, oi);
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_constant__ RouteParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -65,10 +157,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
   const int b_bytes = E_pad * BK * 2;
   const int stage_bytes = a_bytes + b_bytes;
   const int stages = min(4, (196608 / stage_bytes));
+  const uint32_t pstride = 4u * p.chunk + 16u;  // a row of the partial-logit chunk
+  const uint32_t region = max((uint32_t)(stages * stage_bytes), p.splits > 1 ? BM * pstride : 0u);
   const uint32_t sA0 = base;
   const uint32_t sB0 = base + stages * a_bytes;
-  const uint32_t aux_s = base + stages * stage_bytes;
-  uint8_t* aux = gbase + stages * stage_bytes;
+  const uint32_t aux_s = base + region;
+  uint8_t* aux = gbase + region;
   const uint32_t bar_full = aux_s;
   const uint32_t bar_empty = aux_s + 64;
   const uint32_t bar_acc = aux_s + 128;
@@ -100,6 +194,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
+
+  // top-k list of this thread (split path: of its row's columns)
+  float tv[kMaxK];
+  int ti[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) { tv[j] = -INFINITY; ti[j] = -1; }
+  bool acc_ok = false;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -147,14 +248,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const int t = m0 + r;
-    const bool ok = mbar_wait(bar_acc, 0, p.status, s_abort);
+    acc_ok = mbar_wait(bar_acc, 0, p.status, s_abort);
     tc_fence_after();
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    if (ok && p.splits == 1) {
-      float tv[kMaxK];
-      int ti[kMaxK];
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) { tv[j] = -INFINITY; ti[j] = -1; }
+    if (acc_ok && p.splits == 1) {
       for (int c = 0; c < p.E; c += 32) {
         uint32_t v[32];
         tmem_ld32(tacc + c, v);
@@ -170,25 +267,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
         }
       }
       if (t < p.T) write_route(p, t, tv, ti);
-    } else if (ok) {
-      // split K: store this split's partial logits; route_finish_kernel sums the splits
-      float* part = p.partial + ((int64_t)blockIdx.y * p.T + t) * p.E;
-      for (int c = 0; c < p.E; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tacc + c, v);
-        tmem_ld_wait();
-        if (t < p.T) {
+    }
+  }
+
+  __syncwarp();  // the producer and MMA lanes rejoin their warps before any aligned barrier
+  if (p.splits > 1) {
+    // Every thread of every CTA of the cluster takes part in every cluster barrier below,
+    // whatever happened above (a bounded wait that ran out leaves zeros), so none can wait
+    // forever on a CTA that left.
+    const int rank = (int)cluster_ctarank();
+    const int et = tid - 64;  // epilogue thread 0..127
+    const int q = warp & 3;
+    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t part = base;  // the drained stage buffers (every MMA completed: bar_acc)
+    for (int c0 = 0; c0 < E_pad; c0 += p.chunk) {
+      if (warp >= 2) {
+        const uint32_t dst = part + (q * 32 + lane) * pstride;
+        for (int cc = 0; cc < p.chunk; cc += 32) {
+          uint32_t v[32];
+          if (acc_ok && nkb > 0) {
+            tmem_ld32(tacc + c0 + cc, v);
+            tmem_ld_wait();
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            if (c + i < p.E)
-              *reinterpret_cast<float4*>(part + c + i) =
-                  make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                              __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 4 * cc + 16 * i),
+                         "r"(v[4 * i]), "r"(v[4 * i + 1]), "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
+                         : "memory");
         }
       }
+      cluster_sync();  // every CTA's partial chunk is written
+      if (warp >= 2) {
+        if (p.splits == 2) reduce_chunk<2>(p, part, pstride, c0, rank, et, tv, ti);
+        else if (p.splits == 4) reduce_chunk<4>(p, part, pstride, c0, rank, et, tv, ti);
+        else reduce_chunk<8>(p, part, pstride, c0, rank, et, tv, ti);
+      }
+      cluster_sync();  // every CTA is done reading: the chunk may be overwritten, CTAs may leave
     }
-    tc_fence_before();
+    if (warp >= 2) {
+      if (p.splits == 2) finish_split<2>(p, rank, et, tv, ti);
+      else if (p.splits == 4) finish_split<4>(p, rank, et, tv, ti);
+      else finish_split<8>(p, rank, et, tv, ti);
+    }
   }
+  if (warp >= 2) tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -196,107 +321,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
   }
 }
 
-// Split-K router finish, one warp per token: sums the splits' partial logits in split order
-// (bit-identical from run to run), adds the bias, then selects the top k with k rounds of a
-// warp-shuffle argmax (larger logit first, lower expert index on ties) and writes the
-// renormalised softmax weights.  Lane l holds experts l, l+32, ...; loads are coalesced.
-
-// PER: logits per lane (E <= 32 PER), a compile-time size so that the arrays stay in registers
-template <int PER>
-__global__ void __launch_bounds__(256) route_finish_kernel(const __grid_constant__ RouteParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int per = (p.E + 31) / 32;
-  for (int64_t t = w; t < p.T; t += nw) {
-    float v[PER];
-    bool used[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = lane + 32 * i;
-      used[i] = true;
-      v[i] = -INFINITY;
-      if (i < per && e < p.E) {
-        // every split's partial in flight at once, then summed in split order
-        float part[kMaxRouteSplits];
-#pragma unroll
-        for (int sp = 0; sp < kMaxRouteSplits; ++sp)
-          part[sp] = sp < p.splits ? __ldcg(p.partial + ((int64_t)sp * p.T + t) * p.E + e) : 0.0f;
-        float acc = part[0];
-#pragma unroll
-        for (int sp = 1; sp < kMaxRouteSplits; ++sp)
-          if (sp < p.splits) acc += part[sp];
-        v[i] = acc + (p.bias ? p.bias[e] : 0.0f);
-        used[i] = false;
-        if (p.logits) p.logits[t * p.E + e] = v[i];
-      }
-    }
-    float tv[kMaxK];
-    int ti[kMaxK];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      tv[j] = -INFINITY;
-      ti[j] = -1;
-      if (j < p.k) {
-        float best = -INFINITY;
-        int bidx = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-          const int e = lane + 32 * i;
-          if (!used[i] && (v[i] > best || (v[i] == best && e < bidx))) { best = v[i]; bidx = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-          if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
-        }
-        if (bidx != 0x7fffffff && (bidx & 31) == lane) {
-#pragma unroll
-          for (int i = 0; i < PER; ++i)
-            if (i == (bidx >> 5)) used[i] = true;
-        }
-        tv[j] = best;
-        ti[j] = (bidx == 0x7fffffff) ? -1 : bidx;
-      }
-    }
-    if (lane == 0) write_route(p, (int)t, tv, ti);
-  }
-}
-
-// K splits so that the grid fills the GPU about once (T=4096 -> 4 splits of 28 k-blocks at
-// d=7168), at most route_splits_bound(); every split gets at least one k-block.
+// K splits: the largest power of two (at most 8, at most one per k-block) such that the token
+// tiles times the splits still fit on the GPU at once (T=4096 -> 4 splits of 28 k-blocks at
+// d=7168; T=64 -> 8; from 152 SMs' worth of token tiles on, 1).
 int route_splits(int64_t T, int d) {
   const int64_t mt = (T + BM - 1) / BM;
   const int nkb = d / BK;
-  int sp = (int)std::max<int64_t>(1, num_sms() / std::max<int64_t>(mt, 1));
-  sp = std::min(sp, route_splits_bound(T, d));
-  const int kps = (nkb + sp - 1) / sp;
-  return (nkb + kps - 1) / kps;
+  int sp = 1;
+  while (2 * sp <= kMaxRouteSplits && 2 * sp <= nkb && mt * 2 * sp <= num_sms()) sp *= 2;
+  return sp;
 }
 
-cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
+// Columns reduced per pass: all of E rounded up to 64 if 128 rows of them fit in the stage
+// buffers, else half.
+static int route_chunk(int E_pad, int region) {
+  int ch = E_pad;
+  while (ch > 32 && BM * (4 * ch + 16) > region) ch /= 2;
+  return ch;
+}
+
+cudaError_t launch_route(const RouteParams& p_in, cudaStream_t s) {
+  RouteParams p = p_in;
   const int E_pad = (p.E + 63) & ~63;
   const int stage_bytes = BM * BK * 2 + E_pad * BK * 2;
   const int stages = std::min(4, 196608 / stage_bytes);
-  const int smem = stages * stage_bytes + 1024 + 1024;
+  int region = stages * stage_bytes;
+  p.chunk = route_chunk(E_pad, region);
+  if (p.splits > 1) {
+    if (p.chunk % 32 || E_pad % p.chunk || (p.splits != 2 && p.splits != 4 && p.splits != 8))
+      return cudaErrorInvalidValue;
+    region = std::max(region, BM * (4 * p.chunk + 16));
+  }
+  const int smem = region + 1024 + 1024;
   cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.T + BM - 1) / BM, p.splits);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = p.splits;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.splits > 1 ? 1 : 0;
+  cfg.gridDim = dim3((p.T + BM - 1) / BM, p.splits);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
   prof_begin("route", s);
-  route_kernel<<<grid, kGemmThreads, smem, s>>>(p);
+  e = cudaLaunchKernelEx(&cfg, route_kernel, p);
   prof_end(s);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || p.splits == 1) return e;
-  const int64_t blocks = std::min<int64_t>((p.T + 7) / 8, (int64_t)num_sms() * 8);
-  prof_begin("route_finish", s);
-  const int per = (p.E + 31) / 32;
-  if (per <= 2) route_finish_kernel<2><<<(int)blocks, 256, 0, s>>>(p);
-  else if (per <= 4) route_finish_kernel<4><<<(int)blocks, 256, 0, s>>>(p);
-  else if (per <= 8) route_finish_kernel<8><<<(int)blocks, 256, 0, s>>>(p);
-  else route_finish_kernel<kMaxE / 32><<<(int)blocks, 256, 0, s>>>(p);
-  prof_end(s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mok

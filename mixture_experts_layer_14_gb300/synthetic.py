@@ -68,6 +68,10 @@ WORKLOADS = {
                                        0.0, "normal0.1", "mxfp8", False, 8),
     "dsv3_mxfp8_train_slice_e32": LayerShape("dsv3_mxfp8_train_slice_e32", 1024, 7168, 32, 8, 2048,
                                              2048, 1, 0.0, "normal0.1", "mxfp8", True, 11),
+    # a slice of the Kimi-class layer for profiler captures: the same rank-biased routing over 48
+    # experts (a few hot experts hold nearly every token, CTA-pair tiles), about 4 GB of weights
+    "kimi_skew_slice_e48": LayerShape("kimi_skew_slice_e48", 2048, 7168, 48, 8, 2048, 2048, 1, 0.0,
+                                      "zipf", "bf16", False, 12),
 }
 
 

@@ -44,7 +44,6 @@ from .moe import (  # noqa: F401
     moe_backward,
     moe_forward_mxfp8,
     moe_backward_mxfp8,
-    bf16_round,
 )
 from .mxfp8 import (  # noqa: F401
     E4M3_MAX,

@@ -147,10 +147,19 @@ def _experts_used(topk_idx):
     return sorted(set(int(e) for e in np.asarray(topk_idx).ravel()))
 
 
-def moe_forward(x, Wg, Wu, Wd, shared, topk_idx, topk_w):
+def _ffn_rows(job):
+    """Output rows of one expert's FFN (a module-level function so that a process pool can
+    run it)."""
+    X, Wg_e, Wu_e, Wd_e = job
+    return expert_ffn(X, np.asarray(Wg_e, dtype=np.float64), np.asarray(Wu_e, dtype=np.float64),
+                      np.asarray(Wd_e, dtype=np.float64))[3]
+
+
+def moe_forward(x, Wg, Wu, Wd, shared, topk_idx, topk_w, expert_map=map):
     """Layer output for the rows of x.  ``Wg/Wu/Wd`` are indexable by expert id (a stacked
-    array or any lazy accessor returning float64 [d,F] / [F,d] matrices); ``shared`` is
-    (Ws_gate, Ws_up, Ws_down) or None.  Pinned by: k = E with identical experts reduces to
+    array or any lazy accessor returning [d,F] / [F,d] matrices convertible to float64);
+    ``shared`` is (Ws_gate, Ws_up, Ws_down) or None; ``expert_map`` runs the per-expert work
+    (``map`` or a pool's ``imap``).  Pinned by: k = E with identical experts reduces to
     shared + FFN; token permutation permutes outputs; a zero router weight contributes nothing;
     E = k = 1 gives shared + FFN."""
     x = np.asarray(x, dtype=np.float64)
@@ -159,9 +168,10 @@ def moe_forward(x, Wg, Wu, Wd, shared, topk_idx, topk_w):
     y = np.zeros_like(x)
     if shared is not None:
         y += expert_ffn(x, *shared)[3]
-    for e in _experts_used(idx):  # float64: the summation order does not matter here
-        rows, slots = np.nonzero(idx == e)
-        ye = expert_ffn(x[rows], Wg[e], Wu[e], Wd[e])[3]
+    experts = _experts_used(idx)
+    sel = [np.nonzero(idx == e) for e in experts]
+    jobs = ((x[rows], Wg[e], Wu[e], Wd[e]) for e, (rows, _) in zip(experts, sel))
+    for (rows, slots), ye in zip(sel, expert_map(_ffn_rows, jobs)):  # float64: order is moot
         np.add.at(y, rows, w[rows, slots][:, None] * ye)
     return y
 
@@ -178,9 +188,35 @@ def moe_forward_from_logits(x, logits, topk_idx, Wg, Wu, Wd, shared):
 # a token did not select get no gradient from it.  Pinned by central finite differences.
 # --------------------------------------------------------------------------------------
 
-def moe_backward(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_experts=None):
+def _ffn_backward(job):
+    """Backward of one SwiGLU FFN on rows X with upstream dYr and router weights wr (a
+    module-level function so that a process pool can run it).  Returns (dX rows, dW_gate,
+    dW_up, dW_down, dw rows); the weight gradients are None unless job[-1] (weight_grads)."""
+    X, dYr, wr, Wge, Wue, Wde, weight_grads = job
+    Wge = np.asarray(Wge, dtype=np.float64)
+    Wue = np.asarray(Wue, dtype=np.float64)
+    Wde = np.asarray(Wde, dtype=np.float64)
+    g = X @ Wge
+    u = X @ Wue
+    s = 1.0 / (1.0 + np.exp(-g))
+    h = g * s * u
+    a = dYr @ Wde.T                      # dL/d(h) before the router weight
+    dwr = (a * h).sum(axis=1)            # <dY, h Wd> = <a, h>
+    dh = wr[:, None] * a
+    dg = dh * u * s * (1.0 + g * (1.0 - s))   # d SiLU(g)/dg = s (1 + g (1 - s))
+    du = dh * g * s
+    dXr = dg @ Wge.T + du @ Wue.T
+    if not weight_grads:
+        return dXr, None, None, None, dwr
+    return dXr, X.T @ dg, X.T @ du, (wr[:, None] * h).T @ dYr, dwr
+
+
+def moe_backward(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_experts=None,
+                 weight_grads=True, expert_map=map):
     """``only_experts`` (optional) restricts the routed-expert terms to those expert ids (for
     checks of sampled experts on large inputs; dX and the router terms are then partial).
+    ``weight_grads=False`` skips the weight gradients (returned as None); ``expert_map`` runs the
+    per-expert work (``map``, or a process pool's ``imap`` for large layers).
     Returns a dict with dX[T,d], dW_gate/dW_up[E,d,F], dW_down[E,F,d], dWs_gate/dWs_up[d,Fs],
     dWs_down[Fs,d] (None without a shared expert), dlogits[T,E], dW_router[d,E] and the
     per-route router-weight gradients dw[T,k] (= <dY_t, y_{e_j}(x_t)>)."""
@@ -197,34 +233,17 @@ def moe_backward(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_exp
     dWg, dWu, dWd = {}, {}, {}
     dw = np.zeros((T, k))
 
-    def ffn_backward(X, dYr, wr, Wge, Wue, Wde):
-        g = X @ Wge
-        u = X @ Wue
-        s = 1.0 / (1.0 + np.exp(-g))
-        h = g * s * u
-        a = dYr @ Wde.T                      # dL/d(h) before the router weight
-        dwr = (a * h).sum(axis=1)            # <dY, h Wd> = <a, h>
-        dh = wr[:, None] * a
-        dg = dh * u * s * (1.0 + g * (1.0 - s))   # d SiLU(g)/dg = s (1 + g (1 - s))
-        du = dh * g * s
-        dWde = (wr[:, None] * h).T @ dYr
-        dWge = X.T @ dg
-        dWue = X.T @ du
-        dXr = dg @ Wge.T + du @ Wue.T
-        return dXr, dWge, dWue, dWde, dwr
-
-    for e in (range(E) if only_experts is None else only_experts):
-        rows, slots = np.nonzero(idx == e)
-        if rows.size == 0:
-            continue
-        dXr, dWg[e], dWu[e], dWd[e], dwr = ffn_backward(
-            x[rows], dY[rows], w[rows, slots], Wg[e], Wu[e], Wd[e])
+    sel = [(e,) + np.nonzero(idx == e) for e in (range(E) if only_experts is None else only_experts)]
+    sel = [t for t in sel if t[1].size]
+    jobs = ((x[rows], dY[rows], w[rows, slots], Wg[e], Wu[e], Wd[e], weight_grads)
+            for e, rows, slots in sel)
+    for (e, rows, slots), (dXr, dWg[e], dWu[e], dWd[e], dwr) in zip(sel, expert_map(_ffn_backward, jobs)):
         np.add.at(dX, rows, dXr)
         dw[rows, slots] = dwr
 
     dWs = None
     if shared is not None:
-        dXs, dWsg, dWsu, dWsd, _ = ffn_backward(x, dY, np.ones(T), *shared)
+        dXs, dWsg, dWsu, dWsd, _ = _ffn_backward((x, dY, np.ones(T), *shared, weight_grads))
         dX += dXs
         dWs = (dWsg, dWsu, dWsd)
 
@@ -234,8 +253,10 @@ def moe_backward(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_exp
     np.put_along_axis(dl, idx, w * (dw - inner), axis=1)
     dX += dl @ Wr.T
     dWr = x.T @ dl
-    if only_experts is None:
-        Wg0 = np.asarray(Wg[0])
+    if not weight_grads:
+        dWg = dWu = dWd = None
+    elif only_experts is None:
+        Wg0 = np.asarray(Wg[0], dtype=np.float64)
         zg = np.zeros(Wg0.shape)
         zd = np.zeros(Wg0.shape[::-1])
         dWg = np.stack([dWg.get(e, zg) for e in range(E)])
@@ -269,28 +290,36 @@ def _mx_weight(W):
     return _mx_qd(np.asarray(W, dtype=np.float64).T).T
 
 
-def moe_forward_mxfp8(x, Wg, Wu, Wd, shared, topk_idx, topk_w):
+def _mx_ffn(job):
+    """One expert's FFN at the MXFP8 quantisation points, on rows X that are already quantised
+    (a module-level function so that a process pool can run it): g and u from weights quantised
+    along d, h quantised along F, then the down projection with its weight quantised along F."""
+    X, Wg_e, Wu_e, Wd_e = job
+    g = X @ _mx_weight(Wg_e)
+    u = X @ _mx_weight(Wu_e)
+    h = _mx_qd(silu(g) * u)
+    return h @ _mx_weight(Wd_e)
+
+
+def moe_forward_mxfp8(x, Wg, Wu, Wd, shared, topk_idx, topk_w, expert_map=map):
     """Layer output with the MXFP8 quantisation points of the path.  A composition of the
     pinned quantiser and FFN pieces; pinned further by: values exactly representable in MXFP8
-    are fixed points of the quantiser, zero down weights give a zero output, and the distance to
-    moe_forward on random data stays within a few E4M3 steps."""
+    are fixed points of the quantiser, zero down weights give a zero output, the distance to
+    moe_forward on random data stays within a few E4M3 steps, and the locality pins of every
+    quantisation axis.  ``expert_map`` runs the per-expert work (``map`` or a pool's ``imap``)."""
     x = np.asarray(x, dtype=np.float64)
     idx = np.asarray(topk_idx, dtype=np.int64)
     w = np.asarray(topk_w, dtype=np.float64)
     xq = _mx_qd(x)
 
-    def ffn(X, Wg_e, Wu_e, Wd_e):
-        g = X @ _mx_weight(Wg_e)
-        u = X @ _mx_weight(Wu_e)
-        h = _mx_qd(silu(g) * u)
-        return h @ _mx_weight(Wd_e)
-
     y = np.zeros_like(x)
     if shared is not None:
-        y += ffn(xq, *shared)
-    for e in _experts_used(idx):
-        rows, slots = np.nonzero(idx == e)
-        np.add.at(y, rows, w[rows, slots][:, None] * ffn(xq[rows], Wg[e], Wu[e], Wd[e]))
+        y += _mx_ffn((xq, *shared))
+    experts = _experts_used(idx)
+    sel = [np.nonzero(idx == e) for e in experts]
+    jobs = ((xq[rows], Wg[e], Wu[e], Wd[e]) for e, (rows, _) in zip(experts, sel))
+    for (rows, slots), ye in zip(sel, expert_map(_mx_ffn, jobs)):
+        np.add.at(y, rows, w[rows, slots][:, None] * ye)
     return y
 
 
@@ -308,16 +337,6 @@ def moe_forward_mxfp8(x, Wg, Wu, Wd, shared, topk_idx, topk_w):
 # router-weight gradient <a, h> stay unquantised.
 # --------------------------------------------------------------------------------------
 
-def bf16_round(a):
-    """Round to bf16 the way a float32 value is stored as bf16 (round to nearest, ties to even):
-    float64 -> float32 first, then the 16 low bits rounded off.  Pinned against the library's
-    float32 -> bfloat16 conversion."""
-    f = np.asarray(a, dtype=np.float64).astype(np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32).astype(np.float64)
-
-
 def _mx_qd_tokens(A):
     """Quantise-dequantise A[n, C] along its first axis (tokens) in blocks of 32 rows from row 0;
     a last partial block counts as padded with zeros (zeros do not change a block's amax)."""
@@ -328,19 +347,44 @@ def _mx_qd_tokens(A):
     return _mx_qd(Ap.T).T[:n]
 
 
+def _mx_ffn_backward(job):
+    """Backward of one expert's FFN at the MXFP8 quantisation points (a module-level function so
+    that a process pool can run it).  X, Xq: its rows of x and of q_d(x); dYr, dYrq likewise for
+    dY; wr its router weights.  Returns (dX rows, dW_gate, dW_up, dW_down, dw rows); the weight
+    gradients are None unless job[-1] (weight_grads)."""
+    X, Xq, dYr, dYrq, wr, Wge, Wue, Wde, weight_grads = job
+    Wge = np.asarray(Wge, dtype=np.float64)
+    Wue = np.asarray(Wue, dtype=np.float64)
+    Wde = np.asarray(Wde, dtype=np.float64)
+    g = Xq @ _mx_weight(Wge)                 # the MXFP8 forward's gate and up values
+    u = Xq @ _mx_weight(Wue)
+    s = 1.0 / (1.0 + np.exp(-g))
+    h = g * s * u
+    a = dYrq @ _mx_qd(Wde).T                 # W_down [F, d]: blocks along d
+    dwr = (a * h).sum(axis=1)
+    dh = wr[:, None] * a
+    dg = dh * u * s * (1.0 + g * (1.0 - s))
+    du = dh * g * s
+    dXr = _mx_qd(dg) @ _mx_qd(Wge).T + _mx_qd(du) @ _mx_qd(Wue).T   # W_gate [d, F]: along F
+    if not weight_grads:
+        return dXr, None, None, None, dwr
+    hw = wr[:, None] * h
+    Xt = _mx_qd_tokens(X)
+    dWge = Xt.T @ _mx_qd_tokens(dg)
+    dWue = Xt.T @ _mx_qd_tokens(du)
+    dWde = _mx_qd_tokens(hw).T @ _mx_qd_tokens(dYr)
+    return dXr, dWge, dWue, dWde, dwr
+
+
 def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, only_experts=None,
-                       bf16_stored=False):
+                       weight_grads=True, expert_map=map):
     """Gradients with the MXFP8 quantisation points above; same arguments and result keys as
     moe_backward.  Pinned by: every gradient stays within a few E4M3 steps of moe_backward's
     (itself pinned by finite differences) and differs from it; on inputs and weights exactly
     representable in MXFP8 the router-weight gradients, dlogits and dW_router equal the float64
-    ones; the token-axis quantiser matches the pinned quantiser applied column by column.
-
-    bf16_stored: the activations a training step keeps in memory between the forward and the
-    backward, G and U, are rounded to bf16 where they are stored (bf16_round); dG, dU and w h
-    are quantised straight from their values.  E4M3 re-quantisation turns that rounding into
-    whole-step code changes for a few per cent of the elements, so this variant is the closer
-    reference for a path that stores G and U in bf16."""
+    ones; the token-axis quantiser matches the pinned quantiser applied column by column; and
+    by locality pins of every quantisation axis (an outlier coarsens only the values of its own
+    block along that GEMM's reduction dimension)."""
     x = np.asarray(x, dtype=np.float64)
     dY = np.asarray(dY, dtype=np.float64)
     Wr = np.asarray(W_router, dtype=np.float64)
@@ -355,41 +399,17 @@ def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, on
     dWg, dWu, dWd = {}, {}, {}
     dw = np.zeros((T, k))
 
-    def ffn_backward(X, Xq, dYr, dYrq, wr, Wge, Wue, Wde):
-        Wge = np.asarray(Wge, dtype=np.float64)
-        Wue = np.asarray(Wue, dtype=np.float64)
-        Wde = np.asarray(Wde, dtype=np.float64)
-        g = Xq @ _mx_weight(Wge)                 # the MXFP8 forward's gate and up values
-        u = Xq @ _mx_weight(Wue)
-        if bf16_stored:
-            g, u = bf16_round(g), bf16_round(u)
-        s = 1.0 / (1.0 + np.exp(-g))
-        h = g * s * u
-        a = dYrq @ _mx_qd(Wde).T                 # W_down [F, d]: blocks along d
-        dwr = (a * h).sum(axis=1)
-        dh = wr[:, None] * a
-        dg = dh * u * s * (1.0 + g * (1.0 - s))
-        du = dh * g * s
-        dXr = _mx_qd(dg) @ _mx_qd(Wge).T + _mx_qd(du) @ _mx_qd(Wue).T   # W_gate [d, F]: along F
-        hw = wr[:, None] * h
-        Xt = _mx_qd_tokens(X)
-        dWge = Xt.T @ _mx_qd_tokens(dg)
-        dWue = Xt.T @ _mx_qd_tokens(du)
-        dWde = _mx_qd_tokens(hw).T @ _mx_qd_tokens(dYr)
-        return dXr, dWge, dWue, dWde, dwr
-
-    for e in (range(E) if only_experts is None else only_experts):
-        rows, slots = np.nonzero(idx == e)
-        if rows.size == 0:
-            continue
-        dXr, dWg[e], dWu[e], dWd[e], dwr = ffn_backward(
-            x[rows], xq[rows], dY[rows], dYq[rows], w[rows, slots], Wg[e], Wu[e], Wd[e])
+    sel = [(e,) + np.nonzero(idx == e) for e in (range(E) if only_experts is None else only_experts)]
+    sel = [t for t in sel if t[1].size]
+    jobs = ((x[rows], xq[rows], dY[rows], dYq[rows], w[rows, slots], Wg[e], Wu[e], Wd[e], weight_grads)
+            for e, rows, slots in sel)
+    for (e, rows, slots), (dXr, dWg[e], dWu[e], dWd[e], dwr) in zip(sel, expert_map(_mx_ffn_backward, jobs)):
         np.add.at(dX, rows, dXr)
         dw[rows, slots] = dwr
 
     dWs = None
     if shared is not None:
-        dXs, dWsg, dWsu, dWsd, _ = ffn_backward(x, xq, dY, dYq, np.ones(T), *shared)
+        dXs, dWsg, dWsu, dWsd, _ = _mx_ffn_backward((x, xq, dY, dYq, np.ones(T), *shared, weight_grads))
         dX += dXs
         dWs = (dWsg, dWsu, dWsd)
 
@@ -398,8 +418,10 @@ def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, on
     np.put_along_axis(dl, idx, w * (dw - inner), axis=1)
     dX += dl @ Wr.T
     dWr = x.T @ dl
-    if only_experts is None:
-        Wg0 = np.asarray(Wg[0])
+    if not weight_grads:
+        dWg = dWu = dWd = None
+    elif only_experts is None:
+        Wg0 = np.asarray(Wg[0], dtype=np.float64)
         zg = np.zeros(Wg0.shape)
         zd = np.zeros(Wg0.shape[::-1])
         dWg = np.stack([dWg.get(e, zg) for e in range(E)])

@@ -127,3 +127,15 @@ def test_plain_c_program_uses_the_abi():
         env["LD_LIBRARY_PATH"] = ":".join(cuda_libs + [pkg, env.get("LD_LIBRARY_PATH", "")])
         r = subprocess.run([exe], capture_output=True, text=True, env=env, timeout=60)
         assert r.returncode == 0 and "abi_check ok" in r.stdout, r.stdout + r.stderr
+
+
+def test_forward_schedule_values():
+    """The process-wide forward schedule takes its two values and refuses others (host only)."""
+    mok.lib()
+    prev = mok.set_forward_schedule(mok.SCHEDULE_FUSED)
+    try:
+        assert mok.set_forward_schedule(mok.SCHEDULE_TWO_LAUNCHES) == mok.SCHEDULE_FUSED
+        with pytest.raises(mok.MokError):
+            mok.set_forward_schedule(7)
+    finally:
+        mok.set_forward_schedule(prev)

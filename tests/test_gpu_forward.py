@@ -258,3 +258,22 @@ def test_layer_is_cuda_graph_capturable():
     torch.cuda.synchronize()
     assert torch.equal(y_replay, y_eager)
     assert torch.equal(dX_replay, g_eager["dX"])
+
+
+@pytest.mark.parametrize("name", ["tiny", "k_eq_E_noshared", "one_token", "wide_E", "max_E_k"])
+def test_fused_schedule_is_bit_identical(name):
+    """The fused schedule (gate/up and down in one persistent launch, tiles claimed from a device
+    work counter, down tiles gated by per-M-tile readiness counters) gives exactly the output of
+    the two-launch schedule, twice in a row."""
+    shape = CASES[name]
+    L = make_layer(shape, "cpu")
+    D, Ld, ws, idx, w, logits, routing, y0 = _run_gpu(shape, L)
+    prev = mok.set_forward_schedule(mok.SCHEDULE_FUSED)
+    try:
+        y1 = mok.moe_forward(D, Ld, Ld["x"], routing, ws)
+        y2 = mok.moe_forward(D, Ld, Ld["x"], routing, ws)
+        torch.cuda.synchronize()
+    finally:
+        mok.set_forward_schedule(prev)
+    assert mok.read_status(ws) == 0
+    assert torch.equal(y1, y0) and torch.equal(y2, y0)

@@ -1,9 +1,13 @@
 """Parity at the full workload sizes, in the launch configuration bench.py times.
 
 Routing, counts, offsets and the schedule are checked on every token against the oracle (cheap:
-2 T d E flops).  The layer output is checked on sampled tokens, whose rows the oracle computes
-one by one.  The backward is checked on sampled tokens (dX, dlogits) and on sampled experts in
-full (dW over all their tokens), plus the shared expert's weight gradients."""
+2 T d E flops).  The layer output is checked on at least 64 tokens chosen so that every active
+expert is reached (the hottest one, and every expert that holds a single token, included),
+whose rows the oracle computes one expert at a time in a process pool.  The backward is checked
+on 32 tokens that reach as many experts as possible (dX, dlogits), on four experts in full (dW
+over all their tokens: the hottest, the least busy non-empty one, a median one and one whose
+rows end in a part-filled 128-row tile; dlogits of all those tokens and the four experts'
+columns of dW_router), and on the shared expert's weight gradients."""
 
 import numpy as np
 import pytest
@@ -12,12 +16,14 @@ import torch
 import mixture_experts_layer_14_gb300 as mok
 import oracle
 from mixture_experts_layer_14_gb300.synthetic import WORKLOADS, make_layer
-from tests._helpers import NEAR_TIE, LazyExperts, assert_close, dims_of, ensure_lib, f64
+from tests._fullsize import dw_experts, experts_of, most_experts_tokens, oracle_pool, sampled_tokens
+from tests._helpers import NEAR_TIE, assert_close, dims_of, ensure_lib, f64
 
 pytestmark = pytest.mark.gpu
 
 
-def _route_checks(shape, L, layer):
+def route_checks(shape, L, layer):
+    """Selection (bit-exact off near ties), counts, offsets, schedule and weights on all tokens."""
     x64 = f64(L["x"])
     Wr = f64(L["W_router"])
     b = None if L["bias"] is None else f64(L["bias"])
@@ -38,13 +44,12 @@ def _route_checks(shape, L, layer):
     return x64, Wr, l64, got, counts, n_near
 
 
-def _shared(L):
+def shared_of(L):
     return (f64(L["Ws_gate"]), f64(L["Ws_up"]), f64(L["Ws_down"]))
 
 
-@pytest.mark.parametrize("name,samples", [("dsv3_bf16_fwd", 4), ("kimi_skew_bf16_fwd", 4),
-                                          ("dsv3_decode_t64", 4)])
-def test_fullsize_forward(name, samples):
+@pytest.mark.parametrize("name", ["dsv3_bf16_fwd", "kimi_skew_bf16_fwd", "dsv3_decode_t64"])
+def test_fullsize_forward(name):
     ensure_lib()
     shape = WORKLOADS[name]
     L = make_layer(shape, "cuda")
@@ -52,20 +57,27 @@ def test_fullsize_forward(name, samples):
     y = layer.forward(L["x"])
     torch.cuda.synchronize()
     assert mok.read_status(layer.ws) == 0
-    x64, Wr, l64, got, counts, n_near = _route_checks(shape, L, layer)
+    x64, Wr, l64, got, counts, n_near = route_checks(shape, L, layer)
+    toks = sampled_tokens(got, counts, shape.T)
     print(f"{name}: near-tie tokens excluded {n_near}; hottest expert {counts.max()} rows "
-          f"(mean {counts.mean():.1f}); empty experts {(counts == 0).sum()}")
-    # sampled tokens: include one routed to the hottest expert
-    hot = int(np.argmax(counts))
-    toks = [0, shape.T - 1, int(np.nonzero((got == hot).any(1))[0][0]), shape.T // 2][:samples]
+          f"(mean {counts.mean():.1f}); empty experts {(counts == 0).sum()}; {len(toks)} sampled "
+          f"tokens reach all {(counts > 0).sum()} active experts")
     w_ref = oracle.weights_for_selection(l64[toks], got[toks])
-    y_ref = oracle.moe_forward(x64[toks], LazyExperts(L["W_gate"]), LazyExperts(L["W_up"]),
-                               LazyExperts(L["W_down"]), _shared(L), got[toks], w_ref)
-    assert_close("y sampled", f64(y[toks]), y_ref)
-    # bit-identical rerun
+    Wg, Wu, Wd = experts_of(L)
+    with oracle_pool() as pmap:
+        y_ref = oracle.moe_forward(x64[toks], Wg, Wu, Wd, shared_of(L), got[toks], w_ref, expert_map=pmap)
+    mx, mn = assert_close("y sampled", f64(y[toks]), y_ref)
+    print(f"{name}: y on {len(toks)} tokens max_rel {mx:.2e} mean_rel {mn:.2e}")
+    # bit-identical rerun, and the same output from the fused schedule (where it applies)
     y2 = layer.forward(L["x"])
-    torch.cuda.synchronize()
-    assert torch.equal(y, y2)
+    prev = mok.set_forward_schedule(mok.SCHEDULE_FUSED)
+    try:
+        y3 = layer.forward(L["x"])
+        torch.cuda.synchronize()
+    finally:
+        mok.set_forward_schedule(prev)
+    assert mok.read_status(layer.ws) == 0
+    assert torch.equal(y, y2) and torch.equal(y, y3)
 
 
 def test_fullsize_training_backward():
@@ -77,33 +89,44 @@ def test_fullsize_training_backward():
     g = layer.backward(L["x"], L["dY"])
     torch.cuda.synchronize()
     assert mok.read_status(layer.ws) == 0 and mok.read_status(layer._ws_bwd) == 0
-    x64, Wr, l64, got, counts, _ = _route_checks(shape, L, layer)
+    x64, Wr, l64, got, counts, _ = route_checks(shape, L, layer)
     dY = L["dY"]
-    Wg, Wu, Wd = LazyExperts(L["W_gate"]), LazyExperts(L["W_up"]), LazyExperts(L["W_down"])
-    sh = _shared(L)
-    # dX and dlogits on sampled tokens (per-token quantities)
-    toks = [0, 1, shape.T - 1]
-    ref = oracle.moe_backward(x64[toks], f64(dY[toks]), Wr, Wg, Wu, Wd, sh, l64[toks], got[toks])
+    Wg, Wu, Wd = experts_of(L)
+    sh = shared_of(L)
+    toks = most_experts_tokens(got, 32)
+    picks = dw_experts(counts)
+    with oracle_pool() as pmap:
+        # dX and dlogits on sampled tokens (per-token quantities)
+        ref = oracle.moe_backward(x64[toks], f64(dY[toks]), Wr, Wg, Wu, Wd, sh, l64[toks], got[toks],
+                                  weight_grads=False, expert_map=pmap)
+        # dW of four experts in full: all tokens routed to them, one pool job per expert
+        rows = np.nonzero(np.isin(got, picks).any(1))[0]
+        rw = oracle.moe_backward(x64[rows], f64(dY[rows]), Wr, Wg, Wu, Wd, None, l64[rows], got[rows],
+                                 only_experts=picks, expert_map=pmap)
+        # every expert of those tokens: their dlogits, and the columns of dW_router = x^T dl of
+        # the four experts (all tokens with a nonzero dl in such a column are in these rows)
+        rr = oracle.moe_backward(x64[rows], f64(dY[rows]), Wr, Wg, Wu, Wd, sh, l64[rows], got[rows],
+                                 weight_grads=False, expert_map=pmap)
+    n_exp = len(set(got[toks].ravel().tolist()))
     assert_close("dX sampled", f64(g["dX"][toks]), ref["dX"])
     assert_close("dlogits sampled", f64(g["dlogits"][toks]), ref["dlogits"])
-    # dW of two experts in full: all tokens routed to them
-    for e in (int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))):
-        rows = np.nonzero((got == e).any(1))[0]
-        r = oracle.moe_backward(x64[rows], f64(dY[rows]), Wr, Wg, Wu, Wd, None, l64[rows], got[rows],
-                                only_experts=[e])
-        assert_close(f"dW_gate[{e}]", f64(g["dW_gate"][e]), r["dW_gate"][e])
-        assert_close(f"dW_up[{e}]", f64(g["dW_up"][e]), r["dW_up"][e])
-        assert_close(f"dW_down[{e}]", f64(g["dW_down"][e]), r["dW_down"][e])
+    print(f"dX, dlogits on {len(toks)} tokens reaching {n_exp} experts; dW in full for experts "
+          f"{picks} with {[int(counts[e]) for e in picks]} rows")
+    for e in picks:
+        for key in ("dW_gate", "dW_up", "dW_down"):
+            assert_close(f"{key}[{e}]", f64(g[key][e]), rw[key][e])
     # shared expert weight gradients over all tokens (the oracle with no routed-expert terms)
     rs = oracle.moe_backward(x64, f64(dY), Wr, Wg, Wu, Wd, sh, l64, got, only_experts=[])
     for key in ("dWs_gate", "dWs_up", "dWs_down"):
         assert_close(key, f64(g[key]), rs[key])
-    # dW_router = x^T dlogits: consistent with the GPU's own dlogits (property at full size)
+    assert_close("dlogits of those tokens", f64(g["dlogits"][rows]), rr["dlogits"])
+    assert_close("dW_router columns", f64(g["dW_router"][:, picks]), rr["dW_router"][:, picks])
+    # dW_router = x^T dlogits over all tokens: consistent with the GPU's own dlogits
     assert_close("dW_router vs x^T dlogits", f64(g["dW_router"]), x64.T @ f64(g["dlogits"]))
-    _assert_dlogit_rows_sum_to_zero(g["dlogits"])
+    assert_dlogit_rows_sum_to_zero(g["dlogits"])
 
 
-def _assert_dlogit_rows_sum_to_zero(dlogits):
+def assert_dlogit_rows_sum_to_zero(dlogits):
     """Every token's logit gradient sums to zero: dl_m = w_m (dw_m - sum_j w_j dw_j) over the
     selection and sum_m w_m = 1 (the renormalised softmax), a property of all T tokens."""
     dl = f64(dlogits)

@@ -56,3 +56,4 @@ def test_sizes_past_the_scratch_are_refused(T, E):
     fake = ctypes.c_void_p(0x1000)
     rc = L.mok_dispatch_index_noalloc(ctypes.byref(D), fake, fake, fake, fake, fake, fake, fake, None)
     assert rc == -3
+
