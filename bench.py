@@ -502,6 +502,7 @@ def run_mok(args, shape, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     peaks = load_peaks()
+    mok.set_forward_schedule(mok.SCHEDULE_FUSED if args.schedule == "fused" else mok.SCHEDULE_TWO_LAUNCHES)
     res, L = measure(args, shape, args.steps, args.warmup, dev, world, peaks)
     D = mok.dims(shape.T, shape.d, shape.E, shape.k, shape.F, shape.F_shared, shape.n_shared)
     e2e = None
@@ -521,7 +522,7 @@ def run_mok(args, shape, rank, world, local_rank):
                                            "weight_gb_per_step")},
         "tflops": res["tflops"], "tflops_frac_of_bf16_peak": res["tflops_frac_of_bf16_peak"],
         "roofline": res["roofline"], "kernels": res["kernels"], "kernel_timing": res["kernel_timing"],
-        "gpu_launches": res["gpu_launches"],
+        "gpu_launches": res["gpu_launches"], "forward_schedule": args.schedule,
         "clocks": res["clocks"], "e2e": e2e, "cuda_graph": graph,
     }
     for key in ("fp8_cublas_tflops_measured", "tflops_frac_of_measured_fp8_gemm"):
@@ -657,6 +658,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
     ap.add_argument("--workload", default="kimi_skew_bf16_fwd", choices=sorted(WORKLOADS))
+    ap.add_argument("--schedule", choices=["two_launches", "fused"], default="two_launches",
+                    help="schedule of the bf16 forward's expert GEMMs (mok_set_forward_schedule)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

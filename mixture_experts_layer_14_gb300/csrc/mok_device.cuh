@@ -50,13 +50,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// 16 bytes from the shared memory of a CTA of the cluster (`addr` from mapa_shared).
+// 16 bytes from the shared memory of a CTA of the cluster (`addr` from mapa_shared).  Volatile
+// (kept in order with the cluster barriers around it) without a memory clobber, so that several
+// can be in flight at once.
 __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
+               : "r"(addr));
   return v;
 }
 // One arrival on the barrier at a cluster address (any CTA of the cluster, this one included),

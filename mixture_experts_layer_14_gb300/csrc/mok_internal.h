@@ -96,6 +96,7 @@ struct GemmParams {
   int ntb[2];
   int* work;
   int* ready;
+  int nfast_mt;         // M-grouped: groups of at least this many M tiles run N tiles fastest (0: never)
   int* status;
 };
 

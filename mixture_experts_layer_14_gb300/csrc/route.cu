@@ -115,21 +115,34 @@ __device__ __forceinline__ void reduce_chunk(const RouteParams& p, uint32_t part
   uint32_t src[S];
 #pragma unroll
   for (int r = 0; r < S; ++r) src[r] = mapa_shared(mine, r);
-  for (int j = sub; j < p.chunk / 4; j += S) {
-    float4 acc = ld_shared_cluster_v4(src[0] + 16 * j);
+  // two float4 columns per pass, every load issued first
+  const int n4 = p.chunk / 4;
+  for (int j0 = sub; j0 < n4; j0 += 2 * S) {
+    float4 v[2][S];
 #pragma unroll
-    for (int r = 1; r < S; ++r) {
-      const float4 v = ld_shared_cluster_v4(src[r] + 16 * j);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-    }
-    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int e = c0 + 4 * j + c;
-      if (e < p.E) {
-        const float l = a4[c] + (p.bias ? p.bias[e] : 0.0f);
-        if (t < p.T && p.logits) p.logits[(int64_t)t * p.E + e] = l;
-        if (ranks_before(l, e, tv[kMaxK - 1], ti[kMaxK - 1])) topk_insert(tv, ti, l, e);
+      for (int r = 0; r < S; ++r)
+        v[h][r] = (j0 + h * S < n4) ? ld_shared_cluster_v4(src[r] + 16 * (j0 + h * S))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (j0 + h * S >= n4) break;
+      float4 acc = v[h][0];
+#pragma unroll
+      for (int r = 1; r < S; ++r) {
+        acc.x += v[h][r].x; acc.y += v[h][r].y; acc.z += v[h][r].z; acc.w += v[h][r].w;
+      }
+      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+      const int j = j0 + h * S;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int e = c0 + 4 * j + c;
+        if (e < p.E) {
+          const float l = a4[c] + (p.bias ? p.bias[e] : 0.0f);
+          if (t < p.T && p.logits) p.logits[(int64_t)t * p.E + e] = l;
+          if (ranks_before(l, e, tv[kMaxK - 1], ti[kMaxK - 1])) topk_insert(tv, ti, l, e);
+        }
       }
     }
   }
