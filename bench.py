@@ -208,32 +208,28 @@ def work_model(shape, counts):
     return m, layer_flops, e_act
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from ncu slice captures of the
-# DeepSeek-V3-shaped workloads (32-expert slices with the same rows per expert: 33 weight sets),
-# per weight set streamed (routed experts with tokens + shared expert), valid only while the
-# kernel source is the one that was captured (sha1 prefix).
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum, a one-pass ncu metric
+# captured on the full-size workload) for (workload, kernel), valid only while the kernel source
+# is the one that was captured (sha1 prefix of the file); None otherwise.
 _GEMM_SRC = "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"
 PROFILED_TRAFFIC = {
-    "gemm_fwd_gate_up": ("f2054d2aed7b", (2.015065e9 + 19.827712e6) / 33, _GEMM_SRC),
-    "gemm_fwd_down": ("f2054d2aed7b", (0.992473e9 + 61.332736e6) / 33, _GEMM_SRC),
-    "gemm_fwd_gate_up_mx": ("f2054d2aed7b", (1.080146e9 + 20.816640e6) / 33, _GEMM_SRC),
-    "gemm_fwd_down_mx": ("f2054d2aed7b", (0.519241e9 + 114.185216e6) / 33, _GEMM_SRC),
-    "gemm_bwd_da": ("f2054d2aed7b", (1.198966e9 + 0.101213e9) / 33, _GEMM_SRC),
-    "gemm_bwd_dx": ("f2054d2aed7b", (2.062313e9 + 0.127839e9) / 33, _GEMM_SRC),
-    "gemm_bwd_dw": ("f2054d2aed7b", (0.378002e9 + 2.851659e9) / 33, _GEMM_SRC),
+    # ncu captures of the Kimi-class forward at full size (4th step of a 3-warm-up bench run)
+    ("kimi_skew_bf16_fwd", "gemm_fwd_gate_up"): ("a18a59b0736f", 20.885e9 + 0.606e9, _GEMM_SRC),
+    ("kimi_skew_bf16_fwd", "gemm_fwd_down"): ("a18a59b0736f", 4.632e9 + 2.103e9, _GEMM_SRC),
 }
 
 
-def profiled_traffic(name, weight_sets):
+def profiled_traffic(workload, name):
     import hashlib
 
-    if name not in PROFILED_TRAFFIC:
+    key = (workload, name)
+    if key not in PROFILED_TRAFFIC:
         return None
-    sha, per_set, src = PROFILED_TRAFFIC[name]
+    sha, nbytes, src = PROFILED_TRAFFIC[key]
     with open(os.path.join(ROOT, src), "rb") as f:
         if hashlib.sha1(f.read()).hexdigest()[:12] != sha:
             return None  # the kernel changed since the counters were taken
-    return per_set * weight_sets
+    return nbytes
 
 
 # What each forward kernel's algorithmic bytes count (a kernel's own re-reads of rows it
@@ -409,15 +405,13 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
                  "share": round((tms / max(sampled, 1)) / max(ms / steps, 1e-9), 4)}
         if name in model:
             r = roofline_of(name, model, tms / max(n, 1), peaks, sustained)
-            if not shape.backward:
-                r["traffic"] = profiled_traffic(name, e_act + shape.n_shared)
+            r["traffic"] = profiled_traffic(shape.name, name)
             entry["roofline"] = {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in r.items()}
         kernels[name] = entry
     dominant = max((n for n in kern if n in model), key=lambda n: kern[n][1])
     dn, dms = kern[dominant]
     roof = roofline_of(dominant, model, dms / dn, peaks, sustained)
-    roof.update({"kernel": dominant, "traffic": profiled_traffic(dominant, e_act + shape.n_shared)
-                 if not shape.backward else None,
+    roof.update({"kernel": dominant, "traffic": profiled_traffic(shape.name, dominant),
                  "peak_source": "measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
                  else "fallback"})
     tflops = layer_flops * steps / (ms / 1e3) / 1e12
