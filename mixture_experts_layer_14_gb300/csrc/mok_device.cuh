@@ -50,12 +50,19 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// 16 bytes from the shared memory of a CTA of the cluster (`addr` from mapa_shared).  Volatile
-// (kept in order with the cluster barriers around it) without a memory clobber, so that several
-// can be in flight at once.
-__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
+// 16 bytes into the shared memory of a CTA of the cluster (`addr` from mapa_shared); a later
+// cluster barrier (release/acquire) makes them visible there.
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, uint32_t a, uint32_t b,
+                                                     uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+// 16 bytes from this CTA's shared memory.  Volatile (kept in order with the barriers around it)
+// without a memory clobber, so that several can be in flight at once.
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
   float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "r"(addr));
   return v;

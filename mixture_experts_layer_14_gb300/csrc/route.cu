@@ -6,34 +6,39 @@
 //
 // One CTA per (128-token tile, K split).  Warp 0 issues TMA loads of the x tile (K-major) and of
 // all E columns of W_router (MN-major), warp 1 issues the UMMAs (N = E rounded up to 64, split
-// into MMAs of at most 256 columns), warps 2..5 run the epilogue.
+// into MMAs of at most 256 columns), warps 2..5 run the epilogue.  The bias is staged in shared
+// memory once, so the epilogue reads it as broadcast vectors.
 //  - One split (the token tiles alone fill the GPU): each epilogue thread owns one token row of
-//    the accumulator and selects its top k straight from TMEM.
-//  - S > 1 splits (a power of two): the S CTAs of a tile form a thread-block cluster.  Each
-//    writes its partial logits to its own shared memory (reusing the drained stage buffers, a
-//    chunk of columns at a time), and CTA r reduces tile rows r 128/S .. (r+1) 128/S - 1: S
-//    threads per row each sum every CTA's partial of a quarter of the columns in rank order
-//    (distributed shared memory; the same fixed order on every run), keep their own top-k list,
-//    and merge the S lists with warp shuffles.  The partial logits never leave the chip.
+//    the accumulator and selects its top k straight from TMEM, loading the next 32 columns while
+//    it ranks the current ones.
+//  - S > 1 splits (a power of two): the S CTAs of a tile form a thread-block cluster, and CTA r
+//    reduces tile rows r 128/S .. (r+1) 128/S - 1.  Each CTA stores the partial logits of those
+//    rows straight into CTA r's shared memory (the drained stage buffers, one slot per source
+//    CTA, a chunk of columns at a time), so no thread waits on a remote load.  Then S threads
+//    per row each sum the S partials of a quarter of the columns in rank order (the same fixed
+//    order on every run), keep their own top-k list, and merge the S lists with warp shuffles.
+//    The partial logits never leave the chip.
 #include "mok_device.cuh"
 
 namespace mok {
 
+// Inserts (v, e) into the descending list (tv, ti): v lands before the first entry it strictly
+// exceeds and the tail shifts down one place; nothing changes if it exceeds none (also for NaN).
+// Experts arrive in ascending index order, so among equal logits the lower index stays ahead.
+// Every slot's new value is computed from the old list alone, so the update is a few dependent
+// instructions deep instead of a chain through all k slots.
 __device__ __forceinline__ void topk_insert(float (&tv)[kMaxK], int (&ti)[kMaxK], float v, int e) {
-  // Bubble (v, e) into the descending list.  Experts arrive in ascending index order and the
-  // comparison is strict, so among equal logits the lower index stays ahead.
-  float cv = v;
-  int ci = e;
+  bool keep[kMaxK];  // slot j keeps its entry (v does not exceed it)
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    const bool sw = cv > tv[j];
-    const float ov = tv[j];
-    const int oi = ti[j];
-    tv[j] = sw ? cv : ov;
-    ti[j] = sw ? ci : oi;
-    cv = sw ? ov : cv;
-    ci = sw ? oi : ci;
+  for (int j = 0; j < kMaxK; ++j) keep[j] = !(v > tv[j]);
+#pragma unroll
+  for (int j = kMaxK - 1; j >= 1; --j) {
+    const bool here = !keep[j] && keep[j - 1];
+    tv[j] = keep[j] ? tv[j] : (here ? v : tv[j - 1]);
+    ti[j] = keep[j] ? ti[j] : (here ? e : ti[j - 1]);
   }
+  tv[0] = keep[0] ? tv[0] : v;
+  ti[0] = keep[0] ? ti[0] : e;
 }
 
 // w_j = softmax(l)[e_j] / sum_sel softmax(l)[e_i] = exp(l_j - l_0) / sum_i exp(l_i - l_0)
@@ -100,48 +105,47 @@ __device__ __forceinline__ void merge_topk(int k, float (&tv)[kMaxK], int (&ti)[
   }
 }
 
-// Splits > 1, one pass over logit columns c0 .. c0 + p.chunk - 1: thread `et` (0..127) of the
-// epilogue sums the S partials of its row's columns 4 (sub + S i) .. + 3 in cluster rank order,
-// adds the bias and inserts them into its top-k list.
+// Splits > 1, one pass over logit columns c0 .. c0 + p.chunk - 1, after every CTA of the cluster
+// has stored its partials of this CTA's rows: slot r of `part` holds CTA r's partial logits of
+// rows rank 128/S .. (rank+1) 128/S - 1.  Thread `et` (0..127) of the epilogue sums the S
+// partials of its row's columns 4 (sub + S i) .. + 3 in rank order, adds the bias and inserts
+// them into its top-k list.
 template <int S>
-__device__ __forceinline__ void reduce_chunk(const RouteParams& p, uint32_t part, uint32_t pstride,
-                                             int c0, int rank, int et, float (&tv)[kMaxK],
-                                             int (&ti)[kMaxK]) {
-  constexpr int RPC = BM / S;            // rows this CTA reduces
-  const int row = rank * RPC + et / S;   // row of the tile
+__device__ __forceinline__ void reduce_rows(const RouteParams& p, uint32_t part, uint32_t pstride,
+                                            int c0, int rank, int et, const float* s_bias,
+                                            float (&tv)[kMaxK], int (&ti)[kMaxK]) {
+  constexpr int RPC = BM / S;           // rows this CTA reduces
+  const int row = et / S;               // of this CTA's rows
   const int sub = et % S;
-  const int t = blockIdx.x * BM + row;
+  const int t = blockIdx.x * BM + rank * RPC + row;
   const uint32_t mine = part + row * pstride;
-  uint32_t src[S];
-#pragma unroll
-  for (int r = 0; r < S; ++r) src[r] = mapa_shared(mine, r);
-  // two float4 columns per pass, every load issued first
   const int n4 = p.chunk / 4;
+  // two float4 columns per pass, every load issued first
   for (int j0 = sub; j0 < n4; j0 += 2 * S) {
     float4 v[2][S];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int r = 0; r < S; ++r)
-        v[h][r] = (j0 + h * S < n4) ? ld_shared_cluster_v4(src[r] + 16 * (j0 + h * S))
+        v[h][r] = (j0 + h * S < n4) ? ld_shared_v4(mine + r * RPC * pstride + 16 * (j0 + h * S))
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      if (j0 + h * S >= n4) break;
+      const int j = j0 + h * S;
+      if (j >= n4) break;
       float4 acc = v[h][0];
 #pragma unroll
       for (int r = 1; r < S; ++r) {
         acc.x += v[h][r].x; acc.y += v[h][r].y; acc.z += v[h][r].z; acc.w += v[h][r].w;
       }
-      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-      const int j = j0 + h * S;
+      const float4 b4 = reinterpret_cast<const float4*>(s_bias + c0)[j];
+      const float a4[4] = {acc.x + b4.x, acc.y + b4.y, acc.z + b4.z, acc.w + b4.w};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int e = c0 + 4 * j + c;
         if (e < p.E) {
-          const float l = a4[c] + (p.bias ? p.bias[e] : 0.0f);
-          if (t < p.T && p.logits) p.logits[(int64_t)t * p.E + e] = l;
-          if (ranks_before(l, e, tv[kMaxK - 1], ti[kMaxK - 1])) topk_insert(tv, ti, l, e);
+          if (t < p.T && p.logits) p.logits[(int64_t)t * p.E + e] = a4[c];
+          topk_insert(tv, ti, a4[c], e);
         }
       }
     }
@@ -158,6 +162,8 @@ __device__ __forceinline__ void finish_split(const RouteParams& p, int rank, int
   const int t = blockIdx.x * BM + row;
   if (et % S == 0 && t < p.T) write_route(p, t, ov, oi);
 }
+
+constexpr int kRouteAuxBytes = 1024;  // barriers, TMEM address, abort flag
 
 __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_constant__ RouteParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -181,6 +187,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
   const uint32_t bar_acc = aux_s + 128;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(aux + 136);
   volatile int* s_abort = reinterpret_cast<volatile int*>(aux + 140);
+  float* s_bias = reinterpret_cast<float*>(aux + kRouteAuxBytes);  // E_pad floats, zero past E
   const uint32_t tmem_cols = E_pad <= 64 ? 64 : E_pad <= 128 ? 128 : E_pad <= 256 ? 256 : 512;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -199,6 +206,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
     *s_abort = 0;
     fence_barrier_init();
   }
+  for (int i = tid; i < E_pad; i += blockDim.x) s_bias[i] = (i < p.E && p.bias) ? p.bias[i] : 0.0f;
   if (warp == 1) {
     tmem_alloc(smem_u32(s_tmem), tmem_cols);
     tmem_relinquish();
@@ -265,19 +273,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     if (acc_ok && p.splits == 1) {
-      for (int c = 0; c < p.E; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tacc + c, v);
-        tmem_ld_wait();
+      // ranks 32 columns while the next 32 load from TMEM (two named buffers, so both stay in
+      // registers)
+      auto rank_cols = [&](const uint32_t (&v)[32], int c) {
+        float b[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 b4 = reinterpret_cast<const float4*>(s_bias + c)[i];
+          b[4 * i] = b4.x; b[4 * i + 1] = b4.y; b[4 * i + 2] = b4.z; b[4 * i + 3] = b4.w;
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int e = c + i;
           if (e < p.E) {
-            const float l = __uint_as_float(v[i]) + (p.bias ? p.bias[e] : 0.0f);
+            const float l = __uint_as_float(v[i]) + b[i];
             if (t < p.T && p.logits) p.logits[(int64_t)t * p.E + e] = l;
-            if (l > tv[kMaxK - 1]) topk_insert(tv, ti, l, e);
+            topk_insert(tv, ti, l, e);
           }
         }
+      };
+      const int nch = (p.E + 31) / 32;  // 32 nch <= E_pad: every column loaded is allocated
+      uint32_t va[32], vb[32];
+      tmem_ld32(tacc, va);
+      tmem_ld_wait();
+      for (int ch = 0; ch < nch; ch += 2) {
+        if (ch + 1 < nch) tmem_ld32(tacc + 32 * (ch + 1), vb);
+        rank_cols(va, 32 * ch);
+        tmem_ld_wait();
+        if (ch + 1 == nch) break;
+        if (ch + 2 < nch) tmem_ld32(tacc + 32 * (ch + 2), va);
+        rank_cols(vb, 32 * (ch + 1));
+        tmem_ld_wait();
       }
       if (t < p.T) write_route(p, t, tv, ti);
     }
@@ -292,10 +318,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
     const int et = tid - 64;  // epilogue thread 0..127
     const int q = warp & 3;
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t part = base;  // the drained stage buffers (every MMA completed: bar_acc)
+    const int rpc = BM / p.splits;  // rows each CTA of the cluster reduces
+    // the drained stage buffers: slot r (rows r rpc .. r rpc + rpc - 1 of `part`) receives CTA
+    // r's partials of this CTA's rows
+    const uint32_t part = base;
     for (int c0 = 0; c0 < E_pad; c0 += p.chunk) {
+      // every CTA of the cluster is past its MMAs (or the previous pass's reads): its stage
+      // buffers may be written
+      cluster_sync();
       if (warp >= 2) {
-        const uint32_t dst = part + (q * 32 + lane) * pstride;
+        const int rr = q * 32 + lane;  // tile row of this thread's TMEM lane
+        const uint32_t dst = mapa_shared(part + (rank * rpc + rr % rpc) * pstride, rr / rpc);
         for (int cc = 0; cc < p.chunk; cc += 32) {
           uint32_t v[32];
           if (acc_ok && nkb > 0) {
@@ -307,19 +340,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
           }
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 4 * cc + 16 * i),
-                         "r"(v[4 * i]), "r"(v[4 * i + 1]), "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
-                         : "memory");
+            st_shared_cluster_v4(dst + 4 * cc + 16 * i, v[4 * i], v[4 * i + 1], v[4 * i + 2],
+                                 v[4 * i + 3]);
         }
       }
-      cluster_sync();  // every CTA's partial chunk is written
+      cluster_sync();  // every partial of this pass is in its owner's shared memory
       if (warp >= 2) {
-        if (p.splits == 2) reduce_chunk<2>(p, part, pstride, c0, rank, et, tv, ti);
-        else if (p.splits == 4) reduce_chunk<4>(p, part, pstride, c0, rank, et, tv, ti);
-        else reduce_chunk<8>(p, part, pstride, c0, rank, et, tv, ti);
+        if (p.splits == 2) reduce_rows<2>(p, part, pstride, c0, rank, et, s_bias, tv, ti);
+        else if (p.splits == 4) reduce_rows<4>(p, part, pstride, c0, rank, et, s_bias, tv, ti);
+        else reduce_rows<8>(p, part, pstride, c0, rank, et, s_bias, tv, ti);
       }
-      cluster_sync();  // every CTA is done reading: the chunk may be overwritten, CTAs may leave
     }
+    // no cluster barrier at the end: after the last pass's second one no CTA touches another's
+    // shared memory, so each may leave when its own rows are done
     if (warp >= 2) {
       if (p.splits == 2) finish_split<2>(p, rank, et, tv, ti);
       else if (p.splits == 4) finish_split<4>(p, rank, et, tv, ti);
@@ -365,7 +398,7 @@ cudaError_t launch_route(const RouteParams& p_in, cudaStream_t s) {
       return cudaErrorInvalidValue;
     region = std::max(region, BM * (4 * p.chunk + 16));
   }
-  const int smem = region + 1024 + 1024;
+  const int smem = region + kRouteAuxBytes + 4 * kMaxE + 1024;  // + 1024: base alignment
   cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
