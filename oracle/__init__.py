@@ -23,6 +23,8 @@ Sources (page title, section):
     own tokens; worked example E2 <- [0,2,9,15], E5 <- [3,8], E7 <- [1,4,5,6].
   * "Mixture-of-Kittens; MoE megakernel" (news.ditty.ir), key points — bit-deterministic
     output, BF16 and MXFP8.
+  * NVFP4 (oracle/nvfp4.py): the first page names it as the format of the authors' earlier
+    kernels; the format definition and the recipe read from it are in that module.
 
 Every function is pinned by tests under ``tests/`` to something other than itself
 (brute force, closed forms, invariants, finite differences, the worked example, a library
@@ -44,6 +46,7 @@ from .moe import (  # noqa: F401
     moe_backward,
     moe_forward_mxfp8,
     moe_backward_mxfp8,
+    moe_forward_nvfp4,
 )
 from .mxfp8 import (  # noqa: F401
     E4M3_MAX,
@@ -52,4 +55,12 @@ from .mxfp8 import (  # noqa: F401
     mx_scale_exponent,
     mx_quantize,
     mx_dequantize,
+)
+from .nvfp4 import (  # noqa: F401
+    E2M1_VALUES,
+    e2m1_decode,
+    e2m1_encode,
+    nv_tensor_scale,
+    nv_quantize,
+    nv_dequantize,
 )

@@ -434,3 +434,59 @@ def moe_backward_mxfp8(x, dY, W_router, Wg, Wu, Wd, shared, logits, topk_idx, on
         "dWs_down": None if dWs is None else dWs[2],
         "dlogits": dl, "dW_router": dWr, "dw": dw,
     }
+
+
+# --------------------------------------------------------------------------------------
+# NVFP4 reading of the forward (a NEXT variant: the pages name NVFP4 only as the format of
+# their authors' earlier kernels).  Each expert GEMM multiplies NVFP4 operands quantised along
+# its own reduction dimension, with the format and recipe of oracle/nvfp4.py: x and every
+# gate/up weight along d, h and every down weight along F.  Weights carry their own tensor
+# scale (per expert and projection, from the weight's amax); the activations x and h take a
+# calibrated tensor amax given with the layer (amax_x, amax_h), the static form of the
+# per-tensor scale, so a value above it saturates.  h is quantised from its fp32 value.  The
+# router, the weighting and the combine stay in full precision; products and sums are float64.
+# --------------------------------------------------------------------------------------
+
+def _nv_qd(a, tensor_amax=None):
+    from .nvfp4 import nv_dequantize, nv_quantize
+
+    q, sc, g = nv_quantize(a, tensor_amax)
+    return nv_dequantize(q, sc, g)
+
+
+def _nv_weight(W):
+    """[K, N] weight quantised along K (its reduction dimension) with its own tensor scale,
+    returned as [K, N]."""
+    return _nv_qd(np.asarray(W, dtype=np.float64).T).T
+
+
+def _nv_ffn(job):
+    """One expert's FFN at the NVFP4 quantisation points, on rows X that are already quantised
+    (a module-level function so that a process pool can run it)."""
+    X, Wg_e, Wu_e, Wd_e, amax_h = job
+    g = X @ _nv_weight(Wg_e)
+    u = X @ _nv_weight(Wu_e)
+    h = _nv_qd(silu(g) * u, amax_h)
+    return h @ _nv_weight(Wd_e)
+
+
+def moe_forward_nvfp4(x, Wg, Wu, Wd, shared, topk_idx, topk_w, amax_x, amax_h, expert_map=map):
+    """Layer output with the NVFP4 quantisation points of the path; ``amax_x`` and ``amax_h``
+    are the calibrated tensor amaxes of the two activations.  A composition of the pinned
+    quantiser and FFN pieces; pinned further by the axis pins of tests/test_oracle_nvfp4.py
+    (which values an outlier coarsens), zero down weights, and the distance to moe_forward on
+    random data."""
+    x = np.asarray(x, dtype=np.float64)
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    w = np.asarray(topk_w, dtype=np.float64)
+    xq = _nv_qd(x, amax_x)
+
+    y = np.zeros_like(x)
+    if shared is not None:
+        y += _nv_ffn((xq, *shared, amax_h))
+    experts = _experts_used(idx)
+    sel = [np.nonzero(idx == e) for e in experts]
+    jobs = ((xq[rows], Wg[e], Wu[e], Wd[e], amax_h) for e, (rows, _) in zip(experts, sel))
+    for (rows, slots), ye in zip(sel, expert_map(_nv_ffn, jobs)):
+        np.add.at(y, rows, w[rows, slots][:, None] * ye)
+    return y
