@@ -57,14 +57,16 @@ typedef enum {
   MOK_ERR_DEVICE_CHECK = -6 /* (device status) an index failed a device-side range check */
 } mok_status;
 
-typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_dtype;
+typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1, MOK_NVFP4 = 2 } mok_dtype;
 
 typedef enum { MOK_PASS_FORWARD = 0, MOK_PASS_BACKWARD = 1 } mok_pass;
 
 /* Sizes of one layer call.  T tokens, d model dim, E routed experts, k experts per token,
  * F routed-expert intermediate, F_shared shared-expert intermediate, n_shared in {0,1},
  * dtype = arithmetic of the expert GEMMs (MOK_MXFP8: E4M3 values with one UE8M0 scale per
- * 32 elements along the reduction dimension; the router and combine stay fp32/bf16). */
+ * 32 elements along the reduction dimension; MOK_NVFP4: E2M1 values with one E4M3 scale per
+ * 16 elements along the reduction dimension and one fp32 scale per tensor, forward only; the
+ * router and combine stay fp32/bf16). */
 typedef struct {
   int64_t T;
   int32_t d, E, k, F, F_shared, n_shared;
@@ -72,7 +74,7 @@ typedef struct {
 } mok_dims;
 
 /* Layer weights (device, caller-owned). `prepared` is the output of mok_prepare_weights and is
- * required when dtype == MOK_MXFP8 (ignored for MOK_BF16); `prepared_bwd`, the output of
+ * required when dtype is MOK_MXFP8 or MOK_NVFP4 (ignored for MOK_BF16); `prepared_bwd`, the output of
  * mok_prepare_weights_bwd, is required by mok_moe_backward when dtype == MOK_MXFP8. */
 typedef struct {
   const void *W_router;     /* [d,E] bf16 */
@@ -111,6 +113,31 @@ size_t mok_prepared_size(const mok_dims *dims);
  * MXFP8 needs d % 256 == 0. */
 int mok_prepare_weights(const mok_dims *dims, const mok_weights *w, void *prepared,
                         mok_stream_t stream);
+/* NVFP4 (MOK_NVFP4; the first page, "Mixture-of-Kittens: Nhân kernel MoE ...", names NVFP4 as
+ * the format of its authors' earlier kernels and defines neither format nor recipe; the format
+ * is NVIDIA's NVFP4 and the recipe the plain two-level one): mok_prepare_weights quantises every
+ * expert weight along its reduction dimension (K = d for gate and up, F for down), each matrix
+ * with its own tensor scale: A = the matrix's amax, S = 2688 / A in fp32 (1 when A is 0); a block
+ * of 16 with amax a takes the E4M3 scale s = rn((a / 6) * S) (saturating); an element v the E2M1
+ * code rn(v * (S / s)) (ties to the even code, saturating at 6; sign bit when the product is
+ * negative; 0 when s is 0); every step an fp32 operation rounded to nearest even.  Layout, in
+ * this order, each region 1 KB aligned: W_gate codes, W_gate scales, W_up codes, W_up scales,
+ * W_down codes, W_down scales, the shared expert's six likewise (E = 1), then g[3E + 3] fp32
+ * (1 / S of gate e, up e, down e for e < E, then the shared gate, up, down), amax[3E + 3]
+ * (scratch), act[2] fp32 (the calibrated activation amaxes, below).  Codes of a matrix with K
+ * rows and N columns: for each 64-element K block kb and column n, 32 bytes at
+ * ((m * K/64 + kb) * N + n) * 32 (m = the expert), byte j holding elements 2j (low nibble) and
+ * 2j + 1 (high nibble) of the block; its 4 scale bytes (one per 16 elements) at
+ * ((m * K/64 + kb) * N + n) * 4.  The activation amaxes are reset to 0 (tensor scale 1).
+ * NVFP4 needs d % 256 == 0. */
+
+/* NVFP4: sets the calibrated tensor amaxes of the forward's two quantised activations, x (the
+ * layer input, quantised along d) and h (SiLU(G) * U, quantised along F from its fp32 value),
+ * in `prepared` (the static form of the per-tensor scale: values beyond them saturate).  Both
+ * must be finite and >= 0 (0 gives the tensor scale 1).  Returns MOK_ERR_INVALID_ARG for another
+ * dtype, a NULL or unaligned buffer, or a negative or non-finite amax. */
+int mok_nvfp4_set_activation_amax(const mok_dims *dims, void *prepared, float amax_x,
+                                  float amax_h, mok_stream_t stream);
 
 /* MXFP8 backward: the expert weights quantised once more, along the reduction dimension of the
  * backward GEMM that reads each (same rule and atom layout as mok_prepare_weights), in this order
@@ -165,7 +192,10 @@ int mok_dispatch_index(const mok_dims *dims, const int32_t *topk_idx, const floa
  * rounding).
  *   -> y[T,d] bf16.  `saved` (mok_saved_size bytes or NULL) receives what the backward needs:
  *   G and U (bf16; for MOK_MXFP8 the block-scaled products in fp32), and for MOK_BF16 x in
- *   expert order. */
+ *   expert order.  MOK_NVFP4: x is quantised with its calibrated amax, the gate/up GEMM's
+ *   epilogue quantises h along F, both GEMMs multiply f16 NVFP4 values decoded from the
+ *   prepared weights and apply the tensor scales in their epilogues; forward only (`saved` must
+ *   be NULL, else MOK_ERR_UNSUPPORTED). */
 int mok_moe_forward(const mok_dims *dims, const mok_weights *w, const void *x,
                     const int32_t *topk_idx, const int32_t *offsets, const int32_t *sorted_tok,
                     const float *sorted_w, const int32_t *inv_pos, void *y, void *saved,
@@ -185,7 +215,7 @@ int mok_moe_forward(const mok_dims *dims, const mok_weights *w, const void *x,
  * the router terms dlogits W_router^T and x^T dlogits stay bf16.  Needs w->prepared_bwd and a
  * `saved` from an MXFP8 forward; F % 256 == 0, Fs % 256 == 0 and
  * 2 (ceil(T k / 128) + E) d / 64 < 2^31 (T below about 150M tokens at d = 7168, k = 8), else
- * MOK_ERR_UNSUPPORTED. */
+ * MOK_ERR_UNSUPPORTED.  MOK_NVFP4 has no backward: MOK_ERR_UNSUPPORTED. */
 int mok_moe_backward(const mok_dims *dims, const mok_weights *w, const void *x, const void *dY,
                      const void *saved, const int32_t *topk_idx, const float *topk_w,
                      const int32_t *offsets, const int32_t *sorted_tok, const float *sorted_w,

@@ -19,10 +19,11 @@ __all__ = [
     "MokError", "Dims", "Weights", "lib", "lib_path", "dims", "route", "dispatch_index",
     "moe_forward", "moe_backward", "layer_forward_host", "workspace_size", "saved_size",
     "read_status", "clear_status", "last_launch_count", "MoELayer", "EXPORTED_SYMBOLS",
-    "MOK_BF16", "MOK_MXFP8", "prepare_weights", "prepare_weights_bwd", "mx_quantize_rows",
+    "MOK_BF16", "MOK_MXFP8", "MOK_NVFP4", "prepare_weights", "prepare_weights_bwd",
+    "mx_quantize_rows", "nvfp4_set_activation_amax",
 ]
 
-MOK_BF16, MOK_MXFP8 = 0, 1
+MOK_BF16, MOK_MXFP8, MOK_NVFP4 = 0, 1, 2
 PASS_FORWARD, PASS_BACKWARD = 0, 1
 
 EXPORTED_SYMBOLS = [
@@ -32,7 +33,7 @@ EXPORTED_SYMBOLS = [
     "mok_read_device_status", "mok_clear_device_status", "mok_last_launch_count",
     "mok_timing_enable", "mok_timing_collect", "mok_dispatch_index_noalloc",
     "mok_mx_quantize_rows", "mok_selftest_bounded_wait", "mok_prepared_bwd_size",
-    "mok_prepare_weights_bwd", "mok_set_forward_schedule",
+    "mok_prepare_weights_bwd", "mok_set_forward_schedule", "mok_nvfp4_set_activation_amax",
 ]
 
 
@@ -93,6 +94,7 @@ def lib():
             "mok_mx_quantize_rows": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int, _VP, _VP, _VP, _VP]),
             "mok_dispatch_index_noalloc": (ctypes.c_int, [_DP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
             "mok_set_forward_schedule": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
+            "mok_nvfp4_set_activation_amax": (ctypes.c_int, [_DP, _VP, ctypes.c_float, ctypes.c_float, _VP]),
             "mok_timing_collect": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int),
                                                   ctypes.POINTER(ctypes.c_double), ctypes.c_int,
                                                   ctypes.POINTER(ctypes.c_int)]),
@@ -296,8 +298,9 @@ def prepared_size(D):
 
 
 def prepare_weights(D, W):
-    """MXFP8: quantised, K-major copy of the expert weights (uint8 CUDA tensor); returns None for
-    bf16.  Pass it as W["prepared"]."""
+    """MXFP8 / NVFP4: quantised copy of the expert weights in the layout of mok_prepare_weights
+    (uint8 CUDA tensor); returns None for bf16.  Pass it as W["prepared"].  NVFP4: set the
+    calibrated activation amaxes with :func:`nvfp4_set_activation_amax` afterwards."""
     n = prepared_size(D)
     if n == 0:
         return None
@@ -308,6 +311,13 @@ def prepare_weights(D, W):
     st = _weights_struct(D, Wd)
     _check(lib().mok_prepare_weights(ctypes.byref(D), ctypes.byref(st), _ptr(buf), _stream()))
     return buf
+
+
+def nvfp4_set_activation_amax(D, prepared, amax_x, amax_h):
+    """NVFP4: the calibrated tensor amaxes of x and h, written into ``prepared``."""
+    _want(prepared, "prepared", (prepared_size(D),), torch.uint8, prepared.device)
+    _check(lib().mok_nvfp4_set_activation_amax(ctypes.byref(D), _ptr(prepared), float(amax_x),
+                                                float(amax_h), _stream()))
 
 
 def prepare_weights_bwd(D, W):

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmok.so")
-SOURCES = ["api.cu", "route.cu", "dispatch.cu", "elementwise.cu", "moe_gemm.cu", "profile.cu", "noalloc.cu", "mx.cu"]
+SOURCES = ["api.cu", "route.cu", "dispatch.cu", "elementwise.cu", "moe_gemm.cu", "profile.cu", "noalloc.cu", "mx.cu", "nv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]

@@ -83,8 +83,8 @@ static int check_dims(const mok_dims* d) {
   if (d->n_shared != 0 && d->n_shared != 1) return MOK_ERR_UNSUPPORTED;
   if (d->n_shared == 1 && (d->F_shared <= 0 || d->F_shared % 128)) return MOK_ERR_UNSUPPORTED;
   if (d->k < 1 || d->k > kMaxK || d->E < d->k || d->E > kMaxE || d->E % 8) return MOK_ERR_UNSUPPORTED;
-  if (d->dtype != MOK_BF16 && d->dtype != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
-  if (d->dtype == MOK_MXFP8 && d->d % 256) return MOK_ERR_UNSUPPORTED;  // 256-wide down tiles
+  if (d->dtype != MOK_BF16 && d->dtype != MOK_MXFP8 && d->dtype != MOK_NVFP4) return MOK_ERR_INVALID_ARG;
+  if (d->dtype != MOK_BF16 && d->d % 256) return MOK_ERR_UNSUPPORTED;  // 256-wide down tiles
   return MOK_OK;
 }
 
@@ -103,6 +103,10 @@ enum FwdSlot {
 };
 enum PrepSlot {  // MXFP8 prepared weights: K-major codes [n][N][K] and scale atoms
   PR_GQ, PR_GS, PR_UQ, PR_US, PR_DQ, PR_DS, PR_SGQ, PR_SGS, PR_SUQ, PR_SUS, PR_SDQ, PR_SDS, PR_N
+};
+enum PrepNvSlot {  // NVFP4 prepared weights: code rows, scale rows, per-matrix g, scratch, act
+  PN_GQ, PN_GS, PN_UQ, PN_US, PN_DQ, PN_DS, PN_SGQ, PN_SGS, PN_SUQ, PN_SUS, PN_SDQ, PN_SDS,
+  PN_G, PN_AMAX, PN_ACT, PN_N
 };
 enum PrepBwdSlot {  // MXFP8 backward weights: codes quantised along the backward GEMMs' K
   PB_DQ, PB_DS,    // W_down [E][F][d] along d (dY W_down^T)
@@ -159,6 +163,7 @@ static Layout layout_fwd(const mok_dims* d) {
     sz[FW_HQSH] = 1ull * T * Fs;
     sz[FW_HSCSH] = 4ull * BM * mt_x * (Fs / 128);
   }
+  if (d->dtype == MOK_NVFP4) sz[FW_XQ] = 2ull * T * d->d;  // x as f16 NVFP4 values; XS, H, HSH f16
   Layout L{};
   size_t o = 0;
   for (int i = 0; i < FW_N; ++i) { L.off[i] = o; o += al(sz[i]); }
@@ -227,6 +232,20 @@ static Layout layout_prepared(const mok_dims* d) {
   Layout L{};
   size_t o = 0;
   for (int i = 0; i < PR_N; ++i) { L.off[i] = o; o += al(sz[i]); }
+  L.total = o;
+  return L;
+}
+
+// NVFP4: codes 1/2 byte and scales 1/16 byte per weight element; g and amax per matrix
+static Layout layout_prepared_nv(const mok_dims* d) {
+  const uint64_t E = d->E, dd = d->d, F = d->F, Fs = d->n_shared ? d->F_shared : 0;
+  const uint64_t nmat = 3 * E + 3;
+  size_t sz[PN_N] = {E * dd * F / 2, E * dd * F / 16, E * dd * F / 2, E * dd * F / 16,
+                     E * F * dd / 2, E * F * dd / 16, dd * Fs / 2, dd * Fs / 16, dd * Fs / 2,
+                     dd * Fs / 16, Fs * dd / 2, Fs * dd / 16, 4 * nmat, 4 * nmat, 8};
+  Layout L{};
+  size_t o = 0;
+  for (int i = 0; i < PN_N; ++i) { L.off[i] = o; o += al(sz[i]); }
   L.total = o;
   return L;
 }
@@ -531,12 +550,13 @@ size_t mok_workspace_size(const mok_dims* dims, int pass) {
 }
 
 size_t mok_saved_size(const mok_dims* dims) {
-  if (check_dims(dims) != MOK_OK) return 0;
+  if (check_dims(dims) != MOK_OK || dims->dtype == MOK_NVFP4) return 0;
   return layout_saved(dims).total;
 }
 
 size_t mok_prepared_size(const mok_dims* dims) {
   if (check_dims(dims) != MOK_OK) return 0;
+  if (dims->dtype == MOK_NVFP4) return layout_prepared_nv(dims).total;
   return dims->dtype == MOK_MXFP8 ? layout_prepared(dims).total : 0;
 }
 
@@ -545,17 +565,63 @@ size_t mok_layer_host_extra_size(const mok_dims* dims) {
   return layout_host(dims).total;
 }
 
+// NVFP4 weights: per-matrix amax, then code and scale rows (nv.cu); the calibrated activation
+// amaxes start at 0 (tensor scale 1)
+static int prepare_weights_nv(const mok_dims* dims, const mok_weights* w, void* prepared,
+                              cudaStream_t s) {
+  const Layout P = layout_prepared_nv(dims);
+  const int d = dims->d, F = dims->F, Fs = dims->F_shared, E = dims->E;
+  auto q = [&](int i) { return static_cast<char*>(prepared) + P.off[i]; };
+  uint32_t* amax = reinterpret_cast<uint32_t*>(q(PN_AMAX));
+  float* g = reinterpret_cast<float*>(q(PN_G));
+  cudaError_t e = cudaMemsetAsync(amax, 0, 4ull * (3 * E + 3), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(q(PN_ACT), 0, 8, s);
+  // gate/up [E][d][F] (K = d); down [E][F][d] (K = F)
+  if (e == cudaSuccess) e = launch_nv_prepare(w->W_gate, E, d, F, amax, q(PN_GQ), q(PN_GS), g, s);
+  if (e == cudaSuccess) e = launch_nv_prepare(w->W_up, E, d, F, amax + E, q(PN_UQ), q(PN_US), g + E, s);
+  if (e == cudaSuccess)
+    e = launch_nv_prepare(w->W_down, E, F, d, amax + 2 * E, q(PN_DQ), q(PN_DS), g + 2 * E, s);
+  if (dims->n_shared) {
+    if (e == cudaSuccess)
+      e = launch_nv_prepare(w->Ws_gate, 1, d, Fs, amax + 3 * E, q(PN_SGQ), q(PN_SGS), g + 3 * E, s);
+    if (e == cudaSuccess)
+      e = launch_nv_prepare(w->Ws_up, 1, d, Fs, amax + 3 * E + 1, q(PN_SUQ), q(PN_SUS), g + 3 * E + 1, s);
+    if (e == cudaSuccess)
+      e = launch_nv_prepare(w->Ws_down, 1, Fs, d, amax + 3 * E + 2, q(PN_SDQ), q(PN_SDS), g + 3 * E + 2, s);
+  }
+  if (e != cudaSuccess) return MOK_ERR_CUDA;
+  g_last_launches = 2 * (dims->n_shared ? 6 : 3);
+  return MOK_OK;
+}
+
+int mok_nvfp4_set_activation_amax(const mok_dims* dims, void* prepared, float amax_x, float amax_h,
+                                  mok_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != MOK_OK) return rc;
+  g_last_launches = 0;
+  if (dims->dtype != MOK_NVFP4 || !prepared || !aligned16(prepared)) return MOK_ERR_INVALID_ARG;
+  if (!(amax_x >= 0.0f && amax_x <= 3.0e38f) || !(amax_h >= 0.0f && amax_h <= 3.0e38f))
+    return MOK_ERR_INVALID_ARG;  // also rejects NaN
+  const Layout P = layout_prepared_nv(dims);
+  float* act = reinterpret_cast<float*>(static_cast<char*>(prepared) + P.off[PN_ACT]);
+  if (launch_nv_set_act(act, amax_x, amax_h, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOK_ERR_CUDA;
+  g_last_launches = 1;
+  return MOK_OK;
+}
+
 int mok_prepare_weights(const mok_dims* dims, const mok_weights* w, void* prepared,
                         mok_stream_t stream) {
   int rc = check_dims(dims);
   if (rc != MOK_OK) return rc;
   if (!w) return MOK_ERR_INVALID_ARG;
   g_last_launches = 0;
-  if (dims->dtype != MOK_MXFP8) return MOK_OK;
+  if (dims->dtype == MOK_BF16) return MOK_OK;
   if (!prepared || !w->W_gate || !w->W_up || !w->W_down) return MOK_ERR_INVALID_ARG;
   if (dims->n_shared && (!w->Ws_gate || !w->Ws_up || !w->Ws_down)) return MOK_ERR_INVALID_ARG;
   if (!aligned16(prepared)) return MOK_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dims->dtype == MOK_NVFP4) return prepare_weights_nv(dims, w, prepared, s);
   const Layout P = layout_prepared(dims);
   const int d = dims->d, F = dims->F, Fs = dims->F_shared, E = dims->E;
   auto q = [&](int i) { return static_cast<char*>(prepared) + P.off[i]; };
@@ -735,6 +801,90 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
   const Layout S = layout_saved(dims);
   int launches = 0;
   const int grid_cap0 = num_sms();
+
+  if (dims->dtype == MOK_NVFP4) {
+    // NVFP4 path: x quantised once with its calibrated amax (f16 NVFP4 values), pulled into
+    // expert order, the gate/up GEMM decoding the NVFP4 weights in shared memory and quantising h
+    // in its epilogue, the down GEMM likewise with the router weight, and the same combine.
+    if (saved) return MOK_ERR_UNSUPPORTED;
+    if (!w->prepared || !aligned16(w->prepared)) return MOK_ERR_INVALID_ARG;
+    const Layout P = layout_prepared_nv(dims);
+    auto pw = [&](int i) { return reinterpret_cast<const uint8_t*>(w->prepared) + P.off[i]; };
+    const float* g = reinterpret_cast<const float*>(pw(PN_G));
+    const float* act = reinterpret_cast<const float*>(pw(PN_ACT));
+    void* xq = at<void*>(ws, L.off[FW_XQ]);
+    rc = cuda_status(launch_nv_quantize_act(x, T, d, act, xq, s));
+    if (rc == MOK_OK)
+      rc = cuda_status(launch_gather_rows("gather", xq, nullptr, inv_pos, T, dims->k, 2 * d, xs, nullptr, s));
+    if (rc != MOK_OK) return rc;
+    launches += 2;
+    auto common = [&](GemmParams& p) {
+      p.offsets = offsets;
+      p.E = E;
+      p.has_shared = sh;
+      p.T = (int)T;
+      p.d = d;
+      p.F = F;
+      p.Fs = Fs;
+      p.nv_act = act;
+      p.status = static_cast<int*>(ws);
+    };
+    {
+      GemmParams p{};
+      bool ok = true;
+      if (sh) ok &= map2d(&p.maps[MS_A0], xq, T, d, 64, 128);
+      ok &= map2d(&p.maps[MS_A3], xs, R, d, 64, 128);
+      if (!ok) return MOK_ERR_CUDA;
+      common(p);
+      p.nt[0] = Fs / 128;
+      p.nt[1] = F / 128;
+      p.out0[0] = hsh;
+      p.out0[1] = h;
+      p.nvq[0][0] = pw(PN_SGQ);
+      p.nvq[0][1] = pw(PN_SUQ);
+      p.nvs[0][0] = pw(PN_SGS);
+      p.nvs[0][1] = pw(PN_SUS);
+      p.nvg[0][0] = g + 3 * E;
+      p.nvg[0][1] = g + 3 * E + 1;
+      p.nvq[1][0] = pw(PN_GQ);
+      p.nvq[1][1] = pw(PN_UQ);
+      p.nvs[1][0] = pw(PN_GS);
+      p.nvs[1][1] = pw(PN_US);
+      p.nvg[1][0] = g;
+      p.nvg[1][1] = g + E;
+      const int64_t bound = (sh ? (T + BM - 1) / BM * p.nt[0] : 0) + ((R + BM - 1) / BM + E) * p.nt[1];
+      rc = cuda_status(launch_gemm(G_FWD_GU_NV, 256, p, (int)std::min<int64_t>(grid_cap0, bound), s));
+      if (rc != MOK_OK) return rc;
+      ++launches;
+    }
+    {
+      GemmParams p{};
+      bool ok = true;
+      if (sh) ok &= map2d(&p.maps[MS_A0], hsh, T, Fs, 64, 128);
+      ok &= map2d(&p.maps[MS_A3], h, R, F, 64, 128);
+      if (!ok) return MOK_ERR_CUDA;
+      common(p);
+      p.nt[0] = d / 256;
+      p.nt[1] = d / 256;
+      p.out0[0] = Ysh;
+      p.out0[1] = Ys;
+      p.row_w = sorted_w;
+      p.nvq[0][0] = pw(PN_SDQ);
+      p.nvs[0][0] = pw(PN_SDS);
+      p.nvg[0][0] = g + 3 * E + 2;
+      p.nvq[1][0] = pw(PN_DQ);
+      p.nvs[1][0] = pw(PN_DS);
+      p.nvg[1][0] = g + 2 * E;
+      const int64_t bound = (sh ? (T + BM - 1) / BM * p.nt[0] : 0) + ((R + BM - 1) / BM + E) * p.nt[1];
+      rc = cuda_status(launch_gemm(G_FWD_DOWN_NV, 256, p, (int)std::min<int64_t>(grid_cap0, bound), s));
+      if (rc != MOK_OK) return rc;
+      ++launches;
+    }
+    rc = cuda_status(launch_combine(T, d, dims->k, topk_idx, inv_pos, Ys, sh ? Ysh : nullptr, y, s));
+    if (rc != MOK_OK) return rc;
+    g_last_launches = launches + 1;
+    return MOK_OK;
+  }
 
   if (dims->dtype == MOK_MXFP8) {
     // MXFP8 path: x quantised once (E4M3 + UE8M0 per 32 along d), its codes and scale rows
@@ -992,6 +1142,7 @@ int mok_moe_backward(const mok_dims* dims, const mok_weights* w, const void* x, 
                      void* dW_router, void* ws, size_t ws_bytes, mok_stream_t stream) {
   int rc = check_dims(dims);
   if (rc != MOK_OK) return rc;
+  if (dims->dtype == MOK_NVFP4) return MOK_ERR_UNSUPPORTED;  // the NVFP4 variant is forward only
   if (!w || !ws || !dW_gate || !dW_up || !dW_down) return MOK_ERR_INVALID_ARG;
   if (dims->T > 0 && (!x || !dY || !saved || !topk_idx || !topk_w || !offsets || !sorted_tok ||
                       !sorted_w || !inv_pos || !dX || !dlogits))

@@ -13,7 +13,7 @@
 // blocks pulled straight from it).  CTA c takes tiles c, c+grid, c+2*grid, ...  Every output
 // element is produced by exactly one CTA with a fixed K order, so results are bit-identical
 // from run to run.  No host synchronisation: the tile count is read on the device.
-#include "mok_mx.cuh"
+#include "mok_nv.cuh"
 
 namespace mok {
 
@@ -35,12 +35,16 @@ struct Cfg {
   // every stage row is 128 bytes: 64 bf16 or 128 E4M3 elements of K
   static constexpr bool MX = (MODE == G_FWD_GU_MX || MODE == G_FWD_DOWN_MX || MODE == G_BWD_DA_MX ||
                               MODE == G_BWD_DX_MX || MODE == G_BWD_DW_MX);
+  // NVFP4: f16 A tiles by TMA; B arrives as E2M1 codes and E4M3 scales (32 + 4 bytes per row
+  // of a 64-element K block) and converter warps decode it into an f16 K-major tile
+  static constexpr bool NV = (MODE == G_FWD_GU_NV || MODE == G_FWD_DOWN_NV);
   static constexpr int KE = MX ? 128 : BK;            // K elements per stage
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
-  static constexpr int SF_BYTES = MX ? (BM + BN) * 4 : 0;  // UE8M0 atoms of A and B
+  // UE8M0 atoms of A and B (MXFP8); the raw NVFP4 B rows (NVFP4)
+  static constexpr int SF_BYTES = MX ? (BM + BN) * 4 : NV ? BN * 36 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int STAGES = NV ? 3 : (BN == 256) ? 4 : 6;
   static constexpr bool A_MN = (MODE == G_BWD_DW);
   static constexpr bool B_MN = (MODE == G_FWD_GU || MODE == G_FWD_DOWN || MODE == G_BWD_DW ||
                                 MODE == G_FWD_GUD);
@@ -52,19 +56,21 @@ struct Cfg {
   // epilogue warps: two per TMEM lane quarter (each taking half the columns) where the single
   // accumulator leaves the epilogue exposed, one otherwise
   static constexpr int EPI_WARPS = NUM_ACC == 1 ? 8 : 4;
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int CONV_WARPS = NV ? 4 : 0;       // NVFP4 B decoders, after the epilogue warps
+  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + CONV_WARPS);
   // plain row-major outputs go through shared memory one 32-column chunk (32 rows x 64 B) per
   // epilogue warp at a time and are written with coalesced row stores
   static constexpr bool ROW_STAGED = (MODE == G_FWD_DOWN || MODE == G_BWD_DX ||
                                       MODE == G_FWD_DOWN_MX || MODE == G_BWD_DW ||
                                       MODE == G_BWD_DX_MX || MODE == G_BWD_DW_MX ||
-                                      MODE == G_FWD_GUD);
+                                      MODE == G_FWD_GUD || MODE == G_FWD_DOWN_NV);
   // per epilogue warp: a 2 KB row-staging buffer, or (dA MXFP8) a 32 x 36-float transpose buffer
   static constexpr int STG_STRIDE = (MODE == G_BWD_DA_MX) ? 32 * 36 * 4 : 2048;
   static constexpr int STAGING_BYTES = (ROW_STAGED || MODE == G_BWD_DA_MX) ? EPI_WARPS * STG_STRIDE : 0;
   static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
   static constexpr int SF_TMEM_COL = 256;              // MXFP8: 16 columns per stage from here
-  static constexpr uint32_t IDESC = MX ? make_idesc_mxf8(BN) : make_idesc_bf16(BN, A_MN, B_MN);
+  static constexpr uint32_t IDESC =
+      MX ? make_idesc_mxf8(BN) : NV ? make_idesc_f16(BN) : make_idesc_bf16(BN, A_MN, B_MN);
   static constexpr bool K_GROUPED = (MODE == G_BWD_DW || MODE == G_BWD_DW_MX);
 };
 
@@ -159,6 +165,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
     else if constexpr (MODE == G_FWD_DOWN_MX) nkb = (t.g ? p.F : p.Fs) / 128;
     else if constexpr (MODE == G_BWD_DA_MX) nkb = p.d / 128;
     else if constexpr (MODE == G_BWD_DX_MX) nkb = 2 * (t.g ? p.F : p.Fs) / 128;  // dG, then dU
+    else if constexpr (MODE == G_FWD_GU_NV) nkb = p.d / BK;
+    else if constexpr (MODE == G_FWD_DOWN_NV) nkb = (t.g ? p.F : p.Fs) / BK;
     else nkb = p.segkb[t.g][0] + p.segkb[t.g][1] + p.segkb[t.g][2];
     t.nkb = nkb;
   } else {
@@ -334,6 +342,9 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, 
   } else if constexpr (MODE == G_BWD_DA) {
     tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
     tma_load_3d(sB, &M[t.g ? MS_B3 : MS_B0], bar, kb * BK, t.n * BN, t.e);
+  } else if constexpr (MODE == G_FWD_GU_NV || MODE == G_FWD_DOWN_NV) {
+    // f16 A rows (x values / h values); B comes raw through load_nv_raw
+    tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
   } else if constexpr (MODE == G_BWD_DX) {
     int seg = 0, kk = kb;
     while (seg < 2 && kk >= p.segkb[t.g][seg]) { kk -= p.segkb[t.g][seg]; ++seg; }
@@ -489,9 +500,11 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, void* const (
                                               uint32_t release) {
   constexpr int cols = warp_cols<MODE, BN>();
   const int nrows = t.rows - q * 32;  // valid rows among this warp's 32 (may be <= 0)
-  constexpr bool WEIGHTED = (MODE == G_FWD_DOWN || MODE == G_FWD_DOWN_MX);
+  constexpr bool WEIGHTED = (MODE == G_FWD_DOWN || MODE == G_FWD_DOWN_MX || MODE == G_FWD_DOWN_NV);
   float s = 1.0f;
   if (WEIGHTED && t.g == 1 && lane < nrows) s = p.row_w[t.row0 + q * 32 + lane];
+  // NVFP4: the two tensor scales, h's and the expert's down weight's
+  if constexpr (MODE == G_FWD_DOWN_NV) s *= __fmul_rn(nv_decode_g(p.nv_act[1]), p.nvg[t.g][0][t.e]);
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(outs[t.g]) + (int64_t)(t.row0 + q * 32) * p.d +
                      t.n * BN + cols * half;
   store_acc_rows<cols / 32, Cfg<MODE, BN>::NUM_ACC == 1>(o, p.d, nrows, cols, tacc + cols * half,
@@ -706,6 +719,37 @@ __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& 
   }
 }
 
+// G_FWD_GU_NV: G and U are the accumulators times their tensor scales (x's and the expert's gate
+// or up weight's); h = SiLU(G) * U is quantised per 16 columns with h's calibrated tensor amax and
+// stored as f16 NVFP4 values without the tensor scale: the A operand of the NVFP4 down GEMM.
+template <int BN>
+__device__ __forceinline__ void epilogue_gu_nv(const GemmParams& p, const Tile& t, uint32_t tacc, int r) {
+  const bool valid = r < t.rows;
+  const int ld = t.g ? p.F : p.Fs;
+  const float gx = nv_decode_g(p.nv_act[0]);
+  const float ag = __fmul_rn(gx, p.nvg[t.g][0][t.e]);
+  const float au = __fmul_rn(gx, p.nvg[t.g][1][t.e]);
+  const float Sh = nv_tensor_S(p.nv_act[1]);
+  __half* h = static_cast<__half*>(p.out0[t.g]) + (int64_t)(t.row0 + r) * ld + t.n * 128;
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 32) {
+    uint32_t gr[32], ur[32];
+    tmem_ld32(tacc + c, gr);
+    tmem_ld32(tacc + 128 + c, ur);
+    tmem_ld_wait();
+    if (valid) {
+      float hv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        hv[i] = silu_f(ag * __uint_as_float(gr[i])) * (au * __uint_as_float(ur[i]));
+      uint32_t o[16];
+      nv_block16_values(hv, Sh, o);
+      nv_block16_values(hv + 16, Sh, o + 8);
+      st_row64(h + c, o);
+    }
+  }
+}
+
 template <int MODE, int BN>
 __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uint32_t tacc,
                                          int r, int half) {
@@ -832,6 +876,59 @@ __device__ __forceinline__ void load_scale_atoms(const GemmParams& p, const Tile
   }
 }
 
+// ------------------------------------------------------------------ NVFP4 B operand
+// The stage's raw B rows by bulk copies on the stage barrier: BN rows of 32 code bytes, then BN
+// rows of 4 scale bytes.  Gate/up: rows 0-127 are the gate rows, 128-255 the up rows of the h
+// tile's 128 columns; down: 256 consecutive rows (output columns) of the expert's weight.
+template <int MODE, int BN>
+__device__ __forceinline__ void load_nv_raw(const GemmParams& p, const Tile& t, int kb, uint32_t raw,
+                                            uint32_t bar) {
+  const int g = t.g;
+  if constexpr (MODE == G_FWD_GU_NV) {
+    const int N = g ? p.F : p.Fs;
+    const int64_t row = ((int64_t)t.e * (p.d / BK) + kb) * N + t.n * 128;
+    bulk_load(raw, p.nvq[g][0] + row * 32, 128 * 32, bar);
+    bulk_load(raw + 128 * 32, p.nvq[g][1] + row * 32, 128 * 32, bar);
+    bulk_load(raw + BN * 32, p.nvs[g][0] + row * 4, 128 * 4, bar);
+    bulk_load(raw + BN * 32 + 128 * 4, p.nvs[g][1] + row * 4, 128 * 4, bar);
+  } else if constexpr (MODE == G_FWD_DOWN_NV) {
+    const int64_t row = ((int64_t)t.e * ((g ? p.F : p.Fs) / BK) + kb) * p.d + t.n * BN;
+    bulk_load(raw, p.nvq[g][0] + row * 32, BN * 32, bar);
+    bulk_load(raw + BN * 32, p.nvs[g][0] + row * 4, BN * 4, bar);
+  } else {
+    static_assert(MODE == -1, "raw B rows of an NVFP4 mode");
+  }
+}
+
+// Converter thread `ct` (0..127) decodes B rows ct, ct + 128, ... of a stage: each row's 64 codes
+// times their block scales into f16, written K-major with the 128-byte swizzle the MMA reads
+// (row n: 8-row group n / 8 at 1024 bytes, row n % 8 at 128 bytes, 16-byte chunk c at c ^ (n % 8)).
+template <int BN>
+__device__ __forceinline__ void nv_convert_stage(uint32_t raw, uint32_t sB, int ct) {
+#pragma unroll 1
+  for (int n = ct; n < BN; n += 128) {
+    uint32_t w[8];
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(raw + n * 32));
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(raw + n * 32 + 16));
+    uint32_t sc;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(raw + BN * 32 + n * 4));
+    const uint32_t row = sB + (n >> 3) * 1024 + (n & 7) * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {  // K elements 8c .. 8c + 7, scale block c / 2
+      const uint32_t s2 = e4m3_bcast_f16x2((sc >> (8 * (c >> 1))) & 0xFFu);
+      uint32_t o[4];
+      e2m1x8_to_f16x2(w[c], o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = hmul2_u32(o[j], s2);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c ^ (n & 7)) << 4)),
+                   "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                   : "memory");
+    }
+  }
+}
+
 // ------------------------------------------------------------------ K-tail masking
 // G_BWD_DW: the last k-block of a problem may hold rows of the next expert; zero them in both
 // operands (MN-major: K is the row index inside every 64-column box, 128 B per row, and the
@@ -868,6 +965,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
   const uint32_t bar_rfull = aux_s + 16 * C::STAGES + 64;
   const uint32_t bar_rempty = bar_rfull + 8 * kRing;
   volatile int* s_ring = reinterpret_cast<volatile int*>(aux + 16 * C::STAGES + 64 + 16 * kRing);
+  // NVFP4: stage s's B tile decoded (one arrival per converter warp); the ring's space, unused
+  const uint32_t bar_conv = aux_s + 16 * C::STAGES + 64;
   int* s_off = reinterpret_cast<int*>(aux + kAuxBytes);
   int* s_mt = s_off + (kMaxE + 1);
 
@@ -888,6 +987,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
         mbar_init(bar_rfull + 8 * i, 1);
         mbar_init(bar_rempty + 8 * i, 1 + C::EPI_WARPS);
       }
+    }
+    if constexpr (C::NV) {
+      static_assert(!C::FUSED, "the decoded-B barriers use the tile ring's space");
+      for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_conv + 8 * s, C::CONV_WARPS);
     }
     *s_abort = 0;
     fence_barrier_init();
@@ -992,14 +1095,16 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       auto produce = [&](const Tile& t) {
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) return;
-          if (!PAIR || rank == 0)  // a pair's stage: both CTAs' bytes on the even CTA's barrier
-            mbar_arrive_expect_tx(bar_full + 8 * stage,
-                                  (C::A_BYTES + C::B_BYTES + C::SF_BYTES) * (PAIR ? 2 : 1));
+          // a pair's stage: both CTAs' bytes on the even CTA's barrier; NVFP4: A and the raw B rows
+          constexpr uint32_t kTx = C::NV ? C::A_BYTES + C::SF_BYTES : C::A_BYTES + C::B_BYTES + C::SF_BYTES;
+          if (!PAIR || rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, kTx * (PAIR ? 2 : 1));
           issue_loads<MODE, BN, PAIR>(p, t, kb, rank, sA0 + stage * C::A_BYTES,
                                       sB0 + stage * C::B_BYTES,
                                       PAIR ? mapa_shared(bar_full + 8 * stage, 0) : bar_full + 8 * stage);
           if constexpr (C::MX)
             load_scale_atoms<MODE, BN>(p, t, kb, sSF0 + stage * C::SF_BYTES, bar_full + 8 * stage);
+          if constexpr (C::NV)
+            load_nv_raw<MODE, BN>(p, t, kb, sSF0 + stage * C::SF_BYTES, bar_full + 8 * stage);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       };
@@ -1038,6 +1143,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       bool ok = true;
       for (int kb = 0; kb < t.nkb; ++kb) {
         if (!mbar_wait(bar_full + 8 * stage, phase, p.status, s_abort)) { ok = false; break; }
+        if constexpr (C::NV)  // the converter warps have written this stage's f16 B tile
+          if (!mbar_wait(bar_conv + 8 * stage, phase, p.status, s_abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sA = sA0 + stage * C::A_BYTES, sB = sB0 + stage * C::B_BYTES;
         int nk16 = BK / 16;  // MMA K steps of this stage
@@ -1124,6 +1231,25 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       mbar_wait(bar_drain, 0, p.status, &no_abort);
     }
     __syncwarp();
+  } else if (C::NV && warp >= 2 + C::EPI_WARPS) {
+    // converter warps: the same tiles and stages as the MMA warp; each stage's raw B rows are
+    // decoded into the f16 tile once they land, then published to the MMA (async proxy)
+    const int ct = tid - 32 * (2 + C::EPI_WARPS);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = first; tile < ntiles && !*s_abort; tile += step) {
+      const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
+      bool ok = true;
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        if (!mbar_wait(bar_full + 8 * stage, phase, p.status, s_abort)) { ok = false; break; }
+        nv_convert_stage<BN>(sSF0 + stage * C::SF_BYTES, sB0 + stage * C::B_BYTES, ct);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_conv + 8 * stage);
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+    }
   } else if (warp >= 2) {
     const int q = warp & 3;  // TMEM lane quarter accessible to this warp
     const int half = (warp - 2) / 4;  // 8 epilogue warps: which column half
@@ -1154,6 +1280,9 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
         epilogue_rows<MODE, BN>(p, p.out0, t, tacc, stg, q, half, lane, rel);
       } else if constexpr (MODE == G_FWD_GU_MX) {
         epilogue_gu_mx<BN>(p, t, tacc, r, half, rel);
+      } else if constexpr (MODE == G_FWD_GU_NV) {
+        epilogue_gu_nv<BN>(p, t, tacc, r);
+        acc_release(rel, lane);
       } else if constexpr (MODE == G_BWD_DA_MX) {
         epilogue_da_mx<BN>(p, t, tacc, stg, q, half, lane, rel);
       } else {
@@ -1234,7 +1363,8 @@ static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
   static const char* kNames[] = {"gemm_fwd_gate_up", "gemm_fwd_down",      "gemm_bwd_da",
                                  "gemm_bwd_dx",      "gemm_bwd_dw",        "gemm_fwd_gate_up_mx",
                                  "gemm_fwd_down_mx", "gemm_bwd_da_mx",     "gemm_bwd_dx_mx",
-                                 "gemm_bwd_dw_mx",   "gemm_fwd_fused"};
+                                 "gemm_bwd_dw_mx",   "gemm_fwd_fused",     "gemm_fwd_gate_up_nv",
+                                 "gemm_fwd_down_nv"};
   if constexpr (!PAIR) {
     if (grid <= 0) return cudaSuccess;
     prof_begin(kNames[MODE], s);
@@ -1305,6 +1435,8 @@ cudaError_t launch_gemm(int mode, int bn, const GemmParams& p_in, int grid, cuda
     case G_BWD_DX_MX: return launch_one<G_BWD_DX_MX, 256>(p, grid, s);
     case G_BWD_DW_MX: return launch_one<G_BWD_DW_MX, 256>(p, grid, s);
     case G_FWD_GUD: return launch_one<G_FWD_GUD, 256>(p, grid, s);
+    case G_FWD_GU_NV: return launch_one<G_FWD_GU_NV, 256>(p, grid, s);
+    case G_FWD_DOWN_NV: return launch_one<G_FWD_DOWN_NV, 256>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

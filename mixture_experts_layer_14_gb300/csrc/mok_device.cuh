@@ -382,6 +382,17 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int n, bool a_mn_major, b
          | (static_cast<uint32_t>(m >> 4) << 24);     // M >> 4
 }
 
+// Orders this thread's earlier generic-proxy shared-memory stores before async-proxy reads of
+// them (an MMA reading a tile that threads wrote).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The same with f16 A and B (format 0 in both fields).
+__host__ __device__ constexpr uint32_t make_idesc_f16(int n, int m = 128) {
+  return make_idesc_bf16(n, false, false, m) & ~((7u << 7) | (7u << 10));
+}
+
 // ------------------------------------------------------------------ small helpers
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

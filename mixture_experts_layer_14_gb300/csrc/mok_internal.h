@@ -36,6 +36,11 @@ enum GemmMode : int {
   // a device work counter (every gate/up tile before any down tile), and a down tile waits for
   // the readiness counter of its M tile (all its h columns written)
   G_FWD_GUD = 10,
+  // NVFP4 (f16 operands on the tensor cores): A = activations holding NVFP4 values (q * s), B =
+  // NVFP4 weight codes and block scales decoded into f16 in shared memory by converter warps;
+  // the tensor scales are applied in the epilogue
+  G_FWD_GU_NV = 11,   // h = SiLU(X Wg) * (X Wu), quantised to NVFP4 values (f16) in the epilogue
+  G_FWD_DOWN_NV = 12, // Y = w * (h Wd), bf16 out
 };
 
 // Tensor-map slots.  Group 0 is the shared expert (rows = tokens), group 1 the routed experts
@@ -97,6 +102,13 @@ struct GemmParams {
   int* work;
   int* ready;
   int nfast_mt;         // M-grouped: groups of at least this many M tiles run N tiles fastest (0: never)
+  // NVFP4 modes, [group][gate or down, up]: weight code rows (32 bytes) and scale rows (4 bytes)
+  // per (expert, 64-element K block, N row), the per-expert decode scales 1 / S, and the
+  // calibrated activation amaxes {x, h}
+  const uint8_t* nvq[2][2];
+  const uint8_t* nvs[2][2];
+  const float* nvg[2][2];
+  const float* nv_act;
   int* status;
 };
 
@@ -186,6 +198,16 @@ struct TokQuantParams {
   int nkb;
 };
 cudaError_t launch_mx_quantize_tokens(const TokQuantParams& tp, cudaStream_t s);
+// NVFP4 quantisation (nv.cu; format and recipe in mok_nv.cuh).  launch_nv_prepare: per-matrix
+// amax (amax[m] must be zero at launch) then codes and block scales of src [nmat][K][N] as rows
+// of 32 + 4 bytes per (matrix, 64-element K block, column) and g[m] = 1 / S.
+// launch_nv_quantize_act: rows x K bf16 -> f16 NVFP4 values without the tensor scale, with the
+// calibrated tensor amax *amax.
+cudaError_t launch_nv_prepare(const void* src, int64_t nmat, int K, int N, uint32_t* amax, void* q,
+                              void* sc, float* g, cudaStream_t s);
+cudaError_t launch_nv_quantize_act(const void* src, int64_t rows, int K, const float* amax,
+                                   void* dst, cudaStream_t s);
+cudaError_t launch_nv_set_act(float* act, float amax_x, float amax_h, cudaStream_t s);
 // Optional per-launch CUDA-event timing (profile.cu); no-ops unless enabled on this thread.
 void prof_begin(const char* name, cudaStream_t s);
 void prof_end(cudaStream_t s);

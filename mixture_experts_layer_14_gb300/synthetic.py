@@ -27,7 +27,7 @@ class LayerShape:
     n_shared: int = 1
     weight_std: float = 0.0      # 0 -> N(0, 1/sqrt(fan_in))
     bias: str = "none"           # "none" | "normal0.1" | "zipf"
-    dtype: str = "bf16"          # arithmetic of the expert GEMMs: "bf16" | "mxfp8"
+    dtype: str = "bf16"          # arithmetic of the expert GEMMs: "bf16" | "mxfp8" | "nvfp4"
     backward: bool = False
     cid: int = 0                 # seed offset
 
@@ -68,6 +68,11 @@ WORKLOADS = {
                                        0.0, "normal0.1", "mxfp8", False, 8),
     "dsv3_mxfp8_train_slice_e32": LayerShape("dsv3_mxfp8_train_slice_e32", 1024, 7168, 32, 8, 2048,
                                              2048, 1, 0.0, "normal0.1", "mxfp8", True, 11),
+    # the DeepSeek-V3 forward with NVFP4 expert GEMMs, and its decode-sized batch
+    "dsv3_nvfp4_fwd": LayerShape("dsv3_nvfp4_fwd", 4096, 7168, 256, 8, 2048, 2048, 1, 0.0,
+                                 "normal0.1", "nvfp4", False, 13),
+    "dsv3_nvfp4_decode_t64": LayerShape("dsv3_nvfp4_decode_t64", 64, 7168, 256, 8, 2048, 2048, 1,
+                                        0.0, "normal0.1", "nvfp4", False, 14),
     # a slice of the Kimi-class layer for profiler captures: the same rank-biased routing over 48
     # experts (a few hot experts hold nearly every token, CTA-pair tiles), about 4 GB of weights
     "kimi_skew_slice_e48": LayerShape("kimi_skew_slice_e48", 2048, 7168, 48, 8, 2048, 2048, 1, 0.0,

@@ -139,3 +139,31 @@ def test_forward_schedule_values():
             mok.set_forward_schedule(7)
     finally:
         mok.set_forward_schedule(prev)
+
+
+def test_nvfp4_sizes_and_argument_errors():
+    """NVFP4 prepared size (codes 1/2 byte and scales 1/16 byte per weight element, plus the
+    per-matrix scales and the two calibration values); no saved activations (forward only); the
+    backward and invalid calibration values are refused on the host, before any CUDA call."""
+    L = ensure_lib()
+    E, d, F, Fs = 256, 7168, 2048, 2048
+    D = mok.dims(4096, d, E, 8, F, Fs, 1, dtype=mok.MOK_NVFP4)
+    elems = 3 * E * d * F + 3 * d * Fs
+    n = mok.prepared_size(D)
+    assert elems * 9 // 16 <= n <= elems * 9 // 16 + 16 * 1024 + 8 * (3 * E + 3) + 1024
+    assert mok.saved_size(D) == 0
+    assert mok.prepared_size(mok.dims(16, 128, 8, 2, 128, 128, 1, dtype=mok.MOK_NVFP4)) == 0  # d % 256
+    null = None
+    fake = ctypes.c_void_p(0x1000)
+    f = ctypes.c_float
+    Dn = mok.dims(16, 256, 8, 2, 128, 128, 1, dtype=mok.MOK_NVFP4)
+    Db = mok.dims(16, 256, 8, 2, 128, 128, 1)
+    set_amax = L.mok_nvfp4_set_activation_amax
+    assert set_amax(ctypes.byref(Db), fake, f(1.0), f(1.0), null) == -1      # not NVFP4
+    assert set_amax(ctypes.byref(Dn), null, f(1.0), f(1.0), null) == -1      # no buffer
+    assert set_amax(ctypes.byref(Dn), ctypes.c_void_p(0x1001), f(1.0), f(1.0), null) == -1
+    assert set_amax(ctypes.byref(Dn), fake, f(-1.0), f(1.0), null) == -1
+    assert set_amax(ctypes.byref(Dn), fake, f(1.0), f(float("nan")), null) == -1
+    assert set_amax(ctypes.byref(Dn), fake, f(float("inf")), f(1.0), null) == -1
+    rc = L.mok_moe_backward(ctypes.byref(Dn), *([null] * 20), 0, null)
+    assert rc == -2
