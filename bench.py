@@ -173,6 +173,15 @@ def work_model(shape, counts):
         m["gemm_fwd_down_mx"] = {
             "flops": m["gemm_fwd_down"]["flops"], "dtype": "fp8",
             "bytes": wq * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d + Hs) + wb * Rs * d}
+    if shape.dtype == "nvfp4":
+        wq = 0.5 + 1.0 / 16  # an E2M1 nibble + one E4M3 byte per 16 (the per-matrix scales: noise)
+        m["nv_quantize_x"] = {"flops": 0.0, "bytes": T * d * (wb + 2.0)}  # bf16 in, f16 values out
+        m["gemm_fwd_gate_up_nv"] = {  # f16 products at the bf16 rate; x values once, h written
+            "flops": m["gemm_fwd_gate_up"]["flops"], "dtype": "f16",
+            "bytes": wq * (e_act * 2.0 * d * F + ns * 2.0 * d * Fs) + 2.0 * (T * d + Hs)}
+        m["gemm_fwd_down_nv"] = {
+            "flops": m["gemm_fwd_down"]["flops"], "dtype": "f16",
+            "bytes": wq * (e_act * 1.0 * F * d + ns * 1.0 * Fs * d) + 2.0 * Hs + wb * Rs * d}
     if train:
         m["gather_dy"] = {"flops": 0.0, "bytes": wb * (T * d + R * d) + 4.0 * R}
         m["gemm_bwd_da"] = {  # a = dY Wd^T; reads G, U; writes dG, dU, w*h
@@ -237,6 +246,8 @@ def profiled_traffic(workload, name):
 BYTE_BASIS = {
     "gemm_fwd_gate_up": "active gate+up weight sets + x once (T d) + h written (+ G, U saved)",
     "gemm_fwd_gate_up_mx": "active gate+up E4M3 weights and scales + x codes once + h codes written",
+    "gemm_fwd_gate_up_nv": "active gate+up E2M1 weights and E4M3 scales + x values (f16) once + h values (f16) written",
+    "gemm_fwd_down_nv": "active down E2M1 weights and E4M3 scales + h values (f16) read + router-weighted rows Y_s written",
     "gemm_fwd_down": "active down weight sets + h read + router-weighted rows Y_s written",
     "gemm_fwd_down_mx": "active down E4M3 weights and scales + h codes read + Y_s written",
     "combine": "(k + 1) rows read + one row written per token",
@@ -251,7 +262,8 @@ SUSTAINED_AFTER_MS = 2000.0  # timed regions this long run under the power cap: 
 def roofline_of(name, model, ms_per_launch, peaks, sustained=False):
     w = model[name]
     # the measured bf16 peak (burst for a short timed region, the seconds-long sustained figure
-    # for a long one); an FP8 contraction takes it times the nominal fp8/bf16 ratio (2)
+    # for a long one); an FP8 contraction takes it times the nominal fp8/bf16 ratio (2), an f16
+    # one (the NVFP4 GEMMs' decoded operands) the bf16 figure itself
     base = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) if sustained else peaks["bf16_tflops"]
     tpeak = base * (2.0 if w.get("dtype") == "fp8" else 1.0)
     t_flop = w["flops"] / (tpeak * 1e12) if w["flops"] else 0.0
@@ -334,6 +346,9 @@ def cpu_baseline(L, shape, pool_tokens=2, budget_s=12.0, max_steps=64):
 
 # ------------------------------------------------------------------ the GB300 arm
 TIMING_EVERY = 4  # per-launch event timing on every 4th timed step
+# NVFP4: calibrated amax of h for these synthetic inputs (SiLU(g) u with g, u about N(0, 1));
+# the rare larger values saturate, as the recipe has it
+NV_AMAX_H = 8.0
 
 
 def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
@@ -347,12 +362,15 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
     if L is None:
         L = make_layer(shape, dev, with_dy=shape.backward)
     mx = shape.dtype == "mxfp8"
+    nv = shape.dtype == "nvfp4"
     D = mok.dims(shape.T, shape.d, shape.E, shape.k, shape.F, shape.F_shared, shape.n_shared,
-                 mok.MOK_MXFP8 if mx else mok.MOK_BF16)
-    if mx:  # weights are quantised once, outside the timed region
+                 mok.MOK_MXFP8 if mx else mok.MOK_NVFP4 if nv else mok.MOK_BF16)
+    if mx or nv:  # weights are quantised once, outside the timed region
         L["prepared"] = mok.prepare_weights(D, L)
         if shape.backward:
             L["prepared_bwd"] = mok.prepare_weights_bwd(D, L)
+    if nv:  # calibration: x's amax from the batch, h's the value calibrated for these inputs
+        mok.nvfp4_set_activation_amax(D, L["prepared"], float(L["x"].abs().max()), NV_AMAX_H)
     layer = mok.MoELayer(D, L, dev)
     x = L["x"]
     torch.cuda.synchronize()
@@ -422,7 +440,8 @@ def measure(args, shape, steps, warmup, dev, world, peaks, L=None):
         "tflops": round(tflops, 2),
         "tflops_frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
         "tflops_frac_of_dtype_peak": round(tflops / tpeak, 4),
-        "dtype": "mxfp8 (e4m3 + ue8m0/32)" if mx else "bf16",
+        "dtype": "mxfp8 (e4m3 + ue8m0/32)" if mx else
+                 "nvfp4 (e2m1 + e4m3/16 + fp32 per tensor; f16 tensor-core products)" if nv else "bf16",
         "roofline": {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in roof.items()},
         "kernels": kernels, "kernel_timing": f"CUDA events on {sampled} of the {steps} timed steps",
         "gpu_launches": launches, "clocks": clocks,
@@ -467,7 +486,7 @@ def fp8_cublas_tflops(dev):
 
 def weight_bytes_per_step(shape, counts):
     """Bytes of expert weights one forward streams: every active routed expert and the shared."""
-    b = 1.0 + 1.0 / 32 if shape.dtype == "mxfp8" else 2.0
+    b = {"mxfp8": 1.0 + 1.0 / 32, "nvfp4": 0.5 + 1.0 / 16}.get(shape.dtype, 2.0)
     e_act = sum(1 for c in counts if c > 0)
     return b * 3.0 * shape.d * (e_act * shape.F + shape.n_shared * shape.F_shared)
 
@@ -659,7 +678,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--extra", default="dsv3_bf16_fwd,dsv3_bf16_train,dsv3_mxfp8_fwd,"
-                    "dsv3_mxfp8_train,dsv3_decode_t64")
+                    "dsv3_mxfp8_train,dsv3_decode_t64,dsv3_nvfp4_fwd,dsv3_nvfp4_decode_t64")
     ap.add_argument("--extra-steps", type=int, default=30)
     args = ap.parse_args(argv)
     if args.warmup < 3:
