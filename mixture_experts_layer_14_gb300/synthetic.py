@@ -73,6 +73,9 @@ WORKLOADS = {
                                  "normal0.1", "nvfp4", False, 13),
     "dsv3_nvfp4_decode_t64": LayerShape("dsv3_nvfp4_decode_t64", 64, 7168, 256, 8, 2048, 2048, 1,
                                         0.0, "normal0.1", "nvfp4", False, 14),
+    # the NVFP4 forward on 32 experts with the DSV3 rows per expert (128), for profiler captures
+    "dsv3_nvfp4_slice_e32": LayerShape("dsv3_nvfp4_slice_e32", 512, 7168, 32, 8, 2048, 2048, 1, 0.0,
+                                       "normal0.1", "nvfp4", False, 15),
     # a slice of the Kimi-class layer for profiler captures: the same rank-biased routing over 48
     # experts (a few hot experts hold nearly every token, CTA-pair tiles), about 4 GB of weights
     "kimi_skew_slice_e48": LayerShape("kimi_skew_slice_e48", 2048, 7168, 48, 8, 2048, 2048, 1, 0.0,
