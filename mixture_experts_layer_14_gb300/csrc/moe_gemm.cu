@@ -13,6 +13,8 @@
 // blocks pulled straight from it).  CTA c takes tiles c, c+grid, c+2*grid, ...  Every output
 // element is produced by exactly one CTA with a fixed K order, so results are bit-identical
 // from run to run.  No host synchronisation: the tile count is read on the device.
+#include <algorithm>
+
 #include "mok_nv.cuh"
 
 namespace mok {
@@ -173,17 +175,21 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
     // Inside a problem the N tiles run fastest, so the tiles in flight together write whole
     // output rows.  Pairs: the two CTAs take adjacent M tiles of the same N tile (every
     // problem's M-tile count is even).
+    // divisions by the launch's divisors through their precomputed reciprocals (one wide
+    // multiply each instead of an integer-division sequence on the issuing threads)
     constexpr int U = PAIR ? 2 : 1;
-    auto place = [&](int ls, int nt) {  // ls: tile index inside the problem, in single tiles
+    auto div = [](int n, uint64_t m) { return (int)(((uint64_t)(uint32_t)n * m) >> 32); };
+    auto place = [&](int ls, int nt, uint64_t mnt) {  // ls: tile index inside the problem
       const int ps = ls / U;
-      t.n = ps % nt;
-      t.m0 = ((ps / nt) * U + ls % U) * BM;
+      const int q = div(ps, mnt);
+      t.n = ps - q * nt;
+      t.m0 = (q * U + ls % U) * BM;
     };
     int l = PAIR ? 2 * tile + rank : tile;
     if (l < p.router_tiles) {
       t.g = 2;
       t.e = 0;
-      place(l, p.router_tiles / (p.d / BM));
+      place(l, p.router_nt, p.dm_ntr);
       t.row0 = 0;
       t.rows = p.T;
     } else {
@@ -200,7 +206,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
       } else {
         l -= tiles_sh;
         const int per = 2 * (p.d / BM) * (p.F / BN) + (p.F / BM) * (p.d / BN);
-        const int e = l / per;
+        const int e = div(l, p.dm_per);
         l -= e * per;
         t.g = 1;
         t.e = e;
@@ -210,11 +216,11 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* s_of
       }
       const int tg = (p.d / BM) * (Fg / BN);
       if (l < 2 * tg) {
-        t.sub = l / tg;
-        place(l - t.sub * tg, Fg / BN);
+        t.sub = l >= tg ? 1 : 0;
+        place(l - t.sub * tg, Fg / BN, p.dm_nt[t.g]);
       } else {
         t.sub = 2;
-        place(l - 2 * tg, p.d / BN);
+        place(l - 2 * tg, p.d / BN, p.dm_ntd);
       }
     }
     if constexpr (MODE == G_BWD_DW_MX) {
@@ -1353,8 +1359,33 @@ cudaError_t launch_dw_bound_maps(const BoundMapParams& bp, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ceil(2^32 / d): n / d == (n * m) >> 32 for every n with n * d < 2^32
+static uint64_t div_magic(int64_t d) { return d > 0 ? ((uint64_t(1) << 32) + uint64_t(d) - 1) / uint64_t(d) : 0; }
+
+// The K-grouped decode's divisors of this launch (tile counts of its tile numbering); false when
+// a tile index times a divisor could reach 2^32, where the reciprocal division would not be exact.
+template <int BN>
+static bool set_div_magics(GemmParams& p, int64_t ntiles_single) {
+  const int64_t per = 2 * (p.d / BM) * (p.F / BN) + (p.F / BM) * (p.d / BN);
+  const int64_t nts = p.Fs / BN, ntf = p.F / BN, ntd = p.d / BN;
+  p.router_nt = p.router_tiles > 0 ? p.router_tiles / (p.d / BM) : 1;
+  p.dm_per = div_magic(per);
+  p.dm_nt[0] = div_magic(nts > 0 ? nts : 1);
+  p.dm_nt[1] = div_magic(ntf);
+  p.dm_ntd = div_magic(ntd);
+  p.dm_ntr = div_magic(p.router_nt);
+  const int64_t dmax = std::max({per, nts, ntf, ntd, (int64_t)p.router_nt});
+  return ntiles_single * dmax < (int64_t(1) << 32);
+}
+
 template <int MODE, int BN, bool PAIR = false>
-static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
+static cudaError_t launch_one(const GemmParams& p_in, int grid, cudaStream_t s) {
+  GemmParams p = p_in;
+  if constexpr (Cfg<MODE, BN>::K_GROUPED) {
+    const int64_t per = 2 * (p.d / BM) * (p.F / BN) + (p.F / BM) * (p.d / BN);
+    const int64_t sh = p.has_shared ? 2 * (p.d / BM) * (p.Fs / BN) + (p.Fs / BM) * (p.d / BN) : 0;
+    if (!set_div_magics<BN>(p, p.router_tiles + sh + (int64_t)p.E * per)) return cudaErrorInvalidValue;
+  }
   constexpr int smem = smem_bytes_for<MODE, BN, PAIR>();
   static_assert(smem <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
   auto k = moe_gemm_kernel<MODE, BN, PAIR>;

@@ -102,6 +102,12 @@ struct GemmParams {
   int* work;
   int* ready;
   int nfast_mt;         // M-grouped: groups of at least this many M tiles run N tiles fastest (0: never)
+  // K-grouped tile decode: the launch's runtime divisors as m = ceil(2^32 / divisor), so that
+  // n / divisor = (n * m) >> 32 (exact for n * divisor < 2^32, checked at launch): tiles per
+  // routed problem, N tiles per row of a gate/up gradient [group], of a down gradient, and of
+  // the router gradient (router_nt of them)
+  uint64_t dm_per, dm_nt[2], dm_ntd, dm_ntr;
+  int router_nt;
   // NVFP4 modes, [group][gate or down, up]: weight code rows (32 bytes) and scale rows (4 bytes)
   // per (expert, 64-element K block, N row), the per-expert decode scales 1 / S, and the
   // calibrated activation amaxes {x, h}
