@@ -6,18 +6,19 @@
 //
 // One CTA per (128-token tile, K split).  Warp 0 issues TMA loads of the x tile (K-major) and of
 // all E columns of W_router (MN-major), warp 1 issues the UMMAs (N = E rounded up to 64, split
-// into MMAs of at most 256 columns), warps 2..5 run the epilogue.  The bias is staged in shared
-// memory once, so the epilogue reads it as broadcast vectors.
-//  - One split (the token tiles alone fill the GPU): each epilogue thread owns one token row of
-//    the accumulator and selects its top k straight from TMEM, loading the next 32 columns while
-//    it ranks the current ones.
+// into MMAs of at most 256 columns), warps 2..9 run the epilogue, two per TMEM lane quarter.
+// The bias is staged in shared memory once, so the epilogue reads it as broadcast vectors.
+//  - One split (the token tiles alone fill the GPU): the two threads of a token row each select
+//    the top k of half its columns straight from TMEM (loading the next 32 columns while they
+//    rank the current ones), and the lower half inserts the upper half's list into its own
+//    through shared memory.
 //  - S > 1 splits (a power of two): the S CTAs of a tile form a thread-block cluster, and CTA r
 //    reduces tile rows r 128/S .. (r+1) 128/S - 1.  Each CTA stores the partial logits of those
 //    rows straight into CTA r's shared memory (the drained stage buffers, one slot per source
-//    CTA, a chunk of columns at a time), so no thread waits on a remote load.  Then S threads
-//    per row each sum the S partials of a quarter of the columns in rank order (the same fixed
-//    order on every run), keep their own top-k list, and merge the S lists with warp shuffles.
-//    The partial logits never leave the chip.
+//    CTA, a chunk of columns at a time), so no thread waits on a remote load.  Then 2S threads
+//    per row each sum the S partials of their share of the columns in rank order (the same
+//    fixed order on every run), keep their own top-k list, and merge the lists with warp
+//    shuffles.  The partial logits never leave the chip.
 #include "mok_device.cuh"
 
 namespace mok {
@@ -107,31 +108,32 @@ __device__ __forceinline__ void merge_topk(int k, float (&tv)[kMaxK], int (&ti)[
 
 // Splits > 1, one pass over logit columns c0 .. c0 + p.chunk - 1, after every CTA of the cluster
 // has stored its partials of this CTA's rows: slot r of `part` holds CTA r's partial logits of
-// rows rank 128/S .. (rank+1) 128/S - 1.  Thread `et` (0..127) of the epilogue sums the S
-// partials of its row's columns 4 (sub + S i) .. + 3 in rank order, adds the bias and inserts
-// them into its top-k list.
+// rows rank 128/S .. (rank+1) 128/S - 1.  Epilogue thread `et` (0..255; 2S threads per row) sums
+// the S partials of its row's columns 4 (sub + 2S i) .. + 3 in rank order, adds the bias and
+// inserts them into its top-k list.
 template <int S>
 __device__ __forceinline__ void reduce_rows(const RouteParams& p, uint32_t part, uint32_t pstride,
                                             int c0, int rank, int et, const float* s_bias,
                                             float (&tv)[kMaxK], int (&ti)[kMaxK]) {
   constexpr int RPC = BM / S;           // rows this CTA reduces
-  const int row = et / S;               // of this CTA's rows
-  const int sub = et % S;
+  constexpr int TPR = 2 * S;            // threads per row
+  const int row = et / TPR;             // of this CTA's rows
+  const int sub = et % TPR;
   const int t = blockIdx.x * BM + rank * RPC + row;
   const uint32_t mine = part + row * pstride;
   const int n4 = p.chunk / 4;
   // two float4 columns per pass, every load issued first
-  for (int j0 = sub; j0 < n4; j0 += 2 * S) {
+  for (int j0 = sub; j0 < n4; j0 += 2 * TPR) {
     float4 v[2][S];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int r = 0; r < S; ++r)
-        v[h][r] = (j0 + h * S < n4) ? ld_shared_v4(mine + r * RPC * pstride + 16 * (j0 + h * S))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[h][r] = (j0 + h * TPR < n4) ? ld_shared_v4(mine + r * RPC * pstride + 16 * (j0 + h * TPR))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int j = j0 + h * S;
+      const int j = j0 + h * TPR;
       if (j >= n4) break;
       float4 acc = v[h][0];
 #pragma unroll
@@ -157,15 +159,17 @@ __device__ __forceinline__ void finish_split(const RouteParams& p, int rank, int
                                              float (&tv)[kMaxK], int (&ti)[kMaxK]) {
   float ov[kMaxK];
   int oi[kMaxK];
-  merge_topk<S>(p.k, tv, ti, ov, oi);
-  const int row = rank * (BM / S) + et / S;
+  merge_topk<2 * S>(p.k, tv, ti, ov, oi);
+  const int row = rank * (BM / S) + et / (2 * S);
   const int t = blockIdx.x * BM + row;
-  if (et % S == 0 && t < p.T) write_route(p, t, ov, oi);
+  if (et % (2 * S) == 0 && t < p.T) write_route(p, t, ov, oi);
 }
 
 constexpr int kRouteAuxBytes = 1024;  // barriers, TMEM address, abort flag
+// warp 0 loads, warp 1 issues the MMAs, warps 2-9 run the epilogue: two per TMEM lane quarter
+constexpr int kRouteThreads = 64 + 32 * 8;
 
-__global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_constant__ RouteParams p) {
+__global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_constant__ RouteParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -267,14 +271,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
     __syncwarp();
   } else {
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;  // which of the two warps of this lane quarter
     const int r = q * 32 + lane;
     const int t = m0 + r;
-    acc_ok = mbar_wait(bar_acc, 0, p.status, s_abort);
+    // the same in every lane: the warp's TMEM loads below need all 32 lanes
+    acc_ok = __all_sync(0xffffffffu, mbar_wait(bar_acc, 0, p.status, s_abort) ? 1 : 0) != 0;
     tc_fence_after();
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    if (acc_ok && p.splits == 1) {
-      // ranks 32 columns while the next 32 load from TMEM (two named buffers, so both stay in
-      // registers)
+    if (p.splits == 1) {
+      // each of the two threads of a row ranks half of its 32-column chunks, loading the next 32
+      // columns while it ranks the current ones (two named buffers, so both stay in registers)
       auto rank_cols = [&](const uint32_t (&v)[32], int c) {
         float b[32];
 #pragma unroll
@@ -293,19 +299,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
         }
       };
       const int nch = (p.E + 31) / 32;  // 32 nch <= E_pad: every column loaded is allocated
-      uint32_t va[32], vb[32];
-      tmem_ld32(tacc, va);
-      tmem_ld_wait();
-      for (int ch = 0; ch < nch; ch += 2) {
-        if (ch + 1 < nch) tmem_ld32(tacc + 32 * (ch + 1), vb);
-        rank_cols(va, 32 * ch);
+      const int nh = (nch + 1) / 2;
+      const int ch0 = half * nh, ch1 = min(nch, ch0 + nh);
+      if (acc_ok && ch0 < ch1) {
+        uint32_t va[32], vb[32];
+        tmem_ld32(tacc + 32 * ch0, va);
         tmem_ld_wait();
-        if (ch + 1 == nch) break;
-        if (ch + 2 < nch) tmem_ld32(tacc + 32 * (ch + 2), va);
-        rank_cols(vb, 32 * (ch + 1));
-        tmem_ld_wait();
+        for (int ch = ch0; ch < ch1; ch += 2) {
+          if (ch + 1 < ch1) tmem_ld32(tacc + 32 * (ch + 1), vb);
+          rank_cols(va, 32 * ch);
+          tmem_ld_wait();
+          if (ch + 1 == ch1) break;
+          if (ch + 2 < ch1) tmem_ld32(tacc + 32 * (ch + 2), va);
+          rank_cols(vb, 32 * (ch + 1));
+          tmem_ld_wait();
+        }
       }
-      if (t < p.T) write_route(p, t, tv, ti);
+      // the upper half's list goes through shared memory (the drained stage buffers: every MMA
+      // completed) to the lower half, which inserts it into its own: the lower half holds the
+      // lower expert indices, so among equal logits its entries stay ahead
+      uint32_t* lists = reinterpret_cast<uint32_t*>(gbase) + r * 16;
+      if (half == 1) {
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+          lists[j] = __float_as_uint(tv[j]);
+          lists[8 + j] = static_cast<uint32_t>(ti[j]);
+        }
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * 8) : "memory");  // the eight epilogue warps
+      if (half == 0) {
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j)
+          topk_insert(tv, ti, __uint_as_float(lists[j]), static_cast<int>(lists[8 + j]));
+        if (acc_ok && t < p.T) write_route(p, t, tv, ti);
+      }
     }
   }
 
@@ -315,8 +342,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
     // whatever happened above (a bounded wait that ran out leaves zeros), so none can wait
     // forever on a CTA that left.
     const int rank = (int)cluster_ctarank();
-    const int et = tid - 64;  // epilogue thread 0..127
+    const int et = tid - 64;  // epilogue thread 0..255
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const int rpc = BM / p.splits;  // rows each CTA of the cluster reduces
     // the drained stage buffers: slot r (rows r rpc .. r rpc + rpc - 1 of `part`) receives CTA
@@ -329,7 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) route_kernel(const __grid_con
       if (warp >= 2) {
         const int rr = q * 32 + lane;  // tile row of this thread's TMEM lane
         const uint32_t dst = mapa_shared(part + (rank * rpc + rr % rpc) * pstride, rr / rpc);
-        for (int cc = 0; cc < p.chunk; cc += 32) {
+        for (int cc = half * (p.chunk / 2); cc < (half + 1) * (p.chunk / 2); cc += 32) {
           uint32_t v[32];
           if (acc_ok && nkb > 0) {
             tmem_ld32(tacc + c0 + cc, v);
@@ -410,7 +438,7 @@ cudaError_t launch_route(const RouteParams& p_in, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = p.splits > 1 ? 1 : 0;
   cfg.gridDim = dim3((p.T + BM - 1) / BM, p.splits);
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(kRouteThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   prof_begin("route", s);
