@@ -46,7 +46,13 @@ struct Cfg {
   // UE8M0 atoms of A and B (MXFP8); the raw NVFP4 B rows (NVFP4)
   static constexpr int SF_BYTES = MX ? (BM + BN) * 4 : NV ? BN * 36 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
-  static constexpr int STAGES = NV ? 3 : (BN == 256) ? 4 : 6;
+  static constexpr int STAGES = NV ? 4 : (BN == 256) ? 4 : 6;
+  // NVFP4: three rings instead of one: STAGES A tiles; RAW_STAGES raw B rows, deep because they
+  // come from HBM and are small (a stage is 9 KB against 48 KB of decoded f16), so the weight
+  // stream runs far ahead of the MMA; DEC_STAGES decoded B tiles, which live only from the
+  // converters to the MMA
+  static constexpr int RAW_STAGES = NV ? 8 : 0;
+  static constexpr int DEC_STAGES = NV ? 2 : 0;
   static constexpr bool A_MN = (MODE == G_BWD_DW);
   static constexpr bool B_MN = (MODE == G_FWD_GU || MODE == G_FWD_DOWN || MODE == G_BWD_DW ||
                                 MODE == G_FWD_GUD);
@@ -58,8 +64,9 @@ struct Cfg {
   // epilogue warps: two per TMEM lane quarter (each taking half the columns) where the single
   // accumulator leaves the epilogue exposed, one otherwise
   static constexpr int EPI_WARPS = NUM_ACC == 1 ? 8 : 4;
-  static constexpr int CONV_WARPS = NV ? 4 : 0;       // NVFP4 B decoders, after the epilogue warps
-  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + CONV_WARPS);
+  static constexpr int CONV_WARPS = NV ? 8 : 0;       // NVFP4 B decoders, after the epilogue warps
+  // NVFP4: one more warp issues the raw B loads, so they do not wait behind the A ring
+  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + CONV_WARPS + (NV ? 1 : 0));
   // plain row-major outputs go through shared memory one 32-column chunk (32 rows x 64 B) per
   // epilogue warp at a time and are written with coalesced row stores
   static constexpr bool ROW_STAGED = (MODE == G_FWD_DOWN || MODE == G_BWD_DX ||
@@ -70,6 +77,8 @@ struct Cfg {
   static constexpr int STG_STRIDE = (MODE == G_BWD_DA_MX) ? 32 * 36 * 4 : 2048;
   static constexpr int STAGING_BYTES = (ROW_STAGED || MODE == G_BWD_DA_MX) ? EPI_WARPS * STG_STRIDE : 0;
   static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
+  static constexpr int RING_BYTES =
+      NV ? STAGES * A_BYTES + DEC_STAGES * B_BYTES + RAW_STAGES * SF_BYTES : STAGES * STAGE_BYTES;
   static constexpr int SF_TMEM_COL = 256;              // MXFP8: 16 columns per stage from here
   static constexpr uint32_t IDESC =
       MX ? make_idesc_mxf8(BN) : NV ? make_idesc_f16(BN) : make_idesc_bf16(BN, A_MN, B_MN);
@@ -91,6 +100,7 @@ struct KCfg : Cfg<MODE, BN> {
   static constexpr int B_BYTES = PAIR ? Base::B_BYTES / 2 : Base::B_BYTES;
   static constexpr int STAGE_BYTES = Base::A_BYTES + B_BYTES + Base::SF_BYTES;
   static constexpr int STAGES = PAIR ? 6 : Base::STAGES;
+  static constexpr int RING_BYTES = PAIR ? STAGES * STAGE_BYTES : Base::RING_BYTES;
   static constexpr int BMT = PAIR ? 2 * BM : BM;  // rows of an M tile (M-grouped)
   static constexpr uint32_t IDESC =
       PAIR ? make_idesc_bf16(BN, Base::A_MN, Base::B_MN, 256) : Base::IDESC;
@@ -99,7 +109,7 @@ struct KCfg : Cfg<MODE, BN> {
 template <int MODE, int BN, bool PAIR = false>
 constexpr int smem_bytes_for() {
   using C = KCfg<MODE, BN, PAIR>;
-  return C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES + kAuxBytes + kSchedBytes + 1024;
+  return C::RING_BYTES + C::STAGING_BYTES + kAuxBytes + kSchedBytes + 1024;
 }
 
 // ------------------------------------------------------------------ tile decode
@@ -906,18 +916,26 @@ __device__ __forceinline__ void load_nv_raw(const GemmParams& p, const Tile& t, 
   }
 }
 
-// Converter thread `ct` (0..127) decodes B rows ct, ct + 128, ... of a stage: each row's 64 codes
+// Converter thread `ct` (0..NCT-1) decodes B rows ct, ct + NCT, ... of a stage: each row's 64 codes
 // times their block scales into f16, written K-major with the 128-byte swizzle the MMA reads
 // (row n: 8-row group n / 8 at 1024 bytes, row n % 8 at 128 bytes, 16-byte chunk c at c ^ (n % 8)).
-template <int BN>
+// Rows sit 32 bytes apart, so the eight lanes of one 16-byte load phase would meet in pairs on
+// the same banks; lanes with bit 2 of the row set read their second half first instead.
+template <int BN, int NCT>
 __device__ __forceinline__ void nv_convert_stage(uint32_t raw, uint32_t sB, int ct) {
 #pragma unroll 1
-  for (int n = ct; n < BN; n += 128) {
-    uint32_t w[8];
+  for (int n = ct; n < BN; n += NCT) {
+    uint32_t w[8], v[8];
+    const uint32_t h = (n & 4) ? 16u : 0u;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(raw + n * 32));
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(raw + n * 32 + h));
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(raw + n * 32 + 16));
+                 : "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]) : "r"(raw + n * 32 + (16u - h)));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[i] = h ? v[i + 4] : v[i];
+      w[i + 4] = h ? v[i] : v[i + 4];
+    }
     uint32_t sc;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(raw + BN * 32 + n * 4));
     const uint32_t row = sB + (n >> 3) * 1024 + (n & 7) * 128;
@@ -954,10 +972,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA0 = base;
   const uint32_t sB0 = base + C::STAGES * C::A_BYTES;
-  const uint32_t sSF0 = sB0 + C::STAGES * C::B_BYTES;  // MXFP8 scale-factor atoms
-  const uint32_t sSTG0 = sSF0 + C::STAGES * C::SF_BYTES;  // output staging of the epilogue warps
-  uint8_t* aux = gbase + C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES;
-  const uint32_t aux_s = base + C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES;
+  // MXFP8 scale-factor atoms; NVFP4 raw B rows
+  const uint32_t sSF0 = sB0 + (C::NV ? C::DEC_STAGES : C::STAGES) * C::B_BYTES;
+  const uint32_t sSTG0 = base + C::RING_BYTES;  // output staging of the epilogue warps
+  uint8_t* aux = gbase + C::RING_BYTES + C::STAGING_BYTES;
+  const uint32_t aux_s = base + C::RING_BYTES + C::STAGING_BYTES;
   // aux layout: full[S] empty[S] tfull[2] tempty[2] drain | tmem addr | abort
   const uint32_t bar_full = aux_s;
   const uint32_t bar_empty = aux_s + 8 * C::STAGES;
@@ -971,8 +990,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
   const uint32_t bar_rfull = aux_s + 16 * C::STAGES + 64;
   const uint32_t bar_rempty = bar_rfull + 8 * kRing;
   volatile int* s_ring = reinterpret_cast<volatile int*>(aux + 16 * C::STAGES + 64 + 16 * kRing);
-  // NVFP4: stage s's B tile decoded (one arrival per converter warp); the ring's space, unused
+  // NVFP4, in the tile ring's space (unused): decoded B tile full (one arrival per converter
+  // warp) and empty (MMA commit), raw B rows full (bulk copies) and empty (converter warps)
   const uint32_t bar_conv = aux_s + 16 * C::STAGES + 64;
+  const uint32_t bar_dempty = bar_conv + 8 * C::DEC_STAGES;
+  const uint32_t bar_rawfull = bar_dempty + 8 * C::DEC_STAGES;
+  const uint32_t bar_rawempty = bar_rawfull + 8 * C::RAW_STAGES;
+  static_assert(16 * C::STAGES + 64 + 16 * (C::DEC_STAGES + C::RAW_STAGES) <= kAuxBytes, "aux barriers");
   int* s_off = reinterpret_cast<int*>(aux + kAuxBytes);
   int* s_mt = s_off + (kMaxE + 1);
 
@@ -996,7 +1020,14 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
     }
     if constexpr (C::NV) {
       static_assert(!C::FUSED, "the decoded-B barriers use the tile ring's space");
-      for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_conv + 8 * s, C::CONV_WARPS);
+      for (int s = 0; s < C::DEC_STAGES; ++s) {
+        mbar_init(bar_conv + 8 * s, C::CONV_WARPS);
+        mbar_init(bar_dempty + 8 * s, 1);
+      }
+      for (int s = 0; s < C::RAW_STAGES; ++s) {
+        mbar_init(bar_rawfull + 8 * s, 1);
+        mbar_init(bar_rawempty + 8 * s, C::CONV_WARPS);
+      }
     }
     *s_abort = 0;
     fence_barrier_init();
@@ -1101,16 +1132,14 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       auto produce = [&](const Tile& t) {
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) return;
-          // a pair's stage: both CTAs' bytes on the even CTA's barrier; NVFP4: A and the raw B rows
-          constexpr uint32_t kTx = C::NV ? C::A_BYTES + C::SF_BYTES : C::A_BYTES + C::B_BYTES + C::SF_BYTES;
+          // a pair's stage: both CTAs' bytes on the even CTA's barrier; NVFP4: A only
+          constexpr uint32_t kTx = C::NV ? C::A_BYTES : C::A_BYTES + C::B_BYTES + C::SF_BYTES;
           if (!PAIR || rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, kTx * (PAIR ? 2 : 1));
           issue_loads<MODE, BN, PAIR>(p, t, kb, rank, sA0 + stage * C::A_BYTES,
                                       sB0 + stage * C::B_BYTES,
                                       PAIR ? mapa_shared(bar_full + 8 * stage, 0) : bar_full + 8 * stage);
           if constexpr (C::MX)
             load_scale_atoms<MODE, BN>(p, t, kb, sSF0 + stage * C::SF_BYTES, bar_full + 8 * stage);
-          if constexpr (C::NV)
-            load_nv_raw<MODE, BN>(p, t, kb, sSF0 + stage * C::SF_BYTES, bar_full + 8 * stage);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       };
@@ -1139,6 +1168,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
   } else if (warp == 1 && (!PAIR || rank == 0)) {
     int stage = 0;
     uint32_t phase = 0;
+    int ds = 0;  // NVFP4: decoded B ring
+    uint32_t dphase = 0;
     // the MMAs of the it-th tile of this CTA; false when a bounded wait ran out
     auto mma_tile = [&](const Tile& t, int it) -> bool {
       const int buf = it % C::NUM_ACC;
@@ -1149,10 +1180,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       bool ok = true;
       for (int kb = 0; kb < t.nkb; ++kb) {
         if (!mbar_wait(bar_full + 8 * stage, phase, p.status, s_abort)) { ok = false; break; }
-        if constexpr (C::NV)  // the converter warps have written this stage's f16 B tile
-          if (!mbar_wait(bar_conv + 8 * stage, phase, p.status, s_abort)) { ok = false; break; }
+        if constexpr (C::NV)  // the converter warps have written the next f16 B tile
+          if (!mbar_wait(bar_conv + 8 * ds, dphase, p.status, s_abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sA = sA0 + stage * C::A_BYTES, sB = sB0 + stage * C::B_BYTES;
+        const uint32_t sA = sA0 + stage * C::A_BYTES;
+        const uint32_t sB = sB0 + (C::NV ? ds : stage) * C::B_BYTES;
         int nk16 = BK / 16;  // MMA K steps of this stage
         if constexpr (C::K_GROUPED) {
           // last k-block of a problem: issue only the K steps holding rows of this problem (the
@@ -1198,9 +1230,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
             umma_commit_pair_mc(bar_empty + 8 * stage, 3);
           else
             umma_commit(bar_empty + 8 * stage);
+          if constexpr (C::NV) umma_commit(bar_dempty + 8 * ds);
         }
         __syncwarp();
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        if constexpr (C::NV)
+          if (++ds == C::DEC_STAGES) { ds = 0; dphase ^= 1; }
       }
       if (!ok) return false;
       if (lane == 0) {
@@ -1237,22 +1272,49 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
       mbar_wait(bar_drain, 0, p.status, &no_abort);
     }
     __syncwarp();
+  } else if (C::NV && warp == 2 + C::EPI_WARPS + C::CONV_WARPS) {
+    // raw B producer (one lane): the tiles of the MMA warp, each k-block's codes and scales by
+    // bulk copies into the raw ring
+    if (lane == 0) {
+      int rs = 0;
+      uint32_t rphase = 0;
+      for (int tile = first; tile < ntiles && !*s_abort; tile += step) {
+        const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
+        bool ok = true;
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(bar_rawempty + 8 * rs, rphase ^ 1, p.status, s_abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar_rawfull + 8 * rs, C::SF_BYTES);
+          if constexpr (C::NV) load_nv_raw<MODE, BN>(p, t, kb, sSF0 + rs * C::SF_BYTES, bar_rawfull + 8 * rs);
+          if (++rs == C::RAW_STAGES) { rs = 0; rphase ^= 1; }
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
   } else if (C::NV && warp >= 2 + C::EPI_WARPS) {
-    // converter warps: the same tiles and stages as the MMA warp; each stage's raw B rows are
-    // decoded into the f16 tile once they land, then published to the MMA (async proxy)
+    // converter warps: each k-block's raw B rows, once landed, decoded into the next free f16
+    // tile, which is then published to the MMA (async proxy); the raw stage is released first
     const int ct = tid - 32 * (2 + C::EPI_WARPS);
-    int stage = 0;
-    uint32_t phase = 0;
+    int rs = 0, ds = 0;
+    uint32_t rphase = 0, dphase = 0;
     for (int tile = first; tile < ntiles && !*s_abort; tile += step) {
       const Tile t = decode_tile<MODE, BN, PAIR>(p, s_off, s_mt, tile, rank);
       bool ok = true;
       for (int kb = 0; kb < t.nkb; ++kb) {
-        if (!mbar_wait(bar_full + 8 * stage, phase, p.status, s_abort)) { ok = false; break; }
-        nv_convert_stage<BN>(sSF0 + stage * C::SF_BYTES, sB0 + stage * C::B_BYTES, ct);
+        if (!mbar_wait(bar_rawfull + 8 * rs, rphase, p.status, s_abort) ||
+            !mbar_wait(bar_dempty + 8 * ds, dphase ^ 1, p.status, s_abort)) {
+          ok = false;
+          break;
+        }
+        nv_convert_stage<BN, 32 * C::CONV_WARPS>(sSF0 + rs * C::SF_BYTES, sB0 + ds * C::B_BYTES, ct);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_conv + 8 * stage);
-        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        if (lane == 0) {
+          mbar_arrive(bar_rawempty + 8 * rs);
+          mbar_arrive(bar_conv + 8 * ds);
+        }
+        if (++rs == C::RAW_STAGES) { rs = 0; rphase ^= 1; }
+        if (++ds == C::DEC_STAGES) { ds = 0; dphase ^= 1; }
       }
       if (!ok) break;
     }
