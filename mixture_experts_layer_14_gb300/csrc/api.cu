@@ -832,8 +832,8 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
     {
       GemmParams p{};
       bool ok = true;
-      if (sh) ok &= map2d(&p.maps[MS_A0], xq, T, d, 64, 128);
-      ok &= map2d(&p.maps[MS_A3], xs, R, d, 64, 128);
+      if (sh) ok &= map2d(&p.maps[MS_A0], xq, T, d, 64, 128) && map2d(&p.maps[MS_A1], xq, T, d, 64, kNvSmallRows);
+      ok &= map2d(&p.maps[MS_A3], xs, R, d, 64, 128) && map2d(&p.maps[MS_A4], xs, R, d, 64, kNvSmallRows);
       if (!ok) return MOK_ERR_CUDA;
       common(p);
       p.nt[0] = Fs / 128;
@@ -860,8 +860,8 @@ int mok_moe_forward(const mok_dims* dims, const mok_weights* w, const void* x,
     {
       GemmParams p{};
       bool ok = true;
-      if (sh) ok &= map2d(&p.maps[MS_A0], hsh, T, Fs, 64, 128);
-      ok &= map2d(&p.maps[MS_A3], h, R, F, 64, 128);
+      if (sh) ok &= map2d(&p.maps[MS_A0], hsh, T, Fs, 64, 128) && map2d(&p.maps[MS_A1], hsh, T, Fs, 64, kNvSmallRows);
+      ok &= map2d(&p.maps[MS_A3], h, R, F, 64, 128) && map2d(&p.maps[MS_A4], h, R, F, 64, kNvSmallRows);
       if (!ok) return MOK_ERR_CUDA;
       common(p);
       p.nt[0] = d / 256;

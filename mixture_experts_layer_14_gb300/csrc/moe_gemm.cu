@@ -359,8 +359,11 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const Tile& t, 
     tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
     tma_load_3d(sB, &M[t.g ? MS_B3 : MS_B0], bar, kb * BK, t.n * BN, t.e);
   } else if constexpr (MODE == G_FWD_GU_NV || MODE == G_FWD_DOWN_NV) {
-    // f16 A rows (x values / h values); B comes raw through load_nv_raw
-    tma_load_2d(sA, &M[t.g ? MS_A3 : MS_A0], bar, kb * BK, t.row0);
+    // f16 A rows (x values / h values); B comes raw through load_nv_raw.  A tile of at most 32
+    // rows loads only those through the 32-row-box maps: the MMA's other rows are left as they
+    // were, and the epilogue stores no row past t.rows
+    const bool small = t.rows <= kNvSmallRows;
+    tma_load_2d(sA, &M[t.g ? (small ? MS_A4 : MS_A3) : (small ? MS_A1 : MS_A0)], bar, kb * BK, t.row0);
   } else if constexpr (MODE == G_BWD_DX) {
     int seg = 0, kk = kb;
     while (seg < 2 && kk >= p.segkb[t.g][seg]) { kk -= p.segkb[t.g][seg]; ++seg; }
@@ -687,12 +690,13 @@ __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& 
     const int col0 = 128 * kb + c;
     float f[32];
     uint32_t qq[8];
-    // dG = w a u s (1 + g (1 - s)), s = sigmoid(g)
+    // dG = w a u s (1 + g (1 - s)), s = sigmoid(g); gq then holds SiLU(g) = g s
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float g = gq[i], u = uq[i];
       const float sgm = sigmoid_f(g);
       f[i] = valid ? w * __uint_as_float(v[i]) * u * sgm * (1.0f + g * (1.0f - sgm)) : 0.0f;
+      gq[i] = g * sgm;
     }
     if (valid) {
       sg |= mx_block32(f, qq) << (c / 4);  // scale byte c / 32 of the row's atom word
@@ -702,12 +706,9 @@ __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& 
     }
     quant_tokens_chunk(f, stg, p.tq[t.g][0] + (int64_t)col0 * tld + kpos, tld, p.tsc[t.g][0], col0,
                        t.mt, nkbt, q, lane);
-    // dU = w a g s
+    // dU = w a SiLU(g)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float g = gq[i];
-      f[i] = valid ? w * __uint_as_float(v[i]) * g * sigmoid_f(g) : 0.0f;
-    }
+    for (int i = 0; i < 32; ++i) f[i] = valid ? w * __uint_as_float(v[i]) * gq[i] : 0.0f;
     if (valid) {
       su |= mx_block32(f, qq) << (c / 4);
       uint4* dq = reinterpret_cast<uint4*>(dUq + c);
@@ -719,8 +720,7 @@ __device__ __forceinline__ void epilogue_da_mx(const GemmParams& p, const Tile& 
     // w h, h = g s u, and the router partial <a, h>
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float g = gq[i], u = uq[i];
-      const float hv = g * sigmoid_f(g) * u;
+      const float hv = gq[i] * uq[i];
       pacc += __uint_as_float(v[i]) * hv;  // zero on rows past the expert (g = u = 0)
       f[i] = w * hv;
     }
@@ -1133,7 +1133,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN>::THREADS, 1) moe_gemm_kernel(con
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status, s_abort)) return;
           // a pair's stage: both CTAs' bytes on the even CTA's barrier; NVFP4: A only
-          constexpr uint32_t kTx = C::NV ? C::A_BYTES : C::A_BYTES + C::B_BYTES + C::SF_BYTES;
+          const uint32_t kTx = C::NV ? (t.rows <= kNvSmallRows ? kNvSmallRows * 128 : C::A_BYTES)
+                                     : C::A_BYTES + C::B_BYTES + C::SF_BYTES;
           if (!PAIR || rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, kTx * (PAIR ? 2 : 1));
           issue_loads<MODE, BN, PAIR>(p, t, kb, rank, sA0 + stage * C::A_BYTES,
                                       sB0 + stage * C::B_BYTES,

@@ -16,6 +16,9 @@ constexpr int BK = 64;                       // K per pipeline stage: 64 bf16 = 
 constexpr int kGemmThreads = 192;            // warp 0 TMA, warp 1 MMA/TMEM, warps 2..5 epilogue
 constexpr int kDispatchChunk = 64;           // tokens per histogram block of the counting sort
 constexpr int kMaxE = 512;
+// NVFP4 GEMMs: A tiles of at most this many rows are loaded through 32-row-box maps (MS_A1 for
+// the shared expert, MS_A4 for the routed experts)
+constexpr int kNvSmallRows = 32;
 constexpr int kMaxK = 8;
 constexpr int kBoundMaps = 5;                   // G_BWD_DW: expert-bounded maps per expert
 
