@@ -223,8 +223,8 @@ def work_model(shape, counts):
 _GEMM_SRC = "mixture_experts_layer_14_gb300/csrc/moe_gemm.cu"
 PROFILED_TRAFFIC = {
     # ncu captures of the Kimi-class forward at full size (4th step of a 3-warm-up bench run)
-    ("kimi_skew_bf16_fwd", "gemm_fwd_gate_up"): ("7d4cd70092ad", 16.813e9 + 0.606e9, _GEMM_SRC),
-    ("kimi_skew_bf16_fwd", "gemm_fwd_down"): ("7d4cd70092ad", 4.459e9 + 2.105e9, _GEMM_SRC),
+    ("kimi_skew_bf16_fwd", "gemm_fwd_gate_up"): ("296ca27805b4", 23.383e9 + 0.606e9, _GEMM_SRC),
+    ("kimi_skew_bf16_fwd", "gemm_fwd_down"): ("296ca27805b4", 5.944e9 + 2.100e9, _GEMM_SRC),
 }
 
 
