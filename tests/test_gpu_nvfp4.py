@@ -6,8 +6,8 @@
 * Forward: within max|d| <= 2e-2 max|ref| (mean 5e-3) of the oracle's NVFP4 reading (the
   quantisation points of the path, the same calibrated activation amaxes, float64 sums); the
   cases cover ragged experts, no shared expert, and calibrated amaxes below the data (values
-  saturate); bit-identical reruns.  The full NVFP4 forward workload (T=4096, E=256) on at least
-  64 tokens that reach every active expert.
+  saturate); bit-identical reruns.  The full NVFP4 forward workloads (E=256 at T=4096, and the
+  T=64 decode) on at least 64 tokens that reach every active expert.
 * The distance to the unquantised float64 layer is reported: NVFP4 keeps about three
   significant bits per element, so it is several per cent, and the oracle's own distance bounds
   the GPU's.
@@ -89,6 +89,10 @@ CASES = {
     "noshared_nv": (LayerShape("noshared_nv", 130, 256, 8, 8, 128, 0, 0, 0.05, "none", "nvfp4", False, 34), None),
     # calibrated amaxes below the data: x values above half its amax and h values above 1 saturate
     "clip_nv": (LayerShape("clip_nv", 200, 256, 8, 2, 256, 256, 1, 0.0, "normal0.1", "nvfp4", False, 35), (0.5, 1.0)),
+    # about 32 rows per expert: tiles on both sides of the 32-row A boxes
+    "rows32_nv": (LayerShape("rows32_nv", 128, 256, 8, 2, 256, 128, 1, 0.0, "none", "nvfp4", False, 36), None),
+    # fewer tokens than a 32-row box: the shared expert's tile takes it too
+    "t24_nv": (LayerShape("t24_nv", 24, 512, 16, 4, 128, 256, 1, 0.0, "normal0.1", "nvfp4", False, 37), None),
 }
 
 
@@ -150,11 +154,14 @@ def test_nvfp4_rejects_training_and_bad_calibration():
     torch.cuda.synchronize()
 
 
-def test_fullsize_nvfp4_forward_sampled():
-    """The NVFP4 forward workload (T=4096, E=256): y on at least 64 tokens that reach every
-    active expert, against the oracle's NVFP4 reading (one expert per pool job)."""
+@pytest.mark.parametrize("name", ["dsv3_nvfp4_fwd", "dsv3_nvfp4_decode_t64"])
+def test_fullsize_nvfp4_forward_sampled(name):
+    """The NVFP4 forward workloads at full size (E=256; T=4096, and T=64, where every expert
+    tile holds at most 32 rows and loads them through the 32-row maps): y on at least 64 tokens
+    that reach every active expert (every token at T=64), against the oracle's NVFP4 reading
+    (one expert per pool job)."""
     ensure_lib()
-    shape = WORKLOADS["dsv3_nvfp4_fwd"]
+    shape = WORKLOADS[name]
     L = make_layer(shape, "cuda")
     D = dims_of(shape, dtype=mok.MOK_NVFP4)
     L["prepared"] = mok.prepare_weights(D, L)
@@ -176,5 +183,5 @@ def test_fullsize_nvfp4_forward_sampled():
                                         expert_map=pmap)
     mx, mn = assert_close("y sampled vs NVFP4 reading", f64(y[toks]), y_nv, max_rel=NV_MAX_REL,
                           mean_rel=NV_MEAN_REL)
-    print(f"dsv3_nvfp4_fwd: {len(toks)} tokens reaching {(counts > 0).sum()} experts: vs NVFP4 "
+    print(f"{name}: {len(toks)} tokens reaching {(counts > 0).sum()} experts: vs NVFP4 "
           f"reading max_rel {mx:.2e} mean_rel {mn:.2e}")
