@@ -225,6 +225,17 @@ PROFILED_TRAFFIC = {
     # ncu captures of the Kimi-class forward at full size (4th step of a 3-warm-up bench run)
     ("kimi_skew_bf16_fwd", "gemm_fwd_gate_up"): ("296ca27805b4", 23.383e9 + 0.606e9, _GEMM_SRC),
     ("kimi_skew_bf16_fwd", "gemm_fwd_down"): ("296ca27805b4", 5.944e9 + 2.100e9, _GEMM_SRC),
+    # the same one-pass capture on the other forward workloads at full size
+    ("dsv3_bf16_fwd", "gemm_fwd_gate_up"): ("296ca27805b4", 15.922e9 + 0.152e9, _GEMM_SRC),
+    ("dsv3_bf16_fwd", "gemm_fwd_down"): ("296ca27805b4", 7.715e9 + 0.520e9, _GEMM_SRC),
+    ("dsv3_decode_t64", "gemm_fwd_gate_up"): ("296ca27805b4", 13.329e9 + 0.006e9, _GEMM_SRC),
+    ("dsv3_decode_t64", "gemm_fwd_down"): ("296ca27805b4", 6.645e9 + 0.008e9, _GEMM_SRC),
+    ("dsv3_mxfp8_fwd", "gemm_fwd_gate_up_mx"): ("296ca27805b4", 8.524e9 + 0.158e9, _GEMM_SRC),
+    ("dsv3_mxfp8_fwd", "gemm_fwd_down_mx"): ("296ca27805b4", 4.048e9 + 1.036e9, _GEMM_SRC),
+    ("dsv3_nvfp4_fwd", "gemm_fwd_gate_up_nv"): ("296ca27805b4", 5.503e9 + 0.150e9, _GEMM_SRC),
+    ("dsv3_nvfp4_fwd", "gemm_fwd_down_nv"): ("296ca27805b4", 2.592e9 + 0.511e9, _GEMM_SRC),
+    ("dsv3_nvfp4_decode_t64", "gemm_fwd_gate_up_nv"): ("296ca27805b4", 3.585e9 + 0.005e9, _GEMM_SRC),
+    ("dsv3_nvfp4_decode_t64", "gemm_fwd_down_nv"): ("296ca27805b4", 1.786e9 + 0.008e9, _GEMM_SRC),
 }
 
 
