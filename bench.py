@@ -236,6 +236,17 @@ PROFILED_TRAFFIC = {
     ("dsv3_nvfp4_fwd", "gemm_fwd_down_nv"): ("296ca27805b4", 2.592e9 + 0.511e9, _GEMM_SRC),
     ("dsv3_nvfp4_decode_t64", "gemm_fwd_gate_up_nv"): ("296ca27805b4", 3.585e9 + 0.005e9, _GEMM_SRC),
     ("dsv3_nvfp4_decode_t64", "gemm_fwd_down_nv"): ("296ca27805b4", 1.786e9 + 0.008e9, _GEMM_SRC),
+    # the training steps (4th step of a 3-warm-up run), forward and backward expert GEMMs
+    ("dsv3_bf16_train", "gemm_fwd_gate_up"): ("296ca27805b4", 16.875e9 + 0.900e9, _GEMM_SRC),
+    ("dsv3_bf16_train", "gemm_fwd_down"): ("296ca27805b4", 7.851e9 + 1.043e9, _GEMM_SRC),
+    ("dsv3_bf16_train", "gemm_bwd_da"): ("296ca27805b4", 9.480e9 + 0.889e9, _GEMM_SRC),
+    ("dsv3_bf16_train", "gemm_bwd_dx"): ("296ca27805b4", 16.556e9 + 1.049e9, _GEMM_SRC),
+    ("dsv3_bf16_train", "gemm_bwd_dw"): ("296ca27805b4", 5.576e9 + 22.587e9, _GEMM_SRC),
+    ("dsv3_mxfp8_train", "gemm_fwd_gate_up_mx"): ("296ca27805b4", 8.775e9 + 1.350e9, _GEMM_SRC),
+    ("dsv3_mxfp8_train", "gemm_fwd_down_mx"): ("296ca27805b4", 4.048e9 + 1.036e9, _GEMM_SRC),
+    ("dsv3_mxfp8_train", "gemm_bwd_da_mx"): ("296ca27805b4", 5.750e9 + 0.864e9, _GEMM_SRC),
+    ("dsv3_mxfp8_train", "gemm_bwd_dx_mx"): ("296ca27805b4", 8.116e9 + 1.043e9, _GEMM_SRC),
+    ("dsv3_mxfp8_train", "gemm_bwd_dw_mx"): ("296ca27805b4", 2.325e9 + 22.578e9, _GEMM_SRC),
 }
 
 
