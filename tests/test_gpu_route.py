@@ -23,6 +23,9 @@ ROUTE_CASES = {
     "dsv3_decode_t64": WORKLOADS["dsv3_decode_t64"],         # T = 64: 8 splits
     "wide_E_512": LayerShape("wide_E_512", 4000, 7168, 512, 8, 2048, 2048, 1, 0.0, "normal0.1",
                              "bf16", False, 18),            # 4 splits, two column chunks
+    # 39 token tiles (2 splits), E = 128: one 128-column MMA per tile
+    "odd_tiles_E128": LayerShape("odd_tiles_E128", 4992, 7168, 128, 8, 2048, 2048, 1, 0.0,
+                                 "normal0.1", "bf16", False, 19),
 }
 
 
