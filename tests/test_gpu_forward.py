@@ -22,6 +22,10 @@ CASES = {
     # at least 320 routed rows per expert: gate/up and down in CTA pairs of 256-row tiles, skewed
     # so that experts span several pair tiles, end mid-tile or hold no rows
     "pairs": LayerShape("pairs", 720, 256, 8, 4, 256, 256, 1, 0.0, "zipf", "bf16", False, 15),
+    # pairs with a Kimi-like tail: 19 of 32 experts hold at most 128 rows (1 to 109; several at
+    # most 64, so the second CTA of their M = 128 pair tile has no row) beside experts of up to
+    # 2500 rows in many 256-row pair tiles
+    "pairs_tail": LayerShape("pairs_tail", 2600, 256, 32, 4, 256, 256, 1, 0.0, "zipf", "bf16", False, 20),
     # pairs for gate/up only (d not a multiple of 256: 128-column down tiles without pairs)
     "pairs_gu_only": LayerShape("pairs_gu_only", 660, 384, 8, 4, 128, 0, 0, 0.0, "normal0.1", "bf16", False, 16),
     # the largest expert count and top-k the ABI accepts (E = 512, k = 8)
